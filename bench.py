@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark of the decode-step linear set on GB300.
+
+One step = the decode linears of a Qwen2-7B-shaped model: 28 layers x
+(fused QKV 4608x3584, O 3584x3584, fused gate/up 37888x3584, down 3584x18944)
+plus the lm_head 152064x3584, per-row INT4 weights, M tokens (default 1),
+each linear one fused quantize + GEMV launch of libw4a8.so.  The 113
+launches are chained with programmatic dependent launch and replayed from a
+CUDA graph.  Weights (3.5 GB) and activations are synthetic (seeded normal
+draws quantized on the GPU) and resident in HBM; they exceed L2, so no L2
+flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead (host cores, bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bit_quantized_decode_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "W4A8 GEMV achieved HBM GB/s (% of GB300 peak); 7B decode-step linear ms"
+FALLBACK_PEAK_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--M", type=int, default=1, help="tokens sharing one weight pass (1..16)")
+    p.add_argument("--layers", type=int, default=wl.QWEN7B_LAYERS, help="layers in the step (28 = full model)")
+    p.add_argument("--no-lm-head", action="store_true")
+    p.add_argument("--no-pdl", action="store_true")
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--per-linear", action="store_true", help="also time each linear kind on its own")
+    p.add_argument("--ref-budget-s", type=float, default=120.0, help="reference arm: total CPU seconds")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------- workload
+def step_linears(layers: int, lm_head: bool):
+    seq = [(layer, lin) for layer in range(layers) for lin in wl.qwen7b_layer()]
+    if lm_head:
+        seq.append((layers, wl.qwen7b_lm_head()))
+    return seq
+
+
+def algorithmic_bytes(lin, M: int) -> int:
+    """Packed weights (0.5 B each) + per-row scale + bias + fp32 x + fp32 y."""
+    return lin.N * lin.K // 2 + 4 * lin.N + (4 * lin.N if lin.bias else 0) + 4 * M * lin.K + 4 * M * lin.N
+
+
+def workload_config(args, n_gpus):
+    return {
+        "workload": (f"qwen2-7b decode-step linear set: {args.layers} layers x (fused QKV 4608x3584, "
+                     f"O 3584x3584, fused gate/up 37888x3584, down 3584x18944)"
+                     + ("" if args.no_lm_head else " + lm_head 152064x3584")
+                     + f", per-row INT4 weights, INT8 per-token activations, M={args.M}"),
+        "M": args.M,
+        "layers": args.layers,
+        "lm_head": not args.no_lm_head,
+        "launches_per_step": 4 * args.layers + (0 if args.no_lm_head else 1),
+        "l2": "inputs larger than L2 (3.5 GB of weights per step), no flush",
+        "parallelism": f"replicas x{n_gpus}",
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_PEAK_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    try:
+        from bit_quantized_decode_gb300 import build
+        digest = build._inputs_digest()
+        path = os.path.join(ROOT, "profiles", "gemv_w4_fused_qwen7b_step.md")
+        vals = {}
+        with open(path) as f:
+            for line in f:
+                if line.startswith("- ") and ":" in line:
+                    k, v = line[2:].split(":", 1)
+                    vals[k.strip()] = v.strip().strip("`")
+        if vals.get("source_digest") != digest:
+            return None
+        return float(vals["dram_bytes_per_launch_full_step"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------- clock sampler
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "util": float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else 100.0,
+                             "hw": parts[6], "hwt": parts[7], "swt": parts[8], "pcap": parts[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in loaded),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+# --------------------------------------------------------- oracle baseline
+def oracle_layer_sample(M: int, seed: int = 1):
+    """Host-side inputs for one Qwen2-7B layer, quantized by the oracle."""
+    import oracle
+    g = wl.rng(seed)
+    layer = []
+    for lin in wl.qwen7b_layer():
+        W = wl.weights(g, lin.N, lin.K)
+        q, sw = oracle.quantize_rows_int4(W)
+        del W
+        layer.append((lin, oracle.pack_int4(q), sw, wl.activations(g, M, lin.K), wl.bias(g, lin.N)))
+    return layer
+
+
+def time_oracle(layer, M: int, min_seconds: float, row_fraction: float = 1.0):
+    """Run the oracle's decode linear over (a row slice of) the layer until
+    min_seconds of CPU time have passed.  Returns (GB/s, seconds, reps)."""
+    import oracle
+    work = []
+    for lin, packed, sw, x, b in layer:
+        n = max(8, int(lin.N * row_fraction))
+        work.append((packed[:n], sw[:n], x, b[:n], n, lin))
+    nbytes = sum(n * lin.K // 2 + 8 * n + 4 * M * lin.K + 4 * M * n for _, _, _, _, n, lin in work)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for packed, sw, x, b, n, lin in work:
+            oracle.w4a8_linear(packed, sw, x, b)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return nbytes * reps / dt / 1e9, dt, reps
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: host cores, bounded sample per step."""
+    if rank != 0:
+        return 0
+    M = max(1, min(16, args.M))
+    layer = oracle_layer_sample(M)
+    layer_bytes = sum(algorithmic_bytes(lin, M) for lin in wl.qwen7b_layer())
+    # size each step so that warmup + steps fit the budget at ~0.3 GB/s
+    gbs_est, _, _ = time_oracle(layer, M, 0.0, row_fraction=0.02)
+    per_step_s = args.ref_budget_s / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(0.002, per_step_s * gbs_est * 1e9 / layer_bytes))
+    for _ in range(args.warmup):
+        time_oracle(layer, M, 0.0, frac)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        gbs, dt, reps = time_oracle(layer, M, 0.0, frac)
+        times.append(dt)
+        nbytes = gbs * dt * 1e9
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32 (int4 x int8)",
+        "data": "synthetic", "config": workload_config(args, args.gpus),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"rows 0..{frac:.4f}*N of each linear of one Qwen2-7B layer (QKV, O, gate/up, "
+                                   f"down), M={M}, through the single-threaded C oracle, per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- our arm
+def build_step(args, device):
+    import torch
+
+    from bit_quantized_decode_gb300 import QuantLinear
+    seq = step_linears(args.layers, not args.no_lm_head)
+    M = args.M
+    total_x = sum(M * lin.K for _, lin in seq)
+    total_y = sum(M * lin.N for _, lin in seq)
+    x_all = torch.empty(total_x, dtype=torch.float32, device=device)
+    y_all = torch.empty(total_y, dtype=torch.float32, device=device)
+    items = []
+    xo = yo = 0
+    seed = 1000
+    for layer, lin in seq:
+        shards = []
+        for rows in lin.shards:
+            shards.append(wl.torch_normal((rows, lin.K), lin.sigma, seed, device))
+            seed += 1
+        biases = [wl.torch_normal((rows,), 0.01, seed + i, device) for i, rows in enumerate(lin.shards)]
+        seed += len(lin.shards)
+        ql = QuantLinear.from_float("w4", shards, biases)
+        del shards
+        x = x_all[xo: xo + M * lin.K].view(M, lin.K)
+        x.copy_(wl.torch_normal((M, lin.K), 1.0, seed, device))
+        seed += 1
+        y = y_all[yo: yo + M * lin.N].view(M, lin.N)
+        qx = torch.empty((M, lin.K), dtype=torch.int8, device=device)
+        sx = torch.empty(M, dtype=torch.float32, device=device)
+        items.append((layer, lin, ql, x, y, qx, sx))
+        xo += M * lin.K
+        yo += M * lin.N
+    torch.cuda.synchronize()
+    return items, x_all, y_all
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from bit_quantized_decode_gb300 import W4_FLAG_PDL, _lib
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    _lib.load()
+    _lib.clear_device_error()
+    items, x_all, y_all = build_step(args, dev)
+    M = args.M
+    bytes_per_step = sum(algorithmic_bytes(lin, M) for _, lin, *_ in items)
+    launches = len(items)
+    pdl_flag = 0 if args.no_pdl else W4_FLAG_PDL
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for i, (_, lin, ql, x, y, qx, sx) in enumerate(items):
+            ql(x, y, qx, sx, flags=pdl_flag if i > 0 else 0)
+
+    with torch.cuda.stream(stream):
+        step()                     # eager run: sets kernel attributes, checks the path
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+
+    def replay():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if elapsed_ms < 400:
+        time.sleep(0.2)
+    clocks = sampler.stop()
+    err = _lib.device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+
+    t_max = elapsed_ms
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    ms_per_step = t_max / args.steps
+    value = world * bytes_per_step * args.steps / (t_max / 1e3) / 1e9
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
+    x_host = torch.empty(x_all.numel(), dtype=torch.float32, pin_memory=True)
+    x_host.copy_(x_all.cpu())
+    y_host = torch.empty(y_all.numel(), dtype=torch.float32, pin_memory=True)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            x_all.copy_(x_host, non_blocking=True)
+            replay()
+            y_host.copy_(y_all, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            x_all.copy_(x_host, non_blocking=True)
+            replay()
+            y_host.copy_(y_all, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * bytes_per_step * e2e_steps / (e2e_ms / 1e3) / 1e9
+
+    # ---- optional: each linear kind on its own (rotating over the layers' copies)
+    per_linear = None
+    if args.per_linear and rank == 0:
+        per_linear = {}
+        for name in ("qkv", "o", "gate_up", "down", "lm_head"):
+            sel = [it for it in items if it[1].name == name]
+            if not sel:
+                continue
+            reps = max(1, 200 // len(sel))
+            with torch.cuda.stream(stream):
+                for it in sel:
+                    it[2](it[3], it[4], it[5], it[6])
+                a0 = torch.cuda.Event(enable_timing=True)
+                a1 = torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                for _ in range(reps):
+                    for it in sel:
+                        it[2](it[3], it[4], it[5], it[6])
+                a1.record(stream)
+            torch.cuda.synchronize()
+            us = a0.elapsed_time(a1) * 1e3 / (reps * len(sel))
+            b = algorithmic_bytes(sel[0][1], M)
+            per_linear[name] = {"us": round(us, 3), "GB/s": round(b / us / 1e3, 1), "bytes": b}
+
+    if rank != 0:
+        return 0
+
+    cpu_baseline = None
+    if not args.no_cpu_baseline:
+        layer = oracle_layer_sample(M)
+        gbs, dt, reps = time_oracle(layer, M, 10.0)
+        cpu_baseline = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                        "sample": (f"one Qwen2-7B layer (QKV, O, gate/up, down; N(0,0.02) weights drawn on the "
+                                   f"host and quantized by the oracle), M={M}, single-threaded C oracle, "
+                                   f"{reps} passes in {dt:.1f} s")}
+
+    peak, peak_kind = measured_peak()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32 (int4 x int8 dp4a)",
+        "data": "synthetic",
+        "config": workload_config(args, world),
+        "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / world / peak, 4), "traffic": profiled_traffic(),
+                     "peak_kind": peak_kind,
+                     "kernel": "gemv_kernel<W4, M, fused> (all launches of the step; bytes and time per launch "
+                               "averaged over the step)"},
+        "cpu_baseline": cpu_baseline,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(x_all.numel() * 4), "d2h_bytes_per_step": int(y_all.numel() * 4)},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+        "bytes_per_step": bytes_per_step,
+    }
+    if per_linear is not None:
+        line["per_linear"] = per_linear
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if not 1 <= args.M <= 16:
+        raise SystemExit("--M must be in 1..16")
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,269 @@
+"""ctypes binding of ``libw4a8.so`` (C ABI declared in include/w4a8.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the current CUDA device, checks dtypes and shapes, and passes raw
+pointers and the current stream to the C entry point of the same name.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU path.  If the
+library has not been built, loading fails with an error saying how to build
+it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4a8.so")
+
+W4_OK = 0
+STATUS = {
+    0: "W4_OK",
+    1: "W4_ERR_INVALID_ARG",
+    2: "W4_ERR_UNSUPPORTED_SHAPE",
+    3: "W4_ERR_MISALIGNED",
+    4: "W4_ERR_CUDA",
+    5: "W4_ERR_DEVICE_TIMEOUT",
+}
+W4_FLAG_PDL = 1
+W4_MAX_M = 16
+W4_MAX_K = 131072
+W4_MAX_SHARDS = 8
+
+# exported symbol -> (argtypes, restype)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_U = ctypes.c_uint
+_SZ = ctypes.c_size_t
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_PI = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "w4_status_str": ([_I], ctypes.c_char_p),
+    "w4_version": ([], _I),
+    "w4_quantize_rows": ([_P, _I, _I, _P, _P, _P], _I),
+    "q4_0_quantize": ([_P, _I, _I, _P, _P], _I),
+    "i8g32_quantize": ([_P, _I, _I, _P, _P, _P], _I),
+    "w4_repacked_bytes": ([_I, _I], _SZ),
+    "q4_0_repacked_bytes": ([_I, _I], _SZ),
+    "i8g32_repacked_bytes": ([_I, _I], _SZ),
+    "w4_repack": ([_PP, _PI, _I, _I, _P, _SZ, _P], _I),
+    "q4_0_repack": ([_PP, _PI, _I, _I, _P, _SZ, _P], _I),
+    "i8g32_repack": ([_PP, _PP, _PI, _I, _I, _P, _SZ, _P], _I),
+    "w4_concat_f32": ([_PP, _PI, _I, _P, _P], _I),
+    "a8_quantize": ([_P, _I, _I, _P, _P, _P], _I),
+    "w4a8_gemv": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "q4_0_gemv": ([_P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "i8g32_gemv": ([_P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "w4a8_linear": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P], _I),
+    "q4_0_linear": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P], _I),
+    "i8g32_linear": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P], _I),
+    "w4_device_error": ([ctypes.POINTER(ctypes.c_uint)], _I),
+    "w4_clear_device_error": ([], _I),
+}
+
+_lib = None
+
+
+class W4Error(RuntimeError):
+    def __init__(self, name: str, status: int):
+        super().__init__(f"{name}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m bit_quantized_decode_gb300.build` "
+                "(needs nvcc); the decode GEMV has no CPU implementation")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+    return _lib
+
+
+def _check(name: str, st: int):
+    if st != W4_OK:
+        raise W4Error(name, st)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("tensor must live on a CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("tensor must be contiguous")
+
+
+def _ptr_array(ts):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() if t is not None else None for t in ts])
+    return ctypes.cast(arr, _PP), arr
+
+
+def _int_array(vals):
+    arr = (ctypes.c_int * len(vals))(*vals)
+    return ctypes.cast(arr, _PI), arr
+
+
+# ---------------------------------------------------------------- queries
+def status_str(st: int) -> str:
+    return load().w4_status_str(st).decode()
+
+
+def version() -> int:
+    return load().w4_version()
+
+
+def w4_repacked_bytes(N: int, K: int) -> int:
+    return int(load().w4_repacked_bytes(N, K))
+
+
+def q4_0_repacked_bytes(N: int, K: int) -> int:
+    return int(load().q4_0_repacked_bytes(N, K))
+
+
+def i8g32_repacked_bytes(N: int, K: int) -> int:
+    return int(load().i8g32_repacked_bytes(N, K))
+
+
+# ------------------------------------------------------------- quantizers
+def w4_quantize_rows(W, packed, s_w, stream=None):
+    """W float32 [N][K] -> packed int32 [N][K/8] (canonical words), s_w float32 [N]."""
+    _dev(W, packed, s_w)
+    N, K = W.shape
+    _check("w4_quantize_rows", load().w4_quantize_rows(_ptr(W), N, K, _ptr(packed), _ptr(s_w), _stream(stream)))
+
+
+def q4_0_quantize(W, blocks, stream=None):
+    """W float32 [N][K] -> blocks uint8 [N][K/32][18]."""
+    _dev(W, blocks)
+    N, K = W.shape
+    _check("q4_0_quantize", load().q4_0_quantize(_ptr(W), N, K, _ptr(blocks), _stream(stream)))
+
+
+def i8g32_quantize(W, q, d, stream=None):
+    """W float32 [N][K] -> q int8 [N][K], d fp16 bits int16 [N][K/32]."""
+    _dev(W, q, d)
+    N, K = W.shape
+    _check("i8g32_quantize", load().i8g32_quantize(_ptr(W), N, K, _ptr(q), _ptr(d), _stream(stream)))
+
+
+# ---------------------------------------------------------------- repack
+def w4_repack(shards, K, out, stream=None):
+    """shards: list of canonical packed tensors [rows_s][K/8]; out: uint8 buffer."""
+    _dev(out, *shards)
+    pp, keep = _ptr_array(shards)
+    rows, keep2 = _int_array([s.shape[0] for s in shards])
+    _check("w4_repack", load().w4_repack(pp, rows, len(shards), K, _ptr(out), out.numel() * out.element_size(),
+                                         _stream(stream)))
+
+
+def q4_0_repack(shards, K, out, stream=None):
+    _dev(out, *shards)
+    pp, keep = _ptr_array(shards)
+    rows, keep2 = _int_array([s.shape[0] for s in shards])
+    _check("q4_0_repack", load().q4_0_repack(pp, rows, len(shards), K, _ptr(out), out.numel() * out.element_size(),
+                                             _stream(stream)))
+
+
+def i8g32_repack(q_shards, d_shards, K, out, stream=None):
+    _dev(out, *q_shards, *d_shards)
+    qp, keep = _ptr_array(q_shards)
+    dp, keep2 = _ptr_array(d_shards)
+    rows, keep3 = _int_array([s.shape[0] for s in q_shards])
+    _check("i8g32_repack", load().i8g32_repack(qp, dp, rows, len(q_shards), K, _ptr(out),
+                                               out.numel() * out.element_size(), _stream(stream)))
+
+
+def w4_concat_f32(parts, out, stream=None):
+    _dev(out, *parts)
+    pp, keep = _ptr_array(parts)
+    lens, keep2 = _int_array([p.numel() for p in parts])
+    _check("w4_concat_f32", load().w4_concat_f32(pp, lens, len(parts), _ptr(out), _stream(stream)))
+
+
+# ------------------------------------------------------------- per token
+def a8_quantize(x, qx, sx, stream=None):
+    """x float32 [M][K] -> qx int8 [M][K], sx float32 [M]."""
+    _dev(x, qx, sx)
+    M, K = x.shape
+    _check("a8_quantize", load().a8_quantize(_ptr(x), M, K, _ptr(qx), _ptr(sx), _stream(stream)))
+
+
+def w4a8_gemv(w, s_w, bias, qx, sx, y, stream=None):
+    """y[M][N] from repacked per-row INT4 weights and int8 activations."""
+    _dev(w, s_w, bias, qx, sx, y)
+    M, K = qx.shape
+    N = y.shape[1]
+    _check("w4a8_gemv", load().w4a8_gemv(_ptr(w), _ptr(s_w), _ptr(bias), _ptr(qx), _ptr(sx), M, N, K, _ptr(y),
+                                         _stream(stream)))
+
+
+def q4_0_gemv(w, bias, qx, sx, y, stream=None):
+    _dev(w, bias, qx, sx, y)
+    M, K = qx.shape
+    N = y.shape[1]
+    _check("q4_0_gemv", load().q4_0_gemv(_ptr(w), _ptr(bias), _ptr(qx), _ptr(sx), M, N, K, _ptr(y),
+                                         _stream(stream)))
+
+
+def i8g32_gemv(w, bias, qx, sx, y, stream=None):
+    _dev(w, bias, qx, sx, y)
+    M, K = qx.shape
+    N = y.shape[1]
+    _check("i8g32_gemv", load().i8g32_gemv(_ptr(w), _ptr(bias), _ptr(qx), _ptr(sx), M, N, K, _ptr(y),
+                                           _stream(stream)))
+
+
+def w4a8_linear(w, s_w, bias, x, y, qx, sx, flags: int = 0, stream=None):
+    """Quantize x and run the per-row INT4 GEMV in one launch; y[M][N]."""
+    _dev(w, s_w, bias, x, y, qx, sx)
+    M, K = x.shape
+    N = y.shape[1]
+    _check("w4a8_linear", load().w4a8_linear(_ptr(w), _ptr(s_w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx),
+                                             _ptr(sx), flags, _stream(stream)))
+
+
+def q4_0_linear(w, bias, x, y, qx, sx, flags: int = 0, stream=None):
+    _dev(w, bias, x, y, qx, sx)
+    M, K = x.shape
+    N = y.shape[1]
+    _check("q4_0_linear", load().q4_0_linear(_ptr(w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx), _ptr(sx),
+                                             flags, _stream(stream)))
+
+
+def i8g32_linear(w, bias, x, y, qx, sx, flags: int = 0, stream=None):
+    _dev(w, bias, x, y, qx, sx)
+    M, K = x.shape
+    N = y.shape[1]
+    _check("i8g32_linear", load().i8g32_linear(_ptr(w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx), _ptr(sx),
+                                               flags, _stream(stream)))
+
+
+# ---------------------------------------------------------- device errors
+def device_error() -> int:
+    code = ctypes.c_uint(0)
+    st = load().w4_device_error(ctypes.byref(code))
+    if st not in (W4_OK, 5):
+        raise W4Error("w4_device_error", st)
+    return int(code.value)
+
+
+def clear_device_error():
+    _check("w4_clear_device_error", load().w4_clear_device_error())

@@ -1,0 +1,12 @@
+// GEMV kernels for one weight format, kept in a translation unit of their own
+// so the formats compile in parallel.
+#include "gemv_kernel.cuh"
+
+namespace w4k {
+
+cudaError_t launch_gemv_w4(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl, cudaStream_t s)
+{
+    return launch_gemv_fmt<FMT_W4>(a, MT, fused, grid, smem, pdl, s);
+}
+
+}  // namespace w4k

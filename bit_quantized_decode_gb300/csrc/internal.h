@@ -1,0 +1,94 @@
+// Declarations shared by the host API and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace w4k {
+
+enum FmtId { FMT_W4 = 0, FMT_Q4_0 = 1, FMT_I8G32 = 2 };
+
+constexpr int kRows = 8;                 // weight rows per tile
+constexpr int kWarps = 8;                // warps per GEMV thread block
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxStages = 8;            // ring slots per warp, upper bound
+constexpr int kAccWords = 128;           // round_tiles * MT, bounds the per-round accumulator
+
+// Lines (8 rows x one 32-weight chunk) per ring slot and bytes per unit.
+__host__ __device__ constexpr int fmt_unit_bytes(int fmt) { return fmt == FMT_I8G32 ? 32 : 16; }
+__host__ __device__ constexpr bool fmt_group(int fmt) { return fmt != FMT_W4; }
+__host__ __device__ constexpr int fmt_slice_lines(int fmt) { return fmt == FMT_I8G32 ? 16 : 32; }
+__host__ __device__ constexpr int fmt_slot_w_bytes(int fmt) { return fmt_slice_lines(fmt) * kRows * fmt_unit_bytes(fmt); }
+__host__ __device__ constexpr int fmt_slot_s_bytes(int fmt) { return fmt_group(fmt) ? fmt_slice_lines(fmt) * kRows * 2 : 0; }
+__host__ __device__ constexpr int fmt_slot_bytes(int fmt) { return fmt_slot_w_bytes(fmt) + fmt_slot_s_bytes(fmt); }
+
+// Arguments of one GEMV launch (passed by value).
+struct GemvArgs {
+    const uint8_t* w;        // repacked units
+    const uint16_t* wscale;  // fp16 group-scale plane (Q4_0, I8G32), else null
+    const float* s_w;        // per-row scales (W4), else null
+    const float* bias;       // [N] or null
+    const float* x;          // fp32 activations [M][K] (fused quantize), else null
+    const int8_t* qx_in;     // int8 activations [M][K] (unfused), else null
+    const float* sx_in;      // [M] (unfused), else null
+    int8_t* qx_out;          // fused: block 0 writes the codes here (may be null)
+    float* sx_out;           // fused: block 0 writes the scales here (may be null)
+    float* y;                // [M][N]
+    int M, N, K;
+    int C;                   // K / 32
+    int T;                   // ceil(N / 8)
+    int stages;              // ring slots per warp
+    int round_tiles;         // tiles per accumulation round
+    unsigned* err;           // device error word
+};
+
+struct SmemLayout {
+    int bars, sx, red, meta, acc, bnd, ring, xs, total;
+};
+
+__host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, bool fused, int K, int stages, int round_tiles)
+{
+    SmemLayout L;
+    int o = 0;
+    L.bars = o;  o = align_up(o + kWarps * stages * 8, 16);
+    L.sx = o;    o = align_up(o + MT * 4, 16);
+    L.red = o;   o = align_up(o + kWarps * MT * 4, 16);
+    L.meta = o;  o = align_up(o + 2 * kWarps * 2 * 4, 16);
+    L.acc = o;   o = align_up(o + 2 * round_tiles * kRows * MT * 4, 16);
+    L.bnd = o;   o = align_up(o + 2 * kWarps * 2 * kRows * MT * 4, 128);
+    L.ring = o;  o = align_up(o + kWarps * stages * fmt_slot_bytes(fmt), 128);
+    L.xs = o;    o += fused ? MT * K : 0;
+    L.total = o;
+    return L;
+}
+
+// Error codes written to the device error word.
+constexpr unsigned kErrWaitTimeout = 0x57414954u;  // "WAIT"
+
+// Kernel launchers, one translation unit per format.
+cudaError_t launch_gemv_w4(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_gemv_q4_0(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_gemv_i8g32(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl,
+                              cudaStream_t s);
+
+// Load-time and activation kernels (prep_kernels.cu).
+constexpr int kMaxShards = 8;
+struct ShardTable {
+    const void* p[kMaxShards];
+    const void* p2[kMaxShards];
+    int row0[kMaxShards + 1];
+    int n;
+};
+
+cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, cudaStream_t s);
+cudaError_t launch_w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, cudaStream_t s);
+cudaError_t launch_q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, cudaStream_t s);
+cudaError_t launch_i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, cudaStream_t s);
+cudaError_t launch_w4_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
+cudaError_t launch_q4_0_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
+cudaError_t launch_i8g32_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
+
+}  // namespace w4k

@@ -1,0 +1,338 @@
+// Activation quantization, load-time weight quantizers and repack kernels.
+//
+// Quantization decisions are taken in IEEE fp32 with correctly rounded
+// division (__fdiv_rn) and round-half-to-even conversion (__float2int_rn),
+// so the codes are reproducible bit for bit by any IEEE implementation.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace w4k {
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+__device__ __forceinline__ float abs_max4(float4 v)
+{
+    return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+
+// clip(rint(v / s), lo, hi); s == 0 gives 0.
+__device__ __forceinline__ int quant_code(float v, float s, int lo, int hi)
+{
+    if (s == 0.0f) return 0;
+    int q = __float2int_rn(__fdiv_rn(v, s));
+    return q > hi ? hi : (q < lo ? lo : q);
+}
+
+// ------------------------------------------------ per-token INT8 activations
+// "Jetson Orin AGX INT4 推理优化实践", §"从 FP 线性层到 INT4 DP4A 的数学推导":
+// s^x = max|x| / 127, q^x = clip(round(x / s^x), -127, 127).  One block per token.
+constexpr int kQuantThreads = 512;
+
+__global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float* __restrict__ x, int K,
+                                                                     int8_t* __restrict__ qx, float* __restrict__ sx)
+{
+    __shared__ float red[kQuantThreads / 32];
+    const int m = blockIdx.x;
+    const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K);
+    const int K4 = K >> 2;
+    float mx = 0.0f;
+    for (int i = threadIdx.x; i < K4; i += kQuantThreads) mx = fmaxf(mx, abs_max4(xr[i]));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    float amax = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    uint32_t* out = reinterpret_cast<uint32_t*>(qx + static_cast<size_t>(m) * K);
+    for (int i = threadIdx.x; i < K4; i += kQuantThreads) {
+        const float4 v = xr[i];
+        out[i] = (static_cast<uint32_t>(quant_code(v.x, s, -127, 127)) & 0xffu) |
+                 ((static_cast<uint32_t>(quant_code(v.y, s, -127, 127)) & 0xffu) << 8) |
+                 ((static_cast<uint32_t>(quant_code(v.z, s, -127, 127)) & 0xffu) << 16) |
+                 ((static_cast<uint32_t>(quant_code(v.w, s, -127, 127)) & 0xffu) << 24);
+    }
+    if (threadIdx.x == 0) sx[m] = s;
+}
+
+cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, cudaStream_t s)
+{
+    a8_quantize_kernel<<<M, kQuantThreads, 0, s>>>(x, K, qx, sx);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------ per-row INT4 weights
+// s^W_j = max|W_j| / 7, q = clip(rint(W / s^W_j), -8, 7), eight codes per
+// uint32 with weight k in bits 4k..4k+3 (§"DP4A 做了什么").  One warp per row.
+__global__ void __launch_bounds__(256) w4_quantize_rows_kernel(const float* __restrict__ W, int N, int K,
+                                                              uint32_t* __restrict__ packed, float* __restrict__ sw)
+{
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const float4* wr = reinterpret_cast<const float4*>(W + static_cast<size_t>(row) * K);
+    float mx = 0.0f;
+    for (int i = lane; i < K / 4; i += 32) mx = fmaxf(mx, abs_max4(wr[i]));
+    mx = warp_max(mx);
+    const float s = __fdiv_rn(mx, 7.0f);
+    if (lane == 0) sw[row] = s;
+    uint32_t* out = packed + static_cast<size_t>(row) * (K / 8);
+    for (int wi = lane; wi < K / 8; wi += 32) {
+        const float4 v0 = wr[2 * wi], v1 = wr[2 * wi + 1];
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) word |= (static_cast<uint32_t>(quant_code(v[k], s, -8, 7)) & 0xfu) << (4 * k);
+        out[wi] = word;
+    }
+}
+
+cudaError_t launch_w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, cudaStream_t s)
+{
+    w4_quantize_rows_kernel<<<(N + 7) / 8, 256, 0, s>>>(W, N, K, packed, s_w);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- Q4_0
+// "在香橙派上跑 Gemma4", §3.1: 32 weights per block, 16 bytes of nibbles and an
+// fp16 scale; d = fp16(max|w| / 8), n = clip(rint(w / d), -8, 7) + 8.  Block
+// bytes: d (little endian), then byte i = element i | element (i+16) << 4.
+__global__ void __launch_bounds__(256) q4_0_quantize_kernel(const float* __restrict__ W, int N, int K,
+                                                           uint8_t* __restrict__ blocks)
+{
+    const int G = K / 32;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<long long>(N) * G) return;
+    const float4* wp = reinterpret_cast<const float4*>(W + idx * 32);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 t = wp[i];
+        v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    const __half dh = __float2half_rn(__fdiv_rn(mx, 8.0f));
+    const float d = __half2float(dh);
+    // 18-byte blocks are 2-byte aligned: store them as nine 16-bit words
+    // (little endian: the scale first, then nibble bytes 2j and 2j+1).
+    uint16_t* blk = reinterpret_cast<uint16_t*>(blocks + idx * 18);
+    blk[0] = __half_as_ushort(dh);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t pair = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = 2 * j + h;
+            const uint32_t lo = static_cast<uint32_t>(quant_code(v[i], d, -8, 7) + 8);
+            const uint32_t hi = static_cast<uint32_t>(quant_code(v[i + 16], d, -8, 7) + 8);
+            pair |= (lo | (hi << 4)) << (8 * h);
+        }
+        blk[1 + j] = static_cast<uint16_t>(pair);
+    }
+}
+
+cudaError_t launch_q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, cudaStream_t s)
+{
+    const long long n = static_cast<long long>(N) * (K / 32);
+    q4_0_quantize_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(W, N, K, blocks);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- i8g32
+// "在香橙派上跑 Gemma4", §3.2: int8 weights with one fp16 scale per group;
+// here d = fp16(max|w| / 32), q = clip(rint(w / d), -32, 31).
+__global__ void __launch_bounds__(256) i8g32_quantize_kernel(const float* __restrict__ W, int N, int K,
+                                                            int8_t* __restrict__ q, uint16_t* __restrict__ d)
+{
+    const int G = K / 32;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<long long>(N) * G) return;
+    const float4* wp = reinterpret_cast<const float4*>(W + idx * 32);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 t = wp[i];
+        v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    const __half dh = __float2half_rn(__fdiv_rn(mx, 32.0f));
+    const float df = __half2float(dh);
+    d[idx] = __half_as_ushort(dh);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w[i] = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            w[i] |= (static_cast<uint32_t>(quant_code(v[4 * i + b], df, -32, 31)) & 0xffu) << (8 * b);
+    }
+    uint4* out = reinterpret_cast<uint4*>(q + idx * 32);
+    out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+cudaError_t launch_i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, cudaStream_t s)
+{
+    const long long n = static_cast<long long>(N) * (K / 32);
+    i8g32_quantize_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(W, N, K, q, d);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- repack
+// Fused-shard row lookup: row j of the fused matrix is row j - row0[s] of
+// shard s.  Returns -1 for rows past the end (tile padding).
+__device__ __forceinline__ int shard_of(const ShardTable& st, int row, int& local)
+{
+    for (int s = 0; s < st.n; ++s) {
+        if (row < st.row0[s + 1]) {
+            local = row - st.row0[s];
+            return s;
+        }
+    }
+    return -1;
+}
+
+// Canonical word (weight k in nibble k) -> device word: byte b holds weight b
+// in its low nibble and weight b+4 in its high nibble.
+__device__ __forceinline__ uint32_t spread4(uint32_t v)
+{
+    return (v & 0xfu) | ((v & 0xf0u) << 4) | ((v & 0xf00u) << 8) | ((v & 0xf000u) << 12);
+}
+
+__device__ __forceinline__ uint32_t interleave_w4(uint32_t canon)
+{
+    return spread4(canon & 0xffffu) | (spread4(canon >> 16) << 4);
+}
+
+// One thread per unit (t, c, r) -> out unit index ((t*C + c)*8 + r).
+__global__ void w4_repack_kernel(const ShardTable st, int N, int K, long long units, uint4* __restrict__ out)
+{
+    const long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (u >= units) return;
+    const int C = K / 32;
+    const int r = static_cast<int>(u % kRows);
+    const long long tc = u / kRows;
+    const int c = static_cast<int>(tc % C);
+    const long long t = tc / C;
+    const long long row = t * kRows + r;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    int local = 0;
+    if (row < N) {
+        const int s = shard_of(st, static_cast<int>(row), local);
+        const uint32_t* src = static_cast<const uint32_t*>(st.p[s]) + static_cast<size_t>(local) * (K / 8) + c * 4;
+        o.x = interleave_w4(src[0]);
+        o.y = interleave_w4(src[1]);
+        o.z = interleave_w4(src[2]);
+        o.w = interleave_w4(src[3]);
+    }
+    out[u] = o;
+}
+
+// Q4_0 nibble n (value n - 8) -> 4-bit two's complement of n - 8, i.e. n ^ 8.
+__global__ void q4_0_repack_kernel(const ShardTable st, int N, int K, long long units, uint4* __restrict__ out,
+                                   uint16_t* __restrict__ plane)
+{
+    const long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (u >= units) return;
+    const int C = K / 32;
+    const int r = static_cast<int>(u % kRows);
+    const long long tc = u / kRows;
+    const int c = static_cast<int>(tc % C);
+    const long long t = tc / C;
+    const long long row = t * kRows + r;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    uint16_t dbits = 0;
+    int local = 0;
+    if (row < N) {
+        const int s = shard_of(st, static_cast<int>(row), local);
+        const uint8_t* blk = static_cast<const uint8_t*>(st.p[s]) + (static_cast<size_t>(local) * C + c) * 18;
+        dbits = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
+        uint32_t v4[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t byte = blk[2 + i];
+            v4[i] = (byte & 0xfu) ^ 8u;
+            v4[i + 16] = (byte >> 4) ^ 8u;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            w[wi] = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) w[wi] |= (v4[8 * wi + b] | (v4[8 * wi + b + 4] << 4)) << (8 * b);
+        }
+        o = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    out[u] = o;
+    plane[u] = dbits;
+}
+
+__global__ void i8g32_repack_kernel(const ShardTable st, int N, int K, long long units, uint4* __restrict__ out,
+                                    uint16_t* __restrict__ plane)
+{
+    const long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (u >= units) return;
+    const int C = K / 32;
+    const int r = static_cast<int>(u % kRows);
+    const long long tc = u / kRows;
+    const int c = static_cast<int>(tc % C);
+    const long long t = tc / C;
+    const long long row = t * kRows + r;
+    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+    uint16_t dbits = 0;
+    int local = 0;
+    if (row < N) {
+        const int s = shard_of(st, static_cast<int>(row), local);
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(st.p[s]) +
+                                                          static_cast<size_t>(local) * K + c * 32);
+        o0 = src[0];
+        o1 = src[1];
+        dbits = static_cast<const uint16_t*>(st.p2[s])[static_cast<size_t>(local) * C + c];
+    }
+    out[2 * u] = o0;
+    out[2 * u + 1] = o1;
+    plane[u] = dbits;
+}
+
+static inline unsigned blocks_for(long long n, int t) { return static_cast<unsigned>((n + t - 1) / t); }
+
+cudaError_t launch_w4_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s)
+{
+    const long long T = (N + kRows - 1) / kRows;
+    const long long units = T * (K / 32) * kRows;
+    w4_repack_kernel<<<blocks_for(units, 256), 256, 0, s>>>(st, N, K, units, static_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q4_0_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s)
+{
+    const long long T = (N + kRows - 1) / kRows;
+    const long long units = T * (K / 32) * kRows;
+    uint4* o = static_cast<uint4*>(out);
+    uint16_t* plane = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + units * 16);
+    q4_0_repack_kernel<<<blocks_for(units, 256), 256, 0, s>>>(st, N, K, units, o, plane);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_i8g32_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s)
+{
+    const long long T = (N + kRows - 1) / kRows;
+    const long long units = T * (K / 32) * kRows;
+    uint4* o = static_cast<uint4*>(out);
+    uint16_t* plane = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + units * 32);
+    i8g32_repack_kernel<<<blocks_for(units, 256), 256, 0, s>>>(st, N, K, units, o, plane);
+    return cudaGetLastError();
+}
+
+}  // namespace w4k

@@ -1,0 +1,390 @@
+// C ABI of the decode GEMV library (declared in include/w4a8.h): argument
+// checks, launch configuration and dispatch.  No entry point allocates
+// memory or synchronises, except the two device-error-word calls.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/w4a8.h"
+#include "internal.h"
+
+using namespace w4k;
+
+// Device error word written by kernels whose bounded waits run out.
+__device__ unsigned g_w4_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+    unsigned* err = nullptr;
+    bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+w4_status device_info(DeviceInfo** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W4_ERR_CUDA;
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return W4_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return W4_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_w4_error_word) != cudaSuccess) return W4_ERR_CUDA;
+        d.err = static_cast<unsigned*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return W4_OK;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline w4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4_OK : W4_ERR_CUDA; }
+
+inline int round_pow2_tokens(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+
+w4_status check_mk(int M, int K)
+{
+    if (M < 0 || K <= 0) return W4_ERR_INVALID_ARG;
+    if (M > W4_MAX_M || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_UNSUPPORTED_SHAPE;
+    return W4_OK;
+}
+
+w4_status build_shards(const void* const* p, const void* const* p2, const int* rows, int n, ShardTable& st, int& N)
+{
+    if (n < 1 || n > kMaxShards || p == nullptr || rows == nullptr) return W4_ERR_INVALID_ARG;
+    std::memset(&st, 0, sizeof(st));
+    long long total = 0;
+    st.n = n;
+    for (int s = 0; s < n; ++s) {
+        if (rows[s] < 0) return W4_ERR_INVALID_ARG;
+        if (rows[s] > 0 && p[s] == nullptr) return W4_ERR_INVALID_ARG;
+        if (p2 != nullptr && rows[s] > 0 && p2[s] == nullptr) return W4_ERR_INVALID_ARG;
+        st.p[s] = p[s];
+        st.p2[s] = p2 ? p2[s] : nullptr;
+        st.row0[s] = static_cast<int>(total);
+        total += rows[s];
+        if (total > (1LL << 30)) return W4_ERR_UNSUPPORTED_SHAPE;
+    }
+    st.row0[n] = static_cast<int>(total);
+    N = static_cast<int>(total);
+    return W4_OK;
+}
+
+size_t tiles(int N) { return (static_cast<size_t>(N) + kRows - 1) / kRows; }
+
+// Choose the launch configuration of one GEMV and launch it.
+w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t s)
+{
+    DeviceInfo* dev = nullptr;
+    w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    const int MT = round_pow2_tokens(a.M);
+    a.C = a.K / 32;
+    a.T = static_cast<int>(tiles(a.N));
+    a.round_tiles = kAccWords / MT;
+    a.err = dev->err;
+    const int budget = dev->smem_optin;
+    int stages = kMaxStages;
+    while (stages >= 2 && smem_layout(fmt, MT, fused, a.K, stages, a.round_tiles).total > budget) --stages;
+    if (stages < 2) return W4_ERR_UNSUPPORTED_SHAPE;
+    a.stages = stages;
+    const size_t smem = static_cast<size_t>(smem_layout(fmt, MT, fused, a.K, stages, a.round_tiles).total);
+    const int grid = a.T < dev->sms ? a.T : dev->sms;
+    const bool pdl = (flags & W4_FLAG_PDL) != 0;
+    cudaError_t e;
+    if (fmt == FMT_W4) e = launch_gemv_w4(a, MT, fused, grid, smem, pdl, s);
+    else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(a, MT, fused, grid, smem, pdl, s);
+    else e = launch_gemv_i8g32(a, MT, fused, grid, smem, pdl, s);
+    return cuda_status(e);
+}
+
+// Would the fused kernel (x quantized into shared memory) fit?
+bool fused_fits(int fmt, int M, int K)
+{
+    DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != W4_OK) return false;
+    const int MT = round_pow2_tokens(M);
+    return smem_layout(fmt, MT, true, K, 2, kAccWords / MT).total <= dev->smem_optin;
+}
+
+w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bias, const int8_t* qx,
+                      const float* sx, int M, int N, int K, float* y, cudaStream_t s)
+{
+    w4_status st = check_mk(M, K);
+    if (st != W4_OK) return st;
+    if (N < 0) return W4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!w || !qx || !sx || !y || (fmt == FMT_W4 && !s_w)) return W4_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(qx, 16) || !aligned(sx, 4) || !aligned(y, 4) || (s_w && !aligned(s_w, 4)) ||
+        (bias && !aligned(bias, 4)))
+        return W4_ERR_MISALIGNED;
+    GemvArgs a = {};
+    a.w = static_cast<const uint8_t*>(w);
+    const size_t units = tiles(N) * kRows * (K / 32);
+    a.wscale = fmt == FMT_W4 ? nullptr
+                             : reinterpret_cast<const uint16_t*>(a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)));
+    a.s_w = s_w;
+    a.bias = bias;
+    a.qx_in = qx;
+    a.sx_in = sx;
+    a.y = y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    return run_gemv(fmt, a, false, 0u, s);
+}
+
+w4_status linear_common(int fmt, const void* w, const float* s_w, const float* bias, const float* x, int M, int N,
+                        int K, float* y, int8_t* qx, float* sx, unsigned flags, cudaStream_t s)
+{
+    w4_status st = check_mk(M, K);
+    if (st != W4_OK) return st;
+    if (N < 0 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_INVALID_ARG;
+    if (M == 0) return W4_OK;
+    if (!x || !qx || !sx) return W4_ERR_INVALID_ARG;
+    if (N > 0 && (!w || !y || (fmt == FMT_W4 && !s_w))) return W4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(qx, 16) || !aligned(sx, 4) || (w && !aligned(w, 16)) || (y && !aligned(y, 4)) ||
+        (s_w && !aligned(s_w, 4)) || (bias && !aligned(bias, 4)))
+        return W4_ERR_MISALIGNED;
+    if (N == 0 || !fused_fits(fmt, M, K)) {
+        // quantize into the caller's qx/sx, then the GEMV on int8 codes
+        st = cuda_status(launch_a8_quantize(x, M, K, qx, sx, s));
+        if (st != W4_OK || N == 0) return st;
+        return gemv_common(fmt, w, s_w, bias, qx, sx, M, N, K, y, s);
+    }
+    GemvArgs a = {};
+    a.w = static_cast<const uint8_t*>(w);
+    const size_t units = tiles(N) * kRows * (K / 32);
+    a.wscale = fmt == FMT_W4 ? nullptr
+                             : reinterpret_cast<const uint16_t*>(a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)));
+    a.s_w = s_w;
+    a.bias = bias;
+    a.x = x;
+    a.qx_out = qx;
+    a.sx_out = sx;
+    a.y = y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    return run_gemv(fmt, a, true, flags, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w4_status_str(w4_status st)
+{
+    switch (st) {
+        case W4_OK: return "W4_OK";
+        case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG";
+        case W4_ERR_UNSUPPORTED_SHAPE: return "W4_ERR_UNSUPPORTED_SHAPE";
+        case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED";
+        case W4_ERR_CUDA: return "W4_ERR_CUDA";
+        case W4_ERR_DEVICE_TIMEOUT: return "W4_ERR_DEVICE_TIMEOUT";
+    }
+    return "W4_ERR_UNKNOWN";
+}
+
+int w4_version(void) { return 1; }
+
+// ------------------------------------------------------------ quantizers
+w4_status w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, w4_stream_t s)
+{
+    if (N < 0 || K <= 0 || K % 8 != 0) return N < 0 || K <= 0 ? W4_ERR_INVALID_ARG : W4_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!W || !packed || !s_w) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(packed, 4) || !aligned(s_w, 4)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_w4_quantize_rows(W, N, K, packed, s_w, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, w4_stream_t s)
+{
+    if (N < 0 || K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!W || !blocks) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_q4_0_quantize(W, N, K, blocks, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, w4_stream_t s)
+{
+    if (N < 0 || K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!W || !q || !d) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(q, 16) || !aligned(d, 2)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_i8g32_quantize(W, N, K, q, d, reinterpret_cast<cudaStream_t>(s)));
+}
+
+// ---------------------------------------------------------------- repack
+size_t w4_repacked_bytes(int N, int K)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0) return 0;
+    return tiles(N) * kRows * static_cast<size_t>(K) / 2;
+}
+
+size_t q4_0_repacked_bytes(int N, int K)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0) return 0;
+    return tiles(N) * kRows * (static_cast<size_t>(K) / 2 + static_cast<size_t>(K) / 16);
+}
+
+size_t i8g32_repacked_bytes(int N, int K)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0) return 0;
+    return tiles(N) * kRows * (static_cast<size_t>(K) + static_cast<size_t>(K) / 16);
+}
+
+w4_status w4_repack(const uint32_t* const* shard_packed, const int* shard_rows, int n_shards, int K, void* out,
+                    size_t out_bytes, w4_stream_t s)
+{
+    if (K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0 || K > W4_MAX_K) return W4_ERR_UNSUPPORTED_SHAPE;
+    ShardTable st;
+    int N = 0;
+    w4_status r = build_shards(reinterpret_cast<const void* const*>(shard_packed), nullptr, shard_rows, n_shards, st, N);
+    if (r != W4_OK) return r;
+    if (N == 0) return W4_OK;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (out_bytes < w4_repacked_bytes(N, K)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16)) return W4_ERR_MISALIGNED;
+    for (int i = 0; i < n_shards; ++i)
+        if (st.p[i] && !aligned(st.p[i], 16)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_w4_repack(st, N, K, out, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status q4_0_repack(const uint8_t* const* shard_blocks, const int* shard_rows, int n_shards, int K, void* out,
+                      size_t out_bytes, w4_stream_t s)
+{
+    if (K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0 || K > W4_MAX_K) return W4_ERR_UNSUPPORTED_SHAPE;
+    ShardTable st;
+    int N = 0;
+    w4_status r = build_shards(reinterpret_cast<const void* const*>(shard_blocks), nullptr, shard_rows, n_shards, st, N);
+    if (r != W4_OK) return r;
+    if (N == 0) return W4_OK;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (out_bytes < q4_0_repacked_bytes(N, K)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_q4_0_repack(st, N, K, out, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status i8g32_repack(const int8_t* const* shard_q, const uint16_t* const* shard_d, const int* shard_rows,
+                       int n_shards, int K, void* out, size_t out_bytes, w4_stream_t s)
+{
+    if (K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0 || K > W4_MAX_K) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (shard_d == nullptr) return W4_ERR_INVALID_ARG;
+    ShardTable st;
+    int N = 0;
+    w4_status r = build_shards(reinterpret_cast<const void* const*>(shard_q), reinterpret_cast<const void* const*>(shard_d),
+                               shard_rows, n_shards, st, N);
+    if (r != W4_OK) return r;
+    if (N == 0) return W4_OK;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (out_bytes < i8g32_repacked_bytes(N, K)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16)) return W4_ERR_MISALIGNED;
+    for (int i = 0; i < n_shards; ++i) {
+        if (st.p[i] && !aligned(st.p[i], 16)) return W4_ERR_MISALIGNED;
+        if (st.p2[i] && !aligned(st.p2[i], 2)) return W4_ERR_MISALIGNED;
+    }
+    return cuda_status(launch_i8g32_repack(st, N, K, out, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status w4_concat_f32(const float* const* parts, const int* lens, int n_parts, float* out, w4_stream_t s)
+{
+    if (n_parts < 0 || (n_parts > 0 && (!parts || !lens))) return W4_ERR_INVALID_ARG;
+    size_t off = 0;
+    for (int i = 0; i < n_parts; ++i) {
+        if (lens[i] < 0 || (lens[i] > 0 && (!parts[i] || !out))) return W4_ERR_INVALID_ARG;
+        if (lens[i] == 0) continue;
+        cudaError_t e = cudaMemcpyAsync(out + off, parts[i], static_cast<size_t>(lens[i]) * sizeof(float),
+                                        cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(s));
+        if (e != cudaSuccess) return W4_ERR_CUDA;
+        off += static_cast<size_t>(lens[i]);
+    }
+    return W4_OK;
+}
+
+// ------------------------------------------------------------- per token
+w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_stream_t s)
+{
+    w4_status st = check_mk(M, K);
+    if (st != W4_OK) return st;
+    if (M == 0) return W4_OK;
+    if (!x || !qx || !sx) return W4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(qx, 16) || !aligned(sx, 4)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_a8_quantize(x, M, K, qx, sx, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status w4a8_gemv(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx, int M,
+                    int N, int K, float* y, w4_stream_t s)
+{
+    return gemv_common(FMT_W4, w, s_w, bias, qx, sx, M, N, K, y, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status q4_0_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx, int M, int N, int K,
+                    float* y, w4_stream_t s)
+{
+    return gemv_common(FMT_Q4_0, w, nullptr, bias, qx, sx, M, N, K, y, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status i8g32_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx, int M, int N, int K,
+                     float* y, w4_stream_t s)
+{
+    return gemv_common(FMT_I8G32, w, nullptr, bias, qx, sx, M, N, K, y, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status w4a8_linear(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,
+                      float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_W4, w, s_w, bias, x, M, N, K, y, qx, sx, flags, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status q4_0_linear(const void* w, const float* bias, const float* x, int M, int N, int K, float* y, int8_t* qx,
+                      float* sx, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_Q4_0, w, nullptr, bias, x, M, N, K, y, qx, sx, flags, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status i8g32_linear(const void* w, const float* bias, const float* x, int M, int N, int K, float* y, int8_t* qx,
+                       float* sx, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_I8G32, w, nullptr, bias, x, M, N, K, y, qx, sx, flags,
+                         reinterpret_cast<cudaStream_t>(s));
+}
+
+// ------------------------------------------------------ device error word
+w4_status w4_device_error(unsigned* code)
+{
+    if (!code) return W4_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, dev->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return W4_ERR_CUDA;
+    *code = v;
+    return v ? W4_ERR_DEVICE_TIMEOUT : W4_OK;
+}
+
+w4_status w4_clear_device_error(void)
+{
+    DeviceInfo* dev = nullptr;
+    w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    if (cudaMemset(dev->err, 0, sizeof(unsigned)) != cudaSuccess) return W4_ERR_CUDA;
+    return cuda_status(cudaDeviceSynchronize());
+}
+
+}  // extern "C"

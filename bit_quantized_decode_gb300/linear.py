@@ -1,0 +1,124 @@
+"""Load-time preparation of one decode linear and its per-token call.
+
+`QuantLinear.from_float` quantizes float weight shards on the GPU with the
+library's kernels, fuses the shards (q/k/v, gate/up) into one repacked
+matrix, and keeps it resident; `QuantLinear.__call__` runs the fused
+quantize + GEMV launch.  Buffers are torch tensors (device memory only).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+FORMATS = ("w4", "q4_0", "i8g32")
+
+
+class QuantLinear:
+    def __init__(self, fmt: str, N: int, K: int, w: torch.Tensor, s_w=None, bias=None, canonical=None):
+        if fmt not in FORMATS:
+            raise ValueError(fmt)
+        self.fmt, self.N, self.K = fmt, N, K
+        self.w = w                  # repacked device layout, uint8
+        self.s_w = s_w              # float32 [N] (w4 only)
+        self.bias = bias            # float32 [N] or None
+        self.canonical = canonical  # per-shard canonical tensors, if kept
+
+    # ------------------------------------------------------------- building
+    @classmethod
+    def from_float(cls, fmt: str, shards, biases=None, keep_canonical: bool = False) -> "QuantLinear":
+        """shards: float32 CUDA tensors [rows_s][K] concatenated by rows; biases: matching [rows_s] or None."""
+        shards = [s.contiguous() for s in shards]
+        K = shards[0].shape[1]
+        dev = shards[0].device
+        N = sum(s.shape[0] for s in shards)
+        canon, scales = [], []
+        for W in shards:
+            n = W.shape[0]
+            if fmt == "w4":
+                p = torch.empty((n, K // 8), dtype=torch.int32, device=dev)
+                sw = torch.empty(n, dtype=torch.float32, device=dev)
+                _lib.w4_quantize_rows(W, p, sw)
+                canon.append(p)
+                scales.append(sw)
+            elif fmt == "q4_0":
+                b = torch.empty((n, K // 32, 18), dtype=torch.uint8, device=dev)
+                _lib.q4_0_quantize(W, b)
+                canon.append(b)
+            else:
+                q = torch.empty((n, K), dtype=torch.int8, device=dev)
+                d = torch.empty((n, K // 32), dtype=torch.int16, device=dev)
+                _lib.i8g32_quantize(W, q, d)
+                canon.append((q, d))
+        w, s_w = cls._repack(fmt, canon, scales, N, K, dev)
+        bias = None
+        if biases is not None:
+            bias = torch.empty(N, dtype=torch.float32, device=dev)
+            _lib.w4_concat_f32([b.contiguous() for b in biases], bias)
+        return cls(fmt, N, K, w, s_w, bias, canon if keep_canonical else None)
+
+    @classmethod
+    def from_canonical(cls, fmt: str, canon, K: int, scales=None, biases=None) -> "QuantLinear":
+        """Repack already-quantized canonical shards (device tensors)."""
+        dev = (canon[0][0] if fmt == "i8g32" else canon[0]).device
+        N = sum((c[0] if fmt == "i8g32" else c).shape[0] for c in canon)
+        w, s_w = cls._repack(fmt, canon, scales or [], N, K, dev)
+        bias = None
+        if biases is not None:
+            bias = torch.empty(N, dtype=torch.float32, device=dev)
+            _lib.w4_concat_f32([b.contiguous() for b in biases], bias)
+        return cls(fmt, N, K, w, s_w, bias, canon)
+
+    @staticmethod
+    def _repack(fmt, canon, scales, N, K, dev):
+        s_w = None
+        if fmt == "w4":
+            w = torch.empty(_lib.w4_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
+            _lib.w4_repack(canon, K, w)
+            s_w = torch.empty(N, dtype=torch.float32, device=dev)
+            _lib.w4_concat_f32(scales, s_w)
+        elif fmt == "q4_0":
+            w = torch.empty(_lib.q4_0_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
+            _lib.q4_0_repack(canon, K, w)
+        else:
+            w = torch.empty(_lib.i8g32_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
+            _lib.i8g32_repack([c[0] for c in canon], [c[1] for c in canon], K, w)
+        return w, s_w
+
+    # ------------------------------------------------------------ per token
+    def buffers(self, M: int):
+        dev = self.w.device
+        return (torch.empty((M, self.N), dtype=torch.float32, device=dev),
+                torch.empty((M, self.K), dtype=torch.int8, device=dev),
+                torch.empty(M, dtype=torch.float32, device=dev))
+
+    def __call__(self, x, y=None, qx=None, sx=None, flags: int = 0, stream=None):
+        """Quantize x [M][K] and compute y [M][N] (one fused launch when it fits)."""
+        M = x.shape[0]
+        if y is None or qx is None or sx is None:
+            y2, q2, s2 = self.buffers(M)
+            y = y if y is not None else y2
+            qx = qx if qx is not None else q2
+            sx = sx if sx is not None else s2
+        if self.fmt == "w4":
+            _lib.w4a8_linear(self.w, self.s_w, self.bias, x, y, qx, sx, flags, stream)
+        elif self.fmt == "q4_0":
+            _lib.q4_0_linear(self.w, self.bias, x, y, qx, sx, flags, stream)
+        else:
+            _lib.i8g32_linear(self.w, self.bias, x, y, qx, sx, flags, stream)
+        return y
+
+    def gemv(self, qx, sx, y, stream=None):
+        """GEMV on already-quantized activations."""
+        if self.fmt == "w4":
+            _lib.w4a8_gemv(self.w, self.s_w, self.bias, qx, sx, y, stream)
+        elif self.fmt == "q4_0":
+            _lib.q4_0_gemv(self.w, self.bias, qx, sx, y, stream)
+        else:
+            _lib.i8g32_gemv(self.w, self.bias, qx, sx, y, stream)
+        return y
+
+    @property
+    def weight_bytes(self) -> int:
+        """Bytes the GEMV streams: repacked weights (+ group scales) and per-row scales."""
+        return self.w.numel() + (self.s_w.numel() * 4 if self.s_w is not None else 0)

@@ -1,0 +1,191 @@
+/*
+ * w4a8.h -- C ABI of the GB300 (sm_103a) bit-quantized decode GEMV library.
+ *
+ * The library computes the batch-1 (and few-token) decode linear layer
+ *     y[m][j] = W[j][:] . x[m][:] + b[j]
+ * with 4-bit (or 8-bit) weights and per-token INT8 activations, as defined on
+ *   [Orin-INT4]   "Jetson Orin AGX INT4 推理优化实践：super 分支从 9 tok/s 到 24 tok/s"
+ *   [310B-Gemma4] "在香橙派上跑 Gemma4：vLLM 适配昇腾 310B 的内核开发实录"
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless a parameter says "host".  The caller
+ *     allocates and frees every buffer; the library allocates nothing and keeps
+ *     no state beyond cached device attributes and one device error word.
+ *   - Work is enqueued on the caller's stream `s` and nothing synchronises.
+ *   - Arguments are checked on the host before any launch; a failed check
+ *     returns an error and launches nothing.  A launch failure returns
+ *     W4_ERR_CUDA.  Kernels never trap: a bounded wait that runs out sets the
+ *     device error word (see w4_device_error) and the kernel returns.
+ *   - M = 0 or N = 0 is a valid empty call (returns W4_OK, launches nothing).
+ *   - Shapes: 1 <= M <= 16 tokens, K > 0, K % 32 == 0.
+ *   - Alignment: weight buffers, qx and x must be 16-byte aligned; float
+ *     arrays 4-byte aligned.  A violation returns W4_ERR_MISALIGNED.
+ *
+ * Formats ("canonical" = the format a caller stores, before repacking):
+ *   W4    per-row symmetric INT4 [Orin-INT4] §"从 FP 线性层到 INT4 DP4A 的数学推导":
+ *         uint32 [N][K/8], weight k of a word in bits 4k..4k+3 (two's complement,
+ *         §"DP4A 做了什么"), plus float s_w[N].
+ *   Q4_0  [310B-Gemma4] §3.1: 18-byte blocks [N][K/32]: fp16 d (little endian),
+ *         then 16 nibble bytes; byte i holds element i (low) and i+16 (high);
+ *         element value n - 8, weight d*(n - 8).
+ *   I8G32 [310B-Gemma4] §3.2 (lm_head widened to int8 with per-group fp16
+ *         scales): int8 q [N][K] plus fp16 d [N][K/32]; weight d*q.
+ *
+ * Device ("repacked") layouts, produced by the *_repack calls and consumed by
+ * the GEMVs.  Rows are grouped in tiles of 8 (T = ceil(N/8) tiles; rows past N
+ * are zero).  C = K/32 chunks of 32 weights per row.  Unit (t, c, r) is the
+ * 32 weights of row 8t+r in chunk c; units are stored in (t, c, r) order:
+ *   W4, Q4_0: 16 bytes per unit at ((t*C + c)*8 + r)*16.  Word w (0..3) of the
+ *         unit holds weights 32c+8w+b in the low nibble of byte b and
+ *         32c+8w+4+b in the high nibble, as 4-bit two's complement (Q4_0 values
+ *         n - 8).  Q4_0 then has a plane of fp16 d, one per unit, at byte
+ *         T*8*C*16 + ((t*C + c)*8 + r)*2.
+ *   I8G32: 32 bytes per unit (the 32 int8 in order) at ((t*C + c)*8 + r)*32,
+ *         then the fp16 d plane at byte T*8*C*32 + ((t*C + c)*8 + r)*2.
+ */
+#ifndef W4A8_H
+#define W4A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* w4_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    W4_OK = 0,
+    W4_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad shard table */
+    W4_ERR_UNSUPPORTED_SHAPE = 2, /* M > 16, K % 32 != 0, K too large, buffer too small */
+    W4_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rule above */
+    W4_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+    W4_ERR_DEVICE_TIMEOUT = 5     /* a kernel's bounded wait ran out (see w4_device_error) */
+} w4_status;
+
+/* Human-readable name of a status.  Never NULL. */
+const char* w4_status_str(w4_status st);
+
+/* Library ABI version (increases on incompatible change). */
+int w4_version(void);
+
+/* Largest K each GEMV accepts.  W4 and Q4_0 accumulate 16x-scaled int32
+ * partial sums, so K * 16 * 8 * 127 must stay below 2^31: K <= 131072. */
+#define W4_MAX_K 131072
+#define W4_MAX_M 16
+#define W4_MAX_SHARDS 8
+
+/* Flags for the *_linear calls. */
+#define W4_FLAG_PDL 1u /* launch as a programmatic dependent of the previous kernel in
+                          the stream.  Legal only when the previous kernel does not
+                          write this call's weight buffer (weights are prefetched
+                          before the dependency wait); inputs x/qx/sx and outputs are
+                          touched only after it. */
+
+/* ------------------------------------------------------------------------
+ * Load time: quantize float weights (device kernels).
+ * ------------------------------------------------------------------------ */
+
+/* Per-row symmetric INT4, [Orin-INT4] §"从 FP 线性层到 INT4 DP4A 的数学推导":
+ * s_w[j] = max_i |W[j][i]| / 7 (the page leaves s^W open; this maps the row's
+ * absmax to the top code, as s^x does for x), q = clip(rint(W / s_w), -8, 7),
+ * packed into canonical W4 words.  W: float [N][K] (16-B aligned, row-major);
+ * packed: uint32 [N][K/8]; s_w: float [N].  K % 8 == 0. */
+w4_status w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, w4_stream_t s);
+
+/* Q4_0 blocks, [310B-Gemma4] §3.1: d = fp16(max|w| / 8) per 32-block,
+ * n = clip(rint(w / d), -8, 7) + 8.  W: float [N][K]; blocks: [N][K/32][18]. */
+w4_status q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, w4_stream_t s);
+
+/* int8 + fp16 group-32 scales, [310B-Gemma4] §3.2: d = fp16(max|w| / 32),
+ * q = clip(rint(w / d), -32, 31).  q: int8 [N][K]; d: fp16 bits [N][K/32]. */
+w4_status i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Load time: repack canonical weights into the device layout, fusing shards.
+ * [310B-Gemma4] §3.1 (load-time reorder; q/k/v and gate/up concatenated by
+ * rows into one matrix, one repack, one matmul per token).
+ *
+ * shard_* are HOST arrays of n_shards (1..W4_MAX_SHARDS) device pointers;
+ * shard_rows is a HOST array of row counts.  The fused matrix has
+ * N = sum(shard_rows) rows, shard 0 first.  `out` must hold *_repacked_bytes
+ * (N, K) bytes (out_bytes is checked) and must not overlap the shards.
+ * ------------------------------------------------------------------------ */
+size_t w4_repacked_bytes(int N, int K);
+w4_status w4_repack(const uint32_t* const* shard_packed, const int* shard_rows, int n_shards, int K,
+                    void* out, size_t out_bytes, w4_stream_t s);
+
+size_t q4_0_repacked_bytes(int N, int K);
+w4_status q4_0_repack(const uint8_t* const* shard_blocks, const int* shard_rows, int n_shards, int K,
+                      void* out, size_t out_bytes, w4_stream_t s);
+
+size_t i8g32_repacked_bytes(int N, int K);
+w4_status i8g32_repack(const int8_t* const* shard_q, const uint16_t* const* shard_d, const int* shard_rows,
+                       int n_shards, int K, void* out, size_t out_bytes, w4_stream_t s);
+
+/* Concatenate per-shard float vectors (per-row scales s_w, bias) into `out`
+ * in shard order.  parts: HOST array of device pointers; lens: HOST array. */
+w4_status w4_concat_f32(const float* const* parts, const int* lens, int n_parts, float* out, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Per token: activation quantization.
+ * [Orin-INT4] §"从 FP 线性层到 INT4 DP4A 的数学推导":
+ *   sx[m] = max_i |x[m][i]| / 127 (IEEE fp32 division),
+ *   qx[m][i] = clip(rint(x[m][i] / sx[m]), -127, 127); an all-zero token gives
+ *   sx = 0, qx = 0.  NaN/Inf inputs are undefined behaviour.
+ * x: float [M][K]; qx: int8 [M][K]; sx: float [M].
+ * ------------------------------------------------------------------------ */
+w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Per token: GEMV on INT8 activations.
+ *
+ * w4a8_gemv, [Orin-INT4] §"从 FP 线性层到 INT4 DP4A 的数学推导" and §"DP4A 做了什么":
+ *   acc[m][j] = sum_i q_w[j][i] * qx[m][i]   (exact int32, DP4A),
+ *   y[m][j]   = fmaf(s_w[j] * sx[m], (float)acc, b[j])   (b = 0 if bias NULL).
+ * q4_0_gemv / i8g32_gemv, [310B-Gemma4] §3.1 / §3.2:
+ *   acc_g = exact int32 sum over 32-block g,
+ *   y[m][j] = fmaf(sx[m], sum_g d_g * acc_g, b[j])  (fp32; group order unspecified).
+ * w: repacked weights; s_w: float [N]; bias: float [N] or NULL; qx: int8 [M][K];
+ * sx: float [M]; y: float [M][N] (row m at y + m*N).
+ * ------------------------------------------------------------------------ */
+w4_status w4a8_gemv(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx,
+                    int M, int N, int K, float* y, w4_stream_t s);
+w4_status q4_0_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx,
+                    int M, int N, int K, float* y, w4_stream_t s);
+w4_status i8g32_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx,
+                     int M, int N, int K, float* y, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Per token: the whole decode linear, quantization fused into the GEMV
+ * ([Orin-INT4] §"后续还能继续优化什么" item 2 names fusing the activation
+ * quantization with a neighbouring operator).  Each thread block quantizes x
+ * into its shared memory; block 0 also writes qx and sx (caller buffers, same
+ * shapes as a8_quantize) so that the caller sees the codes used.  When M*K
+ * does not fit in shared memory the call runs a8_quantize into qx/sx and then
+ * the *_gemv kernel; results are identical either way.
+ * flags: 0 or W4_FLAG_PDL.
+ * ------------------------------------------------------------------------ */
+w4_status w4a8_linear(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,
+                      float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
+w4_status q4_0_linear(const void* w, const float* bias, const float* x, int M, int N, int K,
+                      float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
+w4_status i8g32_linear(const void* w, const float* bias, const float* x, int M, int N, int K,
+                       float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Device error word.  Kernels that give up a bounded wait (about 0.25 s on an
+ * mbarrier) record a nonzero code here and return early; their outputs are
+ * then undefined.  w4_device_error synchronises the current device, reads the
+ * word into *code (host pointer) and returns W4_ERR_DEVICE_TIMEOUT if it is
+ * nonzero, else W4_OK.  w4_clear_device_error zeroes it (synchronous).
+ * ------------------------------------------------------------------------ */
+w4_status w4_device_error(unsigned* code);
+w4_status w4_clear_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A8_H */

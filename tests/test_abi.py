@@ -1,0 +1,131 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every entry point include/w4a8.h declares, and rejects bad arguments on the
+host before touching the GPU.  The product never imports the oracle."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a8.h")
+PKG = os.path.join(ROOT, "bit_quantized_decode_gb300")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_quantized_decode_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("w4_repack", "a8_quantize", "w4a8_gemv", "q4_0_gemv", "i8g32_gemv", "w4a8_linear",
+                     "q4_0_repack", "i8g32_repack", "w4_quantize_rows", "q4_0_quantize", "i8g32_quantize"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_cover_the_header():
+    from bit_quantized_decode_gb300 import _lib
+    assert set(declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_library_is_built_for_sm_103a():
+    """The build command targets compute_103a/sm_103a only."""
+    from bit_quantized_decode_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert "-prec-div=true" in build.NVCC_FLAGS and "-ftz=false" in build.NVCC_FLAGS
+
+
+def test_status_strings(lib):
+    from bit_quantized_decode_gb300 import _lib
+    for code, name in _lib.STATUS.items():
+        assert _lib.status_str(code) == name
+    assert _lib.version() == 1
+
+
+def test_repacked_sizes(lib):
+    from bit_quantized_decode_gb300 import _lib
+    # 8-row tiles, 0.5 B per weight; Q4_0 adds 2 B per 32; i8g32 1 B + 2 B per 32
+    assert _lib.w4_repacked_bytes(4608, 3584) == 4608 * 3584 // 2
+    assert _lib.w4_repacked_bytes(13, 64) == 16 * 64 // 2
+    assert _lib.q4_0_repacked_bytes(2560, 1536) == 2560 * 1536 * 18 // 32
+    assert _lib.i8g32_repacked_bytes(262144, 1536) == 262144 * 1536 * 34 // 32
+    assert _lib.w4_repacked_bytes(8, 48) == 0          # K % 32 != 0
+    assert _lib.w4_repacked_bytes(-1, 64) == 0
+
+
+FAKE = ctypes.c_void_p(0x1000)       # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x1004)        # 4-byte but not 16-byte aligned
+
+
+def test_gemv_argument_checks_return_before_launch(lib):
+    # M > 16
+    assert lib.w4a8_gemv(FAKE, FAKE, None, FAKE, FAKE, 17, 8, 64, FAKE, None) == 2
+    # K not a multiple of 32, K <= 0, K too large
+    assert lib.w4a8_gemv(FAKE, FAKE, None, FAKE, FAKE, 1, 8, 48, FAKE, None) == 2
+    assert lib.w4a8_gemv(FAKE, FAKE, None, FAKE, FAKE, 1, 8, 0, FAKE, None) == 1
+    assert lib.w4a8_gemv(FAKE, FAKE, None, FAKE, FAKE, 1, 8, 131072 + 32, FAKE, None) == 2
+    # negative sizes, null pointers
+    assert lib.w4a8_gemv(FAKE, FAKE, None, FAKE, FAKE, -1, 8, 64, FAKE, None) == 1
+    assert lib.w4a8_gemv(FAKE, FAKE, None, FAKE, FAKE, 1, -8, 64, FAKE, None) == 1
+    assert lib.w4a8_gemv(None, FAKE, None, FAKE, FAKE, 1, 8, 64, FAKE, None) == 1
+    assert lib.w4a8_gemv(FAKE, None, None, FAKE, FAKE, 1, 8, 64, FAKE, None) == 1
+    assert lib.q4_0_gemv(FAKE, None, None, FAKE, 1, 8, 64, FAKE, None) == 1
+    # misaligned weights / activations
+    assert lib.w4a8_gemv(ODD, FAKE, None, FAKE, FAKE, 1, 8, 64, FAKE, None) == 3
+    assert lib.i8g32_gemv(FAKE, None, ODD, FAKE, 1, 8, 64, FAKE, None) == 3
+    # empty calls succeed without a launch
+    assert lib.w4a8_gemv(None, None, None, None, None, 0, 8, 64, None, None) == 0
+    assert lib.q4_0_gemv(None, None, None, None, 1, 0, 64, None, None) == 0
+
+
+def test_linear_and_quantize_argument_checks(lib):
+    assert lib.w4a8_linear(FAKE, FAKE, None, FAKE, 1, 8, 64, FAKE, FAKE, FAKE, 4, None) == 1   # unknown flag
+    assert lib.w4a8_linear(FAKE, FAKE, None, None, 1, 8, 64, FAKE, FAKE, FAKE, 0, None) == 1   # no x
+    assert lib.q4_0_linear(FAKE, None, ODD, 1, 8, 64, FAKE, FAKE, FAKE, 0, None) == 3
+    assert lib.w4a8_linear(None, None, None, None, 0, 8, 64, None, None, None, 0, None) == 0
+    assert lib.a8_quantize(FAKE, 1, 33, FAKE, FAKE, None) == 2
+    assert lib.a8_quantize(None, 1, 64, FAKE, FAKE, None) == 1
+    assert lib.a8_quantize(FAKE, 0, 64, FAKE, FAKE, None) == 0
+    assert lib.w4_quantize_rows(FAKE, 4, 12, FAKE, FAKE, None) == 2
+    assert lib.q4_0_quantize(FAKE, 4, 48, FAKE, None) == 2
+    assert lib.i8g32_quantize(ODD, 4, 64, FAKE, FAKE, None) == 3
+
+
+def test_repack_argument_checks(lib):
+    from bit_quantized_decode_gb300 import _lib
+    pp, keep = _lib._ptr_array([None])
+    rows, keep2 = _lib._int_array([8])
+    assert lib.w4_repack(pp, rows, 1, 64, FAKE, 1 << 20, None) == 1          # null shard
+    pp2 = (ctypes.c_void_p * 1)(0x1000)
+    ppc = ctypes.cast(pp2, _lib._PP)
+    assert lib.w4_repack(ppc, rows, 1, 64, FAKE, 16, None) == 2              # output too small
+    assert lib.w4_repack(ppc, rows, 0, 64, FAKE, 1 << 20, None) == 1         # no shards
+    assert lib.w4_repack(ppc, rows, 9, 64, FAKE, 1 << 20, None) == 1         # too many shards
+    assert lib.w4_repack(ppc, rows, 1, 64, ODD, 1 << 20, None) == 3
+    neg, keep3 = _lib._int_array([-1])
+    assert lib.w4_repack(ppc, neg, 1, 64, FAKE, 1 << 20, None) == 1
+    assert lib.i8g32_repack(ppc, None, rows, 1, 64, FAKE, 1 << 20, None) == 1
+
+
+def test_product_never_imports_the_oracle():
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle\b|from\s+\.\.?\s*import\s+oracle)|liboracle|oracle/",
+                     re.M)
+    for dirpath, _, files in os.walk(PKG):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                assert not pat.search(open(os.path.join(dirpath, f)).read()), f

@@ -51,6 +51,12 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--per-linear", action="store_true", help="also time each linear kind on its own")
     p.add_argument("--ref-budget-s", type=float, default=120.0, help="reference arm: total CPU seconds")
+    p.add_argument("--tune", action="append", default=[], metavar="KEY=VALUE",
+                   help="launch tuning passed to w4_set_tuning: blocks_per_sm, max_stages, grid_blocks")
+    p.add_argument("--profile", action="store_true",
+                   help="profiler mode: eager step, graph warm-up and timed replays only (no e2e, no CPU "
+                        "baseline, no clock sampling); the launch order is fixed: one eager step, then "
+                        "warmup + steps graph replays")
     return p.parse_args(argv)
 
 
@@ -286,6 +292,11 @@ def run_ours(args, rank, world, local_rank):
 
     _lib.load()
     _lib.clear_device_error()
+    tuning = {}
+    for kv in args.tune:
+        k, v = kv.split("=")
+        _lib.set_tuning(k, int(v))
+        tuning[k] = int(v)
     items, x_all, y_all = build_step(args, dev)
     M = args.M
     bytes_per_step = sum(algorithmic_bytes(lin, M) for _, lin, *_ in items)
@@ -324,8 +335,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
+    if not args.profile:
+        sampler.start()
+        time.sleep(0.3)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -338,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
-    if elapsed_ms < 400:
+    if elapsed_ms < 400 and not args.profile:
         time.sleep(0.2)
     clocks = sampler.stop()
     err = _lib.device_error()
@@ -352,6 +364,13 @@ def run_ours(args, rank, world, local_rank):
         t_max = float(t.item())
     ms_per_step = t_max / args.steps
     value = world * bytes_per_step * args.steps / (t_max / 1e3) / 1e9
+
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile": True, "tuning": tuning or "auto", "ms_per_step": elapsed_ms / args.steps,
+                              "GB/s": bytes_per_step * args.steps / (elapsed_ms / 1e3) / 1e9,
+                              "launches_per_step": launches}), flush=True)
+        return 0
 
     # ---- end to end: pinned host inputs in, results out, every step
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
@@ -444,6 +463,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "bytes_per_step": bytes_per_step,
+        "tuning": tuning or "auto",
     }
     if per_linear is not None:
         line["per_linear"] = per_linear

@@ -27,6 +27,7 @@ STATUS = {
     5: "W4_ERR_DEVICE_TIMEOUT",
 }
 W4_FLAG_PDL = 1
+TUNE_KEYS = {"blocks_per_sm": 0, "max_stages": 1, "grid_blocks": 2}
 W4_MAX_M = 16
 W4_MAX_K = 131072
 W4_MAX_SHARDS = 8
@@ -41,6 +42,8 @@ _PI = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "w4_status_str": ([_I], ctypes.c_char_p),
     "w4_version": ([], _I),
+    "w4_set_tuning": ([_I, _I], _I),
+    "w4_get_tuning": ([_I], _I),
     "w4_quantize_rows": ([_P, _I, _I, _P, _P, _P], _I),
     "q4_0_quantize": ([_P, _I, _I, _P, _P], _I),
     "i8g32_quantize": ([_P, _I, _I, _P, _P, _P], _I),
@@ -128,6 +131,15 @@ def status_str(st: int) -> str:
 
 def version() -> int:
     return load().w4_version()
+
+
+def set_tuning(key: str, value: int):
+    """Launch tuning (see include/w4a8.h): blocks_per_sm, max_stages, grid_blocks; 0 = automatic."""
+    _check("w4_set_tuning", load().w4_set_tuning(TUNE_KEYS[key], int(value)))
+
+
+def get_tuning(key: str) -> int:
+    return int(load().w4_get_tuning(TUNE_KEYS[key]))
 
 
 def w4_repacked_bytes(N: int, K: int) -> int:

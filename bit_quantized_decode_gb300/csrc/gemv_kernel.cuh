@@ -8,29 +8,36 @@
 //          y = fmaf(sx[m], sum_g d_g * acc_g, b[j])
 //
 // How (GB300 design, not the pages'):
-//   * One persistent thread block per SM, 8 warps.  Each block owns a
-//     contiguous, balanced range of 8-row tiles; the range is processed in
-//     rounds and each round's lines (8 rows x 32 weights) are split evenly
-//     among the warps, so every warp streams the same number of bytes.
-//   * Every warp runs its own ring of shared-memory slots fed by 1-D bulk
-//     (TMA) copies: lane 0 issues `cp.async.bulk` of whole slices of its
-//     range with an evict-first L2 policy, the warp waits on the slot's
-//     mbarrier (bounded wait), computes, and refills the slot.  The first
-//     slices are issued before the dependency wait and the activation
-//     prologue, so weight streaming overlaps both.
-//   * Activations: either quantized in the prologue from fp32 x into shared
-//     memory (each block repeats the absmax and the codes; block 0 also
-//     writes them out), or read as int8 codes from global memory through L1.
-//   * Inner loop: lane (l & 7) is a row, (l >> 3) a line; a 16-byte unit is
-//     32 4-bit weights laid out so that (w << 4) & 0xF0F0F0F0 and
-//     w & 0xF0F0F0F0 are four signed bytes each, 16 x the weights, fed
-//     straight to DP4A against the matching int8 activations (the sum is a
-//     multiple of 16 and is shifted back exactly at the end).  This is the
-//     page's "unpack to two int8x4, two DP4A per 8 weights" (§"DP4A 做了什么")
-//     with the sign extension folded into the byte position.
-//   * Lanes sharing a row are reduced with shuffles; tiles split between
-//     warps are merged in shared memory in warp order (deterministic), then
-//     the epilogue writes y coalesced.
+//   * One thread block of 8 warps per SM, sized (shared memory <= ~113 KB,
+//     <= 128 registers) so that the next GEMV in the stream can be resident
+//     beside it: with programmatic dependent launch the next kernel starts,
+//     prefetches its weights and waits at griddepcontrol.wait while this one
+//     finishes.
+//   * Each block owns a contiguous, balanced range of 8-row tiles, processed
+//     in rounds; each round's lines (8 rows x 32 weights) are split evenly
+//     among the warps.  Every warp runs its own ring of shared-memory slots
+//     fed by 1-D bulk (TMA) copies (lane 0 issues, evict-first L2 policy,
+//     bounded mbarrier waits).  The first slices are issued before the
+//     dependency wait and the activation prologue.
+//   * Per-row INT4 weights are stored biased (nibble n = q + 8): with
+//     w & 0x0F0F0F0F and w & 0xF0F0F0F0 a 32-bit word yields four unsigned
+//     bytes n and four bytes 16n, fed to DP4A (u8 x s8) against the matching
+//     int8 activations -- two LOP3 and two DP4A per eight weights.  The bias
+//     is removed exactly once per row in the epilogue with the activation
+//     code sum: sum n x = sum q x + 8 sum x.  Q4_0 nibbles, whose scale
+//     changes every 32 weights, are stored as 4-bit two's complement instead:
+//     (w << 4) & 0xF0F0F0F0 and w & 0xF0F0F0F0 are four signed bytes 16q each,
+//     and the group sum is shifted back exactly.  Both are the page's "two
+//     int8x4, two DP4A per 8 weights" (§"DP4A 做了什么") with the sign
+//     extension folded into an offset or a byte position.
+//   * Lane l works on line (l >> 1) of a 16-line pass and on rows 4(l & 1) ..
+//     4(l & 1) + 3, so one activation chunk feeds four rows (the page's
+//     r-rows-per-block reuse, §"o2-all 和 o4-all 为什么能加速", done per lane).
+//     Lanes read their four units in an XOR-permuted order so shared-memory
+//     reads are conflict-free; the permutation is undone by a shuffle
+//     butterfly at the end of each tile.
+//   * Tiles split between warps are merged in shared memory in warp order
+//     (deterministic); the epilogue writes y coalesced.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -38,43 +45,161 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_a8.cuh"
 
 namespace w4k {
 
 constexpr uint64_t kWaitTimeoutNs = 250ull * 1000ull * 1000ull;
 
-template <int FMT, int MT>
-struct UnitMath {
-    using Acc = typename std::conditional<FMT == FMT_W4, int, float>::type;
-};
-
-// Quantize one activation: clip(rint(v / s), -127, 127); s == 0 gives 0.
-__device__ __forceinline__ uint32_t quant_a8(float v, float s)
+// DP4A with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
 {
-    if (s == 0.0f) return 0u;
-    int q = __float2int_rn(__fdiv_rn(v, s));
-    q = q > 127 ? 127 : (q < -127 ? -127 : q);
-    return static_cast<uint32_t>(q) & 0xffu;
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
-template <int FMT, int MT, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
+// Sum of the four signed bytes of a word.
+__device__ __forceinline__ int bytesum(uint32_t w) { return __dp4a(static_cast<int>(w), 0x01010101, 0); }
+
+// 4-bit units: B = sum n x over the low nibbles, A = sum 16 n x over the high
+// nibbles of one 16-byte unit (32 weights) against its 32 activations.
+__device__ __forceinline__ void unit4(const uint4 w, const uint4 x0, const uint4 x1, int& B, int& A)
 {
-    using Acc = typename UnitMath<FMT, MT>::Acc;
+    B = dp4a_us(w.x & 0x0F0F0F0Fu, x0.x, 0);
+    A = dp4a_us(w.x & 0xF0F0F0F0u, x0.y, 0);
+    B = dp4a_us(w.y & 0x0F0F0F0Fu, x0.z, B);
+    A = dp4a_us(w.y & 0xF0F0F0F0u, x0.w, A);
+    B = dp4a_us(w.z & 0x0F0F0F0Fu, x1.x, B);
+    A = dp4a_us(w.z & 0xF0F0F0F0u, x1.y, A);
+    B = dp4a_us(w.w & 0x0F0F0F0Fu, x1.z, B);
+    A = dp4a_us(w.w & 0xF0F0F0F0u, x1.w, A);
+}
+
+// Signed 4-bit units (Q4_0): 16 * sum q x over one 16-byte unit.
+__device__ __forceinline__ int unit4_signed16(const uint4 w, const uint4 x0, const uint4 x1)
+{
+    int g = dp4a_ss((w.x << 4) & 0xF0F0F0F0u, x0.x, 0);
+    g = dp4a_ss(w.x & 0xF0F0F0F0u, x0.y, g);
+    g = dp4a_ss((w.y << 4) & 0xF0F0F0F0u, x0.z, g);
+    g = dp4a_ss(w.y & 0xF0F0F0F0u, x0.w, g);
+    g = dp4a_ss((w.z << 4) & 0xF0F0F0F0u, x1.x, g);
+    g = dp4a_ss(w.z & 0xF0F0F0F0u, x1.y, g);
+    g = dp4a_ss((w.w << 4) & 0xF0F0F0F0u, x1.z, g);
+    g = dp4a_ss(w.w & 0xF0F0F0F0u, x1.w, g);
+    return g;
+}
+
+// Fused prologue, whole x in registers: NIT float4 per thread and token
+// (a compile-time bound, so no predicated-off iterations are issued).
+// Loads x, reduces the absmax over the block, and writes the int8 codes to
+// shared memory (and, from block 0, to qx_out); tsum gets this thread's code
+// sums.  Contains one block barrier; every thread must call it.
+template <int MT, int NIT, bool kCodeSums>
+__device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, float* red_s, float* sx_s,
+                                                    int8_t* xs, int (&tsum)[MT])
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int M = a.M;
+    const int K = a.K;
+    const int K4 = K >> 2;
+    float4 v[MT][NIT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const int i = tid + it * kThreads;
+            v[m][it] = (m < M && it < nit && i < K4) ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int it = 0; it < NIT; ++it)
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[m][it].x), fabsf(v[m][it].y)), fmaxf(fabsf(v[m][it].z), fabsf(v[m][it].w))));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) red_s[warp * MT + m] = mx;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < M) {
+            float amax = red_s[m];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
+            const A8Scale ks = a8_scale(amax);
+            if (tid == m) {
+                sx_s[m] = ks.s;
+                if (blockIdx.x == 0 && a.sx_out != nullptr) a.sx_out[m] = ks.s;
+            }
+            uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
+            uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
+                                 ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
+                                 : nullptr;
+            uint32_t need = a8_needs_exact(ks) ? 0xffffffffu : 0u;
+            uint32_t qw[NIT];
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) {
+                bool tie = false;
+                qw[it] = a8_pack4_fast(v[m][it], ks, tie);
+                need |= tie ? (1u << it) : 0u;
+            }
+            if (need) {
+                // rare: words with a possible tie (or a tiny scale) get the exact codes;
+                // x is read again so that v need not stay live across this branch
+                const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
+#pragma unroll
+                for (int it = 0; it < NIT; ++it) {
+                    const int i = tid + it * kThreads;
+                    if (((need >> it) & 1u) && it < nit && i < K4) qw[it] = a8_pack4(__ldcg(xr + i), ks);
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) {
+                const int i = tid + it * kThreads;
+                if (it < nit && i < K4) {
+                    dst[i] = qw[it];
+                    if (gout) gout[i] = qw[it];
+                    if constexpr (kCodeSums) tsum[m] += bytesum(qw[it]);
+                }
+            }
+        } else if (tid == m) {
+            sx_s[m] = 0.0f;
+        }
+    }
+}
+
+template <int FMT, int MT, int XM>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a)
+{
+    using Acc = typename std::conditional<FMT == FMT_W4, int, float>::type;
     constexpr int kUnit = fmt_unit_bytes(FMT);
     constexpr int kLineBytes = kRows * kUnit;
     constexpr int kSL = fmt_slice_lines(FMT);
     constexpr int kSlotW = fmt_slot_w_bytes(FMT);
     constexpr int kSlot = fmt_slot_bytes(FMT);
     constexpr bool kGroup = fmt_group(FMT);
+    constexpr bool kCodeSums = FMT == FMT_W4;        // activation code sums for the nibble bias
+    constexpr int kPassLines = 16;
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = a.stages;
     const int RT = a.round_tiles;
-    const SmemLayout L = smem_layout(FMT, MT, FUSED, a.K, S, RT);
+    const int C = a.C;
+    const int M = a.M;
+    const int K = a.K;
+    const SmemLayout L = smem_layout(FMT, MT, XM, K, S, RT);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     float* sx_s = reinterpret_cast<float*>(smem + L.sx);
     float* red_s = reinterpret_cast<float*>(smem + L.red);
+    int* xsum_s = reinterpret_cast<int*>(smem + L.xsum);      // [kWarps][MT] partial code sums (W4)
+    float* bias_s = reinterpret_cast<float*>(smem + L.rowp);  // [kRowCache] this block's bias
+    float* sw_s = bias_s + kRowCache;                         // [kRowCache] and per-row scales (W4)
     int* meta_s = reinterpret_cast<int*>(smem + L.meta);
     Acc* acc_s = reinterpret_cast<Acc*>(smem + L.acc);
     Acc* bnd_s = reinterpret_cast<Acc*>(smem + L.bnd);
@@ -84,9 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int C = a.C;
-    const int M = a.M;
-    const int K = a.K;
 
     // ---- this block's tiles and rounds
     const int G = gridDim.x;
@@ -95,13 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
     const int ntiles = t1 - t0;
     const int nrounds = (ntiles + RT - 1) / RT;
 
-    // Warp w's line range [lo, hi) within a round of nt tiles: an even split,
-    // boundaries rounded down to whole passes of 4 lines.
+    // Warp w's line range [lo, hi) within a round: an even split, boundaries
+    // rounded down to whole passes.
     auto warp_range = [&](int round, int& lo, int& hi) {
         const int nt = min(RT, ntiles - round * RT);
-        const int nL = nt * C;
-        lo = static_cast<int>((static_cast<long long>(warp) * nL / kWarps) & ~3LL);
-        hi = warp == kWarps - 1 ? nL : static_cast<int>((static_cast<long long>(warp + 1) * nL / kWarps) & ~3LL);
+        const long long nL = static_cast<long long>(nt) * C;
+        const long long mask = ~static_cast<long long>(kPassLines - 1);
+        lo = static_cast<int>((warp * nL / kWarps) & mask);
+        hi = warp == kWarps - 1 ? static_cast<int>(nL) : static_cast<int>(((warp + 1) * nL / kWarps) & mask);
     };
 
     // ---- per-warp ring of bulk-copy slots
@@ -112,37 +235,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
         fence_mbar_init();
     }
     __syncwarp();
+    pdl_launch_dependents();          // the next kernel may become resident beside this one
     const uint64_t pol = l2_policy_evict_first();
 
-    // Issue iterator: walks this warp's slices, round by round.
-    int is_round = 0, is_p = 0, is_hi = 0;
-    if (nrounds > 0) warp_range(0, is_p, is_hi);
+    // Issue iterator over this warp's slices: round, line position within the
+    // round's range, and (tile, chunk) of that position, advanced without division.
+    int is_round = 0, is_p = 0, is_hi = 0, is_tl = 0, is_c = 0;
+    if (nrounds > 0) {
+        warp_range(0, is_p, is_hi);
+        is_tl = is_p / C;
+        is_c = is_p - is_tl * C;
+    }
     int issued = 0;
     auto issue_next = [&]() -> bool {
         while (is_round < nrounds) {
             if (is_p < is_hi) {
-                const int tl = is_p / C;
-                const int e = min(min(is_hi, (tl + 1) * C), is_p + kSL);
-                const int n = e - is_p;
-                const int tile = t0 + is_round * RT + tl;
-                const size_t unit0 = (static_cast<size_t>(tile) * C + (is_p - tl * C)) * kRows;
+                const int n = min(min(is_hi - is_p, C - is_c), kSL);
+                const size_t unit0 = (static_cast<size_t>(t0 + is_round * RT + is_tl) * C + is_c) * kRows;
                 if (lane == 0) {
                     const int slot = issued % S;
                     uint8_t* dst = my_ring + static_cast<size_t>(slot) * kSlot;
                     const uint32_t bar = my_bars + 8 * slot;
                     const uint32_t bw = static_cast<uint32_t>(n * kLineBytes);
                     const uint32_t bs = kGroup ? static_cast<uint32_t>(n * kRows * 2) : 0u;
-                    fence_proxy_async_smem();
+                    if (issued >= S) fence_proxy_async_smem();   // the slot was read before
                     mbar_arrive_expect_tx(bar, bw + bs);
                     bulk_g2s(smem_u32(dst), a.w + unit0 * kUnit, bw, bar, pol);
                     if (kGroup) bulk_g2s(smem_u32(dst + kSlotW), a.wscale + unit0, bs, bar, pol);
                 }
                 ++issued;
-                is_p = e;
+                is_p += n;
+                is_c += n;
+                if (is_c == C) {
+                    is_c = 0;
+                    ++is_tl;
+                }
                 return true;
             }
             ++is_round;
-            if (is_round < nrounds) warp_range(is_round, is_p, is_hi);
+            if (is_round < nrounds) {
+                warp_range(is_round, is_p, is_hi);
+                is_tl = is_p / C;
+                is_c = is_p - is_tl * C;
+            }
         }
         return false;
     };
@@ -150,84 +285,174 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
     for (int s = 0; s < S; ++s)
         if (!issue_next()) break;
 
+    // per-row epilogue parameters are static: stage them while the previous kernel runs
+    const int row0 = t0 * kRows;
+    const bool rows_cached = ntiles * kRows <= kRowCache;
+    if (rows_cached) {
+        for (int i = tid; i < ntiles * kRows; i += kThreads) {
+            const int row = row0 + i;
+            bias_s[i] = (a.bias != nullptr && row < a.N) ? __ldg(a.bias + row) : 0.0f;
+            if constexpr (FMT == FMT_W4) sw_s[i] = row < a.N ? __ldg(a.s_w + row) : 0.0f;
+        }
+    }
+
     // ---- inputs produced by earlier kernels are read only from here on
     pdl_wait();
-    pdl_launch_dependents();
 
-    // ---- activation prologue
-    if constexpr (FUSED) {
-        float mx[MT];
+    // ---- activation prologue: int8 codes into shared memory (fused: quantize
+    // here) and, for W4, per-thread code sums that the epilogue reduces.  All
+    // loads of a token are issued before any store, so one memory round trip
+    // covers the vector; two block barriers in all.
+    const int K4 = K >> 2;
+    const int nit = (K4 + kThreads - 1) / kThreads;
+    int tsum[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) mx[m] = 0.0f;
-        const int K4 = K >> 2;
+    for (int m = 0; m < MT; ++m) tsum[m] = 0;
+
+    if constexpr (XM == X_FUSED) {
+        constexpr int kRegF4 = 20;                  // float4 of x held per thread
+        constexpr int kIt = kRegF4 / MT;            // per token
+        constexpr int kB1 = kIt / 5 > 0 ? kIt / 5 : 1;
+        constexpr int kB2 = 2 * kIt / 5 > 0 ? 2 * kIt / 5 : 1;
+        constexpr int kB3 = 3 * kIt / 5 > 0 ? 3 * kIt / 5 : 1;
+        if (nit <= kB1) {
+            fused_prologue_regs<MT, kB1, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+        } else if (nit <= kB2) {
+            fused_prologue_regs<MT, kB2, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+        } else if (nit <= kB3) {
+            fused_prologue_regs<MT, kB3, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+        } else if (nit <= kIt) {
+            fused_prologue_regs<MT, kIt, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+        } else {
+            // large M*K: a first pass for the absmax, a second to quantize; loads batched four at a time
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m < M) {
-                const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
-                for (int i = tid; i < K4; i += kThreads) {
-                    const float4 v = __ldcg(xr + i);
-                    mx[m] = fmaxf(mx[m], fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            for (int m = 0; m < MT; ++m) {
+                float mx = 0.0f;
+                if (m < M) {
+                    const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
+                    for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
+                        float4 b4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int i = i0 + u * kThreads + tid;
+                            b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(b4[u].x), fabsf(b4[u].y)), fmaxf(fabsf(b4[u].z), fabsf(b4[u].w))));
+                    }
                 }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                if (lane == 0) red_s[warp * MT + m] = mx;
             }
+            __syncthreads();
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], off));
-            if (lane == 0) red_s[warp * MT + m] = mx[m];
-        }
-        __syncthreads();
-        if (tid < MT) {
-            float amax = 0.0f;
-            for (int w = 0; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + tid]);
-            const float s = tid < M ? __fdiv_rn(amax, 127.0f) : 0.0f;
-            sx_s[tid] = s;
-            if (blockIdx.x == 0 && tid < M && a.sx_out != nullptr) a.sx_out[tid] = s;
-        }
-        __syncthreads();
+            for (int m = 0; m < MT; ++m) {
+                if (m < M) {
+                    float amax = red_s[m];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
-            if (m < M) {
-                const float s = sx_s[m];
-                const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
-                uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
-                                     ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
-                                     : nullptr;
-                for (int i = tid; i < K4; i += kThreads) {
-                    const float4 v = __ldcg(xr + i);
-                    const uint32_t q = quant_a8(v.x, s) | (quant_a8(v.y, s) << 8) | (quant_a8(v.z, s) << 16) |
-                                       (quant_a8(v.w, s) << 24);
-                    dst[i] = q;
-                    if (gout) gout[i] = q;
+                    for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
+                    const A8Scale ks = a8_scale(amax);
+                    if (tid == m) {
+                        sx_s[m] = ks.s;
+                        if (blockIdx.x == 0 && a.sx_out != nullptr) a.sx_out[m] = ks.s;
+                    }
+                    uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
+                    uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
+                                         ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
+                                         : nullptr;
+                    const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
+                    for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
+                        float4 b4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int i = i0 + u * kThreads + tid;
+                            b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int i = i0 + u * kThreads + tid;
+                            if (i < K4) {
+                                const uint32_t q = a8_pack4(b4[u], ks);
+                                dst[i] = q;
+                                if (gout) gout[i] = q;
+                                if constexpr (kCodeSums) tsum[m] += bytesum(q);
+                            }
+                        }
+                    }
+                } else if (tid == m) {
+                    sx_s[m] = 0.0f;
                 }
-            } else {
-                for (int i = tid; i < K4; i += kThreads) dst[i] = 0u;
             }
         }
     } else {
         if (tid < MT) sx_s[tid] = tid < M ? a.sx_in[tid] : 0.0f;
+        // int8 codes from global memory: into shared memory (smem mode), summed for W4
+        if (XM == X_SMEM || kCodeSums) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < M) {
+                    const uint32_t* qr = reinterpret_cast<const uint32_t*>(a.qx_in + static_cast<size_t>(m) * K);
+                    uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
+                    for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
+                        uint32_t b4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int i = i0 + u * kThreads + tid;
+                            b4[u] = i < K4 ? __ldg(qr + i) : 0u;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int i = i0 + u * kThreads + tid;
+                            if (i < K4) {
+                                if constexpr (XM == X_SMEM) dst[i] = b4[u];
+                                if constexpr (kCodeSums) tsum[m] += bytesum(b4[u]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if constexpr (kCodeSums) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) tsum[m] += __shfl_xor_sync(0xffffffffu, tsum[m], off);
+            if (lane == 0) xsum_s[warp * MT + m] = tsum[m];
+        }
     }
     __syncthreads();
 
     // Activation chunk (32 int8) of token m at chunk c.
     auto load_x = [&](int m, int c, uint4& x0, uint4& x1) {
-        if constexpr (FUSED) {
-            const uint4* p = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * K + c * 32);
-            x0 = p[0];
-            x1 = p[1];
-        } else {
+        if constexpr (XM == X_GLOBAL) {
             const uint4* p = reinterpret_cast<const uint4*>(a.qx_in + static_cast<size_t>(m) * K + c * 32);
             x0 = __ldg(p);
             x1 = __ldg(p + 1);
+        } else {
+            const uint4* p = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * K + c * 32);
+            x0 = p[0];
+            x1 = p[1];
         }
     };
 
-    Acc acc[MT];
+    // acc[m][j]: row 4h + (j ^ pp) of the current tile, token m
+    Acc acc[MT][4];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = Acc(0);
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
+
+    const int h = lane & 1;               // rows 4h .. 4h+3
+    const int pl = lane >> 1;             // line within a pass
+    const int pp = pl & 3;                // read-order permutation
+    const int my_row = 4 * h + pp;        // row held after the tile-end butterfly (lanes < 8)
 
     bool dead = false;      // a bounded wait ran out: stop computing, keep the barrier count
     int consumed = 0;       // slices whose slot has been released
     int observed = 0;       // slices whose copy was seen complete
-    const int r = lane & 7;
 
     for (int round = 0; round < nrounds; ++round) {
         const int buf = round & 1;
@@ -240,12 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
         }
         __syncwarp();
 
-        for (int p = lo; p < hi;) {
-            const int tl = p / C;
-            const int tend = (tl + 1) * C;
-            const int e = min(min(hi, tend), p + kSL);
-            const int n = e - p;
-            const int c0 = p - tl * C;
+        int p = lo;
+        int tl = lo / C;
+        int c = lo - tl * C;
+        while (p < hi) {
+            const int n = min(min(hi - p, C - c), kSL);
             const int slot = consumed % S;
             const uint32_t parity = static_cast<uint32_t>(consumed / S) & 1u;
 
@@ -261,56 +485,69 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
             if (!dead) {
                 const uint8_t* sw = my_ring + static_cast<size_t>(slot) * kSlot;
                 const __half* sd = reinterpret_cast<const __half*>(sw + kSlotW);
-#pragma unroll 2
-                for (int line = lane >> 3; line < n; line += 4) {
-                    const int u = line * kRows + r;
-                    const int chunk = c0 + line;
-                    if constexpr (FMT == FMT_I8G32) {
-                        const uint4 w0 = *reinterpret_cast<const uint4*>(sw + u * 32);
-                        const uint4 w1 = *reinterpret_cast<const uint4*>(sw + u * 32 + 16);
-                        const float d = __half2float(sd[u]);
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            if (MT == 1 || m < M) {
-                                uint4 x0, x1;
-                                load_x(m, chunk, x0, x1);
-                                int g = dp4a_ss(w0.x, x0.x, 0);
-                                g = dp4a_ss(w0.y, x0.y, g);
-                                g = dp4a_ss(w0.z, x0.z, g);
-                                g = dp4a_ss(w0.w, x0.w, g);
-                                g = dp4a_ss(w1.x, x1.x, g);
-                                g = dp4a_ss(w1.y, x1.y, g);
-                                g = dp4a_ss(w1.z, x1.z, g);
-                                g = dp4a_ss(w1.w, x1.w, g);
-                                acc[m] = __fmaf_rn(d, __int2float_rn(g), acc[m]);
+                for (int pass = 0; pass < kSL / kPassLines; ++pass) {
+                    const int line = pass * kPassLines + pl;
+                    if (line < n) {
+                        const int chunk = c + line;
+                        const uint8_t* ub = sw + (line * kRows + 4 * h) * kUnit;
+                        if constexpr (FMT == FMT_I8G32) {
+                            uint4 w0[4], w1[4];
+                            float d[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint8_t* u = ub + ((j ^ pp) << 5);
+                                // the two halves are read in a lane-dependent order to spread banks
+                                const uint4 first = *reinterpret_cast<const uint4*>(u + (h << 4));
+                                const uint4 second = *reinterpret_cast<const uint4*>(u + ((h ^ 1) << 4));
+                                w0[j] = h ? second : first;
+                                w1[j] = h ? first : second;
+                                d[j] = __half2float(sd[line * kRows + 4 * h + (j ^ pp)]);
                             }
-                        }
-                    } else {
-                        const uint4 wv = *reinterpret_cast<const uint4*>(sw + u * 16);
-                        // 16 x (weights 8w..8w+3) and 16 x (weights 8w+4..8w+7) as signed bytes
-                        const uint32_t l0 = (wv.x << 4) & 0xF0F0F0F0u, h0 = wv.x & 0xF0F0F0F0u;
-                        const uint32_t l1 = (wv.y << 4) & 0xF0F0F0F0u, h1 = wv.y & 0xF0F0F0F0u;
-                        const uint32_t l2 = (wv.z << 4) & 0xF0F0F0F0u, h2 = wv.z & 0xF0F0F0F0u;
-                        const uint32_t l3 = (wv.w << 4) & 0xF0F0F0F0u, h3 = wv.w & 0xF0F0F0F0u;
-                        float d = 0.0f;
-                        if constexpr (FMT == FMT_Q4_0) d = __half2float(sd[u]);
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            if (MT == 1 || m < M) {
-                                uint4 x0, x1;
-                                load_x(m, chunk, x0, x1);
-                                int g = dp4a_ss(l0, x0.x, 0);
-                                g = dp4a_ss(h0, x0.y, g);
-                                g = dp4a_ss(l1, x0.z, g);
-                                g = dp4a_ss(h1, x0.w, g);
-                                g = dp4a_ss(l2, x1.x, g);
-                                g = dp4a_ss(h2, x1.y, g);
-                                g = dp4a_ss(l3, x1.z, g);
-                                g = dp4a_ss(h3, x1.w, g);
-                                if constexpr (FMT == FMT_W4) {
-                                    acc[m] += g;
-                                } else {
-                                    acc[m] = __fmaf_rn(d, __int2float_rn(g >> 4), acc[m]);
+                            for (int m = 0; m < MT; ++m) {
+                                if (MT == 1 || m < M) {
+                                    uint4 x0, x1;
+                                    load_x(m, chunk, x0, x1);
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        int g = dp4a_ss(w0[j].x, x0.x, 0);
+                                        g = dp4a_ss(w0[j].y, x0.y, g);
+                                        g = dp4a_ss(w0[j].z, x0.z, g);
+                                        g = dp4a_ss(w0[j].w, x0.w, g);
+                                        g = dp4a_ss(w1[j].x, x1.x, g);
+                                        g = dp4a_ss(w1[j].y, x1.y, g);
+                                        g = dp4a_ss(w1[j].z, x1.z, g);
+                                        g = dp4a_ss(w1[j].w, x1.w, g);
+                                        acc[m][j] = __fmaf_rn(d[j], __int2float_rn(g), acc[m][j]);
+                                    }
+                                }
+                            }
+                        } else {
+                            uint4 wv[4];
+                            float d[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                wv[j] = *reinterpret_cast<const uint4*>(ub + ((j ^ pp) << 4));
+                                if constexpr (FMT == FMT_Q4_0)
+                                    d[j] = __half2float(sd[line * kRows + 4 * h + (j ^ pp)]);
+                            }
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                if (MT == 1 || m < M) {
+                                    uint4 x0, x1;
+                                    load_x(m, chunk, x0, x1);
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        if constexpr (FMT == FMT_W4) {
+                                            int B, A;
+                                            unit4(wv[j], x0, x1, B, A);
+                                            acc[m][j] += B + (A >> 4);
+                                        } else {
+                                            const int g = unit4_signed16(wv[j], x0, x1) >> 4;
+                                            acc[m][j] = __fmaf_rn(d[j], __int2float_rn(g), acc[m][j]);
+                                        }
+                                    }
                                 }
                             }
                         }
@@ -321,35 +558,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
             __syncwarp();
             if (!dead) issue_next();   // refill the slot just released
 
-            if (e == tend || e == hi) {
-                // this warp is done with tile tl: reduce lanes of equal row
+            p += n;
+            c += n;
+            if (c == C || p == hi) {
+                // tile done for this warp: reduce lanes of equal (h, pp), then undo
+                // the read permutation with a two-step butterfly
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    if constexpr (FMT == FMT_W4) {
-                        acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], 8);
-                        acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], 16);
-                    } else {
-                        acc[m] = __fadd_rn(acc[m], __shfl_xor_sync(0xffffffffu, acc[m], 8));
-                        acc[m] = __fadd_rn(acc[m], __shfl_xor_sync(0xffffffffu, acc[m], 16));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if constexpr (FMT == FMT_W4) {
+                            acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 8);
+                            acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 16);
+                        } else {
+                            acc[m][j] = __fadd_rn(acc[m][j], __shfl_xor_sync(0xffffffffu, acc[m][j], 8));
+                            acc[m][j] = __fadd_rn(acc[m][j], __shfl_xor_sync(0xffffffffu, acc[m][j], 16));
+                        }
                     }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const Acc v = __shfl_xor_sync(0xffffffffu, acc[m][j + 2], 4);
+                        if constexpr (FMT == FMT_W4) acc[m][j] += v; else acc[m][j] = __fadd_rn(acc[m][j], v);
+                    }
+                    const Acc v = __shfl_xor_sync(0xffffffffu, acc[m][1], 2);
+                    if constexpr (FMT == FMT_W4) acc[m][0] += v; else acc[m][0] = __fadd_rn(acc[m][0], v);
                 }
+                const int tstart = tl * C;
                 if (lane < kRows) {
-                    const bool full = lo <= tl * C && hi >= tend;
+                    const bool full = lo <= tstart && hi >= tstart + C;
                     Acc* dst;
                     if (full) {
-                        dst = acc_s + (static_cast<size_t>(buf) * RT * kRows + tl * kRows + lane) * MT;
+                        dst = acc_s + (static_cast<size_t>(buf) * RT * kRows + tl * kRows + my_row) * MT;
                     } else {
-                        const int which = (lo >= tl * C && lo < tend) ? 0 : 1;
-                        dst = bnd_s + (((buf * kWarps + warp) * 2 + which) * kRows + lane) * MT;
+                        const int which = (lo >= tstart && lo < tstart + C) ? 0 : 1;
+                        dst = bnd_s + (((buf * kWarps + warp) * 2 + which) * kRows + my_row) * MT;
                         if (lane == 0) meta[which] = tl;
                     }
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) dst[m] = acc[m];
+                    for (int m = 0; m < MT; ++m) dst[m] = acc[m][0];
                 }
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m] = Acc(0);
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
+                if (c == C) {
+                    c = 0;
+                    ++tl;
+                }
             }
-            p = e;
         }
 
         __syncthreads();
@@ -363,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
             const int rl = idx - m * nrows;
             const int row = row_base + rl;
             if (row >= a.N) continue;
-            const int tl = rl >> 3;
+            const int tile = rl >> 3;
             const int rr = rl & 7;
             Acc v = Acc(0);
             bool part = false;
@@ -371,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
                 const int* mw = meta_s + (buf * kWarps + w) * 2;
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
-                    if (mw[which] == tl) {
+                    if (mw[which] == tile) {
                         const Acc pv = bnd_s[(((buf * kWarps + w) * 2 + which) * kRows + rr) * MT + m];
                         if constexpr (FMT == FMT_W4) v += pv; else v = __fadd_rn(v, pv);
                         part = true;
@@ -379,10 +635,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
                 }
             }
             if (!part) v = acc_s[(static_cast<size_t>(buf) * RT * kRows + rl) * MT + m];
-            const float b = a.bias != nullptr ? a.bias[row] : 0.0f;
+            const int ci = row - row0;
+            const float b = rows_cached ? bias_s[ci] : (a.bias != nullptr ? a.bias[row] : 0.0f);
             float out;
             if constexpr (FMT == FMT_W4) {
-                out = __fmaf_rn(__fmul_rn(a.s_w[row], sx_s[m]), __int2float_rn(v >> 4), b);
+                int xsum = 0;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) xsum += xsum_s[w * MT + m];
+                const int accv = v - 8 * xsum;          // remove the +8 nibble bias
+                const float swr = rows_cached ? sw_s[ci] : a.s_w[row];
+                out = __fmaf_rn(__fmul_rn(swr, sx_s[m]), __int2float_rn(accv), b);
             } else {
                 out = __fmaf_rn(sx_s[m], v, b);
             }
@@ -400,10 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvArgs a)
     }
 }
 
-template <int FMT, int MT, bool FUSED>
+template <int FMT, int MT, int XM>
 cudaError_t launch_gemv_t(const GemvArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-    auto kern = gemv_kernel<FMT, MT, FUSED>;
+    auto kern = gemv_kernel<FMT, MT, XM>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -427,12 +689,13 @@ cudaError_t launch_gemv_t(const GemvArgs& a, int grid, size_t smem, bool pdl, cu
 }
 
 template <int FMT>
-cudaError_t launch_gemv_fmt(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl, cudaStream_t s)
+cudaError_t launch_gemv_fmt(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-#define W4_CASE(mt)                                                                   \
-    case mt:                                                                          \
-        return fused ? launch_gemv_t<FMT, mt, true>(a, grid, smem, pdl, s)            \
-                     : launch_gemv_t<FMT, mt, false>(a, grid, smem, pdl, s);
+#define W4_CASE(mt)                                                                              \
+    case mt:                                                                                     \
+        return xmode == X_FUSED  ? launch_gemv_t<FMT, mt, X_FUSED>(a, grid, smem, pdl, s)        \
+               : xmode == X_SMEM ? launch_gemv_t<FMT, mt, X_SMEM>(a, grid, smem, pdl, s)         \
+                                 : launch_gemv_t<FMT, mt, X_GLOBAL>(a, grid, smem, pdl, s);
     switch (MT) {
         W4_CASE(1)
         W4_CASE(2)

@@ -4,9 +4,9 @@
 
 namespace w4k {
 
-cudaError_t launch_gemv_q4_0(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl, cudaStream_t s)
+cudaError_t launch_gemv_q4_0(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-    return launch_gemv_fmt<FMT_Q4_0>(a, MT, fused, grid, smem, pdl, s);
+    return launch_gemv_fmt<FMT_Q4_0>(a, MT, xmode, grid, smem, pdl, s);
 }
 
 }  // namespace w4k

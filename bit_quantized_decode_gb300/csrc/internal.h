@@ -13,7 +13,11 @@ constexpr int kRows = 8;                 // weight rows per tile
 constexpr int kWarps = 8;                // warps per GEMV thread block
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxStages = 8;            // ring slots per warp, upper bound
-constexpr int kAccWords = 128;           // round_tiles * MT, bounds the per-round accumulator
+constexpr int kAccWords = 64;            // round_tiles * MT, bounds the per-round accumulator
+constexpr int kRowCache = 1024;          // rows per block whose s_w / bias are staged in shared memory
+
+// How a GEMV block obtains its int8 activations.
+enum XMode { X_FUSED = 0, X_SMEM = 1, X_GLOBAL = 2 };
 
 // Lines (8 rows x one 32-weight chunk) per ring slot and bytes per unit.
 __host__ __device__ constexpr int fmt_unit_bytes(int fmt) { return fmt == FMT_I8G32 ? 32 : 16; }
@@ -44,23 +48,25 @@ struct GemvArgs {
 };
 
 struct SmemLayout {
-    int bars, sx, red, meta, acc, bnd, ring, xs, total;
+    int bars, sx, red, xsum, rowp, meta, acc, bnd, ring, xs, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, bool fused, int K, int stages, int round_tiles)
+__host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, int K, int stages, int round_tiles)
 {
     SmemLayout L;
     int o = 0;
     L.bars = o;  o = align_up(o + kWarps * stages * 8, 16);
     L.sx = o;    o = align_up(o + MT * 4, 16);
     L.red = o;   o = align_up(o + kWarps * MT * 4, 16);
+    L.xsum = o;  o = align_up(o + kWarps * MT * 4, 16);
+    L.rowp = o;  o = align_up(o + kRowCache * 4 * (fmt == FMT_W4 ? 2 : 1), 16);
     L.meta = o;  o = align_up(o + 2 * kWarps * 2 * 4, 16);
     L.acc = o;   o = align_up(o + 2 * round_tiles * kRows * MT * 4, 16);
     L.bnd = o;   o = align_up(o + 2 * kWarps * 2 * kRows * MT * 4, 128);
     L.ring = o;  o = align_up(o + kWarps * stages * fmt_slot_bytes(fmt), 128);
-    L.xs = o;    o += fused ? MT * K : 0;
+    L.xs = o;    o += xmode != X_GLOBAL ? MT * K : 0;
     L.total = o;
     return L;
 }
@@ -69,9 +75,9 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, bool fused, i
 constexpr unsigned kErrWaitTimeout = 0x57414954u;  // "WAIT"
 
 // Kernel launchers, one translation unit per format.
-cudaError_t launch_gemv_w4(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl, cudaStream_t s);
-cudaError_t launch_gemv_q4_0(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl, cudaStream_t s);
-cudaError_t launch_gemv_i8g32(const GemvArgs& a, int MT, bool fused, int grid, size_t smem, bool pdl,
+cudaError_t launch_gemv_w4(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_gemv_q4_0(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_gemv_i8g32(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl,
                               cudaStream_t s);
 
 // Load-time and activation kernels (prep_kernels.cu).

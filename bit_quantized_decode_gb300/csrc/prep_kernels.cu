@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "quant_a8.cuh"
 
 namespace w4k {
 
@@ -50,16 +51,10 @@ __global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float*
     float amax = 0.0f;
 #pragma unroll
     for (int w = 0; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-    const float s = __fdiv_rn(amax, 127.0f);
+    const A8Scale ks = a8_scale(amax);
     uint32_t* out = reinterpret_cast<uint32_t*>(qx + static_cast<size_t>(m) * K);
-    for (int i = threadIdx.x; i < K4; i += kQuantThreads) {
-        const float4 v = xr[i];
-        out[i] = (static_cast<uint32_t>(quant_code(v.x, s, -127, 127)) & 0xffu) |
-                 ((static_cast<uint32_t>(quant_code(v.y, s, -127, 127)) & 0xffu) << 8) |
-                 ((static_cast<uint32_t>(quant_code(v.z, s, -127, 127)) & 0xffu) << 16) |
-                 ((static_cast<uint32_t>(quant_code(v.w, s, -127, 127)) & 0xffu) << 24);
-    }
-    if (threadIdx.x == 0) sx[m] = s;
+    for (int i = threadIdx.x; i < K4; i += kQuantThreads) out[i] = a8_pack4(xr[i], ks);
+    if (threadIdx.x == 0) sx[m] = ks.s;
 }
 
 cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, cudaStream_t s)
@@ -210,9 +205,11 @@ __device__ __forceinline__ uint32_t spread4(uint32_t v)
     return (v & 0xfu) | ((v & 0xf0u) << 4) | ((v & 0xf00u) << 8) | ((v & 0xf000u) << 12);
 }
 
+// The device stores every nibble biased, n = q + 8, which for a 4-bit two's
+// complement q is q with its top bit flipped.
 __device__ __forceinline__ uint32_t interleave_w4(uint32_t canon)
 {
-    return spread4(canon & 0xffffu) | (spread4(canon >> 16) << 4);
+    return (spread4(canon & 0xffffu) | (spread4(canon >> 16) << 4)) ^ 0x88888888u;
 }
 
 // One thread per unit (t, c, r) -> out unit index ((t*C + c)*8 + r).

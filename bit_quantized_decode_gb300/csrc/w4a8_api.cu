@@ -20,11 +20,16 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;       // largest dynamic shared memory one block may use
+    int smem_per_sm = 0;
+    int smem_reserved = 0;    // per-block shared memory the runtime reserves
     unsigned* err = nullptr;
     bool ready = false;
 };
 DeviceInfo g_dev[kMaxDevices];
+
+// Launch tuning set by w4_set_tuning (0 = automatic).
+int g_tune[3] = {0, 0, 0};
 
 w4_status device_info(DeviceInfo** out)
 {
@@ -34,6 +39,10 @@ w4_status device_info(DeviceInfo** out)
     if (!d.ready) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return W4_ERR_CUDA;
         if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return W4_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+            return W4_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
             return W4_ERR_CUDA;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_w4_error_word) != cudaSuccess) return W4_ERR_CUDA;
@@ -80,7 +89,53 @@ w4_status build_shards(const void* const* p, const void* const* p2, const int* r
 
 size_t tiles(int N) { return (static_cast<size_t>(N) + kRows - 1) / kRows; }
 
-// Choose the launch configuration of one GEMV and launch it.
+// Launch configuration of one GEMV: activation mode, ring depth, shared memory.
+struct Plan {
+    int xmode = X_GLOBAL;
+    int stages = 0;
+    int smem = 0;
+};
+
+// Largest ring (at most the cap) whose layout fits `budget`; 0 if fewer than 2 stages fit.
+int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget)
+{
+    const int cap = g_tune[W4_TUNE_MAX_STAGES] > 0 ? g_tune[W4_TUNE_MAX_STAGES] : kMaxStages;
+    int s = cap < kMaxStages ? cap : kMaxStages;
+    while (s >= 2 && smem_layout(fmt, MT, xmode, K, s, RT).total > budget) --s;
+    return s >= 2 ? s : 0;
+}
+
+// Two blocks per SM (this GEMV beside the next one in the stream) when a
+// ring of at least `min_coresident` stages fits in half the SM; else the
+// whole-block budget.  `fused` asks for the quantize prologue.
+bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p)
+{
+    const int half = d.smem_per_sm / 2 - d.smem_reserved;
+    const int whole = d.smem_optin;
+    const int bps = g_tune[W4_TUNE_BLOCKS_PER_SM];
+    const int min_co = 3;
+    const int modes[2] = {fused ? X_FUSED : X_SMEM, fused ? -1 : X_GLOBAL};
+    for (int pass = 0; pass < 2; ++pass) {
+        // pass 0: co-resident budget (unless forced to one block per SM)
+        if (pass == 0 && bps == 1) continue;
+        if (pass == 1 && bps == 2) break;
+        const int budget = pass == 0 ? half : whole;
+        for (int mi = 0; mi < 2; ++mi) {
+            const int xm = modes[mi];
+            if (xm < 0) continue;
+            const int s = stages_for(fmt, MT, xm, K, RT, budget);
+            if (s >= (pass == 0 && bps == 0 ? min_co : 2)) {
+                p.xmode = xm;
+                p.stages = s;
+                p.smem = smem_layout(fmt, MT, xm, K, s, RT).total;
+                return true;
+            }
+        }
+    }
+    return false;
+}
+
+// Launch one GEMV.
 w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t s)
 {
     DeviceInfo* dev = nullptr;
@@ -91,18 +146,17 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     a.T = static_cast<int>(tiles(a.N));
     a.round_tiles = kAccWords / MT;
     a.err = dev->err;
-    const int budget = dev->smem_optin;
-    int stages = kMaxStages;
-    while (stages >= 2 && smem_layout(fmt, MT, fused, a.K, stages, a.round_tiles).total > budget) --stages;
-    if (stages < 2) return W4_ERR_UNSUPPORTED_SHAPE;
-    a.stages = stages;
-    const size_t smem = static_cast<size_t>(smem_layout(fmt, MT, fused, a.K, stages, a.round_tiles).total);
-    const int grid = a.T < dev->sms ? a.T : dev->sms;
+    Plan p;
+    if (!plan_gemv(*dev, fmt, MT, fused, a.K, a.round_tiles, p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    a.stages = p.stages;
+    int grid = dev->sms;
+    if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
+    if (a.T < grid) grid = a.T;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
     cudaError_t e;
-    if (fmt == FMT_W4) e = launch_gemv_w4(a, MT, fused, grid, smem, pdl, s);
-    else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(a, MT, fused, grid, smem, pdl, s);
-    else e = launch_gemv_i8g32(a, MT, fused, grid, smem, pdl, s);
+    if (fmt == FMT_W4) e = launch_gemv_w4(a, MT, p.xmode, grid, p.smem, pdl, s);
+    else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(a, MT, p.xmode, grid, p.smem, pdl, s);
+    else e = launch_gemv_i8g32(a, MT, p.xmode, grid, p.smem, pdl, s);
     return cuda_status(e);
 }
 
@@ -112,7 +166,8 @@ bool fused_fits(int fmt, int M, int K)
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != W4_OK) return false;
     const int MT = round_pow2_tokens(M);
-    return smem_layout(fmt, MT, true, K, 2, kAccWords / MT).total <= dev->smem_optin;
+    Plan p;
+    return plan_gemv(*dev, fmt, MT, true, K, kAccWords / MT, p);
 }
 
 w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bias, const int8_t* qx,
@@ -195,6 +250,21 @@ const char* w4_status_str(w4_status st)
 }
 
 int w4_version(void) { return 1; }
+
+w4_status w4_set_tuning(int key, int value)
+{
+    if (key < 0 || key > W4_TUNE_GRID_BLOCKS || value < 0) return W4_ERR_INVALID_ARG;
+    if (key == W4_TUNE_BLOCKS_PER_SM && value > 2) return W4_ERR_INVALID_ARG;
+    if (key == W4_TUNE_MAX_STAGES && value == 1) return W4_ERR_INVALID_ARG;
+    g_tune[key] = value;
+    return W4_OK;
+}
+
+int w4_get_tuning(int key)
+{
+    if (key < 0 || key > W4_TUNE_GRID_BLOCKS) return -1;
+    return g_tune[key];
+}
 
 // ------------------------------------------------------------ quantizers
 w4_status w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, w4_stream_t s)

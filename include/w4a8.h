@@ -37,8 +37,10 @@
  * 32 weights of row 8t+r in chunk c; units are stored in (t, c, r) order:
  *   W4, Q4_0: 16 bytes per unit at ((t*C + c)*8 + r)*16.  Word w (0..3) of the
  *         unit holds weights 32c+8w+b in the low nibble of byte b and
- *         32c+8w+4+b in the high nibble, as 4-bit two's complement (Q4_0 values
- *         n - 8).  Q4_0 then has a plane of fp16 d, one per unit, at byte
+ *         32c+8w+4+b in the high nibble.  W4 stores each nibble biased,
+ *         n = q + 8 in 0..15; Q4_0 stores 4-bit two's complement n - 8.
+ *         Padded rows are zero bytes and never reach the output.
+ *         Q4_0 then has a plane of fp16 d, one per unit, at byte
  *         T*8*C*16 + ((t*C + c)*8 + r)*2.
  *   I8G32: 32 bytes per unit (the 32 int8 in order) at ((t*C + c)*8 + r)*32,
  *         then the fp16 d plane at byte T*8*C*32 + ((t*C + c)*8 + r)*2.
@@ -70,8 +72,9 @@ const char* w4_status_str(w4_status st);
 /* Library ABI version (increases on incompatible change). */
 int w4_version(void);
 
-/* Largest K each GEMV accepts.  W4 and Q4_0 accumulate 16x-scaled int32
- * partial sums, so K * 16 * 8 * 127 must stay below 2^31: K <= 131072. */
+/* Largest K each GEMV accepts.  Row sums of biased products n * x
+ * (|n x| <= 15 * 127) are accumulated in int32, which bounds K near 1.1e6;
+ * the library accepts K <= 131072. */
 #define W4_MAX_K 131072
 #define W4_MAX_M 16
 #define W4_MAX_SHARDS 8
@@ -82,6 +85,22 @@ int w4_version(void);
                           write this call's weight buffer (weights are prefetched
                           before the dependency wait); inputs x/qx/sx and outputs are
                           touched only after it. */
+
+/* ------------------------------------------------------------------------
+ * Launch tuning (process-wide; value 0 restores the automatic choice).
+ *   W4_TUNE_BLOCKS_PER_SM  1: one GEMV block per SM with the whole shared
+ *                          memory; 2: half of it, so that a GEMV launched with
+ *                          W4_FLAG_PDL is resident beside the previous one.
+ *   W4_TUNE_MAX_STAGES     cap on the ring depth per warp (>= 2).
+ *   W4_TUNE_GRID_BLOCKS    cap on the grid size (default: the SM count).
+ * Returns W4_ERR_INVALID_ARG for an unknown key or an out-of-range value.
+ * Not thread-safe with concurrent launches; set before launching.
+ * ------------------------------------------------------------------------ */
+#define W4_TUNE_BLOCKS_PER_SM 0
+#define W4_TUNE_MAX_STAGES 1
+#define W4_TUNE_GRID_BLOCKS 2
+w4_status w4_set_tuning(int key, int value);
+int w4_get_tuning(int key); /* current value, -1 for an unknown key */
 
 /* ------------------------------------------------------------------------
  * Load time: quantize float weights (device kernels).

@@ -64,15 +64,19 @@ def _tiles(N):
     return (N + 7) // 8
 
 
-def decode_w4_units(raw: np.ndarray, N: int, K: int) -> np.ndarray:
-    """Repacked W4 nibble units -> int8 weights [N][K]."""
+def decode_w4_units(raw: np.ndarray, N: int, K: int, biased: bool = True) -> np.ndarray:
+    """Repacked 4-bit units -> int8 values [N][K].  biased: nibble n = q + 8
+    (per-row INT4); else 4-bit two's complement (Q4_0)."""
     C = K // 32
     T = _tiles(N)
     units = raw[: T * C * 8 * 16].reshape(T, C, 8, 4, 4)        # t, c, r, word, byte
     lo = (units & 0xF).astype(np.int16)
     hi = (units >> 4).astype(np.int16)
-    lo = np.where(lo >= 8, lo - 16, lo)
-    hi = np.where(hi >= 8, hi - 16, hi)
+    if biased:
+        lo, hi = lo - 8, hi - 8
+    else:
+        lo = np.where(lo >= 8, lo - 16, lo)
+        hi = np.where(hi >= 8, hi - 16, hi)
     # weight index within the chunk: 8*word + byte (low) and 8*word + 4 + byte (high)
     w = np.concatenate([lo, hi], axis=4)                         # t, c, r, word, 8
     w = w.transpose(0, 2, 1, 3, 4).reshape(T * 8, C * 32)

@@ -50,6 +50,19 @@ def test_library_is_built_for_sm_103a():
     assert "-prec-div=true" in build.NVCC_FLAGS and "-ftz=false" in build.NVCC_FLAGS
 
 
+def test_tuning_roundtrip_and_checks(lib):
+    from bit_quantized_decode_gb300 import _lib
+    for key in _lib.TUNE_KEYS:
+        assert _lib.get_tuning(key) == 0
+    _lib.set_tuning("max_stages", 4)
+    assert _lib.get_tuning("max_stages") == 4
+    _lib.set_tuning("max_stages", 0)
+    assert lib.w4_set_tuning(0, 3) == 1          # blocks_per_sm must be 0, 1 or 2
+    assert lib.w4_set_tuning(1, 1) == 1          # a ring needs two stages
+    assert lib.w4_set_tuning(7, 0) == 1          # unknown key
+    assert lib.w4_get_tuning(7) == -1
+
+
 def test_status_strings(lib):
     from bit_quantized_decode_gb300 import _lib
     for code, name in _lib.STATUS.items():

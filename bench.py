@@ -176,16 +176,18 @@ class ClockSampler:
 
 
 # --------------------------------------------------------- oracle baseline
-def oracle_layer_sample(M: int, seed: int = 1):
-    """Host-side inputs for one Qwen2-7B layer, quantized by the oracle."""
+def oracle_layer_sample(M: int, seed: int = 1, row_fraction: float = 1.0):
+    """Host-side inputs for the first rows of each linear of one Qwen2-7B
+    layer, N(0, 0.02) weights quantized by the oracle."""
     import oracle
     g = wl.rng(seed)
     layer = []
     for lin in wl.qwen7b_layer():
-        W = wl.weights(g, lin.N, lin.K)
+        n = max(8, int(lin.N * row_fraction))
+        W = wl.weights(g, n, lin.K)
         q, sw = oracle.quantize_rows_int4(W)
         del W
-        layer.append((lin, oracle.pack_int4(q), sw, wl.activations(g, M, lin.K), wl.bias(g, lin.N)))
+        layer.append((lin, oracle.pack_int4(q), sw, wl.activations(g, M, lin.K), wl.bias(g, n)))
     return layer
 
 
@@ -195,7 +197,7 @@ def time_oracle(layer, M: int, min_seconds: float, row_fraction: float = 1.0):
     import oracle
     work = []
     for lin, packed, sw, x, b in layer:
-        n = max(8, int(lin.N * row_fraction))
+        n = min(packed.shape[0], max(8, int(lin.N * row_fraction)))
         work.append((packed[:n], sw[:n], x, b[:n], n, lin))
     nbytes = sum(n * lin.K // 2 + 8 * n + 4 * M * lin.K + 4 * M * n for _, _, _, _, n, lin in work)
     reps, t0 = 0, time.perf_counter()
@@ -214,12 +216,12 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     M = max(1, min(16, args.M))
-    layer = oracle_layer_sample(M)
     layer_bytes = sum(algorithmic_bytes(lin, M) for lin in wl.qwen7b_layer())
-    # size each step so that warmup + steps fit the budget at ~0.3 GB/s
-    gbs_est, _, _ = time_oracle(layer, M, 0.0, row_fraction=0.02)
+    # size each step so that warmup + steps fit the budget at the oracle's speed
+    gbs_est, _, _ = time_oracle(oracle_layer_sample(M, row_fraction=0.005), M, 0.0, row_fraction=0.005)
     per_step_s = args.ref_budget_s / max(1, args.steps + args.warmup)
     frac = min(1.0, max(0.002, per_step_s * gbs_est * 1e9 / layer_bytes))
+    layer = oracle_layer_sample(M, row_fraction=frac)
     for _ in range(args.warmup):
         time_oracle(layer, M, 0.0, frac)
     times, nbytes = [], 0
@@ -277,6 +279,21 @@ def build_step(args, device):
         yo += M * lin.N
     torch.cuda.synchronize()
     return items, x_all, y_all
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest of every rank's value (identity on one process)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, t_max_ms: float) -> float:
+    """Weak scaling: every rank streams its own copy of the step."""
+    return world * bytes_per_step * steps / (t_max_ms / 1e3) / 1e9
 
 
 def run_ours(args, rank, world, local_rank):
@@ -357,13 +374,9 @@ def run_ours(args, rank, world, local_rank):
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
 
-    t_max = elapsed_ms
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = t_max / args.steps
-    value = world * bytes_per_step * args.steps / (t_max / 1e3) / 1e9
+    value = whole_job_gbs(bytes_per_step, args.steps, world, t_max)
 
     if args.profile:
         if rank == 0:
@@ -394,12 +407,8 @@ def run_ours(args, rank, world, local_rank):
             y_host.copy_(y_all, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * bytes_per_step * e2e_steps / (e2e_ms / 1e3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = whole_job_gbs(bytes_per_step, e2e_steps, world, e2e_ms)
 
     # ---- optional: each linear kind on its own (rotating over the layers' copies)
     per_linear = None

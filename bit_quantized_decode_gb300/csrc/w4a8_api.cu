@@ -106,14 +106,13 @@ int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget)
 }
 
 // Two blocks per SM (this GEMV beside the next one in the stream) when a
-// ring of at least `min_coresident` stages fits in half the SM; else the
-// whole-block budget.  `fused` asks for the quantize prologue.
+// ring of at least two stages fits in half the SM; else the whole-block
+// budget.  `fused` asks for the quantize prologue.
 bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p)
 {
     const int half = d.smem_per_sm / 2 - d.smem_reserved;
     const int whole = d.smem_optin;
     const int bps = g_tune[W4_TUNE_BLOCKS_PER_SM];
-    const int min_co = 3;
     const int modes[2] = {fused ? X_FUSED : X_SMEM, fused ? -1 : X_GLOBAL};
     for (int pass = 0; pass < 2; ++pass) {
         // pass 0: co-resident budget (unless forced to one block per SM)
@@ -124,7 +123,7 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
             const int xm = modes[mi];
             if (xm < 0) continue;
             const int s = stages_for(fmt, MT, xm, K, RT, budget);
-            if (s >= (pass == 0 && bps == 0 ? min_co : 2)) {
+            if (s >= 2) {
                 p.xmode = xm;
                 p.stages = s;
                 p.smem = smem_layout(fmt, MT, xm, K, s, RT).total;

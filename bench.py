@@ -46,6 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--layers", type=int, default=wl.QWEN7B_LAYERS, help="layers in the step (28 = full model)")
     p.add_argument("--no-lm-head", action="store_true")
     p.add_argument("--no-pdl", action="store_true")
+    p.add_argument("--chain", action="store_true",
+                   help="one chained launch per step (w4a8_linear_chain) instead of one PDL launch per linear")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
@@ -82,7 +84,7 @@ def workload_config(args, n_gpus):
         "M": args.M,
         "layers": args.layers,
         "lm_head": not args.no_lm_head,
-        "launches_per_step": 4 * args.layers + (0 if args.no_lm_head else 1),
+        "linears_per_step": 4 * args.layers + (0 if args.no_lm_head else 1),
         "l2": "inputs larger than L2 (3.5 GB of weights per step), no flush",
         "parallelism": f"replicas x{n_gpus}",
     }
@@ -97,22 +99,23 @@ def measured_peak():
         return FALLBACK_PEAK_GBS, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def profiled_traffic(alg_bytes_per_launch: float, chain: bool):
+    """DRAM bytes per launch from the committed ncu summary of this path: the
+    measured traffic / algorithmic ratio times this launch's algorithmic
+    bytes, if the summary was taken on the current kernel sources (else None)."""
     try:
         from bit_quantized_decode_gb300 import build
         digest = build._inputs_digest()
-        path = os.path.join(ROOT, "profiles", "gemv_w4_fused_qwen7b_step.md")
+        name = "gemv_w4_chain_qwen7b_step.md" if chain else "gemv_w4_fused_qwen7b_step.md"
         vals = {}
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
             for line in f:
                 if line.startswith("- ") and ":" in line:
                     k, v = line[2:].split(":", 1)
                     vals[k.strip()] = v.strip().strip("`")
         if vals.get("source_digest") != digest:
             return None
-        return float(vals["dram_bytes_per_launch_full_step"])
+        return round(float(vals["traffic_over_algorithmic"]) * alg_bytes_per_launch)
     except Exception:
         return None
 
@@ -299,7 +302,7 @@ def whole_job_gbs(bytes_per_step: int, steps: int, world: int, t_max_ms: float) 
 def run_ours(args, rank, world, local_rank):
     import torch
 
-    from bit_quantized_decode_gb300 import W4_FLAG_PDL, _lib
+    from bit_quantized_decode_gb300 import W4_FLAG_PDL, LinearChain, W4Error, _lib
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     dist = None
@@ -322,9 +325,33 @@ def run_ours(args, rank, world, local_rank):
 
     stream = torch.cuda.Stream(device=dev)
 
-    def step():
+    def step_per_linear():
         for i, (_, lin, ql, x, y, qx, sx) in enumerate(items):
             ql(x, y, qx, sx, flags=pdl_flag if i > 0 else 0)
+
+    # one chained launch per step (at most W4_MAX_CHAIN linears per launch)
+    chains = []
+    if args.chain:
+        try:
+            for c0 in range(0, len(items), _lib.W4_MAX_CHAIN):
+                part = items[c0: c0 + _lib.W4_MAX_CHAIN]
+                chains.append(LinearChain([(ql, x, y, qx, sx) for _, _, ql, x, y, qx, sx in part], M))
+            with torch.cuda.stream(stream):
+                for ch in chains:
+                    ch()
+            torch.cuda.synchronize()
+        except W4Error as e:
+            if e.status != 2:          # anything but "does not fit" is a real failure
+                raise
+            chains = []
+    launches = len(chains) if chains else launches
+
+    def step():
+        if chains:
+            for ch in chains:
+                ch()
+        else:
+            step_per_linear()
 
     with torch.cuda.stream(stream):
         step()                     # eager run: sets kernel attributes, checks the path
@@ -380,7 +407,8 @@ def run_ours(args, rank, world, local_rank):
 
     if args.profile:
         if rank == 0:
-            print(json.dumps({"profile": True, "tuning": tuning or "auto", "ms_per_step": elapsed_ms / args.steps,
+            print(json.dumps({"profile": True, "chain": bool(chains), "tuning": tuning or "auto",
+                              "ms_per_step": elapsed_ms / args.steps,
                               "GB/s": bytes_per_step * args.steps / (elapsed_ms / 1e3) / 1e9,
                               "launches_per_step": launches}), flush=True)
         return 0
@@ -462,10 +490,13 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": workload_config(args, world),
         "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(value / world / peak, 4), "traffic": profiled_traffic(),
+                     "frac": round(value / world / peak, 4),
+                     "traffic": profiled_traffic(bytes_per_step / launches, bool(chains)),
                      "peak_kind": peak_kind,
-                     "kernel": "gemv_kernel<W4, M, fused> (all launches of the step; bytes and time per launch "
-                               "averaged over the step)"},
+                     "kernel": ("gemv_kernel<W4, M, fused, chain> (one launch per step: the whole linear set)"
+                                if chains else
+                                "gemv_kernel<W4, M, fused> (one launch per linear; bytes and time per launch "
+                                "averaged over the step)")},
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(x_all.numel() * 4), "d2h_bytes_per_step": int(y_all.numel() * 4)},
@@ -473,6 +504,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "bytes_per_step": bytes_per_step,
         "tuning": tuning or "auto",
+        "path": "chain" if chains else "per-linear launches (PDL)",
     }
     if per_linear is not None:
         line["per_linear"] = per_linear

@@ -11,10 +11,10 @@ from ._lib import (W4_FLAG_PDL, W4Error, a8_quantize, clear_device_error, device
                    i8g32_linear, i8g32_quantize, i8g32_repack, i8g32_repacked_bytes, q4_0_gemv, q4_0_linear,
                    q4_0_quantize, q4_0_repack, q4_0_repacked_bytes, w4_concat_f32, w4_quantize_rows, w4_repack,
                    w4_repacked_bytes, w4a8_gemv, w4a8_linear)
-from .linear import QuantLinear
+from .linear import LinearChain, QuantLinear
 
 __all__ = [
-    "W4_FLAG_PDL", "W4Error", "QuantLinear", "a8_quantize", "clear_device_error", "device_error",
+    "W4_FLAG_PDL", "W4Error", "LinearChain", "QuantLinear", "a8_quantize", "clear_device_error", "device_error",
     "i8g32_gemv", "i8g32_linear", "i8g32_quantize", "i8g32_repack", "i8g32_repacked_bytes", "q4_0_gemv",
     "q4_0_linear", "q4_0_quantize", "q4_0_repack", "q4_0_repacked_bytes", "w4_concat_f32", "w4_quantize_rows",
     "w4_repack", "w4_repacked_bytes", "w4a8_gemv", "w4a8_linear",

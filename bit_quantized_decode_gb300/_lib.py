@@ -65,6 +65,17 @@ SIGNATURES = {
     "w4_clear_device_error": ([], _I),
 }
 
+
+class LinearDesc(ctypes.Structure):
+    """w4_linear_desc of include/w4a8.h."""
+    _fields_ = [("w", _P), ("s_w", _P), ("bias", _P), ("x", _P), ("y", _P), ("qx", _P), ("sx", _P),
+                ("N", _I), ("K", _I)]
+
+
+SIGNATURES["w4_chain_workspace_bytes"] = ([], _SZ)
+SIGNATURES["w4a8_linear_chain"] = ([ctypes.POINTER(LinearDesc), _I, _I, _P, _SZ, _P], _I)
+W4_MAX_CHAIN = 128
+
 _lib = None
 
 
@@ -266,6 +277,30 @@ def i8g32_linear(w, bias, x, y, qx, sx, flags: int = 0, stream=None):
     N = y.shape[1]
     _check("i8g32_linear", load().i8g32_linear(_ptr(w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx), _ptr(sx),
                                                flags, _stream(stream)))
+
+
+# ---------------------------------------------------------------- chains
+def chain_workspace_bytes() -> int:
+    return int(load().w4_chain_workspace_bytes())
+
+
+def make_chain_descs(items):
+    """items: sequence of (w, s_w, bias, x, y, qx, sx) tensors (bias, qx, sx may be None)."""
+    arr = (LinearDesc * len(items))()
+    for i, (w, s_w, bias, x, y, qx, sx) in enumerate(items):
+        _dev(w, s_w, bias, x, y, qx, sx)
+        arr[i] = LinearDesc(w.data_ptr(), s_w.data_ptr(), None if bias is None else bias.data_ptr(), x.data_ptr(),
+                            y.data_ptr(), None if qx is None else qx.data_ptr(),
+                            None if sx is None else sx.data_ptr(), y.shape[1], x.shape[1])
+    return arr
+
+
+def w4a8_linear_chain(descs, M: int, workspace, stream=None):
+    """Run a chain of per-row INT4 linears (descs from make_chain_descs) in one launch."""
+    _dev(workspace)
+    _check("w4a8_linear_chain", load().w4a8_linear_chain(descs, len(descs), M, _ptr(workspace),
+                                                         workspace.numel() * workspace.element_size(),
+                                                         _stream(stream)))
 
 
 # ---------------------------------------------------------- device errors

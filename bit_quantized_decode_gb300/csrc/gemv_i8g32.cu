@@ -4,9 +4,10 @@
 
 namespace w4k {
 
-cudaError_t launch_gemv_i8g32(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s)
+cudaError_t launch_gemv_i8g32(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
+                          cudaStream_t s)
 {
-    return launch_gemv_fmt<FMT_I8G32>(a, MT, xmode, grid, smem, pdl, s);
+    return launch_gemv_fmt<FMT_I8G32>(p, MT, xmode, grid, smem, pdl, s);
 }
 
 }  // namespace w4k

@@ -90,6 +90,80 @@ __device__ __forceinline__ int unit4_signed16(const uint4 w, const uint4 x0, con
     return g;
 }
 
+// Fused prologue for large M*K: a first pass over x for the absmax, a second
+// to quantize; loads batched four at a time.  One block barrier.
+template <int MT, bool kCodeSums>
+__device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float* red_s, float* sx_s, int8_t* xs,
+                                                       int (&tsum)[MT])
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int M = a.M;
+    const int K = a.K;
+    const int K4 = K >> 2;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float mx = 0.0f;
+        if (m < M) {
+            const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
+            for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
+                float4 b4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kThreads + tid;
+                    b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(b4[u].x), fabsf(b4[u].y)), fmaxf(fabsf(b4[u].z), fabsf(b4[u].w))));
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) red_s[warp * MT + m] = mx;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < M) {
+            float amax = red_s[m];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
+            const A8Scale ks = a8_scale(amax);
+            if (tid == m) {
+                sx_s[m] = ks.s;
+                if (blockIdx.x == 0 && a.sx_out != nullptr) a.sx_out[m] = ks.s;
+            }
+            uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
+            uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
+                                 ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
+                                 : nullptr;
+            const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
+            for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
+                float4 b4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kThreads + tid;
+                    b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kThreads + tid;
+                    if (i < K4) {
+                        const uint32_t q = a8_pack4(b4[u], ks);
+                        dst[i] = q;
+                        if (gout) gout[i] = q;
+                        if constexpr (kCodeSums) tsum[m] += bytesum(q);
+                    }
+                }
+            }
+        } else if (tid == m) {
+            sx_s[m] = 0.0f;
+        }
+    }
+}
+
 // Fused prologue, whole x in registers: NIT float4 per thread and token
 // (a compile-time bound, so no predicated-off iterations are issued).
 // Loads x, reduces the absmax over the block, and writes the int8 codes to
@@ -174,8 +248,77 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
     }
 }
 
-template <int FMT, int MT, int XM>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a)
+// Tile range of this block in one linear: an even split of the T tiles over
+// the grid, processed in rounds of at most RT tiles.
+struct BlockRange {
+    int t0, ntiles, nrounds;
+};
+
+__device__ __forceinline__ BlockRange block_range(int T, int RT)
+{
+    const long long G = gridDim.x;
+    const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * T) / G);
+    const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * T) / G);
+    return BlockRange{t0, t1 - t0, (t1 - t0 + RT - 1) / RT};
+}
+
+// Warp w's line range [lo, hi) within a round of nt tiles of C lines: an even
+// split, boundaries rounded down to whole 16-line passes.
+__device__ __forceinline__ void warp_lines(int warp, int nt, int C, int& lo, int& hi)
+{
+    const long long nL = static_cast<long long>(nt) * C;
+    lo = static_cast<int>((warp * nL / kWarps) & ~15LL);
+    hi = warp == kWarps - 1 ? static_cast<int>(nL) : static_cast<int>(((warp + 1) * nL / kWarps) & ~15LL);
+}
+
+// Grid-wide barrier between the linears of a chain (cooperative launch, so
+// every block is resident), split into arrive and wait so that independent
+// work can run in between.  state[0] counts arrivals over the whole launch:
+// before linear li a block waits until li * gridDim.x blocks have arrived.
+// After the last linear every block arrives once more; the block that makes
+// the count n * gridDim.x is the last one to touch it and resets it to zero,
+// leaving the state ready for the next launch.  Waits are bounded: after
+// kBarrierTimeoutNs the block records an error and goes on.
+constexpr uint64_t kBarrierTimeoutNs = 500ull * 1000ull * 1000ull;
+
+// All of this block's writes before the call are published to the grid.
+__device__ __forceinline__ unsigned grid_arrive(unsigned* count)
+{
+    __syncthreads();
+    unsigned prev = 0;
+    if (threadIdx.x == 0) prev = atom_add_release_gpu(count, 1u);
+    return prev;   // meaningful in thread 0 only
+}
+
+__device__ __forceinline__ bool grid_wait(const unsigned* count, unsigned target, unsigned* err, int* flag_s)
+{
+    if (threadIdx.x == 0) {
+        bool ok = true;
+        if (ld_acquire_gpu(count) < target) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(count) < target) {
+                if (globaltimer_ns() - t0 > kBarrierTimeoutNs) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        if (!ok && err != nullptr) atomicExch(err, kErrBarrierTimeout);
+        *flag_s = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return *flag_s != 0;
+}
+
+// One launch computes a chain of NCH-at-most linears in order.  NCH == 1 is a
+// single linear (launched with programmatic dependent launch, two blocks per
+// SM); larger NCH is the persistent chain (cooperative launch, one block per
+// SM), where linear i+1 starts reading its activations only after every block
+// has written the outputs of linear i, while each warp's ring keeps streaming
+// the next linear's weights across that barrier.
+template <int FMT, int MT, int XM, int NCH>
+__global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ ChainParams<NCH> P)
 {
     using Acc = typename std::conditional<FMT == FMT_W4, int, float>::type;
     constexpr int kUnit = fmt_unit_bytes(FMT);
@@ -186,46 +329,30 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a)
     constexpr bool kGroup = fmt_group(FMT);
     constexpr bool kCodeSums = FMT == FMT_W4;        // activation code sums for the nibble bias
     constexpr int kPassLines = 16;
+    constexpr int kRowBufs = NCH == 1 ? 1 : 2;       // per-row parameter buffers (by linear parity)
+    constexpr int kRowCap = NCH == 1 ? kRowCache : kRowCache / 2;   // rows per buffer
 
     extern __shared__ __align__(128) uint8_t smem[];
-    const int S = a.stages;
-    const int RT = a.round_tiles;
-    const int C = a.C;
-    const int M = a.M;
-    const int K = a.K;
-    const SmemLayout L = smem_layout(FMT, MT, XM, K, S, RT);
+    const int S = P.stages;
+    const int RT = P.round_tiles;
+    const int NL = P.n;
+    const int M = P.lin[0].M;
+    const SmemLayout L = smem_layout(FMT, MT, XM, P.kmax, S, RT, kRowBufs, kRowCap);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     float* sx_s = reinterpret_cast<float*>(smem + L.sx);
     float* red_s = reinterpret_cast<float*>(smem + L.red);
     int* xsum_s = reinterpret_cast<int*>(smem + L.xsum);      // [kWarps][MT] partial code sums (W4)
-    float* bias_s = reinterpret_cast<float*>(smem + L.rowp);  // [kRowCache] this block's bias
-    float* sw_s = bias_s + kRowCache;                         // [kRowCache] and per-row scales (W4)
+    float* rowp_s = reinterpret_cast<float*>(smem + L.rowp);  // [kRowBufs][bias | s_w][kRowCache]
     int* meta_s = reinterpret_cast<int*>(smem + L.meta);
     Acc* acc_s = reinterpret_cast<Acc*>(smem + L.acc);
     Acc* bnd_s = reinterpret_cast<Acc*>(smem + L.bnd);
     uint8_t* ring = smem + L.ring;
     int8_t* xs = reinterpret_cast<int8_t*>(smem + L.xs);
+    __shared__ int flag_s;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-
-    // ---- this block's tiles and rounds
-    const int G = gridDim.x;
-    const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * a.T) / G);
-    const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.T) / G);
-    const int ntiles = t1 - t0;
-    const int nrounds = (ntiles + RT - 1) / RT;
-
-    // Warp w's line range [lo, hi) within a round: an even split, boundaries
-    // rounded down to whole passes.
-    auto warp_range = [&](int round, int& lo, int& hi) {
-        const int nt = min(RT, ntiles - round * RT);
-        const long long nL = static_cast<long long>(nt) * C;
-        const long long mask = ~static_cast<long long>(kPassLines - 1);
-        lo = static_cast<int>((warp * nL / kWarps) & mask);
-        hi = warp == kWarps - 1 ? static_cast<int>(nL) : static_cast<int>(((warp + 1) * nL / kWarps) & mask);
-    };
 
     // ---- per-warp ring of bulk-copy slots
     uint8_t* my_ring = ring + static_cast<size_t>(warp) * S * kSlot;
@@ -235,317 +362,333 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a)
         fence_mbar_init();
     }
     __syncwarp();
-    pdl_launch_dependents();          // the next kernel may become resident beside this one
+    if (NCH == 1) pdl_launch_dependents();   // the next kernel may become resident beside this one
     const uint64_t pol = l2_policy_evict_first();
 
-    // Issue iterator over this warp's slices: round, line position within the
-    // round's range, and (tile, chunk) of that position, advanced without division.
-    int is_round = 0, is_p = 0, is_hi = 0, is_tl = 0, is_c = 0;
-    if (nrounds > 0) {
-        warp_range(0, is_p, is_hi);
-        is_tl = is_p / C;
-        is_c = is_p - is_tl * C;
-    }
-    int issued = 0;
-    auto issue_next = [&]() -> bool {
-        while (is_round < nrounds) {
-            if (is_p < is_hi) {
-                const int n = min(min(is_hi - is_p, C - is_c), kSL);
-                const size_t unit0 = (static_cast<size_t>(t0 + is_round * RT + is_tl) * C + is_c) * kRows;
-                if (lane == 0) {
-                    const int slot = issued % S;
-                    uint8_t* dst = my_ring + static_cast<size_t>(slot) * kSlot;
-                    const uint32_t bar = my_bars + 8 * slot;
-                    const uint32_t bw = static_cast<uint32_t>(n * kLineBytes);
-                    const uint32_t bs = kGroup ? static_cast<uint32_t>(n * kRows * 2) : 0u;
-                    if (issued >= S) fence_proxy_async_smem();   // the slot was read before
-                    mbar_arrive_expect_tx(bar, bw + bs);
-                    bulk_g2s(smem_u32(dst), a.w + unit0 * kUnit, bw, bar, pol);
-                    if (kGroup) bulk_g2s(smem_u32(dst + kSlotW), a.wscale + unit0, bs, bar, pol);
-                }
-                ++issued;
-                is_p += n;
-                is_c += n;
-                if (is_c == C) {
-                    is_c = 0;
-                    ++is_tl;
+    // Slice cursor over this warp's work: linear, round, line position in the
+    // round's range, and (tile, chunk) of that position, advanced without
+    // division; the TMA cursor fills the ring ahead of the consumer.
+    struct Cursor {
+        int lin, round, p, hi, tl, c;
+        BlockRange r;
+        bool done;
+    };
+    auto enter_round = [&](Cursor& k) {
+        const int C = P.lin[k.lin].C;
+        warp_lines(warp, min(RT, k.r.ntiles - k.round * RT), C, k.p, k.hi);
+        k.tl = k.p / C;
+        k.c = k.p - k.tl * C;
+    };
+    auto cursor_start = [&](Cursor& k) {
+        k.lin = 0;
+        k.round = 0;
+        k.done = false;
+        k.r = block_range(P.lin[0].T, RT);
+        if (k.r.nrounds > 0) enter_round(k);
+    };
+    // Next slice of the cursor: linear index, first unit, lines.  False at the end.
+    auto cursor_next = [&](Cursor& k, int& lin, size_t& unit0, int& n) -> bool {
+        while (!k.done) {
+            if (k.round < k.r.nrounds && k.p < k.hi) {
+                const int C = P.lin[k.lin].C;
+                n = min(min(k.hi - k.p, C - k.c), kSL);
+                lin = k.lin;
+                unit0 = (static_cast<size_t>(k.r.t0 + k.round * RT + k.tl) * C + k.c) * kRows;
+                k.p += n;
+                k.c += n;
+                if (k.c == C) {
+                    k.c = 0;
+                    ++k.tl;
                 }
                 return true;
             }
-            ++is_round;
-            if (is_round < nrounds) {
-                warp_range(is_round, is_p, is_hi);
-                is_tl = is_p / C;
-                is_c = is_p - is_tl * C;
+            // next round of this linear, else the next linear with work for this block
+            if (k.round < k.r.nrounds) ++k.round;
+            while (k.round >= k.r.nrounds) {
+                if (++k.lin >= NL) {
+                    k.done = true;
+                    return false;
+                }
+                k.r = block_range(P.lin[k.lin].T, RT);
+                k.round = 0;
             }
+            enter_round(k);
         }
         return false;
     };
 
-    for (int s = 0; s < S; ++s)
+    Cursor icur;
+    cursor_start(icur);
+    int issued = 0, islot = 0;
+    auto issue_next = [&]() -> bool {
+        int lin, n;
+        size_t unit0;
+        if (!cursor_next(icur, lin, unit0, n)) return false;
+        if (lane == 0) {
+            const GemvArgs& ia = P.lin[lin];
+            uint8_t* dst = my_ring + static_cast<size_t>(islot) * kSlot;
+            const uint32_t bar = my_bars + 8 * islot;
+            const uint32_t bw = static_cast<uint32_t>(n * kLineBytes);
+            const uint32_t bs = kGroup ? static_cast<uint32_t>(n * kRows * 2) : 0u;
+            if (issued >= S) fence_proxy_async_smem();   // the slot was read before
+            mbar_arrive_expect_tx(bar, bw + bs);
+            bulk_g2s(smem_u32(dst), ia.w + unit0 * kUnit, bw, bar, pol);
+            if (kGroup) bulk_g2s(smem_u32(dst + kSlotW), ia.wscale + unit0, bs, bar, pol);
+        }
+        ++issued;
+        if (++islot == S) islot = 0;
+        return true;
+    };
+    // In chains the ring runs at most kAhead slices ahead inside a linear and is
+    // topped up to all S slots when the warp finishes its part of a linear, so
+    // the extra slots are requested during the dependency wait (not before it)
+    // and HBM keeps streaming through it.
+    constexpr int kAhead = NCH > 1 ? 3 : kMaxStages;
+    const int ahead = S < kAhead ? S : kAhead;
+    int consumed = 0;
+
+    for (int s = 0; s < ahead; ++s)
         if (!issue_next()) break;
 
-    // per-row epilogue parameters are static: stage them while the previous kernel runs
-    const int row0 = t0 * kRows;
-    const bool rows_cached = ntiles * kRows <= kRowCache;
-    if (rows_cached) {
-        for (int i = tid; i < ntiles * kRows; i += kThreads) {
-            const int row = row0 + i;
-            bias_s[i] = (a.bias != nullptr && row < a.N) ? __ldg(a.bias + row) : 0.0f;
-            if constexpr (FMT == FMT_W4) sw_s[i] = row < a.N ? __ldg(a.s_w + row) : 0.0f;
-        }
-    }
-
-    // ---- inputs produced by earlier kernels are read only from here on
-    pdl_wait();
-
-    // ---- activation prologue: int8 codes into shared memory (fused: quantize
-    // here) and, for W4, per-thread code sums that the epilogue reduces.  All
-    // loads of a token are issued before any store, so one memory round trip
-    // covers the vector; two block barriers in all.
-    const int K4 = K >> 2;
-    const int nit = (K4 + kThreads - 1) / kThreads;
-    int tsum[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) tsum[m] = 0;
-
-    if constexpr (XM == X_FUSED) {
-        constexpr int kRegF4 = 20;                  // float4 of x held per thread
-        constexpr int kIt = kRegF4 / MT;            // per token
-        constexpr int kB1 = kIt / 5 > 0 ? kIt / 5 : 1;
-        constexpr int kB2 = 2 * kIt / 5 > 0 ? 2 * kIt / 5 : 1;
-        constexpr int kB3 = 3 * kIt / 5 > 0 ? 3 * kIt / 5 : 1;
-        if (nit <= kB1) {
-            fused_prologue_regs<MT, kB1, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
-        } else if (nit <= kB2) {
-            fused_prologue_regs<MT, kB2, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
-        } else if (nit <= kB3) {
-            fused_prologue_regs<MT, kB3, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
-        } else if (nit <= kIt) {
-            fused_prologue_regs<MT, kIt, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
-        } else {
-            // large M*K: a first pass for the absmax, a second to quantize; loads batched four at a time
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                float mx = 0.0f;
-                if (m < M) {
-                    const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
-                    for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
-                        float4 b4[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int i = i0 + u * kThreads + tid;
-                            b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(b4[u].x), fabsf(b4[u].y)), fmaxf(fabsf(b4[u].z), fabsf(b4[u].w))));
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                if (lane == 0) red_s[warp * MT + m] = mx;
+    // Per-row epilogue parameters of linear li into buffer li % kRowBufs:
+    // asynchronous 4-byte copies, complete after cp_async_wait_all().
+    auto stage_rows = [&](int li) {
+        const GemvArgs& ra = P.lin[li];
+        const BlockRange rr = block_range(ra.T, RT);
+        if (rr.ntiles * kRows > kRowCap) return;
+        float* b_s = rowp_s + (li & (kRowBufs - 1)) * 2 * kRowCap;
+        float* w_s = b_s + kRowCap;
+        const int r0 = rr.t0 * kRows;
+        for (int i = tid; i < rr.ntiles * kRows; i += kThreads) {
+            const int row = r0 + i;
+            if (row < ra.N) {
+                if (ra.bias != nullptr) cp_async4(b_s + i, ra.bias + row); else b_s[i] = 0.0f;
+                if constexpr (FMT == FMT_W4) cp_async4(w_s + i, ra.s_w + row);
             }
-            __syncthreads();
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < M) {
-                    float amax = red_s[m];
-#pragma unroll
-                    for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
-                    const A8Scale ks = a8_scale(amax);
-                    if (tid == m) {
-                        sx_s[m] = ks.s;
-                        if (blockIdx.x == 0 && a.sx_out != nullptr) a.sx_out[m] = ks.s;
-                    }
-                    uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
-                    uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
-                                         ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
-                                         : nullptr;
-                    const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
-                    for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
-                        float4 b4[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int i = i0 + u * kThreads + tid;
-                            b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int i = i0 + u * kThreads + tid;
-                            if (i < K4) {
-                                const uint32_t q = a8_pack4(b4[u], ks);
-                                dst[i] = q;
-                                if (gout) gout[i] = q;
-                                if constexpr (kCodeSums) tsum[m] += bytesum(q);
-                            }
-                        }
-                    }
-                } else if (tid == m) {
-                    sx_s[m] = 0.0f;
-                }
-            }
-        }
-    } else {
-        if (tid < MT) sx_s[tid] = tid < M ? a.sx_in[tid] : 0.0f;
-        // int8 codes from global memory: into shared memory (smem mode), summed for W4
-        if (XM == X_SMEM || kCodeSums) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < M) {
-                    const uint32_t* qr = reinterpret_cast<const uint32_t*>(a.qx_in + static_cast<size_t>(m) * K);
-                    uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
-                    for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
-                        uint32_t b4[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int i = i0 + u * kThreads + tid;
-                            b4[u] = i < K4 ? __ldg(qr + i) : 0u;
-                        }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int i = i0 + u * kThreads + tid;
-                            if (i < K4) {
-                                if constexpr (XM == X_SMEM) dst[i] = b4[u];
-                                if constexpr (kCodeSums) tsum[m] += bytesum(b4[u]);
-                            }
-                        }
-                    }
-                }
-            }
-        }
-    }
-    if constexpr (kCodeSums) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) tsum[m] += __shfl_xor_sync(0xffffffffu, tsum[m], off);
-            if (lane == 0) xsum_s[warp * MT + m] = tsum[m];
-        }
-    }
-    __syncthreads();
-
-    // Activation chunk (32 int8) of token m at chunk c.
-    auto load_x = [&](int m, int c, uint4& x0, uint4& x1) {
-        if constexpr (XM == X_GLOBAL) {
-            const uint4* p = reinterpret_cast<const uint4*>(a.qx_in + static_cast<size_t>(m) * K + c * 32);
-            x0 = __ldg(p);
-            x1 = __ldg(p + 1);
-        } else {
-            const uint4* p = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * K + c * 32);
-            x0 = p[0];
-            x1 = p[1];
         }
     };
+    stage_rows(0);
 
-    // acc[m][j]: row 4h + (j ^ pp) of the current tile, token m
-    Acc acc[MT][4];
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
+    bool dead = false;      // a bounded wait ran out: stop computing, keep the barrier count
+    int observed = 0;       // slices whose copy was seen complete
+    int cslot = 0;          // consumer position in the ring, and the parity of its phase
+    uint32_t cphase = 0;
+    int round_count = 0;    // rounds so far over all linears (selects the merge buffers)
 
     const int h = lane & 1;               // rows 4h .. 4h+3
     const int pl = lane >> 1;             // line within a pass
     const int pp = pl & 3;                // read-order permutation
     const int my_row = 4 * h + pp;        // row held after the tile-end butterfly (lanes < 8)
 
-    bool dead = false;      // a bounded wait ran out: stop computing, keep the barrier count
-    int consumed = 0;       // slices whose slot has been released
-    int observed = 0;       // slices whose copy was seen complete
+    for (int li = 0; li < NL; ++li) {
+        const GemvArgs& a = P.lin[li];
+        const int C = a.C;
+        const int K = a.K;
+        const BlockRange br = block_range(a.T, RT);
+        const int t0 = br.t0;
+        const int ntiles = br.ntiles;
+        const int nrounds = br.nrounds;
 
-    for (int round = 0; round < nrounds; ++round) {
-        const int buf = round & 1;
-        int lo, hi;
-        warp_range(round, lo, hi);
-        int* meta = meta_s + (buf * kWarps + warp) * 2;
-        if (lane == 0) {
-            meta[0] = -1;
-            meta[1] = -1;
+        // outputs of the previous linear are written: let the grid know
+        if (NCH > 1 && li > 0) grid_arrive(P.barrier);
+
+        // this linear's per-row parameters were staged one linear ahead
+        float* bias_s = rowp_s + (li & (kRowBufs - 1)) * 2 * kRowCap;
+        float* sw_s = bias_s + kRowCap;
+        const int row0 = t0 * kRows;
+        const bool rows_cached = ntiles * kRows <= kRowCap;
+
+        // ---- inputs produced before this linear are read only from here on
+        if (li == 0) {
+            pdl_wait();
+        } else if (!grid_wait(P.barrier, static_cast<unsigned>(li) * gridDim.x, P.err, &flag_s)) {
+            dead = true;
         }
-        __syncwarp();
+        // the next linear's per-row parameters go to the other buffer (its last
+        // reader, linear li-1's epilogue, finished before the barrier above)
+        cp_async_wait_all();
+        if (li + 1 < NL) stage_rows(li + 1);
 
-        int p = lo;
-        int tl = lo / C;
-        int c = lo - tl * C;
-        while (p < hi) {
-            const int n = min(min(hi - p, C - c), kSL);
-            const int slot = consumed % S;
-            const uint32_t parity = static_cast<uint32_t>(consumed / S) & 1u;
+        // ---- activation prologue: int8 codes into shared memory (fused: quantize
+        // here) and, for W4, per-thread code sums that the epilogue reduces.  All
+        // loads of a token are issued before any store, so one memory round trip
+        // covers the vector; two block barriers in all.
+        const int K4 = K >> 2;
+        const int nit = (K4 + kThreads - 1) / kThreads;
+        int tsum[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) tsum[m] = 0;
 
-            if (!dead) {
-                const bool ok = mbar_wait_bounded(my_bars + 8 * slot, parity, kWaitTimeoutNs);
-                if (__all_sync(0xffffffffu, ok)) {
-                    ++observed;
-                } else {
-                    dead = true;   // warp-uniform from here on
-                    if (lane == 0 && a.err != nullptr) atomicExch(a.err, kErrWaitTimeout);
-                }
+        if constexpr (XM == X_FUSED) {
+            constexpr int kRegF4 = 20;                  // float4 of x held per thread
+            constexpr int kIt = kRegF4 / MT;            // per token
+            constexpr int kB1 = kIt / 5 > 0 ? kIt / 5 : 1;
+            constexpr int kB2 = 2 * kIt / 5 > 0 ? 2 * kIt / 5 : 1;
+            constexpr int kB3 = 3 * kIt / 5 > 0 ? 3 * kIt / 5 : 1;
+            if (nit <= kB1) {
+                fused_prologue_regs<MT, kB1, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+            } else if (nit <= kB2) {
+                fused_prologue_regs<MT, kB2, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+            } else if (nit <= kB3) {
+                fused_prologue_regs<MT, kB3, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+            } else if (nit <= kIt) {
+                fused_prologue_regs<MT, kIt, kCodeSums>(a, nit, red_s, sx_s, xs, tsum);
+            } else {
+                fused_prologue_twopass<MT, kCodeSums>(a, red_s, sx_s, xs, tsum);
             }
-            if (!dead) {
-                const uint8_t* sw = my_ring + static_cast<size_t>(slot) * kSlot;
-                const __half* sd = reinterpret_cast<const __half*>(sw + kSlotW);
+        } else {
+            if (tid < MT) sx_s[tid] = tid < M ? a.sx_in[tid] : 0.0f;
+            // int8 codes from global memory: into shared memory (smem mode), summed for W4
+            if (XM == X_SMEM || kCodeSums) {
 #pragma unroll
-                for (int pass = 0; pass < kSL / kPassLines; ++pass) {
-                    const int line = pass * kPassLines + pl;
-                    if (line < n) {
-                        const int chunk = c + line;
-                        const uint8_t* ub = sw + (line * kRows + 4 * h) * kUnit;
-                        if constexpr (FMT == FMT_I8G32) {
-                            uint4 w0[4], w1[4];
-                            float d[4];
+                for (int m = 0; m < MT; ++m) {
+                    if (m < M) {
+                        const uint32_t* qr = reinterpret_cast<const uint32_t*>(a.qx_in + static_cast<size_t>(m) * K);
+                        uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
+                        for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
+                            uint32_t b4[4];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint8_t* u = ub + ((j ^ pp) << 5);
-                                // the two halves are read in a lane-dependent order to spread banks
-                                const uint4 first = *reinterpret_cast<const uint4*>(u + (h << 4));
-                                const uint4 second = *reinterpret_cast<const uint4*>(u + ((h ^ 1) << 4));
-                                w0[j] = h ? second : first;
-                                w1[j] = h ? first : second;
-                                d[j] = __half2float(sd[line * kRows + 4 * h + (j ^ pp)]);
+                            for (int u = 0; u < 4; ++u) {
+                                const int i = i0 + u * kThreads + tid;
+                                b4[u] = i < K4 ? __ldg(qr + i) : 0u;
                             }
 #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                if (MT == 1 || m < M) {
-                                    uint4 x0, x1;
-                                    load_x(m, chunk, x0, x1);
-#pragma unroll
-                                    for (int j = 0; j < 4; ++j) {
-                                        int g = dp4a_ss(w0[j].x, x0.x, 0);
-                                        g = dp4a_ss(w0[j].y, x0.y, g);
-                                        g = dp4a_ss(w0[j].z, x0.z, g);
-                                        g = dp4a_ss(w0[j].w, x0.w, g);
-                                        g = dp4a_ss(w1[j].x, x1.x, g);
-                                        g = dp4a_ss(w1[j].y, x1.y, g);
-                                        g = dp4a_ss(w1[j].z, x1.z, g);
-                                        g = dp4a_ss(w1[j].w, x1.w, g);
-                                        acc[m][j] = __fmaf_rn(d[j], __int2float_rn(g), acc[m][j]);
-                                    }
+                            for (int u = 0; u < 4; ++u) {
+                                const int i = i0 + u * kThreads + tid;
+                                if (i < K4) {
+                                    if constexpr (XM == X_SMEM) dst[i] = b4[u];
+                                    if constexpr (kCodeSums) tsum[m] += bytesum(b4[u]);
                                 }
                             }
-                        } else {
-                            uint4 wv[4];
-                            float d[4];
+                        }
+                    }
+                }
+            }
+        }
+        if constexpr (kCodeSums) {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                wv[j] = *reinterpret_cast<const uint4*>(ub + ((j ^ pp) << 4));
-                                if constexpr (FMT == FMT_Q4_0)
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) tsum[m] += __shfl_xor_sync(0xffffffffu, tsum[m], off);
+                if (lane == 0) xsum_s[warp * MT + m] = tsum[m];
+            }
+        }
+        __syncthreads();
+
+        // Activation chunk (32 int8) of token m at chunk c.
+        auto load_x = [&](int m, int c, uint4& x0, uint4& x1) {
+            if constexpr (XM == X_GLOBAL) {
+                const uint4* p = reinterpret_cast<const uint4*>(a.qx_in + static_cast<size_t>(m) * K + c * 32);
+                x0 = __ldg(p);
+                x1 = __ldg(p + 1);
+            } else {
+                const uint4* p = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * K + c * 32);
+                x0 = p[0];
+                x1 = p[1];
+            }
+        };
+
+        // acc[m][j]: row 4h + (j ^ pp) of the current tile, token m
+        Acc acc[MT][4];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
+
+        if (NCH > 1 && nrounds == 0 && !dead)
+            while (issued - consumed < S && issue_next()) {
+            }
+        for (int round = 0; round < nrounds; ++round, ++round_count) {
+            const int buf = round_count & 1;
+            int lo, hi;
+            warp_lines(warp, min(RT, ntiles - round * RT), C, lo, hi);
+            int* meta = meta_s + (buf * kWarps + warp) * 2;
+            if (lane == 0) {
+                meta[0] = -1;
+                meta[1] = -1;
+            }
+            __syncwarp();
+
+            int p = lo;
+            int tl = lo / C;
+            int c = lo - tl * C;
+            while (p < hi) {
+                const int n = min(min(hi - p, C - c), kSL);
+                const int slot = cslot;
+                if (!dead) {
+                    const bool ok = mbar_wait_bounded(my_bars + 8 * slot, cphase, kWaitTimeoutNs);
+                    if (__all_sync(0xffffffffu, ok)) {
+                        ++observed;
+                    } else {
+                        dead = true;   // warp-uniform from here on
+                        if (lane == 0 && P.err != nullptr) atomicExch(P.err, kErrWaitTimeout);
+                    }
+                }
+                if (!dead) {
+                    const uint8_t* sw = my_ring + static_cast<size_t>(slot) * kSlot;
+                    const __half* sd = reinterpret_cast<const __half*>(sw + kSlotW);
+#pragma unroll
+                    for (int pass = 0; pass < kSL / kPassLines; ++pass) {
+                        const int line = pass * kPassLines + pl;
+                        if (line < n) {
+                            const int chunk = c + line;
+                            const uint8_t* ub = sw + (line * kRows + 4 * h) * kUnit;
+                            if constexpr (FMT == FMT_I8G32) {
+                                uint4 w0[4], w1[4];
+                                float d[4];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint8_t* u = ub + ((j ^ pp) << 5);
+                                    // the two halves are read in a lane-dependent order to spread banks
+                                    const uint4 first = *reinterpret_cast<const uint4*>(u + (h << 4));
+                                    const uint4 second = *reinterpret_cast<const uint4*>(u + ((h ^ 1) << 4));
+                                    w0[j] = h ? second : first;
+                                    w1[j] = h ? first : second;
                                     d[j] = __half2float(sd[line * kRows + 4 * h + (j ^ pp)]);
-                            }
+                                }
 #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                if (MT == 1 || m < M) {
-                                    uint4 x0, x1;
-                                    load_x(m, chunk, x0, x1);
+                                for (int m = 0; m < MT; ++m) {
+                                    if (MT == 1 || m < M) {
+                                        uint4 x0, x1;
+                                        load_x(m, chunk, x0, x1);
 #pragma unroll
-                                    for (int j = 0; j < 4; ++j) {
-                                        if constexpr (FMT == FMT_W4) {
-                                            int B, A;
-                                            unit4(wv[j], x0, x1, B, A);
-                                            acc[m][j] += B + (A >> 4);
-                                        } else {
-                                            const int g = unit4_signed16(wv[j], x0, x1) >> 4;
+                                        for (int j = 0; j < 4; ++j) {
+                                            int g = dp4a_ss(w0[j].x, x0.x, 0);
+                                            g = dp4a_ss(w0[j].y, x0.y, g);
+                                            g = dp4a_ss(w0[j].z, x0.z, g);
+                                            g = dp4a_ss(w0[j].w, x0.w, g);
+                                            g = dp4a_ss(w1[j].x, x1.x, g);
+                                            g = dp4a_ss(w1[j].y, x1.y, g);
+                                            g = dp4a_ss(w1[j].z, x1.z, g);
+                                            g = dp4a_ss(w1[j].w, x1.w, g);
                                             acc[m][j] = __fmaf_rn(d[j], __int2float_rn(g), acc[m][j]);
+                                        }
+                                    }
+                                }
+                            } else {
+                                uint4 wv[4];
+                                float d[4];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    wv[j] = *reinterpret_cast<const uint4*>(ub + ((j ^ pp) << 4));
+                                    if constexpr (FMT == FMT_Q4_0)
+                                        d[j] = __half2float(sd[line * kRows + 4 * h + (j ^ pp)]);
+                                }
+#pragma unroll
+                                for (int m = 0; m < MT; ++m) {
+                                    if (MT == 1 || m < M) {
+                                        uint4 x0, x1;
+                                        load_x(m, chunk, x0, x1);
+#pragma unroll
+                                        for (int j = 0; j < 4; ++j) {
+                                            if constexpr (FMT == FMT_W4) {
+                                                int B, A;
+                                                unit4(wv[j], x0, x1, B, A);
+                                                acc[m][j] += B + (A >> 4);
+                                            } else {
+                                                const int g = unit4_signed16(wv[j], x0, x1) >> 4;
+                                                acc[m][j] = __fmaf_rn(d[j], __int2float_rn(g), acc[m][j]);
+                                            }
                                         }
                                     }
                                 }
@@ -553,104 +696,119 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a)
                         }
                     }
                 }
-            }
-            ++consumed;
-            __syncwarp();
-            if (!dead) issue_next();   // refill the slot just released
+                if (++cslot == S) {
+                    cslot = 0;
+                    cphase ^= 1u;
+                }
+                ++consumed;
+                __syncwarp();
+                if (!dead && issued - consumed < ahead) issue_next();   // refill the slot just released
 
-            p += n;
-            c += n;
-            if (c == C || p == hi) {
-                // tile done for this warp: reduce lanes of equal (h, pp), then undo
-                // the read permutation with a two-step butterfly
+                p += n;
+                c += n;
+                if (c == C || p == hi) {
+                    // tile done for this warp: reduce lanes of equal (h, pp), then undo
+                    // the read permutation with a two-step butterfly
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
+                    for (int m = 0; m < MT; ++m) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if constexpr (FMT == FMT_W4) {
-                            acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 8);
-                            acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 16);
+                        for (int j = 0; j < 4; ++j) {
+                            if constexpr (FMT == FMT_W4) {
+                                acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 8);
+                                acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 16);
+                            } else {
+                                acc[m][j] = __fadd_rn(acc[m][j], __shfl_xor_sync(0xffffffffu, acc[m][j], 8));
+                                acc[m][j] = __fadd_rn(acc[m][j], __shfl_xor_sync(0xffffffffu, acc[m][j], 16));
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const Acc v = __shfl_xor_sync(0xffffffffu, acc[m][j + 2], 4);
+                            if constexpr (FMT == FMT_W4) acc[m][j] += v; else acc[m][j] = __fadd_rn(acc[m][j], v);
+                        }
+                        const Acc v = __shfl_xor_sync(0xffffffffu, acc[m][1], 2);
+                        if constexpr (FMT == FMT_W4) acc[m][0] += v; else acc[m][0] = __fadd_rn(acc[m][0], v);
+                    }
+                    const int tstart = tl * C;
+                    if (lane < kRows) {
+                        const bool full = lo <= tstart && hi >= tstart + C;
+                        Acc* dst;
+                        if (full) {
+                            dst = acc_s + (static_cast<size_t>(buf) * RT * kRows + tl * kRows + my_row) * MT;
                         } else {
-                            acc[m][j] = __fadd_rn(acc[m][j], __shfl_xor_sync(0xffffffffu, acc[m][j], 8));
-                            acc[m][j] = __fadd_rn(acc[m][j], __shfl_xor_sync(0xffffffffu, acc[m][j], 16));
+                            const int which = (lo >= tstart && lo < tstart + C) ? 0 : 1;
+                            dst = bnd_s + (((buf * kWarps + warp) * 2 + which) * kRows + my_row) * MT;
+                            if (lane == 0) meta[which] = tl;
+                        }
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) dst[m] = acc[m][0];
+                    }
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
+                    if (c == C) {
+                        c = 0;
+                        ++tl;
+                    }
+                }
+            }
+
+            // last round of a chained linear: fill the whole ring for the dependency wait
+            if (NCH > 1 && round == nrounds - 1 && !dead)
+                while (issued - consumed < S && issue_next()) {
+                }
+
+            __syncthreads();
+
+            // ---- epilogue for this round's rows (coalesced over rows)
+            const int rt0 = round * RT;
+            const int nrows = min(RT, ntiles - rt0) * kRows;
+            const int row_base = (t0 + rt0) * kRows;
+            for (int idx = tid; idx < M * nrows; idx += kThreads) {
+                const int m = idx / nrows;
+                const int rl = idx - m * nrows;
+                const int row = row_base + rl;
+                if (row >= a.N) continue;
+                const int tile = rl >> 3;
+                const int rr = rl & 7;
+                Acc v = Acc(0);
+                bool part = false;
+                for (int w = 0; w < kWarps; ++w) {
+                    const int* mw = meta_s + (buf * kWarps + w) * 2;
+#pragma unroll
+                    for (int which = 0; which < 2; ++which) {
+                        if (mw[which] == tile) {
+                            const Acc pv = bnd_s[(((buf * kWarps + w) * 2 + which) * kRows + rr) * MT + m];
+                            if constexpr (FMT == FMT_W4) v += pv; else v = __fadd_rn(v, pv);
+                            part = true;
                         }
                     }
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const Acc v = __shfl_xor_sync(0xffffffffu, acc[m][j + 2], 4);
-                        if constexpr (FMT == FMT_W4) acc[m][j] += v; else acc[m][j] = __fadd_rn(acc[m][j], v);
-                    }
-                    const Acc v = __shfl_xor_sync(0xffffffffu, acc[m][1], 2);
-                    if constexpr (FMT == FMT_W4) acc[m][0] += v; else acc[m][0] = __fadd_rn(acc[m][0], v);
                 }
-                const int tstart = tl * C;
-                if (lane < kRows) {
-                    const bool full = lo <= tstart && hi >= tstart + C;
-                    Acc* dst;
-                    if (full) {
-                        dst = acc_s + (static_cast<size_t>(buf) * RT * kRows + tl * kRows + my_row) * MT;
-                    } else {
-                        const int which = (lo >= tstart && lo < tstart + C) ? 0 : 1;
-                        dst = bnd_s + (((buf * kWarps + warp) * 2 + which) * kRows + my_row) * MT;
-                        if (lane == 0) meta[which] = tl;
-                    }
+                if (!part) v = acc_s[(static_cast<size_t>(buf) * RT * kRows + rl) * MT + m];
+                const int ci = row - row0;
+                const float b = rows_cached ? bias_s[ci] : (a.bias != nullptr ? a.bias[row] : 0.0f);
+                float out;
+                if constexpr (FMT == FMT_W4) {
+                    int xsum = 0;
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) dst[m] = acc[m][0];
+                    for (int w = 0; w < kWarps; ++w) xsum += xsum_s[w * MT + m];
+                    const int accv = v - 8 * xsum;          // remove the +8 nibble bias
+                    const float swr = rows_cached ? sw_s[ci] : a.s_w[row];
+                    out = __fmaf_rn(__fmul_rn(swr, sx_s[m]), __int2float_rn(accv), b);
+                } else {
+                    out = __fmaf_rn(sx_s[m], v, b);
                 }
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
-                if (c == C) {
-                    c = 0;
-                    ++tl;
-                }
+                a.y[static_cast<size_t>(m) * a.N + row] = out;
             }
+            // accumulator and merge buffers alternate between rounds: no barrier here
         }
+    }
 
-        __syncthreads();
-
-        // ---- epilogue for this round's rows (coalesced over rows)
-        const int rt0 = round * RT;
-        const int nrows = min(RT, ntiles - rt0) * kRows;
-        const int row_base = (t0 + rt0) * kRows;
-        for (int idx = tid; idx < M * nrows; idx += kThreads) {
-            const int m = idx / nrows;
-            const int rl = idx - m * nrows;
-            const int row = row_base + rl;
-            if (row >= a.N) continue;
-            const int tile = rl >> 3;
-            const int rr = rl & 7;
-            Acc v = Acc(0);
-            bool part = false;
-            for (int w = 0; w < kWarps; ++w) {
-                const int* mw = meta_s + (buf * kWarps + w) * 2;
-#pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    if (mw[which] == tile) {
-                        const Acc pv = bnd_s[(((buf * kWarps + w) * 2 + which) * kRows + rr) * MT + m];
-                        if constexpr (FMT == FMT_W4) v += pv; else v = __fadd_rn(v, pv);
-                        part = true;
-                    }
-                }
-            }
-            if (!part) v = acc_s[(static_cast<size_t>(buf) * RT * kRows + rl) * MT + m];
-            const int ci = row - row0;
-            const float b = rows_cached ? bias_s[ci] : (a.bias != nullptr ? a.bias[row] : 0.0f);
-            float out;
-            if constexpr (FMT == FMT_W4) {
-                int xsum = 0;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) xsum += xsum_s[w * MT + m];
-                const int accv = v - 8 * xsum;          // remove the +8 nibble bias
-                const float swr = rows_cached ? sw_s[ci] : a.s_w[row];
-                out = __fmaf_rn(__fmul_rn(swr, sx_s[m]), __int2float_rn(accv), b);
-            } else {
-                out = __fmaf_rn(sx_s[m], v, b);
-            }
-            a.y[static_cast<size_t>(m) * a.N + row] = out;
-        }
-        // accumulator and merge buffers alternate between rounds: no barrier here
+    // ---- chains: the final arrival; the block that completes the count resets it
+    if (NCH > 1) {
+        const unsigned prev = grid_arrive(P.barrier);
+        if (threadIdx.x == 0 && prev + 1u == static_cast<unsigned>(NL) * gridDim.x) atomicExch(P.barrier, 0u);
     }
 
     // ---- after a timeout: wait (bounded) for copies still in flight into this warp's ring
@@ -662,10 +820,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a)
     }
 }
 
-template <int FMT, int MT, int XM>
-cudaError_t launch_gemv_t(const GemvArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s)
+template <int FMT, int MT, int XM, int NCH>
+cudaError_t launch_gemv_t(const ChainParams<NCH>& p, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-    auto kern = gemv_kernel<FMT, MT, XM>;
+    auto kern = gemv_kernel<FMT, MT, XM, NCH>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -681,21 +839,28 @@ cudaError_t launch_gemv_t(const GemvArgs& a, int grid, size_t smem, bool pdl, cu
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = pdl ? attr : nullptr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    if (NCH == 1) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    }
+    const bool use_attr = NCH != 1 || pdl;
+    cfg.attrs = use_attr ? attr : nullptr;
+    cfg.numAttrs = use_attr ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int FMT>
-cudaError_t launch_gemv_fmt(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s)
+cudaError_t launch_gemv_fmt(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
+                            cudaStream_t s)
 {
-#define W4_CASE(mt)                                                                              \
-    case mt:                                                                                     \
-        return xmode == X_FUSED  ? launch_gemv_t<FMT, mt, X_FUSED>(a, grid, smem, pdl, s)        \
-               : xmode == X_SMEM ? launch_gemv_t<FMT, mt, X_SMEM>(a, grid, smem, pdl, s)         \
-                                 : launch_gemv_t<FMT, mt, X_GLOBAL>(a, grid, smem, pdl, s);
+#define W4_CASE(mt)                                                                               \
+    case mt:                                                                                      \
+        return xmode == X_FUSED  ? launch_gemv_t<FMT, mt, X_FUSED, 1>(p, grid, smem, pdl, s)      \
+               : xmode == X_SMEM ? launch_gemv_t<FMT, mt, X_SMEM, 1>(p, grid, smem, pdl, s)       \
+                                 : launch_gemv_t<FMT, mt, X_GLOBAL, 1>(p, grid, smem, pdl, s);
     switch (MT) {
         W4_CASE(1)
         W4_CASE(2)
@@ -706,6 +871,19 @@ cudaError_t launch_gemv_fmt(const GemvArgs& a, int MT, int xmode, int grid, size
             return cudaErrorInvalidValue;
     }
 #undef W4_CASE
+}
+
+template <int FMT>
+cudaError_t launch_chain_fmt(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s)
+{
+    switch (MT) {
+        case 1: return launch_gemv_t<FMT, 1, X_FUSED, kMaxChain>(p, grid, smem, false, s);
+        case 2: return launch_gemv_t<FMT, 2, X_FUSED, kMaxChain>(p, grid, smem, false, s);
+        case 4: return launch_gemv_t<FMT, 4, X_FUSED, kMaxChain>(p, grid, smem, false, s);
+        case 8: return launch_gemv_t<FMT, 8, X_FUSED, kMaxChain>(p, grid, smem, false, s);
+        case 16: return launch_gemv_t<FMT, 16, X_FUSED, kMaxChain>(p, grid, smem, false, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace w4k

@@ -4,9 +4,15 @@
 
 namespace w4k {
 
-cudaError_t launch_gemv_w4(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s)
+cudaError_t launch_gemv_w4(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
+                          cudaStream_t s)
 {
-    return launch_gemv_fmt<FMT_W4>(a, MT, xmode, grid, smem, pdl, s);
+    return launch_gemv_fmt<FMT_W4>(p, MT, xmode, grid, smem, pdl, s);
+}
+
+cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s)
+{
+    return launch_chain_fmt<FMT_W4>(p, MT, grid, smem, s);
 }
 
 }  // namespace w4k

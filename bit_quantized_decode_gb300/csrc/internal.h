@@ -27,7 +27,7 @@ __host__ __device__ constexpr int fmt_slot_w_bytes(int fmt) { return fmt_slice_l
 __host__ __device__ constexpr int fmt_slot_s_bytes(int fmt) { return fmt_group(fmt) ? fmt_slice_lines(fmt) * kRows * 2 : 0; }
 __host__ __device__ constexpr int fmt_slot_bytes(int fmt) { return fmt_slot_w_bytes(fmt) + fmt_slot_s_bytes(fmt); }
 
-// Arguments of one GEMV launch (passed by value).
+// One linear of a launch.
 struct GemvArgs {
     const uint8_t* w;        // repacked units
     const uint16_t* wscale;  // fp16 group-scale plane (Q4_0, I8G32), else null
@@ -42,8 +42,18 @@ struct GemvArgs {
     int M, N, K;
     int C;                   // K / 32
     int T;                   // ceil(N / 8)
+};
+
+// Kernel parameters: up to NCH linears computed in order by one launch.
+constexpr int kMaxChain = 128;
+template <int NCH>
+struct ChainParams {
+    GemvArgs lin[NCH];
+    int n;                   // linears in this launch (1..NCH)
+    int kmax;                // largest K: sizes the shared-memory activation buffer
     int stages;              // ring slots per warp
     int round_tiles;         // tiles per accumulation round
+    unsigned* barrier;       // grid barrier state [2] (chains only)
     unsigned* err;           // device error word
 };
 
@@ -53,7 +63,8 @@ struct SmemLayout {
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, int K, int stages, int round_tiles)
+__host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, int K, int stages, int round_tiles,
+                                                  int row_bufs = 1, int row_cap = kRowCache)
 {
     SmemLayout L;
     int o = 0;
@@ -61,7 +72,7 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, in
     L.sx = o;    o = align_up(o + MT * 4, 16);
     L.red = o;   o = align_up(o + kWarps * MT * 4, 16);
     L.xsum = o;  o = align_up(o + kWarps * MT * 4, 16);
-    L.rowp = o;  o = align_up(o + kRowCache * 4 * (fmt == FMT_W4 ? 2 : 1), 16);
+    L.rowp = o;  o = align_up(o + row_bufs * 2 * row_cap * 4, 16);
     L.meta = o;  o = align_up(o + 2 * kWarps * 2 * 4, 16);
     L.acc = o;   o = align_up(o + 2 * round_tiles * kRows * MT * 4, 16);
     L.bnd = o;   o = align_up(o + 2 * kWarps * 2 * kRows * MT * 4, 128);
@@ -72,13 +83,18 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, in
 }
 
 // Error codes written to the device error word.
-constexpr unsigned kErrWaitTimeout = 0x57414954u;  // "WAIT"
+constexpr unsigned kErrWaitTimeout = 0x57414954u;     // "WAIT": an mbarrier wait ran out
+constexpr unsigned kErrBarrierTimeout = 0x42415252u;  // "BARR": a grid barrier wait ran out
 
 // Kernel launchers, one translation unit per format.
-cudaError_t launch_gemv_w4(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s);
-cudaError_t launch_gemv_q4_0(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl, cudaStream_t s);
-cudaError_t launch_gemv_i8g32(const GemvArgs& a, int MT, int xmode, int grid, size_t smem, bool pdl,
+cudaError_t launch_gemv_w4(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
+                           cudaStream_t s);
+cudaError_t launch_gemv_q4_0(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
+                             cudaStream_t s);
+cudaError_t launch_gemv_i8g32(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
                               cudaStream_t s);
+// Chains of per-row INT4 linears (cooperative launch, fused quantization).
+cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
 
 // Load-time and activation kernels (prep_kernels.cu).
 constexpr int kMaxShards = 8;

@@ -90,6 +90,35 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (cp.async), and its completion.
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Atomic add with release semantics at GPU scope: writes made visible to this
+// thread (including a block's writes ordered by a preceding __syncthreads) are
+// visible to any thread that later observes the new value with an acquire.
+__device__ __forceinline__ unsigned atom_add_release_gpu(unsigned* p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Acquire load at GPU scope (pairs with __threadfence + atomics on the writer).
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_wait()
 {

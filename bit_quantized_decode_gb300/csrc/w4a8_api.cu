@@ -97,11 +97,11 @@ struct Plan {
 };
 
 // Largest ring (at most the cap) whose layout fits `budget`; 0 if fewer than 2 stages fit.
-int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget)
+int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget, int row_bufs = 1, int row_cap = kRowCache)
 {
     const int cap = g_tune[W4_TUNE_MAX_STAGES] > 0 ? g_tune[W4_TUNE_MAX_STAGES] : kMaxStages;
     int s = cap < kMaxStages ? cap : kMaxStages;
-    while (s >= 2 && smem_layout(fmt, MT, xmode, K, s, RT).total > budget) --s;
+    while (s >= 2 && smem_layout(fmt, MT, xmode, K, s, RT, row_bufs, row_cap).total > budget) --s;
     return s >= 2 ? s : 0;
 }
 
@@ -143,20 +143,66 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     const int MT = round_pow2_tokens(a.M);
     a.C = a.K / 32;
     a.T = static_cast<int>(tiles(a.N));
-    a.round_tiles = kAccWords / MT;
-    a.err = dev->err;
+    ChainParams<1> cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.lin[0] = a;
+    cp.n = 1;
+    cp.kmax = a.K;
+    cp.round_tiles = kAccWords / MT;
+    cp.err = dev->err;
     Plan p;
-    if (!plan_gemv(*dev, fmt, MT, fused, a.K, a.round_tiles, p)) return W4_ERR_UNSUPPORTED_SHAPE;
-    a.stages = p.stages;
+    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    cp.stages = p.stages;
     int grid = dev->sms;
     if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
     if (a.T < grid) grid = a.T;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
     cudaError_t e;
-    if (fmt == FMT_W4) e = launch_gemv_w4(a, MT, p.xmode, grid, p.smem, pdl, s);
-    else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(a, MT, p.xmode, grid, p.smem, pdl, s);
-    else e = launch_gemv_i8g32(a, MT, p.xmode, grid, p.smem, pdl, s);
+    if (fmt == FMT_W4) e = launch_gemv_w4(cp, MT, p.xmode, grid, p.smem, pdl, s);
+    else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(cp, MT, p.xmode, grid, p.smem, pdl, s);
+    else e = launch_gemv_i8g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
     return cuda_status(e);
+}
+
+// Chain of per-row INT4 linears in one cooperative launch.
+w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cudaStream_t s)
+{
+    DeviceInfo* dev = nullptr;
+    w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    const int MT = round_pow2_tokens(M);
+    static ChainParams<kMaxChain> cp;     // host staging only; copied into the launch
+    std::memset(&cp, 0, sizeof(cp));
+    int kmax = 32;
+    for (int i = 0; i < n; ++i) {
+        GemvArgs& a = cp.lin[i];
+        a.w = static_cast<const uint8_t*>(d[i].w);
+        a.s_w = d[i].s_w;
+        a.bias = d[i].bias;
+        a.x = d[i].x;
+        a.qx_out = d[i].qx;
+        a.sx_out = d[i].sx;
+        a.y = d[i].y;
+        a.M = M;
+        a.N = d[i].N;
+        a.K = d[i].K;
+        a.C = a.K / 32;
+        a.T = static_cast<int>(tiles(a.N));
+        if (a.K > kmax) kmax = a.K;
+    }
+    cp.n = n;
+    cp.kmax = kmax;
+    cp.round_tiles = kAccWords / MT;
+    cp.barrier = barrier;
+    cp.err = dev->err;
+    // one block per SM with the whole shared memory, the x buffer sized for the largest K
+    const int s_max = stages_for(FMT_W4, MT, X_FUSED, kmax, cp.round_tiles, dev->smem_optin, 2, kRowCache / 2);
+    if (s_max < 2) return W4_ERR_UNSUPPORTED_SHAPE;
+    cp.stages = s_max;
+    const int smem = smem_layout(FMT_W4, MT, X_FUSED, kmax, s_max, cp.round_tiles, 2, kRowCache / 2).total;
+    int grid = dev->sms;
+    if (g_tune[W4_TUNE_GRID_BLOCKS] > 0 && g_tune[W4_TUNE_GRID_BLOCKS] < grid) grid = g_tune[W4_TUNE_GRID_BLOCKS];
+    return cuda_status(launch_chain_w4(cp, MT, grid, static_cast<size_t>(smem), s));
 }
 
 // Would the fused kernel (x quantized into shared memory) fit?
@@ -431,6 +477,31 @@ w4_status i8g32_linear(const void* w, const float* bias, const float* x, int M, 
 {
     return linear_common(FMT_I8G32, w, nullptr, bias, x, M, N, K, y, qx, sx, flags,
                          reinterpret_cast<cudaStream_t>(s));
+}
+
+// ----------------------------------------------------------------- chains
+size_t w4_chain_workspace_bytes(void) { return 256; }
+
+w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* workspace, size_t ws_bytes,
+                            w4_stream_t s)
+{
+    if (n < 0 || M < 0 || (n > 0 && descs == nullptr)) return W4_ERR_INVALID_ARG;
+    if (n > W4_MAX_CHAIN || M > W4_MAX_M) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0 || M == 0) return W4_OK;
+    if (workspace == nullptr) return W4_ERR_INVALID_ARG;
+    if (ws_bytes < w4_chain_workspace_bytes()) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(workspace, 16)) return W4_ERR_MISALIGNED;
+    for (int i = 0; i < n; ++i) {
+        const w4_linear_desc& d = descs[i];
+        w4_status st = check_mk(M, d.K);
+        if (st != W4_OK) return st;
+        if (d.N <= 0) return d.N < 0 ? W4_ERR_INVALID_ARG : W4_ERR_UNSUPPORTED_SHAPE;
+        if (!d.w || !d.s_w || !d.x || !d.y) return W4_ERR_INVALID_ARG;
+        if (!aligned(d.w, 16) || !aligned(d.x, 16) || !aligned(d.y, 4) || !aligned(d.s_w, 4) ||
+            (d.bias && !aligned(d.bias, 4)) || (d.qx && !aligned(d.qx, 16)) || (d.sx && !aligned(d.sx, 4)))
+            return W4_ERR_MISALIGNED;
+    }
+    return run_chain(descs, n, M, static_cast<unsigned*>(workspace), reinterpret_cast<cudaStream_t>(s));
 }
 
 // ------------------------------------------------------ device error word

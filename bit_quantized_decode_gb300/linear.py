@@ -122,3 +122,25 @@ class QuantLinear:
     def weight_bytes(self) -> int:
         """Bytes the GEMV streams: repacked weights (+ group scales) and per-row scales."""
         return self.w.numel() + (self.s_w.numel() * 4 if self.s_w is not None else 0)
+
+
+class LinearChain:
+    """A fixed sequence of per-row INT4 linears launched as one chain
+    (w4a8_linear_chain).  Linear i+1 may read (part of) linear i's output:
+    the chain orders every input read after the previous linear completes.
+
+    items: sequence of (QuantLinear, x, y, qx, sx) with x [M][K] and y [M][N]."""
+
+    def __init__(self, items, M: int):
+        if not items:
+            raise ValueError("empty chain")
+        if len(items) > _lib.W4_MAX_CHAIN:
+            raise ValueError(f"at most {_lib.W4_MAX_CHAIN} linears per chain")
+        dev = items[0][0].w.device
+        self.M = M
+        self.items = list(items)
+        self.descs = _lib.make_chain_descs([(ql.w, ql.s_w, ql.bias, x, y, qx, sx) for ql, x, y, qx, sx in items])
+        self.workspace = torch.zeros(_lib.chain_workspace_bytes(), dtype=torch.uint8, device=dev)
+
+    def __call__(self, stream=None):
+        _lib.w4a8_linear_chain(self.descs, self.M, self.workspace, stream)

@@ -194,6 +194,40 @@ w4_status i8g32_linear(const void* w, const float* bias, const float* x, int M, 
                        float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
 
 /* ------------------------------------------------------------------------
+ * A chain of per-row INT4 decode linears in one launch (a decode step's
+ * linear set).  Linear i computes exactly what w4a8_linear computes for
+ * descs[i]; linear i+1 reads its x only after every output of linear i is
+ * written, so descs[i+1].x may alias (part of) descs[i].y.  While a linear's
+ * activations wait on that dependency, the weights of the following linears
+ * keep streaming (one persistent block per SM, cooperative launch).
+ *
+ * descs: HOST array of n (1..W4_MAX_CHAIN) descriptors, all with the same
+ * M tokens.  Per descriptor: w (repacked W4, 16-B aligned), s_w [N], bias [N]
+ * or NULL, x [M][K] (16-B aligned), y [M][N], and qx [M][K] / sx [M] to
+ * receive the activation codes, or NULL.
+ * workspace: device memory of w4_chain_workspace_bytes() bytes, 16-B aligned,
+ * zero-filled before its first use; each call leaves it zero again, ready for
+ * the next.  Calls that share a workspace must not overlap on the GPU.  After
+ * a call that reported W4_ERR_DEVICE_TIMEOUT, zero the workspace again.
+ * ------------------------------------------------------------------------ */
+#define W4_MAX_CHAIN 128
+typedef struct {
+    const void* w;
+    const float* s_w;
+    const float* bias;
+    const float* x;
+    float* y;
+    int8_t* qx;
+    float* sx;
+    int N;
+    int K;
+} w4_linear_desc;
+
+size_t w4_chain_workspace_bytes(void);
+w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* workspace, size_t ws_bytes,
+                            w4_stream_t s);
+
+/* ------------------------------------------------------------------------
  * Device error word.  Kernels that give up a bounded wait (about 0.25 s on an
  * mbarrier) record a nonzero code here and return early; their outputs are
  * then undefined.  w4_device_error synchronises the current device, reads the

@@ -135,6 +135,28 @@ def test_repack_argument_checks(lib):
     assert lib.i8g32_repack(ppc, None, rows, 1, 64, FAKE, 1 << 20, None) == 1
 
 
+def test_chain_argument_checks(lib):
+    from bit_quantized_decode_gb300 import _lib
+    d = (_lib.LinearDesc * 2)()
+    for i in range(2):
+        d[i] = _lib.LinearDesc(0x1000, 0x1000, None, 0x1000, 0x1000, None, None, 8, 64)
+    ws = FAKE
+    assert lib.w4_chain_workspace_bytes() >= 8
+    assert lib.w4a8_linear_chain(d, 0, 1, ws, 256, None) == 0                    # empty chain
+    assert lib.w4a8_linear_chain(d, 2, 0, ws, 256, None) == 0                    # no tokens
+    assert lib.w4a8_linear_chain(d, 129, 1, ws, 256, None) == 2                  # chain too long
+    assert lib.w4a8_linear_chain(d, 2, 17, ws, 256, None) == 2                   # M > 16
+    assert lib.w4a8_linear_chain(d, 2, 1, None, 256, None) == 1                  # no workspace
+    assert lib.w4a8_linear_chain(d, 2, 1, ws, 8, None) == 2                      # workspace too small
+    assert lib.w4a8_linear_chain(d, 2, 1, ODD, 256, None) == 3                   # misaligned workspace
+    d[1] = _lib.LinearDesc(0x1000, 0x1000, None, 0x1000, 0x1000, None, None, 8, 48)
+    assert lib.w4a8_linear_chain(d, 2, 1, ws, 256, None) == 2                    # K % 32 != 0
+    d[1] = _lib.LinearDesc(0x1000, None, None, 0x1000, 0x1000, None, None, 8, 64)
+    assert lib.w4a8_linear_chain(d, 2, 1, ws, 256, None) == 1                    # no s_w
+    d[1] = _lib.LinearDesc(0x1004, 0x1000, None, 0x1000, 0x1000, None, None, 8, 64)
+    assert lib.w4a8_linear_chain(d, 2, 1, ws, 256, None) == 3                    # misaligned weights
+
+
 def test_product_never_imports_the_oracle():
     pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle\b|from\s+\.\.?\s*import\s+oracle)|liboracle|oracle/",
                      re.M)

@@ -73,6 +73,8 @@ class LinearDesc(ctypes.Structure):
 
 
 SIGNATURES["w4_chain_workspace_bytes"] = ([], _SZ)
+SIGNATURES["w4_chain_noalloc_scratch_bytes"] = ([], _SZ)
+SIGNATURES["w4a8_linear_chain_noalloc"] = ([ctypes.POINTER(LinearDesc), _I, _I, _P], _I)
 SIGNATURES["w4a8_linear_chain"] = ([ctypes.POINTER(LinearDesc), _I, _I, _P, _SZ, _P], _I)
 W4_MAX_CHAIN = 128
 
@@ -301,6 +303,13 @@ def w4a8_linear_chain(descs, M: int, workspace, stream=None):
     _check("w4a8_linear_chain", load().w4a8_linear_chain(descs, len(descs), M, _ptr(workspace),
                                                          workspace.numel() * workspace.element_size(),
                                                          _stream(stream)))
+
+
+def w4a8_linear_chain_noalloc(descs, M: int, stream=None):
+    """w4a8_linear_chain with the library's own fixed barrier scratch: for
+    callers that cannot allocate device memory.  Calls sharing the scratch
+    must not overlap on the GPU."""
+    _check("w4a8_linear_chain_noalloc", load().w4a8_linear_chain_noalloc(descs, len(descs), M, _stream(stream)))
 
 
 # ---------------------------------------------------------- device errors

@@ -504,6 +504,49 @@ w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* wor
     return run_chain(descs, n, M, static_cast<unsigned*>(workspace), reinterpret_cast<cudaStream_t>(s));
 }
 
+// ------------------------------------------- chains without caller memory
+// For callers that cannot allocate device memory (see w4a8.h): the chain's
+// grid-barrier state lives in this fixed array instead of a caller workspace.
+// In host code `g_chain_scratch` is only a host-side stand-in for the symbol;
+// the kernel gets the device address from cudaGetSymbolAddress.
+constexpr size_t kChainScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_chain_scratch[kChainScratchBytes];
+
+namespace {
+unsigned* g_chain_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device, looked up once per device.
+w4_status chain_scratch(unsigned** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W4_ERR_CUDA;
+    if (g_chain_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_chain_scratch) != cudaSuccess || p == nullptr) return W4_ERR_CUDA;
+        g_chain_scratch_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    *out = g_chain_scratch_ptr[dev];
+    return W4_OK;
+}
+}  // namespace
+
+size_t w4_chain_noalloc_scratch_bytes(void) { return kChainScratchBytes; }
+
+w4_status w4a8_linear_chain_noalloc(const w4_linear_desc* descs, int n, int M, w4_stream_t s)
+{
+    if (w4_chain_workspace_bytes() > kChainScratchBytes) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (n < 0 || M < 0 || (n > 0 && descs == nullptr)) return W4_ERR_INVALID_ARG;
+    if (n > W4_MAX_CHAIN || M > W4_MAX_M) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0 || M == 0) return W4_OK;
+    unsigned* scratch = nullptr;
+    w4_status st = chain_scratch(&scratch);
+    if (st != W4_OK) return st;
+    // the array keeps the previous call's contents: the barrier count must start at zero
+    if (cudaMemsetAsync(scratch, 0, w4_chain_workspace_bytes(), reinterpret_cast<cudaStream_t>(s)) != cudaSuccess)
+        return W4_ERR_CUDA;
+    return w4a8_linear_chain(descs, n, M, scratch, kChainScratchBytes, s);
+}
+
 // ------------------------------------------------------ device error word
 w4_status w4_device_error(unsigned* code)
 {

@@ -228,6 +228,30 @@ w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* wor
                             w4_stream_t s);
 
 /* ------------------------------------------------------------------------
+ * w4a8_linear_chain without caller-provided device memory.  The source pages
+ * have no counterpart of this entry point: it exists for callers that cannot
+ * allocate device memory at the point of the call -- for example code running
+ * under an engine whose memory planner owns every device allocation, or code
+ * that must not call cudaMalloc while a stream is being captured into a CUDA
+ * graph -- and therefore cannot provide the chain's workspace.
+ *
+ * The grid-barrier state lives in a fixed array of
+ * w4_chain_noalloc_scratch_bytes() (256) bytes inside the library; every GPU
+ * that loads the library holds it until the process exits.  Each call clears
+ * it (cudaMemsetAsync on `s`) and then runs exactly w4a8_linear_chain.  The
+ * call allocates nothing and frees nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race on it and must be serialised by the caller.
+ *   - A workspace need above the array's size is rejected with
+ *     W4_ERR_UNSUPPORTED_SHAPE; all other arguments are checked as in
+ *     w4a8_linear_chain.
+ * ------------------------------------------------------------------------ */
+size_t w4_chain_noalloc_scratch_bytes(void);
+w4_status w4a8_linear_chain_noalloc(const w4_linear_desc* descs, int n, int M, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
  * Device error word.  Kernels that give up a bounded wait (about 0.25 s on an
  * mbarrier) record a nonzero code here and return early; their outputs are
  * then undefined.  w4_device_error synchronises the current device, reads the

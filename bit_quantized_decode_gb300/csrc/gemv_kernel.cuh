@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = P.stages;
     const int RT = P.round_tiles;
-    const int NL = P.n;
+    const int NL = NCH == 1 ? 1 : P.n;
     const int M = P.lin[0].M;
     const SmemLayout L = smem_layout(FMT, MT, XM, P.kmax, S, RT, kRowBufs, kRowCap);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);

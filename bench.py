@@ -6,9 +6,12 @@ One step = the decode linears of a Qwen2-7B-shaped model: 28 layers x
 plus the lm_head 152064x3584, per-row INT4 weights, M tokens (default 1),
 each linear one fused quantize + GEMV launch of libw4a8.so.  The 113
 launches are chained with programmatic dependent launch and replayed from a
-CUDA graph.  Weights (3.5 GB) and activations are synthetic (seeded normal
-draws quantized on the GPU) and resident in HBM; they exceed L2, so no L2
-flush is needed between steps.
+CUDA graph.  As in a decoder, each linear reads what the previous one wrote:
+its x[M][K] is the first M*K values of the previous linear's output (the
+attention, norm and activation between them are not part of this path);
+the first linear reads the step's input x[M][3584] ~ N(0, 1).  Weights
+(3.5 GB) are synthetic (seeded N(0, 0.02) draws quantized on the GPU) and
+resident in HBM; they exceed L2, so no L2 flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
 instead (host cores, bounded sample per step).
@@ -49,6 +52,8 @@ def parse_args(argv=None):
     p.add_argument("--chain", action="store_true",
                    help="one chained launch per step (w4a8_linear_chain) instead of one PDL launch per linear")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--independent-x", action="store_true",
+                   help="every linear reads its own static input buffer instead of the previous output")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--per-linear", action="store_true", help="also time each linear kind on its own")
@@ -86,6 +91,8 @@ def workload_config(args, n_gpus):
         "lm_head": not args.no_lm_head,
         "linears_per_step": 4 * args.layers + (0 if args.no_lm_head else 1),
         "l2": "inputs larger than L2 (3.5 GB of weights per step), no flush",
+        "dataflow": ("independent static inputs" if args.independent_x else
+                     "each linear reads the previous linear's output (first M*K values)"),
         "parallelism": f"replicas x{n_gpus}",
     }
 
@@ -250,18 +257,24 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------- our arm
 def build_step(args, device):
+    """Resident weights and per-linear buffers.  Returns (items, x_in, y_out):
+    x_in is the step's input, y_out the last linear's output (the logits
+    with the lm_head); with --independent-x, x_in and y_out hold every
+    linear's input and output instead."""
     import torch
 
     from bit_quantized_decode_gb300 import QuantLinear
     seq = step_linears(args.layers, not args.no_lm_head)
     M = args.M
-    total_x = sum(M * lin.K for _, lin in seq)
-    total_y = sum(M * lin.N for _, lin in seq)
-    x_all = torch.empty(total_x, dtype=torch.float32, device=device)
-    y_all = torch.empty(total_y, dtype=torch.float32, device=device)
+    if args.independent_x:
+        x_all = torch.empty(sum(M * lin.K for _, lin in seq), dtype=torch.float32, device=device)
+        y_all = torch.empty(sum(M * lin.N for _, lin in seq), dtype=torch.float32, device=device)
+    else:
+        x_all = torch.empty(M * seq[0][1].K, dtype=torch.float32, device=device)
     items = []
     xo = yo = 0
     seed = 1000
+    prev_y = None
     for layer, lin in seq:
         shards = []
         for rows in lin.shards:
@@ -271,17 +284,27 @@ def build_step(args, device):
         seed += len(lin.shards)
         ql = QuantLinear.from_float("w4", shards, biases)
         del shards
-        x = x_all[xo: xo + M * lin.K].view(M, lin.K)
-        x.copy_(wl.torch_normal((M, lin.K), 1.0, seed, device))
+        if args.independent_x or prev_y is None:
+            x = x_all[xo: xo + M * lin.K].view(M, lin.K)
+            x.copy_(wl.torch_normal((M, lin.K), 1.0, seed, device))
+            xo += M * lin.K
+        else:
+            if prev_y.numel() < M * lin.K:
+                raise ValueError(f"{lin.name}: the previous output has fewer than M*K values")
+            x = prev_y.view(-1)[: M * lin.K].view(M, lin.K)
         seed += 1
-        y = y_all[yo: yo + M * lin.N].view(M, lin.N)
+        if args.independent_x:
+            y = y_all[yo: yo + M * lin.N].view(M, lin.N)
+            yo += M * lin.N
+        else:
+            y = torch.empty((M, lin.N), dtype=torch.float32, device=device)
         qx = torch.empty((M, lin.K), dtype=torch.int8, device=device)
         sx = torch.empty(M, dtype=torch.float32, device=device)
         items.append((layer, lin, ql, x, y, qx, sx))
-        xo += M * lin.K
-        yo += M * lin.N
+        prev_y = y
     torch.cuda.synchronize()
-    return items, x_all, y_all
+    y_out = y_all if args.independent_x else prev_y.view(-1)
+    return items, x_all, y_out
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:

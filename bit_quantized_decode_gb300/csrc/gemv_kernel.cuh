@@ -215,31 +215,36 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
             uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
                                  ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
                                  : nullptr;
-            uint32_t need = a8_needs_exact(ks) ? 0xffffffffu : 0u;
-            uint32_t qw[NIT];
+            const uint32_t all_exact = a8_needs_exact(ks) ? 0xffffffffu : 0u;
+            // Groups of kG words: the fast codes of a group are straight-line code
+            // (independent chains, no branch between them); words with a possible
+            // tie (or every word, for a tiny scale) are then redone exactly from
+            // the values still in registers.
+            constexpr int kG = NIT < 5 ? NIT : 5;
 #pragma unroll
-            for (int it = 0; it < NIT; ++it) {
-                bool tie = false;
-                qw[it] = a8_pack4_fast(v[m][it], ks, tie);
-                need |= tie ? (1u << it) : 0u;
-            }
-            if (need) {
-                // rare: words with a possible tie (or a tiny scale) get the exact codes;
-                // x is read again so that v need not stay live across this branch
-                const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
+            for (int g0 = 0; g0 < NIT; g0 += kG) {
+                uint32_t qw[kG];
+                uint32_t need = all_exact;
 #pragma unroll
-                for (int it = 0; it < NIT; ++it) {
-                    const int i = tid + it * kThreads;
-                    if (((need >> it) & 1u) && it < nit && i < K4) qw[it] = a8_pack4(__ldcg(xr + i), ks);
+                for (int u = 0; u < kG; ++u) {
+                    bool tie = false;
+                    if (g0 + u < NIT) qw[u] = a8_pack4_fast(v[m][g0 + u], ks, tie);
+                    need |= tie ? (1u << u) : 0u;
                 }
-            }
+                if (need) {
 #pragma unroll
-            for (int it = 0; it < NIT; ++it) {
-                const int i = tid + it * kThreads;
-                if (it < nit && i < K4) {
-                    dst[i] = qw[it];
-                    if (gout) gout[i] = qw[it];
-                    if constexpr (kCodeSums) tsum[m] += bytesum(qw[it]);
+                    for (int u = 0; u < kG; ++u)
+                        if (g0 + u < NIT && ((need >> u) & 1u)) qw[u] = a8_pack4(v[m][g0 + u], ks);
+                }
+#pragma unroll
+                for (int u = 0; u < kG; ++u) {
+                    const int it = g0 + u;
+                    const int i = tid + it * kThreads;
+                    if (it < NIT && it < nit && i < K4) {
+                        dst[i] = qw[u];
+                        if (gout) gout[i] = qw[u];
+                        if constexpr (kCodeSums) tsum[m] += bytesum(qw[u]);
+                    }
                 }
             }
         } else if (tid == m) {

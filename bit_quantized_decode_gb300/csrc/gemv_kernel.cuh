@@ -216,6 +216,7 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
                                  ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
                                  : nullptr;
             const uint32_t all_exact = a8_needs_exact(ks) ? 0xffffffffu : 0u;
+            const uint64_t rr = f2_pack(ks.r, ks.r);
             // Groups of kG words: the fast codes of a group are straight-line code
             // (independent chains, no branch between them); words with a possible
             // tie (or every word, for a tiny scale) are then redone exactly from
@@ -227,9 +228,9 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
                 uint32_t need = all_exact;
 #pragma unroll
                 for (int u = 0; u < kG; ++u) {
-                    bool tie = false;
-                    if (g0 + u < NIT) qw[u] = a8_pack4_fast(v[m][g0 + u], ks, tie);
-                    need |= tie ? (1u << u) : 0u;
+                    uint32_t ok = 0xffffffffu;
+                    if (g0 + u < NIT) qw[u] = a8_pack4_fast2(v[m][g0 + u], rr, ok);
+                    need |= ((~ok) >> 31) << u;
                 }
                 if (need) {
 #pragma unroll

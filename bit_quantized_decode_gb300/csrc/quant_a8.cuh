@@ -56,6 +56,35 @@ __device__ __forceinline__ int a8_code_fast(float v, const A8Scale& k, bool& tie
     return __float_as_int(big) - 0x4B400000;
 }
 
+// Packed pairs of fp32 (sm_100 and later): one instruction performs two IEEE
+// fp32 operations, each rounded exactly as its scalar form.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint32_t f2_lo(uint64_t v) { return static_cast<uint32_t>(v); }
+__device__ __forceinline__ uint32_t f2_hi(uint64_t v) { return static_cast<uint32_t>(v >> 32); }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // Low bytes of four ints, packed little-endian into one word.
 __device__ __forceinline__ uint32_t pack_low_bytes(int a, int b, int c, int d)
 {
@@ -67,6 +96,31 @@ __device__ __forceinline__ uint32_t a8_pack4_fast(float4 v, const A8Scale& k, bo
 {
     return pack_low_bytes(a8_code_fast(v.x, k, tie), a8_code_fast(v.y, k, tie), a8_code_fast(v.z, k, tie),
                           a8_code_fast(v.w, k, tie));
+}
+
+// The fast path of a8_pack4_fast on packed pairs, with the same roundings:
+// t = fl(x * r), big = fl(t + 1.5 * 2^23) (so rint(t) is in big's low
+// mantissa bits and the code is big's low byte), d = t - rint(t) exactly,
+// and the tie test d^2 - 0.49997^2 >= 0, whose sign one FMA gets exactly.
+// The sign bit of `ok` is cleared when some code of the four may be a tie
+// (|d| within ~1e-8 of 0.49997 or above).  rr holds r in both halves.
+__device__ __forceinline__ uint32_t a8_pack4_fast2(float4 v, uint64_t rr, uint32_t& ok)
+{
+    const uint64_t kBig = f2_pack(12582912.0f, 12582912.0f);
+    const uint64_t kNegBig = f2_pack(-12582912.0f, -12582912.0f);
+    const uint64_t kNegOne = f2_pack(-1.0f, -1.0f);
+    const uint64_t kNegTie = f2_pack(-0.2499700009f, -0.2499700009f);   // -(0.49997^2)
+    const uint64_t t01 = f2_mul(f2_pack(v.x, v.y), rr);
+    const uint64_t t23 = f2_mul(f2_pack(v.z, v.w), rr);
+    const uint64_t b01 = f2_add(t01, kBig);
+    const uint64_t b23 = f2_add(t23, kBig);
+    const uint64_t d01 = f2_fma(f2_add(b01, kNegBig), kNegOne, t01);
+    const uint64_t d23 = f2_fma(f2_add(b23, kNegBig), kNegOne, t23);
+    const uint64_t e01 = f2_fma(d01, d01, kNegTie);
+    const uint64_t e23 = f2_fma(d23, d23, kNegTie);
+    ok &= f2_lo(e01) & f2_hi(e01) & f2_lo(e23) & f2_hi(e23);
+    return __byte_perm(__byte_perm(f2_lo(b01), f2_hi(b01), 0x0040), __byte_perm(f2_lo(b23), f2_hi(b23), 0x0040),
+                       0x5410);
 }
 
 // True when the fast path may not be used at all for this scale.

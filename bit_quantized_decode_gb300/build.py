@@ -30,7 +30,7 @@ NVCC_FLAGS = [
     "-Xptxas", "-v",
     "-I", INCLUDE,
 ]
-SOURCES = ["w4a8_api.cu", "prep_kernels.cu", "gemv_w4.cu", "gemv_q4_0.cu", "gemv_i8g32.cu"]
+SOURCES = ["w4a8_api.cu", "prep_kernels.cu", "gemv_w4.cu", "gemv_q4_0.cu", "gemv_i8g32.cu", "gemv_tc.cu"]
 
 
 def nvcc() -> str:

@@ -1,0 +1,422 @@
+// Multi-token per-row INT4 decode GEMV on the 5th-generation tensor cores.
+//
+// What it computes ("Jetson Orin AGX INT4 推理优化实践", §"从 FP 线性层到 INT4 DP4A
+// 的数学推导"; the multi-token verify case of "在香橙派上跑 Gemma4", §五):
+//   acc[m][j] = sum_i q_w[j][i] qx[m][i]  (exact),
+//   y[m][j]   = fmaf(s_w[j] * sx[m], (float)acc[m][j], b[j])
+// for M = 8..16 tokens sharing one pass over the weights.  The int8 codes and
+// scales come from the activation quantizer launched before this kernel.
+//
+// How (GB300 design): the product is a GEMM of N x K by K x 16, so it runs on
+// tcgen05.mma (kind::f16, M = 128 rows, N = 16 tokens, K = 16 per
+// instruction).  int4 weights and int8 codes are exact in fp16, each product
+// |q_w q_x| <= 1016 is exact, and every partial sum is an integer below 2^24
+// in magnitude (a split covers at most 16384 K), so the fp32 accumulator in
+// tensor memory holds the exact integer sum.
+//   * One block of 128 threads per (128-row group, K split); thread t owns
+//     row t and tensor-memory lane t.  K splits of a row group form one
+//     thread-block cluster and add their partial sums in the leader's shared
+//     memory (distributed shared memory), which writes y.
+//   * Packed weights stream through a ring of stages (512 K x 128 rows,
+//     32 KB: one 2 KB bulk copy per 8-row tile) issued before the dependency
+//     wait; the operand pipeline steps through 128-K blocks of a stage.
+//   * Each thread turns its row's nibbles into fp16 pairs with one LOP3 and
+//     one HSUB2 per pair (0x6400 | n is 1024 + n; minus 1032 gives q) and
+//     stores them into tensor memory as the MMA's A operand (two buffers).
+//     The pairs come out in the K order (0,2),(1,3),(4,6),(5,7) within each
+//     8 weights; the fp16 activation tile (B, shared memory, K-major, no
+//     swizzle) is written in the same order, so the sum is unchanged.
+//   * Warps 0-3 dequantize (thread t: row t); warp 4 is the control warp: its
+//     lane 0 issues the weight copies and the MMAs.  They hand K blocks over
+//     through mbarriers only (ring slot full / empty, operand buffer ready /
+//     free, three operand buffers), so no block-wide barrier sits in the
+//     K loop and the MMAs of one block overlap the dequantization of the next.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace w4k {
+namespace {
+
+constexpr uint64_t kTcWaitNs = 250ull * 1000ull * 1000ull;
+constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 3 (64 each), D x 4 (16 each)
+constexpr uint32_t kTcColA = 0;
+constexpr uint32_t kTcColD = 192;
+constexpr int kTcAccs = 4;            // independent accumulators: consecutive MMAs do not wait on each other
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+// (bits 7-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcTok >> 3) << 17) |
+                              (static_cast<uint32_t>(kTcRows >> 4) << 24);
+// B tile: core matrices of 8 tokens x 8 K (16 B rows), token groups 128 B
+// apart, K groups 256 B apart.
+constexpr uint32_t kTcBsbo = 128;
+constexpr uint32_t kTcBlbo = 256;
+
+// 32 biased nibbles (n = q + 8) of one row -> 16 fp16 pairs q, in the K order
+// (8w+0, 8w+2), (8w+1, 8w+3), (8w+4, 8w+6), (8w+5, 8w+7) for word w.
+__device__ __forceinline__ void tc_dequant_unit(const uint4 u, uint32_t (&h)[16])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408u), __ushort_as_half(0x6408u));   // 1032
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t v = w[i];
+        const uint32_t p[4] = {(v & 0x000F000Fu) | 0x64006400u, ((v >> 8) & 0x000F000Fu) | 0x64006400u,
+                               ((v >> 4) & 0x000F000Fu) | 0x64006400u, ((v >> 12) & 0x000F000Fu) | 0x64006400u};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __half2 x = *reinterpret_cast<const __half2*>(&p[e]);
+            x = __hsub2(x, bias);
+            h[4 * i + e] = *reinterpret_cast<const uint32_t*>(&x);
+        }
+    }
+}
+
+// Eight int8 codes at K offsets 0..7 (words lo, hi) -> eight fp16 in the A
+// operand's K order: 0x6400 | (c + 128) is 1024 + c + 128 in fp16, minus 1152
+// gives c; byte permutes pick the pairs (0,2), (1,3), (4,6), (5,7).
+__device__ __forceinline__ uint4 tc_codes8(uint32_t lo, uint32_t hi)
+{
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));   // 1152
+    const uint32_t ul = lo ^ 0x80808080u;
+    const uint32_t uh = hi ^ 0x80808080u;
+    const uint32_t p[4] = {__byte_perm(ul, 0x64646464u, 0x4240), __byte_perm(ul, 0x64646464u, 0x4341),
+                           __byte_perm(uh, 0x64646464u, 0x4240), __byte_perm(uh, 0x64646464u, 0x4341)};
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __half2 x = *reinterpret_cast<const __half2*>(&p[e]);
+        x = __hsub2(x, off);
+        r[e] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_constant__ TcArgs A)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const bool control = warp == 4;
+    const int S = A.stages;
+    const int ks = A.splits;
+    const TcSmem L = tc_smem(S, ks);
+    uint8_t* ring = smem + L.ring;
+    uint8_t* bbuf = smem + L.bbuf;
+    uint8_t* codes = smem + L.codes;
+    const uint32_t bars = smem_u32(smem + L.bars);
+    const uint32_t full_b = bars;                        // [S]  stage landed (1 arrival + bytes)
+    const uint32_t empty_b = bars + 8 * S;               // [S]  stage read by warps 0-3 (4 arrivals)
+    const uint32_t ready_b = bars + 16 * S;              // [3]  operand buffer written (4 arrivals)
+    const uint32_t free_b = ready_b + 8 * kTcBufs;       // [3]  MMAs reading it completed (4 commits)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem);   // [0] base address, [1] stop flag
+    volatile uint32_t* dead_s = tmem_slot + 1;
+
+    constexpr int kSubs = kTcStageChunks / kTcChunks;      // K blocks per ring stage
+    const int g = blockIdx.x / ks;                         // row group
+    const int split = blockIdx.x - g * ks;                 // = rank in the cluster
+    const int cb = static_cast<int>(static_cast<long long>(split) * A.C / ks);
+    const int ce = static_cast<int>(static_cast<long long>(split + 1) * A.C / ks);
+    const int nb = (ce - cb + kTcChunks - 1) / kTcChunks;  // K blocks of this split
+    const int nst = (ce - cb + kTcStageChunks - 1) / kTcStageChunks;   // ring stages
+    const int tile0 = g * (kTcRows / kRows);
+    const int ntl = min(kTcRows / kRows, A.T - tile0);     // 8-row tiles present
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_b + 8 * s, 1);
+            mbar_init(empty_b + 8 * s, 4);
+        }
+        for (int j = 0; j < kTcBufs; ++j) {
+            mbar_init(ready_b + 8 * j, 4);
+            mbar_init(free_b + 8 * j, kTcAccs);   // one commit per issuing lane
+        }
+        fence_mbar_init();
+        *dead_s = 0u;
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    // stage st of the weights into ring slot st % S (control warp: lane 0 sets
+    // the byte count, lane l < 16 copies 8-row tile l: up to 16 chunks, 2 KB)
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue = [&](int st) {
+        const int slot = st % S;
+        const int c0 = cb + st * kTcStageChunks;
+        const int nch = min(kTcStageChunks, ce - c0);
+        const uint32_t bar = full_b + 8 * slot;
+        if (lane == 0) {
+            if (st >= S) fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ntl * nch * kRows * 16));
+        }
+        __syncwarp();
+        if (lane < ntl)
+            bulk_g2s(smem_u32(ring + static_cast<size_t>(slot) * kTcStageBytes + lane * kTcStageChunks * kRows * 16),
+                     A.w + (static_cast<size_t>(tile0 + lane) * A.C + c0) * kRows * 16,
+                     static_cast<uint32_t>(nch * kRows * 16), bar, pol);
+    };
+    int issued = 0;      // stages whose weights were requested (control warp)
+    if (control)
+        for (; issued < S && issued < nst; ++issued) issue(issued);
+
+    // ---- inputs produced by earlier kernels (codes, scales) from here on
+    pdl_wait();
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTcCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    auto fail = [&]() {
+        *dead_s = 1u;
+        if (A.err != nullptr) atomicExch(A.err, kErrWaitTimeout);
+    };
+
+    int committed = 0;   // K blocks whose MMAs were committed (control warp)
+    if (control) {
+        // ------------------------------------------------------ control warp
+        // Lane l fetches and converts token l / 2, K offsets 64 (l % 2) .. +63 of
+        // each K block: codes through a small ring (cp.async, its own bytes
+        // only), then the fp16 B tile; lanes 0-3 issue the MMAs.
+        const int cn = lane >> 1;
+        const int chalf = lane & 1;
+        auto fetch_codes = [&](int b) {
+            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + lane * 64;
+            const int kofs = (cb + b * kTcChunks) * 32 + chalf * 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool ok = b < nb && cn < A.M && kofs + 16 * q < ce * 32;
+                cp_async16(dst + 16 * q, ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs + 16 * q : A.qx,
+                           ok ? 16u : 0u);
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int i = 0; i < kTcCodeRing - 1; ++i) fetch_codes(i);
+        for (int b = 0; b < nb; ++b) {
+            const int j = b % kTcBufs;
+            const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
+            fetch_codes(b + kTcCodeRing - 1);
+            // B[j] is free once the MMAs of block b - 3 completed
+            bool ok = !*dead_s;
+            if (ok && b >= kTcBufs)
+                ok = mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>((b - kTcBufs) / kTcBufs) & 1u, kTcWaitNs);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0 && !*dead_s) fail();
+                break;
+            }
+            cp_async_wait_group<kTcCodeRing - 1>();
+            const uint4* cs = reinterpret_cast<const uint4*>(codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + lane * 64);
+            uint8_t* bt = bbuf + j * kTcBBytes + (cn >> 3) * kTcBsbo + (cn & 7) * 16 + chalf * 8 * kTcBlbo;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 c = cs[q];
+                *reinterpret_cast<uint4*>(bt + (2 * q) * kTcBlbo) = tc_codes8(c.x, c.y);
+                *reinterpret_cast<uint4*>(bt + (2 * q + 1) * kTcBlbo) = tc_codes8(c.z, c.w);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            // A[j] written by warps 0-3
+            bool rdy = true;
+            if (lane == 0) {
+                rdy = mbar_wait_bounded(ready_b + 8 * j, static_cast<uint32_t>(b / kTcBufs) & 1u, kTcWaitNs);
+                if (!rdy) fail();
+            }
+            if (!__shfl_sync(0xffffffffu, static_cast<int>(rdy), 0)) break;
+            if (lane < kTcAccs) {
+                // lane l issues K slices l and l + 4 into its own accumulator D[l]
+                // (the first use overwrites) and commits them
+                tc_fence_after();
+                const uint32_t bb = smem_u32(bbuf + j * kTcBBytes);
+                for (int kk = lane; kk < 2 * nch; kk += kTcAccs)
+                    tc_mma_f16_ts(tbase + kTcColD + lane * kTcTok, tbase + kTcColA + j * 64 + kk * 8,
+                                  smem_desc_noswizzle(bb + kk * 2 * kTcBlbo, kTcBlbo, kTcBsbo), kTcIdesc,
+                                  (b > 0 || kk >= kTcAccs) ? 1u : 0u);
+                tc_commit(free_b + 8 * j);
+            }
+            committed = b + 1;
+            // after the last K block of a stage: refill its slot once warps 0-3 read it
+            const int st = b / kSubs;
+            if ((b % kSubs == kSubs - 1 || b == nb - 1) && issued < nst) {
+                bool ok2 = true;
+                if (lane == 0)
+                    ok2 = mbar_wait_bounded(empty_b + 8 * (st % S), static_cast<uint32_t>(st / S) & 1u, kTcWaitNs);
+                if (!__shfl_sync(0xffffffffu, static_cast<int>(ok2), 0)) {
+                    if (lane == 0) fail();
+                    break;
+                }
+                issue(issued++);
+            }
+        }
+        cp_async_wait_group<0>();
+        if (lane == 0) {
+            // every committed MMA (all four lanes) completes before tensor memory is read or freed
+            if (committed > 0) {
+                const int last = committed - 1;
+                if (!mbar_wait_bounded(free_b + 8 * (last % kTcBufs), static_cast<uint32_t>(last / kTcBufs) & 1u,
+                                       kTcWaitNs) && !*dead_s)
+                    fail();
+            }
+            if (committed < nb && !*dead_s) fail();
+            // after a failure: copies still in flight land before the ring is reused or the block exits
+            if (*dead_s)
+                for (int k = issued - S > 0 ? issued - S : 0; k < issued; ++k)
+                    if (!mbar_wait_bounded(full_b + 8 * (k % S), static_cast<uint32_t>(k / S) & 1u, kTcWaitNs)) break;
+        }
+    } else {
+        // --------------------------------------------------- warps 0-3: A
+        const uint32_t tlane = static_cast<uint32_t>(warp * 32) << 16;
+        const uint8_t* my_units = ring + (tid >> 3) * (kTcStageChunks * kRows * 16) + (tid & 7) * 16;
+        for (int b = 0; b < nb; ++b) {
+            const int st = b / kSubs;
+            const int sub = b - st * kSubs;
+            const int slot = st % S;
+            const int j = b % kTcBufs;
+            const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
+            bool ok = !*dead_s;
+            if (ok && sub == 0)
+                ok = mbar_wait_bounded(full_b + 8 * slot, static_cast<uint32_t>(st / S) & 1u, kTcWaitNs);
+            if (ok && b >= kTcBufs)
+                ok = mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>((b - kTcBufs) / kTcBufs) & 1u, kTcWaitNs);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0 && !*dead_s) fail();
+                break;
+            }
+            tc_fence_after();
+            uint4 u[kTcChunks];
+#pragma unroll
+            for (int cl = 0; cl < kTcChunks; ++cl)
+                if (cl < nch)
+                    u[cl] = *reinterpret_cast<const uint4*>(my_units + static_cast<size_t>(slot) * kTcStageBytes +
+                                                            (sub * kTcChunks + cl) * kRows * 16);
+            if (sub == kSubs - 1 || b == nb - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // the stage's bytes are in registers
+            }
+#pragma unroll
+            for (int cl = 0; cl < kTcChunks; ++cl) {
+                if (cl < nch) {
+                    uint32_t h[16];
+                    tc_dequant_unit(u[cl], h);
+                    tmem_st16(tbase + tlane + kTcColA + j * 64 + cl * 16, h);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ready_b + 8 * j);
+        }
+    }
+    __syncthreads();
+
+    // ---- the accumulator: row tid, tokens 0..15 (warps 0-3)
+    const bool dead = *dead_s != 0u;
+    int acc[kTcTok];
+#pragma unroll
+    for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
+    if (!control && !dead && nb > 0) {
+        // the control warp saw the last commit complete before the barrier above;
+        // each accumulator holds an exact integer, so their sum is exact in int
+        tc_fence_after();
+        const int used = min(kTcAccs, 2 * min(kTcChunks, ce - cb));   // accumulators written at all
+        for (int q = 0; q < used; ++q) {
+            uint32_t d[kTcTok];
+            tmem_ld16(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcTok, d);
+#pragma unroll
+            for (int n = 0; n < kTcTok; ++n) acc[n] += __float2int_rn(__uint_as_float(d[n]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTcCols);
+    }
+
+    // ---- K splits: partial sums into the leader's ring (every block of the
+    // cluster is past its K loop after the first cluster barrier)
+    if (ks > 1) {
+        int* red = reinterpret_cast<int*>(smem + L.red);
+        cluster_sync();
+        if (!control) {
+            const uint32_t dst = mapa_shared(smem_u32(red + (split * kTcRows + tid) * kTcTok), 0);
+#pragma unroll
+            for (int n = 0; n < kTcTok; n += 4)
+                st_cluster_v4(dst + 4 * n, static_cast<uint32_t>(acc[n]), static_cast<uint32_t>(acc[n + 1]),
+                              static_cast<uint32_t>(acc[n + 2]), static_cast<uint32_t>(acc[n + 3]));
+        }
+        cluster_sync();
+        if (split != 0 || control) return;
+#pragma unroll
+        for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
+        for (int r = 0; r < ks; ++r) {
+            const int4* p = reinterpret_cast<const int4*>(red + (r * kTcRows + tid) * kTcTok);
+#pragma unroll
+            for (int q = 0; q < kTcTok / 4; ++q) {
+                const int4 v = p[q];
+                acc[4 * q] += v.x;
+                acc[4 * q + 1] += v.y;
+                acc[4 * q + 2] += v.z;
+                acc[4 * q + 3] += v.w;
+            }
+        }
+    }
+    if (control) return;
+
+    // ---- epilogue: y = fmaf(s_w s_x, acc, b), coalesced over rows per token
+    // (a partial sum of a dead split makes the row wrong: the error word says so)
+    const int row = g * kTcRows + tid;
+    if (row < A.N && !dead) {
+        const float sw = A.s_w[row];
+        const float bv = A.bias != nullptr ? A.bias[row] : 0.0f;
+#pragma unroll
+        for (int n = 0; n < kTcTok; ++n)
+            if (n < A.M)
+                A.y[static_cast<size_t>(n) * A.N + row] = __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_w4_tc(const TcArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s)
+{
+    auto kern = gemv_w4_tc_kernel;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int configured[64] = {0};
+    if (dev < 64 && configured[dev] < static_cast<int>(smem)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured[dev] = static_cast<int>(smem);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (a.splits > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(a.splits);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = na > 0 ? attr : nullptr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace w4k

@@ -96,6 +96,56 @@ cudaError_t launch_gemv_i8g32(const ChainParams<1>& p, int MT, int xmode, int gr
 // Chains of per-row INT4 linears (cooperative launch, fused quantization).
 cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
 
+// ---------------------------------------------- multi-token tensor-core GEMV
+// Per-row INT4 GEMV for 8..16 tokens on the tcgen05 tensor cores
+// (gemv_tc.cu): one block of kTcThreads per (128-row group, K split), the
+// K splits of a row group forming one thread-block cluster.
+constexpr int kTcThreads = 160;                  // warps 0-3: row t = thread t (tensor-memory lane t); warp 4: control
+constexpr int kTcRows = 128;                     // MMA M: weight rows per block
+constexpr int kTcTok = 16;                       // MMA N: tokens (fewer are zero-padded)
+constexpr int kTcChunks = 4;                     // 32-weight chunks per K block
+constexpr int kTcKb = 32 * kTcChunks;            // K per block: 128
+constexpr int kTcStageChunks = 16;              // chunks per weight-ring stage (4 K blocks): 2 KB copies per tile
+constexpr int kTcStageBytes = (kTcRows / kRows) * kTcStageChunks * kRows * 16;   // 32 KB of packed weights
+constexpr int kTcBBytes = kTcTok * kTcKb * 2;    // fp16 activation tile per K block
+constexpr int kTcCodeRing = 4;                   // K blocks of int8 codes in flight
+constexpr int kTcBufs = 3;                       // A (tensor memory) / B (shared memory) operand buffers
+constexpr int kTcMaxSplit = 8;                   // K splits (cluster size) at most
+constexpr int kTcMaxSplitK = 16384;              // K per split at most: partial sums stay below 2^24
+
+struct TcArgs {
+    const uint8_t* w;       // repacked per-row INT4 (8-row tiles)
+    const float* s_w;       // [N]
+    const float* bias;      // [N] or null
+    const int8_t* qx;       // [M][K] activation codes
+    const float* sx;        // [M]
+    float* y;               // [M][N]
+    int M, N, K, C, T;      // C = K / 32 chunks, T = row tiles
+    int splits;             // K splits per row group (= cluster size)
+    int stages;             // weight ring depth (K blocks)
+    unsigned* err;
+};
+
+struct TcSmem {
+    int ring, bbuf, codes, red, bars, tmem, total;
+};
+
+__host__ __device__ inline TcSmem tc_smem(int stages, int splits)
+{
+    TcSmem L;
+    int o = 0;
+    L.ring = o;  o += stages * kTcStageBytes;
+    L.bbuf = o;  o += kTcBufs * kTcBBytes;
+    L.codes = o; o += kTcCodeRing * kTcTok * kTcKb;
+    L.red = L.ring;   // K-split partial sums reuse the ring once every block is past its K loop
+    L.bars = o;  o += (2 * stages + 2 * kTcBufs) * 8;
+    L.tmem = o;  o += 16;
+    L.total = o;
+    return L;
+}
+
+cudaError_t launch_gemv_w4_tc(const TcArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s);
+
 // Load-time and activation kernels (prep_kernels.cu).
 constexpr int kMaxShards = 8;
 struct ShardTable {
@@ -105,7 +155,7 @@ struct ShardTable {
     int n;
 };
 
-cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, cudaStream_t s);
+cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, bool pdl, cudaStream_t s);
 cudaError_t launch_w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, cudaStream_t s);
 cudaError_t launch_q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, cudaStream_t s);
 cudaError_t launch_i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, cudaStream_t s);

@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "quant_a8.cuh"
 
 namespace w4k {
@@ -33,34 +34,85 @@ __device__ __forceinline__ int quant_code(float v, float s, int lo, int hi)
 
 // ------------------------------------------------ per-token INT8 activations
 // "Jetson Orin AGX INT4 推理优化实践", §"从 FP 线性层到 INT4 DP4A 的数学推导":
-// s^x = max|x| / 127, q^x = clip(round(x / s^x), -127, 127).  One block per token.
+// s^x = max|x| / 127, q^x = clip(round(x / s^x), -127, 127).  One block per
+// token.  Codes come from the fast path (multiply by fl(1/s), packed pairs)
+// and, for words with a possible tie or a tiny scale, the exact quotient; the
+// result is bit-identical to the definition (quant_a8.cuh).  The token stays
+// in registers (NIT float4 per thread) when it fits, else it is read twice.
+// Launched with programmatic dependent launch it waits for the previous
+// kernel before reading x and lets the next kernel start at once.
 constexpr int kQuantThreads = 512;
 
+template <int NIT>
 __global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float* __restrict__ x, int K,
-                                                                     int8_t* __restrict__ qx, float* __restrict__ sx)
+                                                                    int8_t* __restrict__ qx, float* __restrict__ sx)
 {
     __shared__ float red[kQuantThreads / 32];
+    pdl_launch_dependents();
+    pdl_wait();
     const int m = blockIdx.x;
+    const int tid = threadIdx.x;
     const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K);
     const int K4 = K >> 2;
+    constexpr bool kRegs = NIT > 0;
+    constexpr int kN = kRegs ? NIT : 1;
+    float4 v[kN];
     float mx = 0.0f;
-    for (int i = threadIdx.x; i < K4; i += kQuantThreads) mx = fmaxf(mx, abs_max4(xr[i]));
+    if constexpr (kRegs) {
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const int i = tid + it * kQuantThreads;
+            v[it] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) mx = fmaxf(mx, abs_max4(v[it]));
+    } else {
+        for (int i = tid; i < K4; i += kQuantThreads) mx = fmaxf(mx, abs_max4(__ldcg(xr + i)));
+    }
     mx = warp_max(mx);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    if ((tid & 31) == 0) red[tid >> 5] = mx;
     __syncthreads();
     float amax = 0.0f;
 #pragma unroll
     for (int w = 0; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     const A8Scale ks = a8_scale(amax);
+    const bool all_exact = a8_needs_exact(ks);
+    const uint64_t rr = f2_pack(ks.r, ks.r);
     uint32_t* out = reinterpret_cast<uint32_t*>(qx + static_cast<size_t>(m) * K);
-    for (int i = threadIdx.x; i < K4; i += kQuantThreads) out[i] = a8_pack4(xr[i], ks);
-    if (threadIdx.x == 0) sx[m] = ks.s;
+    auto code = [&](float4 f) -> uint32_t {
+        uint32_t ok = 0xffffffffu;
+        const uint32_t q = a8_pack4_fast2(f, rr, ok);
+        return (all_exact || (ok >> 31) == 0) ? a8_pack4(f, ks) : q;
+    };
+    if constexpr (kRegs) {
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const int i = tid + it * kQuantThreads;
+            if (i < K4) out[i] = code(v[it]);
+        }
+    } else {
+        for (int i = tid; i < K4; i += kQuantThreads) out[i] = code(__ldcg(xr + i));
+    }
+    if (tid == 0) sx[m] = ks.s;
 }
 
-cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, cudaStream_t s)
+cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, bool pdl, cudaStream_t s)
 {
-    a8_quantize_kernel<<<M, kQuantThreads, 0, s>>>(x, K, qx, sx);
-    return cudaGetLastError();
+    const int nit = (K / 4 + kQuantThreads - 1) / kQuantThreads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(kQuantThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (nit <= 2) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<2>, x, K, qx, sx);
+    if (nit <= 4) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<4>, x, K, qx, sx);
+    if (nit <= 10) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<10>, x, K, qx, sx);
+    if (nit <= 16) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<16>, x, K, qx, sx);
+    return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<0>, x, K, qx, sx);
 }
 
 // ------------------------------------------------------ per-row INT4 weights

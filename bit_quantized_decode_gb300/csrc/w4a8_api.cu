@@ -29,7 +29,7 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 
 // Launch tuning set by w4_set_tuning (0 = automatic).
-int g_tune[3] = {0, 0, 0};
+int g_tune[4] = {0, 0, 0, 0};
 
 w4_status device_info(DeviceInfo** out)
 {
@@ -215,8 +215,55 @@ bool fused_fits(int fmt, int M, int K)
     return plan_gemv(*dev, fmt, MT, true, K, kAccWords / MT, p);
 }
 
+// Per-row INT4 with this many tokens runs on the tensor cores (gemv_tc.cu).
+bool use_tc(int fmt, int M)
+{
+    const int lo = g_tune[W4_TUNE_TC_MIN_M] > 0 ? g_tune[W4_TUNE_TC_MIN_M] : 8;
+    return fmt == FMT_W4 && M >= lo && M <= kTcTok;
+}
+
+// Tensor-core GEMV: one block per (128-row group, K split); enough splits to
+// cover the SMs (at most kTcMaxSplit) and to keep every split within
+// kTcMaxSplitK; the deepest weight ring that leaves room for a second block
+// per SM.
+w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx, int M,
+                      int N, int K, float* y, bool pdl, cudaStream_t s)
+{
+    DeviceInfo* dev = nullptr;
+    w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    TcArgs a = {};
+    a.w = static_cast<const uint8_t*>(w);
+    a.s_w = s_w;
+    a.bias = bias;
+    a.qx = qx;
+    a.sx = sx;
+    a.y = y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.C = K / 32;
+    a.T = static_cast<int>(tiles(N));
+    a.err = dev->err;
+    const int G = (N + kTcRows - 1) / kTcRows;
+    int ks = (dev->sms + G - 1) / G;
+    if (ks > kTcMaxSplit) ks = kTcMaxSplit;
+    const int need = (K + kTcMaxSplitK - 1) / kTcMaxSplitK;
+    if (ks < need) ks = need;
+    if (ks > a.C) ks = a.C;
+    if (ks < need || ks > kTcMaxSplit) return W4_ERR_UNSUPPORTED_SHAPE;
+    a.splits = ks;
+    const int half = dev->smem_per_sm / 2 - dev->smem_reserved;
+    int S = 4;
+    while (S > 2 && tc_smem(S, ks).total > half) --S;
+    if (tc_smem(S, ks).total > dev->smem_optin) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (S * kTcStageBytes < ks * kTcRows * kTcTok * 4) return W4_ERR_UNSUPPORTED_SHAPE;   // partial sums fit the ring
+    a.stages = S;
+    return cuda_status(launch_gemv_w4_tc(a, G * ks, static_cast<size_t>(tc_smem(S, ks).total), pdl, s));
+}
+
 w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bias, const int8_t* qx,
-                      const float* sx, int M, int N, int K, float* y, cudaStream_t s)
+                      const float* sx, int M, int N, int K, float* y, cudaStream_t s, bool pdl = false)
 {
     w4_status st = check_mk(M, K);
     if (st != W4_OK) return st;
@@ -226,6 +273,7 @@ w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bia
     if (!aligned(w, 16) || !aligned(qx, 16) || !aligned(sx, 4) || !aligned(y, 4) || (s_w && !aligned(s_w, 4)) ||
         (bias && !aligned(bias, 4)))
         return W4_ERR_MISALIGNED;
+    if (use_tc(fmt, M)) return run_gemv_tc(w, s_w, bias, qx, sx, M, N, K, y, pdl, s);
     GemvArgs a = {};
     a.w = static_cast<const uint8_t*>(w);
     const size_t units = tiles(N) * kRows * (K / 32);
@@ -239,7 +287,7 @@ w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bia
     a.M = M;
     a.N = N;
     a.K = K;
-    return run_gemv(fmt, a, false, 0u, s);
+    return run_gemv(fmt, a, false, pdl ? W4_FLAG_PDL : 0u, s);
 }
 
 w4_status linear_common(int fmt, const void* w, const float* s_w, const float* bias, const float* x, int M, int N,
@@ -254,11 +302,12 @@ w4_status linear_common(int fmt, const void* w, const float* s_w, const float* b
     if (!aligned(x, 16) || !aligned(qx, 16) || !aligned(sx, 4) || (w && !aligned(w, 16)) || (y && !aligned(y, 4)) ||
         (s_w && !aligned(s_w, 4)) || (bias && !aligned(bias, 4)))
         return W4_ERR_MISALIGNED;
-    if (N == 0 || !fused_fits(fmt, M, K)) {
-        // quantize into the caller's qx/sx, then the GEMV on int8 codes
-        st = cuda_status(launch_a8_quantize(x, M, K, qx, sx, s));
+    if (N == 0 || use_tc(fmt, M) || !fused_fits(fmt, M, K)) {
+        // quantize into the caller's qx/sx once, then the GEMV on int8 codes
+        // (tensor cores for many tokens), chained by programmatic dependent launch
+        st = cuda_status(launch_a8_quantize(x, M, K, qx, sx, (flags & W4_FLAG_PDL) != 0, s));
         if (st != W4_OK || N == 0) return st;
-        return gemv_common(fmt, w, s_w, bias, qx, sx, M, N, K, y, s);
+        return gemv_common(fmt, w, s_w, bias, qx, sx, M, N, K, y, s, true);
     }
     GemvArgs a = {};
     a.w = static_cast<const uint8_t*>(w);
@@ -298,7 +347,8 @@ int w4_version(void) { return 1; }
 
 w4_status w4_set_tuning(int key, int value)
 {
-    if (key < 0 || key > W4_TUNE_GRID_BLOCKS || value < 0) return W4_ERR_INVALID_ARG;
+    if (key < 0 || key > W4_TUNE_TC_MIN_M || value < 0) return W4_ERR_INVALID_ARG;
+    if (key == W4_TUNE_TC_MIN_M && value > W4_MAX_M + 1) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_BLOCKS_PER_SM && value > 2) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_MAX_STAGES && value == 1) return W4_ERR_INVALID_ARG;
     g_tune[key] = value;
@@ -307,7 +357,7 @@ w4_status w4_set_tuning(int key, int value)
 
 int w4_get_tuning(int key)
 {
-    if (key < 0 || key > W4_TUNE_GRID_BLOCKS) return -1;
+    if (key < 0 || key > W4_TUNE_TC_MIN_M) return -1;
     return g_tune[key];
 }
 
@@ -439,7 +489,7 @@ w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_st
     if (M == 0) return W4_OK;
     if (!x || !qx || !sx) return W4_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(qx, 16) || !aligned(sx, 4)) return W4_ERR_MISALIGNED;
-    return cuda_status(launch_a8_quantize(x, M, K, qx, sx, reinterpret_cast<cudaStream_t>(s)));
+    return cuda_status(launch_a8_quantize(x, M, K, qx, sx, false, reinterpret_cast<cudaStream_t>(s)));
 }
 
 w4_status w4a8_gemv(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx, int M,

@@ -93,12 +93,15 @@ int w4_version(void);
  *                          W4_FLAG_PDL is resident beside the previous one.
  *   W4_TUNE_MAX_STAGES     cap on the ring depth per warp (>= 2).
  *   W4_TUNE_GRID_BLOCKS    cap on the grid size (default: the SM count).
+ *   W4_TUNE_TC_MIN_M       per-row INT4 calls with at least this many tokens
+ *                          run on the tensor cores (default 0: 8; 17: never).
  * Returns W4_ERR_INVALID_ARG for an unknown key or an out-of-range value.
  * Not thread-safe with concurrent launches; set before launching.
  * ------------------------------------------------------------------------ */
 #define W4_TUNE_BLOCKS_PER_SM 0
 #define W4_TUNE_MAX_STAGES 1
 #define W4_TUNE_GRID_BLOCKS 2
+#define W4_TUNE_TC_MIN_M 3
 w4_status w4_set_tuning(int key, int value);
 int w4_get_tuning(int key); /* current value, -1 for an unknown key */
 

@@ -13,24 +13,26 @@
 // |q_w q_x| <= 1016 is exact, and every partial sum is an integer below 2^24
 // in magnitude (a split covers at most 16384 K), so the fp32 accumulator in
 // tensor memory holds the exact integer sum.
-//   * One block of 128 threads per (128-row group, K split); thread t owns
-//     row t and tensor-memory lane t.  K splits of a row group form one
-//     thread-block cluster and add their partial sums in the leader's shared
-//     memory (distributed shared memory), which writes y.
+//   * One block of six warps per (128-row group, K split).  K splits of a row
+//     group form one thread-block cluster and add their partial sums in the
+//     leader's shared memory (distributed shared memory), which writes y.
 //   * Packed weights stream through a ring of stages (512 K x 128 rows,
 //     32 KB: one 2 KB bulk copy per 8-row tile) issued before the dependency
 //     wait; the operand pipeline steps through 128-K blocks of a stage.
-//   * Each thread turns its row's nibbles into fp16 pairs with one LOP3 and
-//     one HSUB2 per pair (0x6400 | n is 1024 + n; minus 1032 gives q) and
-//     stores them into tensor memory as the MMA's A operand (two buffers).
-//     The pairs come out in the K order (0,2),(1,3),(4,6),(5,7) within each
-//     8 weights; the fp16 activation tile (B, shared memory, K-major, no
-//     swizzle) is written in the same order, so the sum is unchanged.
-//   * Warps 0-3 dequantize (thread t: row t); warp 4 is the control warp: its
-//     lane 0 issues the weight copies and the MMAs.  They hand K blocks over
-//     through mbarriers only (ring slot full / empty, operand buffer ready /
-//     free, three operand buffers), so no block-wide barrier sits in the
-//     K loop and the MMAs of one block overlap the dequantization of the next.
+//   * Warps 0-3 (thread t: row t) turn their row's nibbles into fp16 pairs
+//     with one LOP3 and one HSUB2 per pair (0x6400 | n is 1024 + n; minus
+//     1032 gives q) and store them into tensor memory as the MMA's A operand
+//     (three buffers).  The pairs come out in the K order (0,2), (1,3),
+//     (4,6), (5,7) within each 8 weights; the same warps write the fp16
+//     activation tile (B, shared memory, K-major, no swizzle) in that order,
+//     so the sum is unchanged.
+//   * Warp 4 issues the MMAs (lanes 0-3, one accumulator each, so consecutive
+//     MMAs are independent; the four exact partial sums are added at the
+//     end); warp 5 issues the weight copies.  The roles hand K blocks over
+//     through mbarriers only (stage full / empty, operand buffer ready /
+//     free), so no block-wide barrier sits in the K loop.
+//   * The tensor cores are far from busy at N = 16: about 125 cycles per
+//     128 x 16 x 16 MMA per SM bound this kernel, not HBM.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -100,7 +102,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const bool control = warp == 4;
+    const bool mma_warp = warp == 4;
+    const bool producer = warp == 5;
+    const bool control = warp >= 4;
     const int S = A.stages;
     const int ks = A.splits;
     const TcSmem L = tc_smem(S, ks);
@@ -158,8 +162,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                      A.w + (static_cast<size_t>(tile0 + lane) * A.C + c0) * kRows * 16,
                      static_cast<uint32_t>(nch * kRows * 16), bar, pol);
     };
-    int issued = 0;      // stages whose weights were requested (control warp)
-    if (control)
+    int issued = 0;      // stages whose weights were requested (producer warp)
+    if (producer)
         for (; issued < S && issued < nst; ++issued) issue(issued);
 
     // ---- inputs produced by earlier kernels (codes, scales) from here on
@@ -177,55 +181,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
         if (A.err != nullptr) atomicExch(A.err, kErrWaitTimeout);
     };
 
-    int committed = 0;   // K blocks whose MMAs were committed (control warp)
-    if (control) {
-        // ------------------------------------------------------ control warp
-        // Lane l fetches and converts token l / 2, K offsets 64 (l % 2) .. +63 of
-        // each K block: codes through a small ring (cp.async, its own bytes
-        // only), then the fp16 B tile; lanes 0-3 issue the MMAs.
-        const int cn = lane >> 1;
-        const int chalf = lane & 1;
-        auto fetch_codes = [&](int b) {
-            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + lane * 64;
-            const int kofs = (cb + b * kTcChunks) * 32 + chalf * 64;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const bool ok = b < nb && cn < A.M && kofs + 16 * q < ce * 32;
-                cp_async16(dst + 16 * q, ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs + 16 * q : A.qx,
-                           ok ? 16u : 0u);
-            }
-            cp_async_commit();
-        };
-#pragma unroll
-        for (int i = 0; i < kTcCodeRing - 1; ++i) fetch_codes(i);
+    int committed = 0;   // K blocks whose MMAs were committed (MMA warp)
+    if (mma_warp) {
+        // --------------------------------------------------------- MMA warp
         for (int b = 0; b < nb; ++b) {
             const int j = b % kTcBufs;
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
-            fetch_codes(b + kTcCodeRing - 1);
-            // B[j] is free once the MMAs of block b - 3 completed
-            bool ok = !*dead_s;
-            if (ok && b >= kTcBufs)
-                ok = mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>((b - kTcBufs) / kTcBufs) & 1u, kTcWaitNs);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0 && !*dead_s) fail();
-                break;
-            }
-            cp_async_wait_group<kTcCodeRing - 1>();
-            const uint4* cs = reinterpret_cast<const uint4*>(codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + lane * 64);
-            uint8_t* bt = bbuf + j * kTcBBytes + (cn >> 3) * kTcBsbo + (cn & 7) * 16 + chalf * 8 * kTcBlbo;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 c = cs[q];
-                *reinterpret_cast<uint4*>(bt + (2 * q) * kTcBlbo) = tc_codes8(c.x, c.y);
-                *reinterpret_cast<uint4*>(bt + (2 * q + 1) * kTcBlbo) = tc_codes8(c.z, c.w);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            // A[j] written by warps 0-3
+            // A[j] and B[j] written by warps 0-3
             bool rdy = true;
             if (lane == 0) {
-                rdy = mbar_wait_bounded(ready_b + 8 * j, static_cast<uint32_t>(b / kTcBufs) & 1u, kTcWaitNs);
-                if (!rdy) fail();
+                rdy = !*dead_s && mbar_wait_bounded(ready_b + 8 * j, static_cast<uint32_t>(b / kTcBufs) & 1u, kTcWaitNs);
+                if (!rdy && !*dead_s) fail();
             }
             if (!__shfl_sync(0xffffffffu, static_cast<int>(rdy), 0)) break;
             if (lane < kTcAccs) {
@@ -240,20 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                 tc_commit(free_b + 8 * j);
             }
             committed = b + 1;
-            // after the last K block of a stage: refill its slot once warps 0-3 read it
-            const int st = b / kSubs;
-            if ((b % kSubs == kSubs - 1 || b == nb - 1) && issued < nst) {
-                bool ok2 = true;
-                if (lane == 0)
-                    ok2 = mbar_wait_bounded(empty_b + 8 * (st % S), static_cast<uint32_t>(st / S) & 1u, kTcWaitNs);
-                if (!__shfl_sync(0xffffffffu, static_cast<int>(ok2), 0)) {
-                    if (lane == 0) fail();
-                    break;
-                }
-                issue(issued++);
-            }
         }
-        cp_async_wait_group<0>();
         if (lane == 0) {
             // every committed MMA (all four lanes) completes before tensor memory is read or freed
             if (committed > 0) {
@@ -263,21 +216,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                     fail();
             }
             if (committed < nb && !*dead_s) fail();
-            // after a failure: copies still in flight land before the ring is reused or the block exits
-            if (*dead_s)
-                for (int k = issued - S > 0 ? issued - S : 0; k < issued; ++k)
-                    if (!mbar_wait_bounded(full_b + 8 * (k % S), static_cast<uint32_t>(k / S) & 1u, kTcWaitNs)) break;
         }
+    } else if (producer) {
+        // ---------------------------------------------------- producer warp
+        // refill each stage's slot once warps 0-3 have read it
+        for (; issued < nst; ++issued) {
+            const int prev = issued - S;
+            bool ok = true;
+            if (lane == 0)
+                ok = !*dead_s && mbar_wait_bounded(empty_b + 8 * (prev % S), static_cast<uint32_t>(prev / S) & 1u, kTcWaitNs);
+            if (!__shfl_sync(0xffffffffu, static_cast<int>(ok), 0)) {
+                if (lane == 0 && !*dead_s) fail();
+                break;
+            }
+            issue(issued);
+        }
+        // after a failure: copies still in flight land before the ring is reused or the block exits
+        if (lane == 0 && *dead_s)
+            for (int k = issued - S > 0 ? issued - S : 0; k < issued; ++k)
+                if (!mbar_wait_bounded(full_b + 8 * (k % S), static_cast<uint32_t>(k / S) & 1u, kTcWaitNs)) break;
     } else {
-        // --------------------------------------------------- warps 0-3: A
+        // ------------------------------------------- warps 0-3: A and B
         const uint32_t tlane = static_cast<uint32_t>(warp * 32) << 16;
         const uint8_t* my_units = ring + (tid >> 3) * (kTcStageChunks * kRows * 16) + (tid & 7) * 16;
+        // Activation codes: thread t copies token t / 8, 16 codes at K offset
+        // 16 (t % 8) of each K block through a small ring (its own bytes only)
+        // and writes them to B as fp16.
+        const int cn = tid >> 3;
+        const int cpart = tid & 7;
+        auto fetch_codes = [&](int b) {
+            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + tid * 16;
+            const int kofs = (cb + b * kTcChunks) * 32 + cpart * 16;
+            const bool ok = b < nb && cn < A.M && kofs < ce * 32;
+            cp_async16(dst, ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx, ok ? 16u : 0u);
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int i = 0; i < kTcCodeRing - 1; ++i) fetch_codes(i);
         for (int b = 0; b < nb; ++b) {
             const int st = b / kSubs;
             const int sub = b - st * kSubs;
             const int slot = st % S;
             const int j = b % kTcBufs;
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
+            fetch_codes(b + kTcCodeRing - 1);
             bool ok = !*dead_s;
             if (ok && sub == 0)
                 ok = mbar_wait_bounded(full_b + 8 * slot, static_cast<uint32_t>(st / S) & 1u, kTcWaitNs);
@@ -306,11 +288,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                     tmem_st16(tbase + tlane + kTcColA + j * 64 + cl * 16, h);
                 }
             }
+            // B: token cn, K positions 16 cpart .. +15 of the block, fp16 in A's order
+            cp_async_wait_group<kTcCodeRing - 1>();
+            const uint4 c = *reinterpret_cast<const uint4*>(codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + tid * 16);
+            uint8_t* bt = bbuf + j * kTcBBytes + (cn >> 3) * kTcBsbo + (cn & 7) * 16;
+            *reinterpret_cast<uint4*>(bt + (2 * cpart) * kTcBlbo) = tc_codes8(c.x, c.y);
+            *reinterpret_cast<uint4*>(bt + (2 * cpart + 1) * kTcBlbo) = tc_codes8(c.z, c.w);
+            fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ready_b + 8 * j);
         }
+        cp_async_wait_group<0>();
     }
     __syncthreads();
 

@@ -100,7 +100,7 @@ cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, s
 // Per-row INT4 GEMV for 8..16 tokens on the tcgen05 tensor cores
 // (gemv_tc.cu): one block of kTcThreads per (128-row group, K split), the
 // K splits of a row group forming one thread-block cluster.
-constexpr int kTcThreads = 160;                  // warps 0-3: row t = thread t (tensor-memory lane t); warp 4: control
+constexpr int kTcThreads = 192;                  // warps 0-3: row t = thread t (tensor-memory lane t); 4: MMA; 5: copies
 constexpr int kTcRows = 128;                     // MMA M: weight rows per block
 constexpr int kTcTok = 16;                       // MMA N: tokens (fewer are zero-padded)
 constexpr int kTcChunks = 4;                     // 32-weight chunks per K block

@@ -52,6 +52,11 @@ def parse_args(argv=None):
     p.add_argument("--chain", action="store_true",
                    help="one chained launch per step (w4a8_linear_chain) instead of one PDL launch per linear")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--suite", action="store_true",
+                   help="instead of the step line: every GEMV of the single, 7B-layer, Gemma Q4_0 and lm_head "
+                        "workloads on its own, then the full step at M = 1, 2, 4, 8, 16 (one JSON line each)")
+    p.add_argument("--suite-ms", default="1,2,4,8,16", help="token counts of the suite's full-step lines")
+    p.add_argument("--suite-only-steps", action="store_true", help="suite: skip the single-GEMV lines")
     p.add_argument("--independent-x", action="store_true",
                    help="every linear reads its own static input buffer instead of the previous output")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -76,8 +81,16 @@ def step_linears(layers: int, lm_head: bool):
 
 
 def algorithmic_bytes(lin, M: int) -> int:
-    """Packed weights (0.5 B each) + per-row scale + bias + fp32 x + fp32 y."""
-    return lin.N * lin.K // 2 + 4 * lin.N + (4 * lin.N if lin.bias else 0) + 4 * M * lin.K + 4 * M * lin.N
+    """Bytes one decode linear must move: its weights in their packed format
+    (per-row INT4: 0.5 B a weight + a 4-byte scale a row; Q4_0: 18 B per 32
+    weights; i8g32: 1 B a weight + 2 B per 32), the bias, fp32 x and fp32 y."""
+    if lin.fmt == "w4":
+        w = lin.N * lin.K // 2 + 4 * lin.N
+    elif lin.fmt == "q4_0":
+        w = lin.N * (lin.K // 32) * 18
+    else:
+        w = lin.N * lin.K + lin.N * (lin.K // 32) * 2
+    return w + (4 * lin.N if lin.bias else 0) + 4 * M * lin.K + 4 * M * lin.N
 
 
 def workload_config(args, n_gpus):
@@ -256,35 +269,42 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------- our arm
-def build_step(args, device):
-    """Resident weights and per-linear buffers.  Returns (items, x_in, y_out):
-    x_in is the step's input, y_out the last linear's output (the logits
-    with the lm_head); with --independent-x, x_in and y_out hold every
-    linear's input and output instead."""
+def build_weights(args, device):
+    """The step's linears with resident repacked weights: [(layer, lin, QuantLinear)]."""
     import torch
 
     from bit_quantized_decode_gb300 import QuantLinear
-    seq = step_linears(args.layers, not args.no_lm_head)
-    M = args.M
-    if args.independent_x:
-        x_all = torch.empty(sum(M * lin.K for _, lin in seq), dtype=torch.float32, device=device)
-        y_all = torch.empty(sum(M * lin.N for _, lin in seq), dtype=torch.float32, device=device)
-    else:
-        x_all = torch.empty(M * seq[0][1].K, dtype=torch.float32, device=device)
-    items = []
-    xo = yo = 0
+    out = []
     seed = 1000
-    prev_y = None
-    for layer, lin in seq:
+    for layer, lin in step_linears(args.layers, not args.no_lm_head):
         shards = []
         for rows in lin.shards:
             shards.append(wl.torch_normal((rows, lin.K), lin.sigma, seed, device))
             seed += 1
         biases = [wl.torch_normal((rows,), 0.01, seed + i, device) for i, rows in enumerate(lin.shards)]
         seed += len(lin.shards)
-        ql = QuantLinear.from_float("w4", shards, biases)
+        out.append((layer, lin, QuantLinear.from_float("w4", shards, biases)))
         del shards
-        if args.independent_x or prev_y is None:
+    torch.cuda.synchronize()
+    return out
+
+
+def make_buffers(weights, M: int, independent_x: bool, device, seed: int = 5000):
+    """Per-linear activation buffers for M tokens.  Returns (items, x_in, y_out):
+    x_in is the step's input, y_out the last linear's output (the logits with
+    the lm_head); with independent_x, x_in and y_out hold every linear's input
+    and output instead.  items: (layer, lin, ql, x, y, qx, sx)."""
+    import torch
+    if independent_x:
+        x_all = torch.empty(sum(M * lin.K for _, lin, _ in weights), dtype=torch.float32, device=device)
+        y_all = torch.empty(sum(M * lin.N for _, lin, _ in weights), dtype=torch.float32, device=device)
+    else:
+        x_all = torch.empty(M * weights[0][1].K, dtype=torch.float32, device=device)
+    items = []
+    xo = yo = 0
+    prev_y = None
+    for layer, lin, ql in weights:
+        if independent_x or prev_y is None:
             x = x_all[xo: xo + M * lin.K].view(M, lin.K)
             x.copy_(wl.torch_normal((M, lin.K), 1.0, seed, device))
             xo += M * lin.K
@@ -293,7 +313,7 @@ def build_step(args, device):
                 raise ValueError(f"{lin.name}: the previous output has fewer than M*K values")
             x = prev_y.view(-1)[: M * lin.K].view(M, lin.K)
         seed += 1
-        if args.independent_x:
+        if independent_x:
             y = y_all[yo: yo + M * lin.N].view(M, lin.N)
             yo += M * lin.N
         else:
@@ -303,8 +323,12 @@ def build_step(args, device):
         items.append((layer, lin, ql, x, y, qx, sx))
         prev_y = y
     torch.cuda.synchronize()
-    y_out = y_all if args.independent_x else prev_y.view(-1)
+    y_out = y_all if independent_x else prev_y.view(-1)
     return items, x_all, y_out
+
+
+def build_step(args, device):
+    return make_buffers(build_weights(args, device), args.M, args.independent_x, device)
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:
@@ -537,6 +561,117 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+# ------------------------------------------------------------- suite
+L2_BYTES = 129e6
+
+
+def _timed_graph(fn, stream, steps: int, warmup: int) -> float:
+    """ms per replay of a CUDA graph of fn() on `stream` (CUDA events)."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def suite_gemv(wname: str, lin, M: int, device, stream, steps: int, warmup: int, peak: float) -> dict:
+    """One decode linear timed on its own: back-to-back fused launches (PDL)
+    rotating over enough distinct weight copies (>= 4, > 2.5x L2 in all)
+    that L2 cannot serve the weights."""
+    import math
+
+    import torch
+
+    from bit_quantized_decode_gb300 import W4_FLAG_PDL, QuantLinear
+    b = algorithmic_bytes(lin, M)
+    wbytes = b - 4 * M * (lin.K + lin.N)
+    copies = max(4, math.ceil(2.5 * L2_BYTES / wbytes))
+    qls = []
+    seed = 7000 + lin.N + lin.K
+    for c in range(copies):
+        shards = [wl.torch_normal((rows, lin.K), lin.sigma, seed + 31 * c + i, device) for i, rows in enumerate(lin.shards)]
+        biases = ([wl.torch_normal((rows,), 0.01, seed + 31 * c + 17 + i, device) for i, rows in enumerate(lin.shards)]
+                  if lin.bias else None)
+        qls.append(QuantLinear.from_float(lin.fmt, shards, biases))
+        del shards
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn((M, lin.K), generator=g, device=device, dtype=torch.float32)
+    if wname == "w4a8_single":           # 0.1% of the entries scaled by 20 (seeded choice)
+        n_out = max(1, (M * lin.K) // 1000)
+        idx = torch.randperm(M * lin.K, generator=g, device=device)[:n_out]
+        x.view(-1)[idx] *= 20.0
+    y, qx, sx = qls[0].buffers(M)
+
+    def run():
+        for i, ql in enumerate(qls):
+            ql(x, y, qx, sx, flags=W4_FLAG_PDL if i else 0)
+
+    reps = max(3, min(steps, int(2e5 / copies)))
+    ms = _timed_graph(run, stream, reps, warmup)
+    us = ms * 1e3 / copies
+    gbs = b / us / 1e3
+    del qls
+    torch.cuda.synchronize()
+    return {"suite": wname, "linear": lin.name, "fmt": lin.fmt, "N": lin.N, "K": lin.K, "M": M,
+            "us_per_gemv": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "bytes": b, "weight_copies": copies, "replays": reps}
+
+
+def run_suite(args, local_rank):
+    """Configs 1-4 GEMV by GEMV, then the full step at M = 1, 2, 4, 8, 16.
+    One JSON line per entry."""
+    import torch
+
+    from bit_quantized_decode_gb300 import W4_FLAG_PDL, _lib
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    _lib.clear_device_error()
+    peak, _ = measured_peak()
+    stream = torch.cuda.Stream(device=dev)
+    for wname in (() if args.suite_only_steps else ("w4a8_single", "qwen7b_layer", "gemma_q4_0", "lm_head")):
+        for lin in wl.workload(wname).linears:
+            print(json.dumps(suite_gemv(wname, lin, 1, dev, stream, args.steps, args.warmup, peak)), flush=True)
+    weights = build_weights(args, dev)
+    for kv in args.tune:
+        k, v = kv.split("=")
+        _lib.set_tuning(k, int(v))
+    for M in (int(m) for m in args.suite_ms.split(",")):
+        items, _, _ = make_buffers(weights, M, args.independent_x, dev)
+
+        def step():
+            for i, (_, lin, ql, x, y, qx, sx) in enumerate(items):
+                ql(x, y, qx, sx, flags=W4_FLAG_PDL if i else 0)
+
+        ms = _timed_graph(step, stream, max(3, min(args.steps, 400)), args.warmup)
+        b = sum(algorithmic_bytes(lin, M) for _, lin, *_ in items)
+        gbs = b / (ms / 1e3) / 1e9
+        print(json.dumps({"suite": "qwen7b_step", "M": M, "linears": len(items), "ms_per_step": round(ms, 5),
+                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": b,
+                          "ms_per_token": round(ms / M, 5)}), flush=True)
+        del items
+    err = _lib.device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -546,6 +681,8 @@ def main(argv=None):
         raise SystemExit("--M must be in 1..16")
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.suite:
+        return run_suite(args, local_rank) if rank == 0 else 0
     return run_ours(args, rank, world, local_rank)
 
 

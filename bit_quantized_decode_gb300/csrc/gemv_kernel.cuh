@@ -91,7 +91,8 @@ __device__ __forceinline__ int unit4_signed16(const uint4 w, const uint4 x0, con
 }
 
 // Fused prologue for large M*K: a first pass over x for the absmax, a second
-// to quantize; loads batched four at a time.  One block barrier.
+// to quantize, each in batches of 16 float4 per thread spread over the
+// tokens (all loads of a batch in flight at once).  One block barrier.
 template <int MT, bool kCodeSums>
 __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float* red_s, float* sx_s, int8_t* xs,
                                                        int (&tsum)[MT])
@@ -102,64 +103,81 @@ __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float*
     const int M = a.M;
     const int K = a.K;
     const int K4 = K >> 2;
+    constexpr int kB = MT >= 16 ? 1 : 16 / MT;        // float4 per token per batch
+    float mx[MT];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        float mx = 0.0f;
-        if (m < M) {
+    for (int m = 0; m < MT; ++m) mx[m] = 0.0f;
+    for (int i0 = 0; i0 < K4; i0 += kB * kThreads) {
+        float4 v[MT][kB];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
             const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
-            for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
-                float4 b4[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = i0 + u * kThreads + tid;
-                    b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(b4[u].x), fabsf(b4[u].y)), fmaxf(fabsf(b4[u].z), fabsf(b4[u].w))));
+            for (int u = 0; u < kB; ++u) {
+                const int i = i0 + u * kThreads + tid;
+                v[m][u] = (m < M && i < K4) ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (lane == 0) red_s[warp * MT + m] = mx;
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int u = 0; u < kB; ++u)
+                mx[m] = fmaxf(mx[m], fmaxf(fmaxf(fabsf(v[m][u].x), fabsf(v[m][u].y)),
+                                           fmaxf(fabsf(v[m][u].z), fabsf(v[m][u].w))));
     }
-    __syncthreads();
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        if (m < M) {
-            float amax = red_s[m];
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
-            const A8Scale ks = a8_scale(amax);
-            if (tid == m) {
-                sx_s[m] = ks.s;
-                if (blockIdx.x == 0 && a.sx_out != nullptr) a.sx_out[m] = ks.s;
-            }
-            uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
-            uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
-                                 ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
-                                 : nullptr;
+        for (int off = 16; off > 0; off >>= 1) mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], off));
+        if (lane == 0) red_s[warp * MT + m] = mx[m];
+    }
+    __syncthreads();
+    A8Scale ks[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float amax = red_s[m];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
+        ks[m] = a8_scale(m < M ? amax : 0.0f);
+        if (tid == m) {
+            sx_s[m] = m < M ? ks[m].s : 0.0f;
+            if (m < M && blockIdx.x == 0 && a.sx_out != nullptr) a.sx_out[m] = ks[m].s;
+        }
+    }
+    for (int i0 = 0; i0 < K4; i0 += kB * kThreads) {
+        float4 v[MT][kB];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
             const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
-            for (int i0 = 0; i0 < K4; i0 += 4 * kThreads) {
-                float4 b4[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = i0 + u * kThreads + tid;
-                    b4[u] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+            for (int u = 0; u < kB; ++u) {
+                const int i = i0 + u * kThreads + tid;
+                v[m][u] = (m < M && i < K4) ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                uint32_t* dst = reinterpret_cast<uint32_t*>(xs + static_cast<size_t>(m) * K);
+                uint32_t* gout = (blockIdx.x == 0 && a.qx_out != nullptr)
+                                     ? reinterpret_cast<uint32_t*>(a.qx_out + static_cast<size_t>(m) * K)
+                                     : nullptr;
+                const bool all_exact = a8_needs_exact(ks[m]);
+                const uint64_t rr = f2_pack(ks[m].r, ks[m].r);
+#pragma unroll
+                for (int u = 0; u < kB; ++u) {
                     const int i = i0 + u * kThreads + tid;
                     if (i < K4) {
-                        const uint32_t q = a8_pack4(b4[u], ks);
+                        uint32_t ok = 0xffffffffu;
+                        uint32_t q = a8_pack4_fast2(v[m][u], rr, ok);
+                        // rare: a possible tie (or a tiny scale): the exact quotient decides
+                        if (all_exact || (ok >> 31) == 0u) q = a8_pack4(v[m][u], ks[m]);
                         dst[i] = q;
                         if (gout) gout[i] = q;
                         if constexpr (kCodeSums) tsum[m] += bytesum(q);
                     }
                 }
             }
-        } else if (tid == m) {
-            sx_s[m] = 0.0f;
         }
     }
 }

@@ -105,14 +105,17 @@ int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget, int row_bu
     return s >= 2 ? s : 0;
 }
 
-// Two blocks per SM (this GEMV beside the next one in the stream) when a
-// ring of at least two stages fits in half the SM; else the whole-block
-// budget.  `fused` asks for the quantize prologue.
+// One token: two blocks per SM (this GEMV beside the next one in the stream)
+// when a ring of at least two stages fits in half the SM, else the whole-block
+// budget.  Several tokens: the whole-block budget (a deeper ring pays more
+// than the early start of the next GEMV once the inner loop does M times the
+// DP4A work).  `fused` asks for the quantize prologue.
 bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p)
 {
     const int half = d.smem_per_sm / 2 - d.smem_reserved;
     const int whole = d.smem_optin;
-    const int bps = g_tune[W4_TUNE_BLOCKS_PER_SM];
+    int bps = g_tune[W4_TUNE_BLOCKS_PER_SM];
+    if (bps == 0 && MT > 1) bps = 1;
     const int modes[2] = {fused ? X_FUSED : X_SMEM, fused ? -1 : X_GLOBAL};
     for (int pass = 0; pass < 2; ++pass) {
         // pass 0: co-resident budget (unless forced to one block per SM)

@@ -91,6 +91,8 @@ int w4_version(void);
  *   W4_TUNE_BLOCKS_PER_SM  1: one GEMV block per SM with the whole shared
  *                          memory; 2: half of it, so that a GEMV launched with
  *                          W4_FLAG_PDL is resident beside the previous one.
+ *                          Default: 2 for one token (when a ring fits), 1 for
+ *                          several.
  *   W4_TUNE_MAX_STAGES     cap on the ring depth per warp (>= 2).
  *   W4_TUNE_GRID_BLOCKS    cap on the grid size (default: the SM count).
  *   W4_TUNE_TC_MIN_M       per-row INT4 calls with at least this many tokens

@@ -196,13 +196,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             if (!__shfl_sync(0xffffffffu, static_cast<int>(rdy), 0)) break;
             if (lane < kTcAccs) {
                 // lane l issues K slices l and l + 4 into its own accumulator D[l]
-                // (the first use overwrites) and commits them
+                // (the first use overwrites) and commits them.  A slice is 16 K:
+                // 8 tensor-memory columns of A and 512 B of B (32 in the
+                // descriptor's address field, which cannot carry: B < 2^18 B).
                 tc_fence_after();
-                const uint32_t bb = smem_u32(bbuf + j * kTcBBytes);
-                for (int kk = lane; kk < 2 * nch; kk += kTcAccs)
-                    tc_mma_f16_ts(tbase + kTcColD + lane * kTcTok, tbase + kTcColA + j * 64 + kk * 8,
-                                  smem_desc_noswizzle(bb + kk * 2 * kTcBlbo, kTcBlbo, kTcBsbo), kTcIdesc,
-                                  (b > 0 || kk >= kTcAccs) ? 1u : 0u);
+                const uint64_t bdesc =
+                    smem_desc_noswizzle(smem_u32(bbuf + j * kTcBBytes), kTcBlbo, kTcBsbo) + static_cast<uint64_t>(lane * 32);
+                const uint32_t dcol = tbase + kTcColD + lane * kTcTok;
+                const uint32_t acol = tbase + kTcColA + j * 64 + lane * 8;
+                if (lane < 2 * nch) tc_mma_f16_ts(dcol, acol, bdesc, kTcIdesc, b > 0 ? 1u : 0u);
+                if (lane + kTcAccs < 2 * nch) tc_mma_f16_ts(dcol, acol + kTcAccs * 8, bdesc + kTcAccs * 32, kTcIdesc, 1u);
                 tc_commit(free_b + 8 * j);
             }
             committed = b + 1;

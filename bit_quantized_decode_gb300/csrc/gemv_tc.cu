@@ -26,13 +26,15 @@
 //     (4,6), (5,7) within each 8 weights; the same warps write the fp16
 //     activation tile (B, shared memory, K-major, no swizzle) in that order,
 //     so the sum is unchanged.
-//   * Warp 4 issues the MMAs (lanes 0-3, one accumulator each, so consecutive
-//     MMAs are independent; the four exact partial sums are added at the
-//     end); warp 5 issues the weight copies.  The roles hand K blocks over
-//     through mbarriers only (stage full / empty, operand buffer ready /
-//     free), so no block-wide barrier sits in the K loop.
-//   * The tensor cores are far from busy at N = 16: about 125 cycles per
-//     128 x 16 x 16 MMA per SM bound this kernel, not HBM.
+//   * Lane 0 of warp 4 issues a block's MMAs (K slice kk into accumulator
+//     kk % 4, so consecutive MMAs are independent; the four exact partial sums
+//     are added at the end) and commits them; warp 5 issues the weight copies.
+//     "Operands written" is a named barrier per buffer (warps 0-4), "operands
+//     read" the MMA commit's mbarrier, and the ring has full / empty
+//     mbarriers: no block-wide barrier sits in the K loop.
+//   * What bounds it is the MMA issue inside this pipeline (one block's eight
+//     128 x 16 x 16 MMAs take 900-1900 cycles to issue, against about 45 per
+//     MMA in an isolated loop), not HBM and not the tensor cores' arithmetic.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -114,8 +116,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     const uint32_t bars = smem_u32(smem + L.bars);
     const uint32_t full_b = bars;                        // [S]  stage landed (1 arrival + bytes)
     const uint32_t empty_b = bars + 8 * S;               // [S]  stage read by warps 0-3 (4 arrivals)
-    const uint32_t ready_b = bars + 16 * S;              // [3]  operand buffer written (4 arrivals)
-    const uint32_t free_b = ready_b + 8 * kTcBufs;       // [3]  MMAs reading it completed (4 commits)
+    const uint32_t free_b = bars + 16 * S;               // [3]  MMAs reading an operand buffer completed
+    // operand buffer j written by warps 0-3: named barrier 1 + j (warps 0-4)
+    constexpr uint32_t kReadyCount = 5 * 32;
+    auto ready_arrive = [](int j) {
+        if (j == 0) named_arrive(1, kReadyCount); else if (j == 1) named_arrive(2, kReadyCount); else named_arrive(3, kReadyCount);
+    };
+    auto ready_sync = [](int j) {
+        if (j == 0) named_sync(1, kReadyCount); else if (j == 1) named_sync(2, kReadyCount); else named_sync(3, kReadyCount);
+    };
+    static_assert(kTcBufs == 3, "one named barrier per operand buffer");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem);   // [0] base address, [1] stop flag
     volatile uint32_t* dead_s = tmem_slot + 1;
 
@@ -135,8 +145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             mbar_init(empty_b + 8 * s, 4);
         }
         for (int j = 0; j < kTcBufs; ++j) {
-            mbar_init(ready_b + 8 * j, 4);
-            mbar_init(free_b + 8 * j, kTcAccs);   // one commit per issuing lane
+            mbar_init(free_b + 8 * j, 1);         // the MMA lane's commit
         }
         fence_mbar_init();
         *dead_s = 0u;
@@ -184,34 +193,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     int committed = 0;   // K blocks whose MMAs were committed (MMA warp)
     if (mma_warp) {
         // --------------------------------------------------------- MMA warp
+        // Every K block is synchronised (named barrier) and committed even after a
+        // failure, so that warps 0-3, which arrive once per block and wait for each
+        // buffer's commit in order, never block on a missing step.
         for (int b = 0; b < nb; ++b) {
             const int j = b % kTcBufs;
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
-            // A[j] and B[j] written by warps 0-3
-            bool rdy = true;
+            ready_sync(j);                           // A[j] and B[j] written by warps 0-3
             if (lane == 0) {
-                rdy = !*dead_s && mbar_wait_bounded(ready_b + 8 * j, static_cast<uint32_t>(b / kTcBufs) & 1u, kTcWaitNs);
-                if (!rdy && !*dead_s) fail();
-            }
-            if (!__shfl_sync(0xffffffffu, static_cast<int>(rdy), 0)) break;
-            if (lane < kTcAccs) {
-                // lane l issues K slices l and l + 4 into its own accumulator D[l]
-                // (the first use overwrites) and commits them.  A slice is 16 K:
-                // 8 tensor-memory columns of A and 512 B of B (32 in the
-                // descriptor's address field, which cannot carry: B < 2^18 B).
-                tc_fence_after();
-                const uint64_t bdesc =
-                    smem_desc_noswizzle(smem_u32(bbuf + j * kTcBBytes), kTcBlbo, kTcBsbo) + static_cast<uint64_t>(lane * 32);
-                const uint32_t dcol = tbase + kTcColD + lane * kTcTok;
-                const uint32_t acol = tbase + kTcColA + j * 64 + lane * 8;
-                if (lane < 2 * nch) tc_mma_f16_ts(dcol, acol, bdesc, kTcIdesc, b > 0 ? 1u : 0u);
-                if (lane + kTcAccs < 2 * nch) tc_mma_f16_ts(dcol, acol + kTcAccs * 8, bdesc + kTcAccs * 32, kTcIdesc, 1u);
+                if (!*dead_s) {
+                    // K slice kk (16 K: 8 tensor-memory columns of A, 512 B of B, which is
+                    // 32 in the descriptor's address field and cannot carry) accumulates
+                    // into D[kk % 4]; the first use of each overwrites.
+                    tc_fence_after();
+                    const uint64_t bdesc = smem_desc_noswizzle(smem_u32(bbuf + j * kTcBBytes), kTcBlbo, kTcBsbo);
+                    const uint32_t acol = tbase + kTcColA + j * 64;
+#pragma unroll
+                    for (int kk = 0; kk < 2 * kTcChunks; ++kk)
+                        if (kk < 2 * nch)
+                            tc_mma_f16_ts(tbase + kTcColD + (kk % kTcAccs) * kTcTok, acol + kk * 8,
+                                          bdesc + static_cast<uint64_t>(kk * 32), kTcIdesc,
+                                          (b > 0 || kk >= kTcAccs) ? 1u : 0u);
+                }
                 tc_commit(free_b + 8 * j);
             }
             committed = b + 1;
         }
         if (lane == 0) {
-            // every committed MMA (all four lanes) completes before tensor memory is read or freed
+            // every committed MMA completes before tensor memory is read or freed
             if (committed > 0) {
                 const int last = committed - 1;
                 if (!mbar_wait_bounded(free_b + 8 * (last % kTcBufs), static_cast<uint32_t>(last / kTcBufs) & 1u,
@@ -263,14 +272,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             const int j = b % kTcBufs;
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
             fetch_codes(b + kTcCodeRing - 1);
-            bool ok = !*dead_s;
-            if (ok && sub == 0)
+            // buffer j is free once the commit of block b - 3 arrived (the MMA lane
+            // commits every block, failed or not, so this wait keeps its order)
+            bool ok = b < kTcBufs ||
+                      mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>((b - kTcBufs) / kTcBufs) & 1u, kTcWaitNs);
+            if (ok && !*dead_s && sub == 0)
                 ok = mbar_wait_bounded(full_b + 8 * slot, static_cast<uint32_t>(st / S) & 1u, kTcWaitNs);
-            if (ok && b >= kTcBufs)
-                ok = mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>((b - kTcBufs) / kTcBufs) & 1u, kTcWaitNs);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0 && !*dead_s) fail();
-                break;
+            if (!__all_sync(0xffffffffu, ok) && lane == 0 && !*dead_s) fail();
+            if (*dead_s) {
+                // stop working but keep the per-block handshake
+                cp_async_wait_group<kTcCodeRing - 1>();
+                ready_arrive(j);
+                continue;
             }
             tc_fence_after();
             uint4 u[kTcChunks];
@@ -300,8 +313,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ready_b + 8 * j);
+            ready_arrive(j);
         }
         cp_async_wait_group<0>();
     }

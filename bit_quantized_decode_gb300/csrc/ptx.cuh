@@ -249,6 +249,17 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t
            (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46);
 }
 
+// Named barriers (ids 1..15; id 0 is __syncthreads): `count` threads, a
+// multiple of 32, take part; arrive does not wait, sync waits for all.
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // --------------------------------------------------------------- integer
 // DP4A: c + sum_k a_k * b_k over the four signed bytes of a and b.
 __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)

@@ -226,7 +226,8 @@ bool use_tc(int fmt, int M)
 }
 
 // Tensor-core GEMV: one block per (128-row group, K split); enough splits to
-// cover the SMs (at most kTcMaxSplit) and to keep every split within
+// cover the SMs, rounded down to a power of two (clusters of 5 or 6 blocks
+// measured slower), at most kTcMaxSplit, and enough to keep every split within
 // kTcMaxSplitK; the deepest weight ring that leaves room for a second block
 // per SM.
 w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx, int M,
@@ -251,6 +252,7 @@ w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const 
     const int G = (N + kTcRows - 1) / kTcRows;
     int ks = (dev->sms + G - 1) / G;
     if (ks > kTcMaxSplit) ks = kTcMaxSplit;
+    while (ks & (ks - 1)) --ks;                 // clusters of 1, 2, 4 or 8 blocks
     const int need = (K + kTcMaxSplitK - 1) / kTcMaxSplitK;
     if (ks < need) ks = need;
     if (ks > a.C) ks = a.C;

@@ -125,7 +125,7 @@ def profiled_traffic(alg_bytes_per_launch: float, chain: bool):
     bytes, if the summary was taken on the current kernel sources (else None)."""
     try:
         from bit_quantized_decode_gb300 import build
-        digest = build._inputs_digest()
+        digest = build.kernel_digest()
         name = "gemv_w4_chain_qwen7b_step.md" if chain else "gemv_w4_fused_qwen7b_step.md"
         vals = {}
         with open(os.path.join(ROOT, "profiles", name)) as f:

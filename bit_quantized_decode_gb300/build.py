@@ -52,6 +52,21 @@ def _inputs_digest() -> str:
     return h.hexdigest()
 
 
+# Sources that define the one-token decode GEMV (gemv_kernel<W4, 1, fused>):
+# a profile summary taken on them stays valid while they are unchanged.
+GEMV_W4_SOURCES = ("gemv_kernel.cuh", "quant_a8.cuh", "ptx.cuh", "internal.h", "gemv_w4.cu")
+
+
+def kernel_digest(names=GEMV_W4_SOURCES) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
 def _stamp_path() -> str:
     return LIB + ".stamp"
 

@@ -83,11 +83,14 @@ def step_linears(layers: int, lm_head: bool):
 def algorithmic_bytes(lin, M: int) -> int:
     """Bytes one decode linear must move: its weights in their packed format
     (per-row INT4: 0.5 B a weight + a 4-byte scale a row; Q4_0: 18 B per 32
-    weights; i8g32: 1 B a weight + 2 B per 32), the bias, fp32 x and fp32 y."""
+    weights; i8g32: 1 B a weight + 2 B per 32; q6g32: 26 B per 32), the bias,
+    fp32 x and fp32 y."""
     if lin.fmt == "w4":
         w = lin.N * lin.K // 2 + 4 * lin.N
     elif lin.fmt == "q4_0":
         w = lin.N * (lin.K // 32) * 18
+    elif lin.fmt == "q6g32":
+        w = lin.N * (lin.K // 32) * 26
     else:
         w = lin.N * lin.K + lin.N * (lin.K // 32) * 2
     return w + (4 * lin.N if lin.bias else 0) + 4 * M * lin.K + 4 * M * lin.N
@@ -646,7 +649,10 @@ def run_suite(args, local_rank):
     peak, _ = measured_peak()
     stream = torch.cuda.Stream(device=dev)
     for wname in (() if args.suite_only_steps else ("w4a8_single", "qwen7b_layer", "gemma_q4_0", "lm_head")):
-        for lin in wl.workload(wname).linears:
+        lins = list(wl.workload(wname).linears)
+        if wname == "lm_head":
+            lins.append(wl.gemma_lm_head_q6g32())   # the same values packed in 6 bits
+        for lin in lins:
             print(json.dumps(suite_gemv(wname, lin, 1, dev, stream, args.steps, args.warmup, peak)), flush=True)
     weights = build_weights(args, dev)
     for kv in args.tune:

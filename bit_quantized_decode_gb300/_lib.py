@@ -50,17 +50,21 @@ SIGNATURES = {
     "w4_repacked_bytes": ([_I, _I], _SZ),
     "q4_0_repacked_bytes": ([_I, _I], _SZ),
     "i8g32_repacked_bytes": ([_I, _I], _SZ),
+    "q6g32_repacked_bytes": ([_I, _I], _SZ),
     "w4_repack": ([_PP, _PI, _I, _I, _P, _SZ, _P], _I),
     "q4_0_repack": ([_PP, _PI, _I, _I, _P, _SZ, _P], _I),
     "i8g32_repack": ([_PP, _PP, _PI, _I, _I, _P, _SZ, _P], _I),
+    "q6g32_repack": ([_PP, _PP, _PI, _I, _I, _P, _SZ, _P], _I),
     "w4_concat_f32": ([_PP, _PI, _I, _P, _P], _I),
     "a8_quantize": ([_P, _I, _I, _P, _P, _P], _I),
     "w4a8_gemv": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
     "q4_0_gemv": ([_P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
     "i8g32_gemv": ([_P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "q6g32_gemv": ([_P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
     "w4a8_linear": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P], _I),
     "q4_0_linear": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P], _I),
     "i8g32_linear": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P], _I),
+    "q6g32_linear": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _U, _P], _I),
     "w4_device_error": ([ctypes.POINTER(ctypes.c_uint)], _I),
     "w4_clear_device_error": ([], _I),
 }
@@ -163,6 +167,10 @@ def q4_0_repacked_bytes(N: int, K: int) -> int:
     return int(load().q4_0_repacked_bytes(N, K))
 
 
+def q6g32_repacked_bytes(N: int, K: int) -> int:
+    return int(load().q6g32_repacked_bytes(N, K))
+
+
 def i8g32_repacked_bytes(N: int, K: int) -> int:
     return int(load().i8g32_repacked_bytes(N, K))
 
@@ -216,6 +224,16 @@ def i8g32_repack(q_shards, d_shards, K, out, stream=None):
                                                out.numel() * out.element_size(), _stream(stream)))
 
 
+def q6g32_repack(q_shards, d_shards, K, out, stream=None):
+    """Pack I8G32 canonical shards (codes in [-32, 31]) into the 6-bit device layout."""
+    _dev(out, *q_shards, *d_shards)
+    qp, keep = _ptr_array(q_shards)
+    dp, keep2 = _ptr_array(d_shards)
+    rows, keep3 = _int_array([s.shape[0] for s in q_shards])
+    _check("q6g32_repack", load().q6g32_repack(qp, dp, rows, len(q_shards), K, _ptr(out),
+                                               out.numel() * out.element_size(), _stream(stream)))
+
+
 def w4_concat_f32(parts, out, stream=None):
     _dev(out, *parts)
     pp, keep = _ptr_array(parts)
@@ -256,6 +274,14 @@ def i8g32_gemv(w, bias, qx, sx, y, stream=None):
                                            _stream(stream)))
 
 
+def q6g32_gemv(w, bias, qx, sx, y, stream=None):
+    _dev(w, bias, qx, sx, y)
+    M, K = qx.shape
+    N = y.shape[1]
+    _check("q6g32_gemv", load().q6g32_gemv(_ptr(w), _ptr(bias), _ptr(qx), _ptr(sx), M, N, K, _ptr(y),
+                                           _stream(stream)))
+
+
 def w4a8_linear(w, s_w, bias, x, y, qx, sx, flags: int = 0, stream=None):
     """Quantize x and run the per-row INT4 GEMV in one launch; y[M][N]."""
     _dev(w, s_w, bias, x, y, qx, sx)
@@ -278,6 +304,14 @@ def i8g32_linear(w, bias, x, y, qx, sx, flags: int = 0, stream=None):
     M, K = x.shape
     N = y.shape[1]
     _check("i8g32_linear", load().i8g32_linear(_ptr(w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx), _ptr(sx),
+                                               flags, _stream(stream)))
+
+
+def q6g32_linear(w, bias, x, y, qx, sx, flags: int = 0, stream=None):
+    _dev(w, bias, x, y, qx, sx)
+    M, K = x.shape
+    N = y.shape[1]
+    _check("q6g32_linear", load().q6g32_linear(_ptr(w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx), _ptr(sx),
                                                flags, _stream(stream)))
 
 

@@ -30,7 +30,8 @@ NVCC_FLAGS = [
     "-Xptxas", "-v",
     "-I", INCLUDE,
 ]
-SOURCES = ["w4a8_api.cu", "prep_kernels.cu", "gemv_w4.cu", "gemv_q4_0.cu", "gemv_i8g32.cu", "gemv_tc.cu"]
+SOURCES = ["w4a8_api.cu", "prep_kernels.cu", "gemv_w4.cu", "gemv_q4_0.cu", "gemv_i8g32.cu", "gemv_q6g32.cu",
+           "gemv_tc.cu"]
 
 
 def nvcc() -> str:

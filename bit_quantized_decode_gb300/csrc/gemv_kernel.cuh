@@ -351,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
     constexpr int kSlotW = fmt_slot_w_bytes(FMT);
     constexpr int kSlot = fmt_slot_bytes(FMT);
     constexpr bool kGroup = fmt_group(FMT);
+    constexpr int kHi = fmt_hi_bytes(FMT);           // Q6G32 high-part plane, bytes per unit
+    constexpr int kSlotH = fmt_slot_h_bytes(FMT);
     constexpr bool kCodeSums = FMT == FMT_W4;        // activation code sums for the nibble bias
     constexpr int kPassLines = 16;
     constexpr int kRowBufs = NCH == 1 ? 1 : 2;       // per-row parameter buffers (by linear parity)
@@ -454,10 +456,12 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
             const uint32_t bar = my_bars + 8 * islot;
             const uint32_t bw = static_cast<uint32_t>(n * kLineBytes);
             const uint32_t bs = kGroup ? static_cast<uint32_t>(n * kRows * 2) : 0u;
+            const uint32_t bh = static_cast<uint32_t>(n * kRows * kHi);
             if (issued >= S) fence_proxy_async_smem();   // the slot was read before
-            mbar_arrive_expect_tx(bar, bw + bs);
+            mbar_arrive_expect_tx(bar, bw + bh + bs);
             bulk_g2s(smem_u32(dst), ia.w + unit0 * kUnit, bw, bar, pol);
-            if (kGroup) bulk_g2s(smem_u32(dst + kSlotW), ia.wscale + unit0, bs, bar, pol);
+            if (kHi > 0) bulk_g2s(smem_u32(dst + kSlotW), ia.whi + unit0 * kHi, bh, bar, pol);
+            if (kGroup) bulk_g2s(smem_u32(dst + kSlotW + kSlotH), ia.wscale + unit0, bs, bar, pol);
         }
         ++issued;
         if (++islot == S) islot = 0;
@@ -650,14 +654,53 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
                 }
                 if (!dead) {
                     const uint8_t* sw = my_ring + static_cast<size_t>(slot) * kSlot;
-                    const __half* sd = reinterpret_cast<const __half*>(sw + kSlotW);
+                    const __half* sd = reinterpret_cast<const __half*>(sw + kSlotW + kSlotH);
 #pragma unroll
                     for (int pass = 0; pass < kSL / kPassLines; ++pass) {
                         const int line = pass * kPassLines + pl;
                         if (line < n) {
                             const int chunk = c + line;
                             const uint8_t* ub = sw + (line * kRows + 4 * h) * kUnit;
-                            if constexpr (FMT == FMT_I8G32) {
+                            if constexpr (FMT == FMT_Q6G32) {
+                                // n = q + 32 = lo + 16 hi: sum n x from the two planes,
+                                // minus 32 sum x, is the exact group sum of q x
+                                const uint8_t* hb = sw + kSlotW + (line * kRows + 4 * h) * kHi;
+                                uint4 wv[4];
+                                uint2 hv[4];
+                                float d[4];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    wv[j] = *reinterpret_cast<const uint4*>(ub + ((j ^ pp) << 4));
+                                    hv[j] = *reinterpret_cast<const uint2*>(hb + ((j ^ pp) << 3));
+                                    d[j] = __half2float(sd[line * kRows + 4 * h + (j ^ pp)]);
+                                }
+#pragma unroll
+                                for (int m = 0; m < MT; ++m) {
+                                    if (MT == 1 || m < M) {
+                                        uint4 x0, x1;
+                                        load_x(m, chunk, x0, x1);
+                                        int xs32 = bytesum(x0.x) + bytesum(x0.y) + bytesum(x0.z) + bytesum(x0.w);
+                                        xs32 += bytesum(x1.x) + bytesum(x1.y) + bytesum(x1.z) + bytesum(x1.w);
+#pragma unroll
+                                        for (int j = 0; j < 4; ++j) {
+                                            int B, A;
+                                            unit4(wv[j], x0, x1, B, A);
+                                            // high part of weight 16w+4s+b: word w, byte b, bits 2s..2s+1
+                                            int s0 = dp4a_us(hv[j].x & 0x03030303u, x0.x, 0);
+                                            s0 = dp4a_us(hv[j].y & 0x03030303u, x1.x, s0);
+                                            int s1 = dp4a_us(hv[j].x & 0x0C0C0C0Cu, x0.y, 0);
+                                            s1 = dp4a_us(hv[j].y & 0x0C0C0C0Cu, x1.y, s1);
+                                            int s2 = dp4a_us(hv[j].x & 0x30303030u, x0.z, 0);
+                                            s2 = dp4a_us(hv[j].y & 0x30303030u, x1.z, s2);
+                                            int s3 = dp4a_us(hv[j].x & 0xC0C0C0C0u, x0.w, 0);
+                                            s3 = dp4a_us(hv[j].y & 0xC0C0C0C0u, x1.w, s3);
+                                            const int hs = s0 + (s1 >> 2) + (s2 >> 4) + (s3 >> 6);
+                                            const int g = B + (A >> 4) + 16 * hs - 32 * xs32;
+                                            acc[m][j] = __fmaf_rn(d[j], __int2float_rn(g), acc[m][j]);
+                                        }
+                                    }
+                                }
+                            } else if constexpr (FMT == FMT_I8G32) {
                                 uint4 w0[4], w1[4];
                                 float d[4];
 #pragma unroll

@@ -7,7 +7,7 @@
 
 namespace w4k {
 
-enum FmtId { FMT_W4 = 0, FMT_Q4_0 = 1, FMT_I8G32 = 2 };
+enum FmtId { FMT_W4 = 0, FMT_Q4_0 = 1, FMT_I8G32 = 2, FMT_Q6G32 = 3 };
 
 constexpr int kRows = 8;                 // weight rows per tile
 constexpr int kWarps = 8;                // warps per GEMV thread block
@@ -20,17 +20,25 @@ constexpr int kRowCache = 1024;          // rows per block whose s_w / bias are 
 enum XMode { X_FUSED = 0, X_SMEM = 1, X_GLOBAL = 2 };
 
 // Lines (8 rows x one 32-weight chunk) per ring slot and bytes per unit.
+// Q6G32 keeps each unit in two planes: 16 bytes of low nibbles and 8 bytes
+// of 2-bit high parts (fmt_hi_bytes).
 __host__ __device__ constexpr int fmt_unit_bytes(int fmt) { return fmt == FMT_I8G32 ? 32 : 16; }
+__host__ __device__ constexpr int fmt_hi_bytes(int fmt) { return fmt == FMT_Q6G32 ? 8 : 0; }
 __host__ __device__ constexpr bool fmt_group(int fmt) { return fmt != FMT_W4; }
-__host__ __device__ constexpr int fmt_slice_lines(int fmt) { return fmt == FMT_I8G32 ? 16 : 32; }
+__host__ __device__ constexpr int fmt_slice_lines(int fmt) { return fmt == FMT_I8G32 || fmt == FMT_Q6G32 ? 16 : 32; }
 __host__ __device__ constexpr int fmt_slot_w_bytes(int fmt) { return fmt_slice_lines(fmt) * kRows * fmt_unit_bytes(fmt); }
+__host__ __device__ constexpr int fmt_slot_h_bytes(int fmt) { return fmt_slice_lines(fmt) * kRows * fmt_hi_bytes(fmt); }
 __host__ __device__ constexpr int fmt_slot_s_bytes(int fmt) { return fmt_group(fmt) ? fmt_slice_lines(fmt) * kRows * 2 : 0; }
-__host__ __device__ constexpr int fmt_slot_bytes(int fmt) { return fmt_slot_w_bytes(fmt) + fmt_slot_s_bytes(fmt); }
+__host__ __device__ constexpr int fmt_slot_bytes(int fmt)
+{
+    return fmt_slot_w_bytes(fmt) + fmt_slot_h_bytes(fmt) + fmt_slot_s_bytes(fmt);
+}
 
 // One linear of a launch.
 struct GemvArgs {
     const uint8_t* w;        // repacked units
-    const uint16_t* wscale;  // fp16 group-scale plane (Q4_0, I8G32), else null
+    const uint16_t* wscale;  // fp16 group-scale plane (Q4_0, I8G32, Q6G32), else null
+    const uint8_t* whi;      // high-part plane (Q6G32), else null
     const float* s_w;        // per-row scales (W4), else null
     const float* bias;       // [N] or null
     const float* x;          // fp32 activations [M][K] (fused quantize), else null
@@ -92,6 +100,8 @@ cudaError_t launch_gemv_w4(const ChainParams<1>& p, int MT, int xmode, int grid,
 cudaError_t launch_gemv_q4_0(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
                              cudaStream_t s);
 cudaError_t launch_gemv_i8g32(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
+                              cudaStream_t s);
+cudaError_t launch_gemv_q6g32(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
                               cudaStream_t s);
 // Chains of per-row INT4 linears (cooperative launch, fused quantization).
 cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
@@ -162,5 +172,6 @@ cudaError_t launch_i8g32_quantize(const float* W, int N, int K, int8_t* q, uint1
 cudaError_t launch_w4_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
 cudaError_t launch_q4_0_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
 cudaError_t launch_i8g32_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
+cudaError_t launch_q6g32_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
 
 }  // namespace w4k

@@ -354,7 +354,61 @@ __global__ void i8g32_repack_kernel(const ShardTable st, int N, int K, long long
     plane[u] = dbits;
 }
 
+// Q6G32: the i8g32 codes q in [-32, 31], biased n = q + 32 (6 bits), packed
+// into a low plane (n & 15, same nibble places as the per-row INT4 unit: word
+// w, byte b holds weight 8w+b low and 8w+4+b high) and a high plane (n >> 4,
+// two bits: word h, byte b, bits 2s..2s+1 hold weight 16h+4s+b).
+__global__ void q6g32_repack_kernel(const ShardTable st, int N, int K, long long units, uint4* __restrict__ lo,
+                                    uint2* __restrict__ hi, uint16_t* __restrict__ plane)
+{
+    const long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (u >= units) return;
+    const int C = K / 32;
+    const int r = static_cast<int>(u % kRows);
+    const long long tc = u / kRows;
+    const int c = static_cast<int>(tc % C);
+    const long long t = tc / C;
+    const long long row = t * kRows + r;
+    uint32_t lw[4] = {0u, 0u, 0u, 0u};
+    uint32_t hw[2] = {0u, 0u};
+    uint16_t dbits = 0;
+    int local = 0;
+    if (row < N) {
+        const int s = shard_of(st, static_cast<int>(row), local);
+        const int8_t* src = static_cast<const int8_t*>(st.p[s]) + static_cast<size_t>(local) * K + c * 32;
+        uint32_t n[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) n[k] = static_cast<uint32_t>(src[k] + 32) & 63u;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                lw[w] |= ((n[8 * w + b] & 15u) | ((n[8 * w + 4 + b] & 15u) << 4)) << (8 * b);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) hw[h] |= (n[16 * h + 4 * s2 + b] >> 4) << (8 * b + 2 * s2);
+        dbits = static_cast<const uint16_t*>(st.p2[s])[static_cast<size_t>(local) * C + c];
+    }
+    lo[u] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    hi[u] = make_uint2(hw[0], hw[1]);
+    plane[u] = dbits;
+}
+
 static inline unsigned blocks_for(long long n, int t) { return static_cast<unsigned>((n + t - 1) / t); }
+
+cudaError_t launch_q6g32_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s)
+{
+    const long long T = (N + kRows - 1) / kRows;
+    const long long units = T * (K / 32) * kRows;
+    uint8_t* base = static_cast<uint8_t*>(out);
+    q6g32_repack_kernel<<<blocks_for(units, 256), 256, 0, s>>>(st, N, K, units, reinterpret_cast<uint4*>(base),
+                                                              reinterpret_cast<uint2*>(base + units * 16),
+                                                              reinterpret_cast<uint16_t*>(base + units * 24));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_w4_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s)
 {

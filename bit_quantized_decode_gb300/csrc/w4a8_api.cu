@@ -163,7 +163,8 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     cudaError_t e;
     if (fmt == FMT_W4) e = launch_gemv_w4(cp, MT, p.xmode, grid, p.smem, pdl, s);
     else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(cp, MT, p.xmode, grid, p.smem, pdl, s);
-    else e = launch_gemv_i8g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
+    else if (fmt == FMT_I8G32) e = launch_gemv_i8g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
+    else e = launch_gemv_q6g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
     return cuda_status(e);
 }
 
@@ -282,8 +283,10 @@ w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bia
     GemvArgs a = {};
     a.w = static_cast<const uint8_t*>(w);
     const size_t units = tiles(N) * kRows * (K / 32);
+    a.whi = fmt_hi_bytes(fmt) > 0 ? a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)) : nullptr;
     a.wscale = fmt == FMT_W4 ? nullptr
-                             : reinterpret_cast<const uint16_t*>(a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)));
+                             : reinterpret_cast<const uint16_t*>(
+                                   a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt) + fmt_hi_bytes(fmt)));
     a.s_w = s_w;
     a.bias = bias;
     a.qx_in = qx;
@@ -317,8 +320,10 @@ w4_status linear_common(int fmt, const void* w, const float* s_w, const float* b
     GemvArgs a = {};
     a.w = static_cast<const uint8_t*>(w);
     const size_t units = tiles(N) * kRows * (K / 32);
+    a.whi = fmt_hi_bytes(fmt) > 0 ? a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)) : nullptr;
     a.wscale = fmt == FMT_W4 ? nullptr
-                             : reinterpret_cast<const uint16_t*>(a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)));
+                             : reinterpret_cast<const uint16_t*>(
+                                   a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt) + fmt_hi_bytes(fmt)));
     a.s_w = s_w;
     a.bias = bias;
     a.x = x;
@@ -415,6 +420,12 @@ size_t i8g32_repacked_bytes(int N, int K)
     return tiles(N) * kRows * (static_cast<size_t>(K) + static_cast<size_t>(K) / 16);
 }
 
+size_t q6g32_repacked_bytes(int N, int K)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0) return 0;
+    return tiles(N) * kRows * (static_cast<size_t>(K) / 2 + static_cast<size_t>(K) / 4 + static_cast<size_t>(K) / 16);
+}
+
 w4_status w4_repack(const uint32_t* const* shard_packed, const int* shard_rows, int n_shards, int K, void* out,
                     size_t out_bytes, w4_stream_t s)
 {
@@ -471,6 +482,26 @@ w4_status i8g32_repack(const int8_t* const* shard_q, const uint16_t* const* shar
     return cuda_status(launch_i8g32_repack(st, N, K, out, reinterpret_cast<cudaStream_t>(s)));
 }
 
+w4_status q6g32_repack(const int8_t* const* shard_q, const uint16_t* const* shard_d, const int* shard_rows,
+                       int n_shards, int K, void* out, size_t out_bytes, w4_stream_t s)
+{
+    if (K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0 || K > W4_MAX_K) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (shard_d == nullptr) return W4_ERR_INVALID_ARG;
+    ShardTable st;
+    int N = 0;
+    w4_status r = build_shards(reinterpret_cast<const void* const*>(shard_q), reinterpret_cast<const void* const*>(shard_d),
+                               shard_rows, n_shards, st, N);
+    if (r != W4_OK) return r;
+    if (N == 0) return W4_OK;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (out_bytes < q6g32_repacked_bytes(N, K)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16)) return W4_ERR_MISALIGNED;
+    for (int i = 0; i < n_shards; ++i)
+        if (st.p2[i] && !aligned(st.p2[i], 2)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_q6g32_repack(st, N, K, out, reinterpret_cast<cudaStream_t>(s)));
+}
+
 w4_status w4_concat_f32(const float* const* parts, const int* lens, int n_parts, float* out, w4_stream_t s)
 {
     if (n_parts < 0 || (n_parts > 0 && (!parts || !lens))) return W4_ERR_INVALID_ARG;
@@ -513,6 +544,19 @@ w4_status i8g32_gemv(const void* w, const float* bias, const int8_t* qx, const f
                      float* y, w4_stream_t s)
 {
     return gemv_common(FMT_I8G32, w, nullptr, bias, qx, sx, M, N, K, y, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status q6g32_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx, int M, int N, int K,
+                     float* y, w4_stream_t s)
+{
+    return gemv_common(FMT_Q6G32, w, nullptr, bias, qx, sx, M, N, K, y, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status q6g32_linear(const void* w, const float* bias, const float* x, int M, int N, int K, float* y, int8_t* qx,
+                       float* sx, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_Q6G32, w, nullptr, bias, x, M, N, K, y, qx, sx, flags,
+                         reinterpret_cast<cudaStream_t>(s));
 }
 
 w4_status w4a8_linear(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,

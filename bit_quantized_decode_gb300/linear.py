@@ -11,7 +11,7 @@ import torch
 
 from . import _lib
 
-FORMATS = ("w4", "q4_0", "i8g32")
+FORMATS = ("w4", "q4_0", "i8g32", "q6g32")
 
 
 class QuantLinear:
@@ -45,7 +45,7 @@ class QuantLinear:
                 b = torch.empty((n, K // 32, 18), dtype=torch.uint8, device=dev)
                 _lib.q4_0_quantize(W, b)
                 canon.append(b)
-            else:
+            else:   # i8g32 and q6g32 share the canonical codes (6-bit values in int8)
                 q = torch.empty((n, K), dtype=torch.int8, device=dev)
                 d = torch.empty((n, K // 32), dtype=torch.int16, device=dev)
                 _lib.i8g32_quantize(W, q, d)
@@ -60,8 +60,9 @@ class QuantLinear:
     @classmethod
     def from_canonical(cls, fmt: str, canon, K: int, scales=None, biases=None) -> "QuantLinear":
         """Repack already-quantized canonical shards (device tensors)."""
-        dev = (canon[0][0] if fmt == "i8g32" else canon[0]).device
-        N = sum((c[0] if fmt == "i8g32" else c).shape[0] for c in canon)
+        grouped = fmt in ("i8g32", "q6g32")
+        dev = (canon[0][0] if grouped else canon[0]).device
+        N = sum((c[0] if grouped else c).shape[0] for c in canon)
         w, s_w = cls._repack(fmt, canon, scales or [], N, K, dev)
         bias = None
         if biases is not None:
@@ -80,9 +81,12 @@ class QuantLinear:
         elif fmt == "q4_0":
             w = torch.empty(_lib.q4_0_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
             _lib.q4_0_repack(canon, K, w)
-        else:
+        elif fmt == "i8g32":
             w = torch.empty(_lib.i8g32_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
             _lib.i8g32_repack([c[0] for c in canon], [c[1] for c in canon], K, w)
+        else:
+            w = torch.empty(_lib.q6g32_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
+            _lib.q6g32_repack([c[0] for c in canon], [c[1] for c in canon], K, w)
         return w, s_w
 
     # ------------------------------------------------------------ per token
@@ -104,8 +108,10 @@ class QuantLinear:
             _lib.w4a8_linear(self.w, self.s_w, self.bias, x, y, qx, sx, flags, stream)
         elif self.fmt == "q4_0":
             _lib.q4_0_linear(self.w, self.bias, x, y, qx, sx, flags, stream)
-        else:
+        elif self.fmt == "i8g32":
             _lib.i8g32_linear(self.w, self.bias, x, y, qx, sx, flags, stream)
+        else:
+            _lib.q6g32_linear(self.w, self.bias, x, y, qx, sx, flags, stream)
         return y
 
     def gemv(self, qx, sx, y, stream=None):
@@ -114,8 +120,10 @@ class QuantLinear:
             _lib.w4a8_gemv(self.w, self.s_w, self.bias, qx, sx, y, stream)
         elif self.fmt == "q4_0":
             _lib.q4_0_gemv(self.w, self.bias, qx, sx, y, stream)
-        else:
+        elif self.fmt == "i8g32":
             _lib.i8g32_gemv(self.w, self.bias, qx, sx, y, stream)
+        else:
+            _lib.q6g32_gemv(self.w, self.bias, qx, sx, y, stream)
         return y
 
     @property

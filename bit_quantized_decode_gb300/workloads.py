@@ -78,6 +78,11 @@ def gemma_lm_head_i8g32() -> Linear:
     return Linear("lm_head_i8g32", (GEMMA_VOCAB,), GEMMA_HIDDEN, fmt="i8g32", bias=True, sigma=0.02)
 
 
+def gemma_lm_head_q6g32() -> Linear:
+    """The same 6-bit lm_head values packed in 6 bits instead of widened to int8."""
+    return Linear("lm_head_q6g32", (GEMMA_VOCAB,), GEMMA_HIDDEN, fmt="q6g32", bias=True, sigma=0.02)
+
+
 @dataclass(frozen=True)
 class Workload:
     name: str

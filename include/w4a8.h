@@ -44,6 +44,13 @@
  *         T*8*C*16 + ((t*C + c)*8 + r)*2.
  *   I8G32: 32 bytes per unit (the 32 int8 in order) at ((t*C + c)*8 + r)*32,
  *         then the fp16 d plane at byte T*8*C*32 + ((t*C + c)*8 + r)*2.
+ *   Q6G32 (the I8G32 values, q in [-32, 31], packed in 6 bits; a layout of
+ *         this library, [310B-Gemma4] §3.2 widens them to int8 instead):
+ *         n = q + 32.  A low plane of 16 bytes per unit at ((t*C + c)*8 + r)*16
+ *         holding n & 15 with the W4 nibble places; a high plane of 8 bytes per
+ *         unit at T*8*C*16 + ((t*C + c)*8 + r)*8 holding n >> 4, weight
+ *         32c+16h+4s+b in bits 2s..2s+1 of byte b of word h; then the fp16 d
+ *         plane at T*8*C*24 + ((t*C + c)*8 + r)*2.  0.8125 bytes per weight.
  */
 #ifndef W4A8_H
 #define W4A8_H
@@ -148,6 +155,12 @@ size_t i8g32_repacked_bytes(int N, int K);
 w4_status i8g32_repack(const int8_t* const* shard_q, const uint16_t* const* shard_d, const int* shard_rows,
                        int n_shards, int K, void* out, size_t out_bytes, w4_stream_t s);
 
+/* Q6G32 from the I8G32 canonical format (codes must lie in [-32, 31], as
+ * i8g32_quantize makes them; other codes are packed modulo 64). */
+size_t q6g32_repacked_bytes(int N, int K);
+w4_status q6g32_repack(const int8_t* const* shard_q, const uint16_t* const* shard_d, const int* shard_rows,
+                       int n_shards, int K, void* out, size_t out_bytes, w4_stream_t s);
+
 /* Concatenate per-shard float vectors (per-row scales s_w, bias) into `out`
  * in shard order.  parts: HOST array of device pointers; lens: HOST array. */
 w4_status w4_concat_f32(const float* const* parts, const int* lens, int n_parts, float* out, w4_stream_t s);
@@ -168,7 +181,7 @@ w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_st
  * w4a8_gemv, [Orin-INT4] §"从 FP 线性层到 INT4 DP4A 的数学推导" and §"DP4A 做了什么":
  *   acc[m][j] = sum_i q_w[j][i] * qx[m][i]   (exact int32, DP4A),
  *   y[m][j]   = fmaf(s_w[j] * sx[m], (float)acc, b[j])   (b = 0 if bias NULL).
- * q4_0_gemv / i8g32_gemv, [310B-Gemma4] §3.1 / §3.2:
+ * q4_0_gemv / i8g32_gemv / q6g32_gemv, [310B-Gemma4] §3.1 / §3.2:
  *   acc_g = exact int32 sum over 32-block g,
  *   y[m][j] = fmaf(sx[m], sum_g d_g * acc_g, b[j])  (fp32; group order unspecified).
  * w: repacked weights; s_w: float [N]; bias: float [N] or NULL; qx: int8 [M][K];
@@ -179,6 +192,8 @@ w4_status w4a8_gemv(const void* w, const float* s_w, const float* bias, const in
 w4_status q4_0_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx,
                     int M, int N, int K, float* y, w4_stream_t s);
 w4_status i8g32_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx,
+                     int M, int N, int K, float* y, w4_stream_t s);
+w4_status q6g32_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx,
                      int M, int N, int K, float* y, w4_stream_t s);
 
 /* ------------------------------------------------------------------------
@@ -196,6 +211,8 @@ w4_status w4a8_linear(const void* w, const float* s_w, const float* bias, const 
 w4_status q4_0_linear(const void* w, const float* bias, const float* x, int M, int N, int K,
                       float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
 w4_status i8g32_linear(const void* w, const float* bias, const float* x, int M, int N, int K,
+                       float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
+w4_status q6g32_linear(const void* w, const float* bias, const float* x, int M, int N, int K,
                        float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
 
 /* ------------------------------------------------------------------------

@@ -97,3 +97,23 @@ def decode_i8_units(raw: np.ndarray, N: int, K: int) -> np.ndarray:
     T = _tiles(N)
     units = raw[: T * C * 8 * 32].view(np.int8).reshape(T, C, 8, 32)
     return units.transpose(0, 2, 1, 3).reshape(T * 8, K)[:N]
+
+
+def decode_q6g32(raw: np.ndarray, N: int, K: int):
+    """Q6G32 device layout -> (int8 codes [N][K], float64 scales [N][K/32])."""
+    C = K // 32
+    T = _tiles(N)
+    units = T * C * 8
+    lo = raw[: units * 16].reshape(T, C, 8, 4, 4)                       # t, c, r, word, byte
+    lo_l = (lo & 0xF).astype(np.int16)
+    lo_h = (lo >> 4).astype(np.int16)
+    low = np.concatenate([lo_l, lo_h], axis=4).reshape(T, C, 8, 32)    # weight 8w+b, 8w+4+b
+    hi = raw[units * 16: units * 24].reshape(T, C, 8, 2, 4)            # t, c, r, word h, byte b
+    shifts = np.array([0, 2, 4, 6], np.uint8)
+    hv = (hi[..., None, :] >> shifts[:, None]) & 3                     # t, c, r, h, s, b
+    high = hv.reshape(T, C, 8, 32).astype(np.int16)                    # weight 16h + 4s + b
+    n = low + 16 * high
+    q = (n - 32).transpose(0, 2, 1, 3).reshape(T * 8, K)[:N].astype(np.int8)
+    plane = raw[units * 24: units * 26].view(np.uint16).reshape(T, C, 8)
+    d = plane.transpose(0, 2, 1).reshape(T * 8, C)[:N].view(np.float16).astype(np.float64)
+    return q, d

@@ -69,10 +69,13 @@ def _load():
                 "orc_gemv_q4_0": [P, P, P, P, I, I, I, P, P],
                 "orc_quantize_i8g32": [P, I, I, P, P],
                 "orc_gemv_i8g32": [P, P, P, P, P, I, I, I, P, P],
+                "orc_glu": [P, P, I, I, P],
             }.items():
                 f = getattr(lib, name)
                 f.argtypes = args
                 f.restype = ctypes.c_int
+            lib.orc_rmsnorm_f32.argtypes = [P, P, ctypes.c_float, I, I, P]
+            lib.orc_rmsnorm_f32.restype = ctypes.c_int
             lib.orc_dp4a.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int32]
             lib.orc_dp4a.restype = ctypes.c_int32
             lib.orc_q4_0_block_bytes.argtypes = []
@@ -251,3 +254,38 @@ def gemv_i8g32(q, d, qx, sx, bias=None, want_acc=False):
 
 def row_weight_bytes(K: int, bits: int) -> int:
     return int(_load().orc_row_weight_bytes(K, bits))
+
+
+# ---------------------------------------------- operators around the linear
+GLU_SILU = 1
+GLU_GELU_TANH = 2
+
+
+def rmsnorm_f32(x, g, eps):
+    """RMSNorm per token in fp32 steps: (x * (1 / sqrt(sum x^2 / K + eps))) * g."""
+    x = _c(np.atleast_2d(x), np.float32)
+    M, K = x.shape
+    g = _c(g, np.float32)
+    assert g.shape == (K,)
+    out = np.zeros((M, K), np.float32)
+    _check(_load().orc_rmsnorm_f32(_ptr(x), _ptr(g), float(eps), M, K, _ptr(out)), "rmsnorm_f32")
+    return out
+
+
+def glu(gate, up, kind):
+    """act(gate) * up in fp64; kind GLU_SILU (SwiGLU) or GLU_GELU_TANH."""
+    gate = _c(gate, np.float64)
+    up = _c(up, np.float64)
+    assert gate.shape == up.shape
+    out = np.zeros(gate.shape, np.float64)
+    _check(_load().orc_glu(_ptr(gate), _ptr(up), gate.size, int(kind), _ptr(out)), "glu")
+    return out
+
+
+def rmsnorm_w4a8_linear(packed, sw, x, g, eps, bias=None):
+    """RMSNorm, then the per-row INT4 decode linear on the normalized tokens.
+
+    Returns (y fp64 [M][N], qx, sx, acc, xn)."""
+    xn = rmsnorm_f32(x, g, eps)
+    y, qx, sx, acc = w4a8_linear(packed, sw, xn, bias)
+    return y, qx, sx, acc, xn

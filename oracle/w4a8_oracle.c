@@ -406,3 +406,54 @@ long long orc_row_weight_bytes(int K, int bits)
     if (K < 0 || (bits != 16 && bits != 8 && bits != 4)) return -1;
     return (long long)K * bits / 8;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Operators around the linear.  [Orin-INT4] §"后续还能继续优化什么" item 1    */
+/* lists RMSNorm, the activation quantization, the linear, SwiGLU and the    */
+/* residual add as the operators with kernel boundaries between them;        */
+/* [310B-Gemma4] §4.2 names add+rmsnorm and gelu+mul as the fusions to make. */
+/* Neither page writes the operators out; the readings taken here are the    */
+/* usual definitions in the models those pages run (Qwen2-architecture      */
+/* DeepSeek-R1-Distill-Qwen-7B: RMSNorm and a SiLU-gated MLP; Gemma: a      */
+/* GELU(tanh)-gated MLP).                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* RMSNorm of each token, every step in IEEE fp32 (the precision in which   */
+/* the codes that follow are decided):                                       */
+/*   S   = sum_i x_i^2, rounded once to fp32 (accumulated here in fp64, each */
+/*         square exact in fp64),                                            */
+/*   ms  = S / K,  r = 1 / sqrt(ms + eps),                                   */
+/*   out_i = (x_i * r) * g_i.                                                */
+/* x, out: [M][K]; g: [K]; eps >= 0 (an all-zero token with eps = 0 gives   */
+/* NaN, as the formula does).                                                */
+int orc_rmsnorm_f32(const float* x, const float* g, float eps, int M, int K, float* out)
+{
+    if (M < 0 || K <= 0 || !(eps >= 0.0f) || (M && (!x || !g || !out))) return ORC_ERR_ARG;
+    for (int m = 0; m < M; ++m) {
+        const float* xr = x + (size_t)m * K;
+        double S = 0.0;
+        for (int i = 0; i < K; ++i) S += (double)xr[i] * (double)xr[i];
+        const float S32 = (float)S;
+        const float ms = S32 / (float)K;
+        const float r = 1.0f / sqrtf(ms + eps);
+        for (int i = 0; i < K; ++i) out[(size_t)m * K + i] = (xr[i] * r) * g[i];
+    }
+    return ORC_OK;
+}
+
+/* Gated activations of the MLP, in fp64: out_i = act(gate_i) * up_i with   */
+/*   kind 1 (SwiGLU):    act(v) = v / (1 + exp(-v))          (SiLU),         */
+/*   kind 2 (GELU tanh): act(v) = v/2 (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))). */
+int orc_glu(const double* gate, const double* up, int n, int kind, double* out)
+{
+    if (n < 0 || (kind != 1 && kind != 2) || (n && (!gate || !up || !out))) return ORC_ERR_ARG;
+    const double k0 = sqrt(2.0 / 3.14159265358979323846);
+    for (int i = 0; i < n; ++i) {
+        const double v = gate[i];
+        double a;
+        if (kind == 1) a = v / (1.0 + exp(-v));
+        else a = 0.5 * v * (1.0 + tanh(k0 * (v + 0.044715 * v * v * v)));
+        out[i] = a * up[i];
+    }
+    return ORC_OK;
+}

@@ -389,3 +389,101 @@ def test_i8g32_gemv_against_numpy():
     ref_acc = np.einsum("mgi,ngi->mng", qx.reshape(M, K // 32, 32).astype(np.int64),
                         q.reshape(N, K // 32, 32).astype(np.int64))
     assert np.array_equal(acc.astype(np.int64), ref_acc)
+
+
+# ------------------------------------------------ operators around the linear
+# RMSNorm and the gated MLP activations ([Orin-INT4] §"后续还能继续优化什么"
+# item 1; [310B-Gemma4] §4.2), pinned by invariants and closed forms.
+
+def test_rmsnorm_scale_invariant_bit_exact():
+    """With eps = 0, scaling x by 4 (exact in fp32) scales S by 16 and r by
+    1/4 exactly (correct rounding commutes with powers of two), so the output
+    is bit-identical.  A missing square root, a missing square or a mean taken
+    over |x| instead of x^2 breaks this."""
+    g = wl.rng(11)
+    x = g.standard_normal((3, 1536)).astype(np.float32)
+    gam = (1.0 + 0.1 * g.standard_normal(1536)).astype(np.float32)
+    a = oracle.rmsnorm_f32(x, gam, 0.0)
+    b = oracle.rmsnorm_f32(4.0 * x, gam, 0.0)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    c = oracle.rmsnorm_f32(0.25 * x, gam, 0.0)
+    assert np.array_equal(a.view(np.uint32), c.view(np.uint32))
+
+
+@pytest.mark.parametrize("K", [32, 3584, 18944])
+def test_rmsnorm_one_hot_closed_form(K):
+    """x = v e_0, g = 1, eps = 0: ms = v^2 / K, so out_0 = sign(v) sqrt(K) and
+    every other element is 0.  A mean over K - 1 or a sum without the 1/K
+    fails."""
+    for v in (3.0, -0.0625, 1234.5):
+        x = np.zeros((1, K), np.float32)
+        x[0, 0] = v
+        out = oracle.rmsnorm_f32(x, np.ones(K, np.float32), 0.0)
+        assert abs(out[0, 0] - np.sign(v) * np.sqrt(K)) <= 2 * np.spacing(np.float32(np.sqrt(K)))
+        assert np.all(out[0, 1:] == 0)
+
+
+def test_rmsnorm_eps_closed_form():
+    """x = c everywhere and eps = c^2: ms + eps = 2 c^2, so out = 1 / sqrt(2)
+    (to fp32 rounding).  eps added after the square root, or omitted, gives
+    another value."""
+    for c in (0.5, 2.0, 0.125):
+        x = np.full((1, 256), c, np.float32)
+        out = oracle.rmsnorm_f32(x, np.ones(256, np.float32), c * c)
+        assert np.allclose(out, 1.0 / np.sqrt(2.0), rtol=3e-7, atol=0)
+
+
+def test_rmsnorm_unit_mean_square_and_gamma_per_element():
+    """With g = 1 and eps = 0 the output has mean square 1; with a random g
+    every element is exactly fl(out1_i * g_i) (the weight multiplies last,
+    element by element, not a shifted or reversed g)."""
+    g = wl.rng(12)
+    x = (3.0 * g.standard_normal((2, 3584))).astype(np.float32)
+    one = oracle.rmsnorm_f32(x, np.ones(3584, np.float32), 0.0)
+    ms = np.mean(one.astype(np.float64) ** 2, axis=1)
+    assert np.all(np.abs(ms - 1.0) < 1e-5)
+    gam = g.standard_normal(3584).astype(np.float32)
+    out = oracle.rmsnorm_f32(x, gam, 0.0)
+    assert np.array_equal(out.view(np.uint32), (one * gam[None, :]).astype(np.float32).view(np.uint32))
+
+
+def test_rmsnorm_tokens_independent():
+    g = wl.rng(13)
+    x = g.standard_normal((4, 512)).astype(np.float32)
+    x[2] *= 100.0
+    gam = g.standard_normal(512).astype(np.float32)
+    allm = oracle.rmsnorm_f32(x, gam, 1e-6)
+    for m in range(4):
+        assert np.array_equal(allm[m], oracle.rmsnorm_f32(x[m:m + 1], gam, 1e-6)[0])
+
+
+def test_silu_against_logistic_and_identity():
+    """SwiGLU: act(v) = v * logistic(v) (scipy's expit, a library routine),
+    and the exact identity silu(-v) = silu(v) - v; the up factor multiplies."""
+    special = pytest.importorskip("scipy.special")
+    v = np.linspace(-30, 30, 6001)
+    one = np.ones_like(v)
+    s = oracle.glu(v, one, oracle.GLU_SILU)
+    assert np.allclose(s, v * special.expit(v), rtol=1e-14, atol=1e-300)
+    assert np.allclose(oracle.glu(-v, one, oracle.GLU_SILU), s - v, rtol=0, atol=1e-13)
+    u = np.linspace(-2, 2, 6001)
+    assert np.allclose(oracle.glu(v, u, oracle.GLU_SILU), s * u, rtol=1e-15, atol=0)
+    assert oracle.glu(np.array([0.0]), np.array([5.0]), oracle.GLU_SILU)[0] == 0.0
+
+
+def test_gelu_tanh_against_erf_gelu():
+    """GELU(tanh): the identity act(v) - act(-v) = v, and the known accuracy
+    of the tanh form against the exact v * Phi(v) (math.erf): within 5e-4
+    everywhere and about 4.7e-4 at its worst near |v| = 2.7, so a dropped cubic
+    term (error 0.034) or a wrong constant (0.09) fails."""
+    import math
+    v = np.linspace(-12, 12, 24001)
+    one = np.ones_like(v)
+    a = oracle.glu(v, one, oracle.GLU_GELU_TANH)
+    assert np.allclose(a - oracle.glu(-v, one, oracle.GLU_GELU_TANH), v, rtol=0, atol=1e-12)
+    exact = np.array([0.5 * t * (1.0 + math.erf(t / math.sqrt(2.0))) for t in v])
+    err = np.abs(a - exact)
+    assert err.max() < 5e-4
+    assert err.max() > 4e-4
+    u = np.full_like(v, -3.0)
+    assert np.allclose(oracle.glu(v, u, oracle.GLU_GELU_TANH), -3.0 * a, rtol=1e-15, atol=0)

@@ -52,11 +52,16 @@ def parse_args(argv=None):
     p.add_argument("--chain", action="store_true",
                    help="one chained launch per step (w4a8_linear_chain) instead of one PDL launch per linear")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--decoder", choices=("off", "fused", "unfused"), default="off",
+                   help="run the step with the RMSNorm, SwiGLU and residual adds of a decoder layer around "
+                        "the linears: fused into them, or as separate kernels")
     p.add_argument("--suite", action="store_true",
                    help="instead of the step line: every GEMV of the single, 7B-layer, Gemma Q4_0 and lm_head "
                         "workloads on its own, then the full step at M = 1, 2, 4, 8, 16 (one JSON line each)")
     p.add_argument("--suite-ms", default="1,2,4,8,16", help="token counts of the suite's full-step lines")
     p.add_argument("--suite-only-steps", action="store_true", help="suite: skip the single-GEMV lines")
+    p.add_argument("--suite-decoder-ms", default="1,16",
+                   help="token counts of the suite's decoder-step lines (operators unfused, then fused)")
     p.add_argument("--independent-x", action="store_true",
                    help="every linear reads its own static input buffer instead of the previous output")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -110,7 +115,13 @@ def workload_config(args, n_gpus):
         "dataflow": ("independent static inputs" if args.independent_x else
                      "each linear reads the previous linear's output (first M*K values)"),
         "parallelism": f"replicas x{n_gpus}",
-    }
+    } | ({} if args.decoder == "off" else {
+        "decoder": args.decoder,
+        "dataflow": ("decoder layers: RMSNorm -> QKV -> O (+ residual) -> RMSNorm -> gate/up -> SwiGLU -> down "
+                     "(+ residual); final RMSNorm -> lm_head; O reads the first M*3584 QKV outputs"),
+        "operators": ("fused into the linears (norm prologue, SwiGLU and residual epilogues)"
+                      if args.decoder == "fused" else "separate kernels (w4_rmsnorm, w4_glu, w4_add)"),
+    })
 
 
 def measured_peak():
@@ -334,6 +345,108 @@ def build_step(args, device):
     return make_buffers(build_weights(args, device), args.M, args.independent_x, device)
 
 
+NORM_EPS = 1e-6
+
+
+def build_decoder(args, device):
+    """The step with the operators a decoder layer runs around its linears:
+    per layer h += O(QKV(RMSNorm(h))[:, :3584]) and h += down(SiLU(gate) * up
+    of RMSNorm(h)), then logits = lm_head(RMSNorm(h)); attention is out of the
+    path (O reads the first M*3584 values of the QKV output in its place).
+    decoder="fused": RMSNorm in the quantize prologue, SwiGLU and the residual
+    add in the epilogue (gate/up paired per tile): 4 launches a layer + 1.
+    decoder="unfused": the same arithmetic with w4_rmsnorm, w4_glu and w4_add
+    as separate kernels between plain linears: 9 launches a layer + 2.
+    The step input h_in (residual stream, N(0, 4^2)) is read, never written,
+    so replays are identical.  Returns (ops, h_in, logits, bytes_per_step);
+    each op takes the launch flags."""
+    import torch
+
+    from bit_quantized_decode_gb300 import QuantLinear, _lib
+    fused = args.decoder == "fused"
+    M = args.M
+    H = wl.QWEN7B_HIDDEN
+    seed = 1000
+    F32 = torch.float32
+
+    def norm_weight():
+        nonlocal seed
+        seed += 1
+        return (1.0 + wl.torch_normal((H,), 0.1, seed, device)).contiguous()
+
+    def linear(lin, paired=False):
+        nonlocal seed
+        shards = [wl.torch_normal((rows, lin.K), lin.sigma, seed + i, device) for i, rows in enumerate(lin.shards)]
+        seed += len(lin.shards)
+        biases = [wl.torch_normal((rows,), 0.01, seed + i, device) for i, rows in enumerate(lin.shards)]
+        seed += len(lin.shards)
+        return QuantLinear.from_float("w4", shards, biases, glu_pairs=paired)
+
+    def buf(*shape, dtype=F32):
+        return torch.empty(*shape, dtype=dtype, device=device)
+
+    h_in = wl.torch_normal((M, H), 4.0, 4999, device).contiguous()
+    h = buf(M, H)
+    xn = buf(M, H)
+    ops = []
+    bytes_per_step = 0
+    for layer in range(args.layers):
+        qkv_l, o_l, gu_l, down_l = wl.qwen7b_layer()
+        g_attn, g_mlp = norm_weight(), norm_weight()
+        qkv, o, down = linear(qkv_l), linear(o_l), linear(down_l)
+        gu = linear(gu_l, paired=fused)
+        h_src = h_in if layer == 0 else h
+        y_qkv = buf(M, qkv_l.N)
+        x_o = y_qkv.view(-1)[: M * H].view(M, H)
+        act = buf(M, wl.QWEN7B_INTERMEDIATE)
+        q1, q2, q3, q4 = buf(M, H, dtype=torch.int8), buf(M, H, dtype=torch.int8), \
+            buf(M, H, dtype=torch.int8), buf(M, down_l.K, dtype=torch.int8)
+        s1, s2, s3, s4 = buf(M), buf(M), buf(M), buf(M)
+        if fused:
+            ops += [
+                lambda f, a=h_src, y=y_qkv, q=q1, s=s1, L=qkv, g=g_attn: L(a, y, q, s, f, norm=g, eps=NORM_EPS),
+                lambda f, a=x_o, r=h_src, q=q2, s=s2, L=o: L(a, h, q, s, f, residual=r),
+                lambda f, y=act, q=q3, s=s3, L=gu, g=g_mlp: L(h, y, q, s, f, norm=g, eps=NORM_EPS,
+                                                               glu=_lib.W4_GLU_SILU),
+                lambda f, a=act, q=q4, s=s4, L=down: L(a, h, q, s, f, residual=h),
+            ]
+        else:
+            y_o = buf(M, H)
+            y_gu = buf(M, gu_l.N)
+            y_d = buf(M, H)
+            ops += [
+                lambda f, a=h_src, g=g_attn: _lib.w4_rmsnorm(a, g, NORM_EPS, xn, f),
+                lambda f, y=y_qkv, q=q1, s=s1, L=qkv: L(xn, y, q, s, f),
+                lambda f, y=y_o, a=x_o, q=q2, s=s2, L=o: L(a, y, q, s, f),
+                lambda f, a=h_src, y=y_o: _lib.w4_add(a, y, h, f),
+                lambda f, g=g_mlp: _lib.w4_rmsnorm(h, g, NORM_EPS, xn, f),
+                lambda f, y=y_gu, q=q3, s=s3, L=gu: L(xn, y, q, s, f),
+                lambda f, y=y_gu: _lib.w4_glu(y, _lib.W4_GLU_SILU, act, f),
+                lambda f, y=y_d, q=q4, s=s4, L=down: L(act, y, q, s, f),
+                lambda f, y=y_d: _lib.w4_add(h, y, h, f),
+            ]
+        # the linears' bytes, plus what the fused operators must read: the norm
+        # weights and the residual stream (the gated output is I values, not 2I)
+        for lin in (qkv_l, o_l, gu_l, down_l):
+            bytes_per_step += algorithmic_bytes(lin, M)
+        bytes_per_step += 2 * 4 * H + 2 * 4 * M * H - 4 * M * wl.QWEN7B_INTERMEDIATE
+    head_l = wl.qwen7b_lm_head()
+    head = linear(head_l)
+    g_final = norm_weight()
+    logits = buf(M, head_l.N)
+    qh, sh = buf(M, H, dtype=torch.int8), buf(M)
+    h_last = h if args.layers > 0 else h_in
+    if not args.no_lm_head:
+        if fused:
+            ops.append(lambda f: head(h_last, logits, qh, sh, f, norm=g_final, eps=NORM_EPS))
+        else:
+            ops.append(lambda f: _lib.w4_rmsnorm(h_last, g_final, NORM_EPS, xn, f))
+            ops.append(lambda f: head(xn, logits, qh, sh, f))
+        bytes_per_step += algorithmic_bytes(head_l, M) + 4 * H
+    torch.cuda.synchronize()
+    return ops, h_in.view(-1), (logits if not args.no_lm_head else h).view(-1), bytes_per_step
+
+
 def max_over_ranks(value: float, dist=None, device=None) -> float:
     """The largest of every rank's value (identity on one process)."""
     if dist is None:
@@ -367,21 +480,27 @@ def run_ours(args, rank, world, local_rank):
         k, v = kv.split("=")
         _lib.set_tuning(k, int(v))
         tuning[k] = int(v)
-    items, x_all, y_all = build_step(args, dev)
     M = args.M
-    bytes_per_step = sum(algorithmic_bytes(lin, M) for _, lin, *_ in items)
-    launches = len(items)
     pdl_flag = 0 if args.no_pdl else W4_FLAG_PDL
+    if args.decoder != "off":
+        ops, x_all, y_all, bytes_per_step = build_decoder(args, dev)
+        items = []
+        launches = len(ops)
+    else:
+        items, x_all, y_all = build_step(args, dev)
+        bytes_per_step = sum(algorithmic_bytes(lin, M) for _, lin, *_ in items)
+        launches = len(items)
+        ops = [lambda f, it=it: it[2](it[3], it[4], it[5], it[6], flags=f) for it in items]
 
     stream = torch.cuda.Stream(device=dev)
 
     def step_per_linear():
-        for i, (_, lin, ql, x, y, qx, sx) in enumerate(items):
-            ql(x, y, qx, sx, flags=pdl_flag if i > 0 else 0)
+        for i, op in enumerate(ops):
+            op(pdl_flag if i > 0 else 0)
 
     # one chained launch per step (at most W4_MAX_CHAIN linears per launch)
     chains = []
-    if args.chain:
+    if args.chain and args.decoder == "off":
         try:
             for c0 in range(0, len(items), _lib.W4_MAX_CHAIN):
                 part = items[c0: c0 + _lib.W4_MAX_CHAIN]
@@ -672,6 +791,25 @@ def run_suite(args, local_rank):
                           "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": b,
                           "ms_per_token": round(ms / M, 5)}), flush=True)
         del items
+    del weights
+    # the decoder step: RMSNorm / SwiGLU / residual as separate kernels, then fused
+    for M in (int(m) for m in args.suite_decoder_ms.split(",") if m):
+        for mode in ("unfused", "fused"):
+            a2 = argparse.Namespace(**vars(args))
+            a2.decoder, a2.M = mode, M
+            ops, _, _, b = build_decoder(a2, dev)
+
+            def dstep(ops=ops):
+                for i, op in enumerate(ops):
+                    op(W4_FLAG_PDL if i else 0)
+
+            ms = _timed_graph(dstep, stream, max(3, min(args.steps, 400)), args.warmup)
+            gbs = b / (ms / 1e3) / 1e9
+            print(json.dumps({"suite": "qwen7b_decoder_step", "operators": mode, "M": M, "launches": len(ops),
+                              "ms_per_step": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "bytes": b}), flush=True)
+            del ops
+            torch.cuda.empty_cache()
     err = _lib.device_error()
     if err:
         raise RuntimeError(f"device error word {err:#x}")

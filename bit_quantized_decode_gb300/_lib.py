@@ -70,6 +70,33 @@ SIGNATURES = {
 }
 
 
+class Fusion(ctypes.Structure):
+    """w4_fusion of include/w4a8.h."""
+    _fields_ = [("norm_weight", _P), ("norm_eps", ctypes.c_float), ("glu", _I), ("residual", _P)]
+
+
+W4_GLU_NONE = 0
+W4_GLU_SILU = 1
+W4_GLU_GELU_TANH = 2
+_F = ctypes.c_float
+_LL = ctypes.c_longlong
+_PF = ctypes.POINTER(Fusion)
+SIGNATURES.update({
+    "w4_glu_repacked_bytes": ([_I, _I], _SZ),
+    "q4_0_glu_repacked_bytes": ([_I, _I], _SZ),
+    "w4_repack_glu": ([_P, _P, _I, _I, _P, _SZ, _P], _I),
+    "q4_0_repack_glu": ([_P, _P, _I, _I, _P, _SZ, _P], _I),
+    "w4a8_linear_fused": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _PF, _U, _P], _I),
+    "q4_0_linear_fused": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _PF, _U, _P], _I),
+    "i8g32_linear_fused": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _PF, _U, _P], _I),
+    "q6g32_linear_fused": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _PF, _U, _P], _I),
+    "rms_a8_quantize": ([_P, _P, _F, _I, _I, _P, _P, _U, _P], _I),
+    "w4_rmsnorm": ([_P, _P, _F, _I, _I, _P, _U, _P], _I),
+    "w4_glu": ([_P, _I, _I, _I, _P, _U, _P], _I),
+    "w4_add": ([_P, _P, _LL, _P, _U, _P], _I),
+})
+
+
 class LinearDesc(ctypes.Structure):
     """w4_linear_desc of include/w4a8.h."""
     _fields_ = [("w", _P), ("s_w", _P), ("bias", _P), ("x", _P), ("y", _P), ("qx", _P), ("sx", _P),
@@ -313,6 +340,104 @@ def q6g32_linear(w, bias, x, y, qx, sx, flags: int = 0, stream=None):
     N = y.shape[1]
     _check("q6g32_linear", load().q6g32_linear(_ptr(w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx), _ptr(sx),
                                                flags, _stream(stream)))
+
+
+# ------------------------------------------------ fusions around the linear
+def w4_glu_repacked_bytes(I: int, K: int) -> int:
+    return int(load().w4_glu_repacked_bytes(I, K))
+
+
+def q4_0_glu_repacked_bytes(I: int, K: int) -> int:
+    return int(load().q4_0_glu_repacked_bytes(I, K))
+
+
+def w4_repack_glu(gate, up, K, out, stream=None):
+    """Canonical packed gate and up [I][K/8] -> the paired device layout."""
+    _dev(gate, up, out)
+    assert gate.shape == up.shape
+    _check("w4_repack_glu", load().w4_repack_glu(_ptr(gate), _ptr(up), gate.shape[0], K, _ptr(out),
+                                                 out.numel() * out.element_size(), _stream(stream)))
+
+
+def q4_0_repack_glu(gate, up, K, out, stream=None):
+    """Q4_0 blocks of gate and up [I][K/32][18] -> the paired device layout."""
+    _dev(gate, up, out)
+    assert gate.shape == up.shape
+    _check("q4_0_repack_glu", load().q4_0_repack_glu(_ptr(gate), _ptr(up), gate.shape[0], K, _ptr(out),
+                                                     out.numel() * out.element_size(), _stream(stream)))
+
+
+def fusion(norm_weight=None, eps: float = 0.0, glu: int = W4_GLU_NONE, residual=None):
+    """A w4_fusion descriptor.  It holds references to its tensors, so their
+    memory stays allocated while the descriptor is alive."""
+    _dev(norm_weight, residual)
+    fz = Fusion(None if norm_weight is None else norm_weight.data_ptr(), float(eps), int(glu),
+                None if residual is None else residual.data_ptr())
+    fz._tensors = (norm_weight, residual)
+    return fz
+
+
+def _fused_args(fz):
+    return None if fz is None else ctypes.byref(fz)
+
+
+def w4a8_linear_fused(w, s_w, bias, x, y, qx, sx, fz=None, flags: int = 0, stream=None):
+    """w4a8_linear with RMSNorm / GLU / residual fused (fz from fusion()); y[M][N]."""
+    _dev(w, s_w, bias, x, y, qx, sx)
+    M, K = x.shape
+    N = y.shape[1]
+    _check("w4a8_linear_fused", load().w4a8_linear_fused(_ptr(w), _ptr(s_w), _ptr(bias), _ptr(x), M, N, K, _ptr(y),
+                                                         _ptr(qx), _ptr(sx), _fused_args(fz), flags,
+                                                         _stream(stream)))
+
+
+def _grouped_fused(name, w, bias, x, y, qx, sx, fz, flags, stream):
+    _dev(w, bias, x, y, qx, sx)
+    M, K = x.shape
+    N = y.shape[1]
+    _check(name, getattr(load(), name)(_ptr(w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), _ptr(qx), _ptr(sx),
+                                       _fused_args(fz), flags, _stream(stream)))
+
+
+def q4_0_linear_fused(w, bias, x, y, qx, sx, fz=None, flags: int = 0, stream=None):
+    _grouped_fused("q4_0_linear_fused", w, bias, x, y, qx, sx, fz, flags, stream)
+
+
+def i8g32_linear_fused(w, bias, x, y, qx, sx, fz=None, flags: int = 0, stream=None):
+    _grouped_fused("i8g32_linear_fused", w, bias, x, y, qx, sx, fz, flags, stream)
+
+
+def q6g32_linear_fused(w, bias, x, y, qx, sx, fz=None, flags: int = 0, stream=None):
+    _grouped_fused("q6g32_linear_fused", w, bias, x, y, qx, sx, fz, flags, stream)
+
+
+def rms_a8_quantize(x, norm_weight, eps, qx, sx, flags: int = 0, stream=None):
+    """RMSNorm(x) then the activation quantizer: qx int8 [M][K], sx float32 [M]."""
+    _dev(x, norm_weight, qx, sx)
+    M, K = x.shape
+    _check("rms_a8_quantize", load().rms_a8_quantize(_ptr(x), _ptr(norm_weight), float(eps), M, K, _ptr(qx),
+                                                     _ptr(sx), flags, _stream(stream)))
+
+
+def w4_rmsnorm(x, norm_weight, eps, out, flags: int = 0, stream=None):
+    _dev(x, norm_weight, out)
+    M, K = x.shape
+    _check("w4_rmsnorm", load().w4_rmsnorm(_ptr(x), _ptr(norm_weight), float(eps), M, K, _ptr(out), flags,
+                                           _stream(stream)))
+
+
+def w4_glu(gu, kind, out, flags: int = 0, stream=None):
+    """out[M][I] = act(gu[:, :I]) * gu[:, I:] for a gate|up output gu [M][2I]."""
+    _dev(gu, out)
+    M, I = out.shape
+    assert gu.shape == (M, 2 * I)
+    _check("w4_glu", load().w4_glu(_ptr(gu), int(kind), M, I, _ptr(out), flags, _stream(stream)))
+
+
+def w4_add(a, b, out, flags: int = 0, stream=None):
+    _dev(a, b, out)
+    assert a.numel() == b.numel() == out.numel()
+    _check("w4_add", load().w4_add(_ptr(a), _ptr(b), a.numel(), _ptr(out), flags, _stream(stream)))
 
 
 # ---------------------------------------------------------------- chains

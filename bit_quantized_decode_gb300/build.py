@@ -30,7 +30,7 @@ NVCC_FLAGS = [
     "-Xptxas", "-v",
     "-I", INCLUDE,
 ]
-SOURCES = ["w4a8_api.cu", "prep_kernels.cu", "gemv_w4.cu", "gemv_q4_0.cu", "gemv_i8g32.cu", "gemv_q6g32.cu",
+SOURCES = ["gemv_w4.cu", "gemv_q4_0.cu", "gemv_q6g32.cu", "gemv_i8g32.cu", "w4a8_api.cu", "prep_kernels.cu",
            "gemv_tc.cu"]
 
 
@@ -55,7 +55,7 @@ def _inputs_digest() -> str:
 
 # Sources that define the one-token decode GEMV (gemv_kernel<W4, 1, fused>):
 # a profile summary taken on them stays valid while they are unchanged.
-GEMV_W4_SOURCES = ("gemv_kernel.cuh", "quant_a8.cuh", "ptx.cuh", "internal.h", "gemv_w4.cu")
+GEMV_W4_SOURCES = ("gemv_kernel.cuh", "quant_a8.cuh", "fusion.cuh", "ptx.cuh", "internal.h", "gemv_w4.cu")
 
 
 def kernel_digest(names=GEMV_W4_SOURCES) -> str:

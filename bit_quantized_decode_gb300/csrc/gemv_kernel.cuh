@@ -43,6 +43,7 @@
 
 #include <type_traits>
 
+#include "fusion.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_a8.cuh"
@@ -187,9 +188,16 @@ __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float*
 // Loads x, reduces the absmax over the block, and writes the int8 codes to
 // shared memory (and, from block 0, to qx_out); tsum gets this thread's code
 // sums.  Contains one block barrier; every thread must call it.
-template <int MT, int NIT, bool kCodeSums>
+//
+// kNorm: RMSNorm in front of the quantizer (fusion.cuh).  The norm weight
+// does not depend on the previous kernel: it is loaded first and the
+// dependency wait (griddepcontrol.wait) is taken here, after those loads are
+// in flight and before x is read.  Each token's compensated sum of squares is
+// reduced over the block through nrm_s (2 kWarps MT floats, free until the
+// first merge), then x is normalized in registers.  One more block barrier.
+template <int MT, int NIT, bool kCodeSums, bool kNorm = false>
 __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, float* red_s, float* sx_s,
-                                                    int8_t* xs, int (&tsum)[MT])
+                                                    int8_t* xs, int (&tsum)[MT], float* nrm_s = nullptr)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -197,6 +205,16 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
     const int M = a.M;
     const int K = a.K;
     const int K4 = K >> 2;
+    float4 gv[kNorm ? NIT : 1];
+    if constexpr (kNorm) {
+        const float4* gr = reinterpret_cast<const float4*>(a.gamma);
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const int i = tid + it * kThreads;
+            gv[it] = (it < nit && i < K4) ? __ldg(gr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        pdl_wait();
+    }
     float4 v[MT][NIT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
@@ -205,6 +223,29 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
         for (int it = 0; it < NIT; ++it) {
             const int i = tid + it * kThreads;
             v[m][it] = (m < M && it < nit && i < K4) ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    if constexpr (kNorm) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) sq_acc4(v[m][it], hi, lo);
+            warp_pair_sum(hi, lo);
+            if (lane == 0) {
+                nrm_s[(warp * MT + m) * 2] = hi;
+                nrm_s[(warp * MT + m) * 2 + 1] = lo;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float hi = nrm_s[m * 2], lo = nrm_s[m * 2 + 1];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) pair_merge(hi, lo, nrm_s[(w * MT + m) * 2], nrm_s[(w * MT + m) * 2 + 1]);
+            const float r = rms_scale(hi, lo, K, a.eps);
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) v[m][it] = rms_apply(v[m][it], r, gv[it]);
         }
     }
 #pragma unroll
@@ -357,6 +398,9 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
     constexpr int kPassLines = 16;
     constexpr int kRowBufs = NCH == 1 ? 1 : 2;       // per-row parameter buffers (by linear parity)
     constexpr int kRowCap = NCH == 1 ? kRowCache : kRowCache / 2;   // rows per buffer
+    // single linears with up to four tokens take the RMSNorm prologue when
+    // a.gamma is set (one kernel for both, so alternating launches share code)
+    constexpr bool kNormable = NCH == 1 && XM == X_FUSED && MT <= 4;
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = P.stages;
@@ -489,9 +533,10 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
         const int r0 = rr.t0 * kRows;
         for (int i = tid; i < rr.ntiles * kRows; i += kThreads) {
             const int row = r0 + i;
-            if (row < ra.N) {
-                if (ra.bias != nullptr) cp_async4(b_s + i, ra.bias + row); else b_s[i] = 0.0f;
-                if constexpr (FMT == FMT_W4) cp_async4(w_s + i, ra.s_w + row);
+            const int prow = ra.glu != GLU_NONE ? glu_param_row(row, ra.n_out) : (row < ra.N ? row : -1);
+            if (prow >= 0) {
+                if (ra.bias != nullptr) cp_async4(b_s + i, ra.bias + prow); else b_s[i] = 0.0f;
+                if constexpr (FMT == FMT_W4) cp_async4(w_s + i, ra.s_w + prow);
             }
         }
     };
@@ -528,7 +573,8 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
 
         // ---- inputs produced before this linear are read only from here on
         if (li == 0) {
-            pdl_wait();
+            // with the RMSNorm prologue the wait is taken inside it, after the norm weight loads
+            if (!(kNormable && a.gamma != nullptr)) pdl_wait();
         } else if (!grid_wait(P.barrier, static_cast<unsigned>(li) * gridDim.x, P.err, &flag_s)) {
             dead = true;
         }
@@ -547,7 +593,26 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
 #pragma unroll
         for (int m = 0; m < MT; ++m) tsum[m] = 0;
 
-        if constexpr (XM == X_FUSED) {
+        bool normed = false;
+        if constexpr (kNormable) {
+            if (a.gamma != nullptr) {
+                // RMSNorm, then the quantizer; x and the norm weight in registers
+                // (the host asks for it only when nit <= norm_max_nit(MT))
+                constexpr int kIt = norm_max_nit(MT);
+                constexpr int kN1 = kIt < 2 ? kIt : 2;
+                constexpr int kN2 = kIt < 4 ? kIt : 4;
+                float* nrm_s = reinterpret_cast<float*>(acc_s);
+                if (nit <= kN1)
+                    fused_prologue_regs<MT, kN1, kCodeSums, true>(a, nit, red_s, sx_s, xs, tsum, nrm_s);
+                else if (nit <= kN2)
+                    fused_prologue_regs<MT, kN2, kCodeSums, true>(a, nit, red_s, sx_s, xs, tsum, nrm_s);
+                else
+                    fused_prologue_regs<MT, kIt, kCodeSums, true>(a, nit, red_s, sx_s, xs, tsum, nrm_s);
+                normed = true;
+            }
+        }
+        if (normed) {
+        } else if constexpr (XM == X_FUSED) {
             constexpr int kRegF4 = 20;                  // float4 of x held per thread
             constexpr int kIt = kRegF4 / MT;            // per token
             constexpr int kB1 = kIt / 5 > 0 ? kIt / 5 : 1;
@@ -832,11 +897,8 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
             const int rt0 = round * RT;
             const int nrows = min(RT, ntiles - rt0) * kRows;
             const int row_base = (t0 + rt0) * kRows;
-            for (int idx = tid; idx < M * nrows; idx += kThreads) {
-                const int m = idx / nrows;
-                const int rl = idx - m * nrows;
-                const int row = row_base + rl;
-                if (row >= a.N) continue;
+            // linear output of round row rl (kernel row `row`), token m
+            auto lin_out = [&](int m, int rl, int row) -> float {
                 const int tile = rl >> 3;
                 const int rr = rl & 7;
                 Acc v = Acc(0);
@@ -854,19 +916,47 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
                 }
                 if (!part) v = acc_s[(static_cast<size_t>(buf) * RT * kRows + rl) * MT + m];
                 const int ci = row - row0;
-                const float b = rows_cached ? bias_s[ci] : (a.bias != nullptr ? a.bias[row] : 0.0f);
-                float out;
+                const int prow = a.glu != GLU_NONE ? glu_param_row(row, a.n_out) : row;
+                const float b = rows_cached ? bias_s[ci] : (a.bias != nullptr ? a.bias[prow] : 0.0f);
                 if constexpr (FMT == FMT_W4) {
                     int xsum = 0;
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w) xsum += xsum_s[w * MT + m];
                     const int accv = v - 8 * xsum;          // remove the +8 nibble bias
-                    const float swr = rows_cached ? sw_s[ci] : a.s_w[row];
-                    out = __fmaf_rn(__fmul_rn(swr, sx_s[m]), __int2float_rn(accv), b);
+                    const float swr = rows_cached ? sw_s[ci] : a.s_w[prow];
+                    return __fmaf_rn(__fmul_rn(swr, sx_s[m]), __int2float_rn(accv), b);
                 } else {
-                    out = __fmaf_rn(sx_s[m], v, b);
+                    return __fmaf_rn(sx_s[m], v, b);
                 }
-                a.y[static_cast<size_t>(m) * a.N + row] = out;
+            };
+            if (a.glu == GLU_NONE) {
+                for (int idx = tid; idx < M * nrows; idx += kThreads) {
+                    const int m = idx / nrows;
+                    const int rl = idx - m * nrows;
+                    const int row = row_base + rl;
+                    if (row >= a.N) continue;
+                    float out = lin_out(m, rl, row);
+                    const size_t o = static_cast<size_t>(m) * a.N + row;
+                    if (a.residual != nullptr) out = __fadd_rn(a.residual[o], out);
+                    a.y[o] = out;
+                }
+            } else {
+                // gated: output j pairs gate row 8(j/4) + j%4 with the up row 4 below it
+                const int nout = nrows >> 1;
+                const int j0 = row_base >> 1;
+                for (int idx = tid; idx < M * nout; idx += kThreads) {
+                    const int m = idx / nout;
+                    const int jo = idx - m * nout;
+                    const int j = j0 + jo;
+                    if (j >= a.n_out) continue;
+                    const int rlg = (jo >> 2) * kRows + (jo & 3);
+                    const float g = lin_out(m, rlg, row_base + rlg);
+                    const float u = lin_out(m, rlg + 4, row_base + rlg + 4);
+                    float out = glu_act(a.glu, g, u);
+                    const size_t o = static_cast<size_t>(m) * a.n_out + j;
+                    if (a.residual != nullptr) out = __fadd_rn(a.residual[o], out);
+                    a.y[o] = out;
+                }
             }
             // accumulator and merge buffers alternate between rounds: no barrier here
         }

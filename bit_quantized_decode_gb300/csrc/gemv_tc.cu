@@ -37,6 +37,7 @@
 //     MMA in an isolated loop), not HBM and not the tensor cores' arithmetic.
 #include <cuda_fp16.h>
 
+#include "fusion.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -376,13 +377,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     // ---- epilogue: y = fmaf(s_w s_x, acc, b), coalesced over rows per token
     // (a partial sum of a dead split makes the row wrong: the error word says so)
     const int row = g * kTcRows + tid;
-    if (row < A.N && !dead) {
-        const float sw = A.s_w[row];
-        const float bv = A.bias != nullptr ? A.bias[row] : 0.0f;
+    if (A.glu == GLU_NONE) {
+        if (row < A.N && !dead) {
+            const float sw = A.s_w[row];
+            const float bv = A.bias != nullptr ? A.bias[row] : 0.0f;
 #pragma unroll
-        for (int n = 0; n < kTcTok; ++n)
-            if (n < A.M)
-                A.y[static_cast<size_t>(n) * A.N + row] = __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv);
+            for (int n = 0; n < kTcTok; ++n) {
+                if (n < A.M) {
+                    const size_t o = static_cast<size_t>(n) * A.N + row;
+                    float out = __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv);
+                    if (A.residual != nullptr) out = __fadd_rn(A.residual[o], out);
+                    A.y[o] = out;
+                }
+            }
+        }
+    } else {
+        // gated: this thread's row pairs with the row 4 lanes up (the up row of
+        // the same tile); the gate lanes (row % 8 < 4) write output j
+        const int prow = glu_param_row(row, A.n_out);
+        const bool have = row < A.N && prow >= 0 && !dead;
+        const float sw = have ? A.s_w[prow] : 0.0f;
+        const float bv = have && A.bias != nullptr ? A.bias[prow] : 0.0f;
+        const int j = (row >> 3) * 4 + (row & 3);
+#pragma unroll
+        for (int n = 0; n < kTcTok; ++n) {
+            const float v = n < A.M ? __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv) : 0.0f;
+            const float u = __shfl_down_sync(0xffffffffu, v, 4);
+            if (have && (row & 4) == 0 && n < A.M) {
+                const size_t o = static_cast<size_t>(n) * A.n_out + j;
+                float out = glu_act(A.glu, v, u);
+                if (A.residual != nullptr) out = __fadd_rn(A.residual[o], out);
+                A.y[o] = out;
+            }
+        }
     }
 }
 

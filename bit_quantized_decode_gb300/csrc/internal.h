@@ -17,7 +17,23 @@ constexpr int kAccWords = 64;            // round_tiles * MT, bounds the per-rou
 constexpr int kRowCache = 1024;          // rows per block whose s_w / bias are staged in shared memory
 
 // How a GEMV block obtains its int8 activations.
+// Activation source of a GEMV: quantized in the prologue (from x, or from
+// RMSNorm(x) when GemvArgs::gamma is set), int8 codes copied into shared
+// memory, or codes read from global memory in the inner loop.
 enum XMode { X_FUSED = 0, X_SMEM = 1, X_GLOBAL = 2 };
+
+// Gated MLP activation applied by the epilogue (fusion.cuh).
+enum GluKind { GLU_NONE = 0, GLU_SILU = 1, GLU_GELU_TANH = 2 };
+
+// Row pairing of a gated linear: tile t holds gate rows 4t..4t+3 as its rows
+// 0-3 and the matching up rows as rows 4-7.  Kernel row R -> row of the
+// caller's [gate; up] parameter arrays (n_out = I gate rows), or -1 past I.
+__host__ __device__ inline int glu_param_row(int R, int n_out)
+{
+    const int j = (R >> 3) * 4 + (R & 3);
+    if (j >= n_out) return -1;
+    return (R & 4) ? n_out + j : j;
+}
 
 // Lines (8 rows x one 32-weight chunk) per ring slot and bytes per unit.
 // Q6G32 keeps each unit in two planes: 16 bytes of low nibbles and 8 bytes
@@ -46,8 +62,13 @@ struct GemvArgs {
     const float* sx_in;      // [M] (unfused), else null
     int8_t* qx_out;          // fused: block 0 writes the codes here (may be null)
     float* sx_out;           // fused: block 0 writes the scales here (may be null)
-    float* y;                // [M][N]
-    int M, N, K;
+    float* y;                // [M][n_out]
+    const float* gamma;      // RMSNorm weight [K] (fused prologue, one to four tokens), else null
+    float eps;               // RMSNorm epsilon
+    const float* residual;   // [M][n_out] added to the output (may alias y), else null
+    int glu;                 // GluKind: rows paired per tile (glu_param_row), n_out = I
+    int n_out;               // outputs per token: N, or I for a gated linear
+    int M, N, K;             // N: weight rows (a gated linear: 8 ceil(I / 4))
     int C;                   // K / 32
     int T;                   // ceil(N / 8)
 };
@@ -103,6 +124,9 @@ cudaError_t launch_gemv_i8g32(const ChainParams<1>& p, int MT, int xmode, int gr
                               cudaStream_t s);
 cudaError_t launch_gemv_q6g32(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
                               cudaStream_t s);
+// Largest x float4 per thread and token the RMSNorm prologue holds in
+// registers (x and the norm weight together).
+__host__ __device__ constexpr int norm_max_nit(int MT) { return MT >= 4 ? 4 : 20 / (MT + 1); }
 // Chains of per-row INT4 linears (cooperative launch, fused quantization).
 cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
 
@@ -125,11 +149,14 @@ constexpr int kTcMaxSplitK = 16384;              // K per split at most: partial
 
 struct TcArgs {
     const uint8_t* w;       // repacked per-row INT4 (8-row tiles)
-    const float* s_w;       // [N]
-    const float* bias;      // [N] or null
+    const float* s_w;       // [N] (a gated linear: [2 n_out], gate rows then up rows)
+    const float* bias;      // same rows as s_w, or null
     const int8_t* qx;       // [M][K] activation codes
     const float* sx;        // [M]
-    float* y;               // [M][N]
+    float* y;               // [M][n_out]
+    const float* residual;  // [M][n_out] added to the output (may alias y), or null
+    int glu;                // GluKind
+    int n_out;              // outputs per token
     int M, N, K, C, T;      // C = K / 32 chunks, T = row tiles
     int splits;             // K splits per row group (= cluster size)
     int stages;             // weight ring depth (K blocks)
@@ -163,9 +190,19 @@ struct ShardTable {
     const void* p2[kMaxShards];
     int row0[kMaxShards + 1];
     int n;
+    int glu_rows;           // > 0: two shards (gate, up) of this many rows, paired per tile
 };
 
 cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, bool pdl, cudaStream_t s);
+// RMSNorm then the activation quantizer (one block per token).
+cudaError_t launch_rms_a8_quantize(const float* x, const float* gamma, float eps, int M, int K, int8_t* qx,
+                                   float* sx, bool pdl, cudaStream_t s);
+// The operators on their own (fp32 out): RMSNorm, gated activation of a
+// [M][2I] gate|up output, elementwise add.
+cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int M, int K, float* out, bool pdl,
+                           cudaStream_t s);
+cudaError_t launch_glu(const float* gu, int kind, int M, int I, float* out, bool pdl, cudaStream_t s);
+cudaError_t launch_add(const float* a, const float* b, long long n, float* out, bool pdl, cudaStream_t s);
 cudaError_t launch_w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, cudaStream_t s);
 cudaError_t launch_q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, cudaStream_t s);
 cudaError_t launch_i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, cudaStream_t s);

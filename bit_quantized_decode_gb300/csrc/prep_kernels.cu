@@ -5,6 +5,7 @@
 // so the codes are reproducible bit for bit by any IEEE implementation.
 #include <cuda_fp16.h>
 
+#include "fusion.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_a8.cuh"
@@ -42,21 +43,59 @@ __device__ __forceinline__ int quant_code(float v, float s, int lo, int hi)
 // Launched with programmatic dependent launch it waits for the previous
 // kernel before reading x and lets the next kernel start at once.
 constexpr int kQuantThreads = 512;
+constexpr int kQuantWarps = kQuantThreads / 32;
 
-template <int NIT>
-__global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float* __restrict__ x, int K,
-                                                                    int8_t* __restrict__ qx, float* __restrict__ sx)
+// RMSNorm scale of one token over the block (fusion.cuh): the thread's
+// compensated sum of squares (hi, lo) merged per warp, then over the warps in
+// order.  Every thread returns r.  Two block barriers (red2 is reused).
+__device__ __forceinline__ float block_rms_scale(float hi, float lo, int K, float eps, float* red2)
 {
-    __shared__ float red[kQuantThreads / 32];
-    pdl_launch_dependents();
-    pdl_wait();
+    warp_pair_sum(hi, lo);
+    const int tid = threadIdx.x;
+    if ((tid & 31) == 0) {
+        red2[2 * (tid >> 5)] = hi;
+        red2[2 * (tid >> 5) + 1] = lo;
+    }
+    __syncthreads();
+    hi = red2[0];
+    lo = red2[1];
+#pragma unroll
+    for (int w = 1; w < kQuantWarps; ++w) pair_merge(hi, lo, red2[2 * w], red2[2 * w + 1]);
+    __syncthreads();
+    return rms_scale(hi, lo, K, eps);
+}
+
+// kNorm: RMSNorm(x; gamma, eps) first (fusion.cuh), then the quantizer on the
+// normalized values; gamma is read with x.  Without room in registers the
+// token is read three times (sum of squares, absmax, codes).
+template <int NIT, bool kNorm>
+__global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float* __restrict__ x,
+                                                                    const float* __restrict__ gamma, float eps,
+                                                                    int K, int8_t* __restrict__ qx,
+                                                                    float* __restrict__ sx)
+{
+    __shared__ float red[kQuantWarps];
+    __shared__ float red2[2 * kQuantWarps];
+    constexpr bool kRegs = NIT > 0;
+    constexpr int kN = kRegs ? NIT : 1;
     const int m = blockIdx.x;
     const int tid = threadIdx.x;
     const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K);
+    const float4* gr = reinterpret_cast<const float4*>(gamma);
     const int K4 = K >> 2;
-    constexpr bool kRegs = NIT > 0;
-    constexpr int kN = kRegs ? NIT : 1;
+    pdl_launch_dependents();
+    // the norm weight does not depend on the previous kernel: load it first
+    float4 gv[kNorm && kRegs ? kN : 1];
+    if constexpr (kNorm && kRegs) {
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+            const int i = tid + it * kQuantThreads;
+            gv[it] = i < K4 ? __ldg(gr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    pdl_wait();
     float4 v[kN];
+    float r = 1.0f;
     float mx = 0.0f;
     if constexpr (kRegs) {
 #pragma unroll
@@ -64,17 +103,32 @@ __global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float*
             const int i = tid + it * kQuantThreads;
             v[it] = i < K4 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        if constexpr (kNorm) {
+            float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) sq_acc4(v[it], hi, lo);
+            r = block_rms_scale(hi, lo, K, eps, red2);
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) v[it] = rms_apply(v[it], r, gv[it]);
+        }
 #pragma unroll
         for (int it = 0; it < NIT; ++it) mx = fmaxf(mx, abs_max4(v[it]));
     } else {
-        for (int i = tid; i < K4; i += kQuantThreads) mx = fmaxf(mx, abs_max4(__ldcg(xr + i)));
+        if constexpr (kNorm) {
+            float hi = 0.0f, lo = 0.0f;
+            for (int i = tid; i < K4; i += kQuantThreads) sq_acc4(__ldcg(xr + i), hi, lo);
+            r = block_rms_scale(hi, lo, K, eps, red2);
+            for (int i = tid; i < K4; i += kQuantThreads) mx = fmaxf(mx, abs_max4(rms_apply(__ldcg(xr + i), r, __ldg(gr + i))));
+        } else {
+            for (int i = tid; i < K4; i += kQuantThreads) mx = fmaxf(mx, abs_max4(__ldcg(xr + i)));
+        }
     }
     mx = warp_max(mx);
     if ((tid & 31) == 0) red[tid >> 5] = mx;
     __syncthreads();
     float amax = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    for (int w = 0; w < kQuantWarps; ++w) amax = fmaxf(amax, red[w]);
     const A8Scale ks = a8_scale(amax);
     const bool all_exact = a8_needs_exact(ks);
     const uint64_t rr = f2_pack(ks.r, ks.r);
@@ -91,28 +145,125 @@ __global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float*
             if (i < K4) out[i] = code(v[it]);
         }
     } else {
-        for (int i = tid; i < K4; i += kQuantThreads) out[i] = code(__ldcg(xr + i));
+        for (int i = tid; i < K4; i += kQuantThreads) {
+            float4 f = __ldcg(xr + i);
+            if constexpr (kNorm) f = rms_apply(f, r, __ldg(gr + i));
+            out[i] = code(f);
+        }
     }
     if (tid == 0) sx[m] = ks.s;
 }
 
-cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, bool pdl, cudaStream_t s)
+namespace {
+
+cudaLaunchConfig_t token_launch(int M, bool pdl, cudaStream_t s, cudaLaunchAttribute* attr)
 {
-    const int nit = (K / 4 + kQuantThreads - 1) / kQuantThreads;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(M));
     cfg.blockDim = dim3(kQuantThreads);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = pdl ? attr : nullptr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (nit <= 2) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<2>, x, K, qx, sx);
-    if (nit <= 4) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<4>, x, K, qx, sx);
-    if (nit <= 10) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<10>, x, K, qx, sx);
-    if (nit <= 16) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<16>, x, K, qx, sx);
-    return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<0>, x, K, qx, sx);
+    return cfg;
+}
+
+template <bool kNorm>
+cudaError_t launch_quant(const float* x, const float* gamma, float eps, int M, int K, int8_t* qx, float* sx, bool pdl,
+                         cudaStream_t s)
+{
+    const int nit = (K / 4 + kQuantThreads - 1) / kQuantThreads;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = token_launch(M, pdl, s, attr);
+    if (nit <= 2) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<2, kNorm>, x, gamma, eps, K, qx, sx);
+    if (nit <= 4) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<4, kNorm>, x, gamma, eps, K, qx, sx);
+    if (nit <= 10) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<10, kNorm>, x, gamma, eps, K, qx, sx);
+    if (!kNorm && nit <= 16) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<16, kNorm>, x, gamma, eps, K, qx, sx);
+    return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<0, kNorm>, x, gamma, eps, K, qx, sx);
+}
+
+}  // namespace
+
+cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, bool pdl, cudaStream_t s)
+{
+    return launch_quant<false>(x, nullptr, 0.0f, M, K, qx, sx, pdl, s);
+}
+
+cudaError_t launch_rms_a8_quantize(const float* x, const float* gamma, float eps, int M, int K, int8_t* qx,
+                                   float* sx, bool pdl, cudaStream_t s)
+{
+    return launch_quant<true>(x, gamma, eps, M, K, qx, sx, pdl, s);
+}
+
+// ----------------------------------------- the fused operators on their own
+// RMSNorm to fp32 (one block per token, same arithmetic as the fused
+// prologue), the gated activation of a [M][2I] gate|up output, and an
+// elementwise add: the separate kernels a decoder runs without the fusions.
+__global__ void __launch_bounds__(kQuantThreads) rmsnorm_kernel(const float* __restrict__ x,
+                                                                const float* __restrict__ gamma, float eps, int K,
+                                                                float* __restrict__ out)
+{
+    __shared__ float red2[2 * kQuantWarps];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int m = blockIdx.x;
+    const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K);
+    const float4* gr = reinterpret_cast<const float4*>(gamma);
+    float4* orow = reinterpret_cast<float4*>(out + static_cast<size_t>(m) * K);
+    const int K4 = K >> 2;
+    float hi = 0.0f, lo = 0.0f;
+    for (int i = threadIdx.x; i < K4; i += kQuantThreads) sq_acc4(__ldcg(xr + i), hi, lo);
+    const float r = block_rms_scale(hi, lo, K, eps, red2);
+    for (int i = threadIdx.x; i < K4; i += kQuantThreads) orow[i] = rms_apply(__ldcg(xr + i), r, __ldg(gr + i));
+}
+
+__global__ void glu_kernel(const float* __restrict__ gu, int kind, int I, long long n, float* __restrict__ out)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (k >= n) return;
+    const long long m = k / I;
+    const long long j = k - m * I;
+    const float* row = gu + m * 2 * I;
+    out[k] = glu_act(kind, __ldcg(row + j), __ldcg(row + I + j));
+}
+
+__global__ void add_kernel(const float* __restrict__ a, const float* __restrict__ b, long long n,
+                           float* __restrict__ out)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (k < n) out[k] = __fadd_rn(__ldcg(a + k), __ldcg(b + k));
+}
+
+cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int M, int K, float* out, bool pdl,
+                           cudaStream_t s)
+{
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = token_launch(M, pdl, s, attr);
+    return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, x, gamma, eps, K, out);
+}
+
+cudaError_t launch_glu(const float* gu, int kind, int M, int I, float* out, bool pdl, cudaStream_t s)
+{
+    const long long n = static_cast<long long>(M) * I;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = token_launch(1, pdl, s, attr);
+    cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256));
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, glu_kernel, gu, kind, I, n, out);
+}
+
+cudaError_t launch_add(const float* a, const float* b, long long n, float* out, bool pdl, cudaStream_t s)
+{
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = token_launch(1, pdl, s, attr);
+    cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256));
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, add_kernel, a, b, n, out);
 }
 
 // ------------------------------------------------------ per-row INT4 weights
@@ -241,6 +392,13 @@ cudaError_t launch_i8g32_quantize(const float* W, int N, int K, int8_t* q, uint1
 // shard s.  Returns -1 for rows past the end (tile padding).
 __device__ __forceinline__ int shard_of(const ShardTable& st, int row, int& local)
 {
+    if (st.glu_rows > 0) {
+        // gated pairing: kernel row -> gate (shard 0) or up (shard 1) row
+        const int pr = glu_param_row(row, st.glu_rows);
+        if (pr < 0) return -1;
+        local = pr < st.glu_rows ? pr : pr - st.glu_rows;
+        return pr < st.glu_rows ? 0 : 1;
+    }
     for (int s = 0; s < st.n; ++s) {
         if (row < st.row0[s + 1]) {
             local = row - st.row0[s];
@@ -277,8 +435,8 @@ __global__ void w4_repack_kernel(const ShardTable st, int N, int K, long long un
     const long long row = t * kRows + r;
     uint4 o = make_uint4(0, 0, 0, 0);
     int local = 0;
-    if (row < N) {
-        const int s = shard_of(st, static_cast<int>(row), local);
+    const int s = row < N ? shard_of(st, static_cast<int>(row), local) : -1;
+    if (s >= 0) {
         const uint32_t* src = static_cast<const uint32_t*>(st.p[s]) + static_cast<size_t>(local) * (K / 8) + c * 4;
         o.x = interleave_w4(src[0]);
         o.y = interleave_w4(src[1]);
@@ -303,8 +461,8 @@ __global__ void q4_0_repack_kernel(const ShardTable st, int N, int K, long long 
     uint4 o = make_uint4(0, 0, 0, 0);
     uint16_t dbits = 0;
     int local = 0;
-    if (row < N) {
-        const int s = shard_of(st, static_cast<int>(row), local);
+    const int s = row < N ? shard_of(st, static_cast<int>(row), local) : -1;
+    if (s >= 0) {
         const uint8_t* blk = static_cast<const uint8_t*>(st.p[s]) + (static_cast<size_t>(local) * C + c) * 18;
         dbits = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
         uint32_t v4[32];
@@ -341,8 +499,8 @@ __global__ void i8g32_repack_kernel(const ShardTable st, int N, int K, long long
     uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
     uint16_t dbits = 0;
     int local = 0;
-    if (row < N) {
-        const int s = shard_of(st, static_cast<int>(row), local);
+    const int s = row < N ? shard_of(st, static_cast<int>(row), local) : -1;
+    if (s >= 0) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(st.p[s]) +
                                                           static_cast<size_t>(local) * K + c * 32);
         o0 = src[0];
@@ -373,8 +531,8 @@ __global__ void q6g32_repack_kernel(const ShardTable st, int N, int K, long long
     uint32_t hw[2] = {0u, 0u};
     uint16_t dbits = 0;
     int local = 0;
-    if (row < N) {
-        const int s = shard_of(st, static_cast<int>(row), local);
+    const int s = row < N ? shard_of(st, static_cast<int>(row), local) : -1;
+    if (s >= 0) {
         const int8_t* src = static_cast<const int8_t*>(st.p[s]) + static_cast<size_t>(local) * K + c * 32;
         uint32_t n[32];
 #pragma unroll

@@ -189,6 +189,7 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
         a.y = d[i].y;
         a.M = M;
         a.N = d[i].N;
+        a.n_out = d[i].N;
         a.K = d[i].K;
         a.C = a.K / 32;
         a.T = static_cast<int>(tiles(a.N));
@@ -210,14 +211,44 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
 }
 
 // Would the fused kernel (x quantized into shared memory) fit?
-bool fused_fits(int fmt, int M, int K)
+bool fused_fits(int fmt, int M, int K, bool norm = false)
 {
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != W4_OK) return false;
     const int MT = round_pow2_tokens(M);
+    if (norm && (MT > 4 || (K / 4 + kThreads - 1) / kThreads > norm_max_nit(MT))) return false;
     Plan p;
     return plan_gemv(*dev, fmt, MT, true, K, kAccWords / MT, p);
 }
+
+// Operators fused around one linear (w4_fusion, checked).
+struct Fuse {
+    const float* gamma = nullptr;
+    float eps = 0.0f;
+    int glu = GLU_NONE;
+    const float* residual = nullptr;
+};
+
+w4_status check_fusion(int fmt, const w4_fusion* f, Fuse& z)
+{
+    z = Fuse();
+    if (f == nullptr) return W4_OK;
+    if (f->glu < W4_GLU_NONE || f->glu > W4_GLU_GELU_TANH) return W4_ERR_INVALID_ARG;
+    if (f->glu != W4_GLU_NONE && fmt != FMT_W4 && fmt != FMT_Q4_0) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (f->norm_weight != nullptr) {
+        if (!(f->norm_eps > 0.0f) || !(f->norm_eps < 3.0e38f)) return W4_ERR_INVALID_ARG;
+        if (!aligned(f->norm_weight, 16)) return W4_ERR_MISALIGNED;
+    }
+    if (f->residual != nullptr && !aligned(f->residual, 4)) return W4_ERR_MISALIGNED;
+    z.gamma = f->norm_weight;
+    z.eps = f->norm_weight != nullptr ? f->norm_eps : 0.0f;
+    z.glu = f->glu;
+    z.residual = f->residual;
+    return W4_OK;
+}
+
+// Weight rows behind n outputs: a gated linear pairs 4 gate and 4 up rows per tile.
+inline int weight_rows(int n, int glu) { return glu != GLU_NONE ? 8 * ((n + 3) / 4) : n; }
 
 // Per-row INT4 with this many tokens runs on the tensor cores (gemv_tc.cu).
 bool use_tc(int fmt, int M)
@@ -232,7 +263,7 @@ bool use_tc(int fmt, int M)
 // kTcMaxSplitK; the deepest weight ring that leaves room for a second block
 // per SM.
 w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx, int M,
-                      int N, int K, float* y, bool pdl, cudaStream_t s)
+                      int N, int K, float* y, bool pdl, cudaStream_t s, int n_out, int glu, const float* residual)
 {
     DeviceInfo* dev = nullptr;
     w4_status st = device_info(&dev);
@@ -244,6 +275,9 @@ w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const 
     a.qx = qx;
     a.sx = sx;
     a.y = y;
+    a.residual = residual;
+    a.glu = glu;
+    a.n_out = n_out;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -268,8 +302,11 @@ w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const 
     return cuda_status(launch_gemv_w4_tc(a, G * ks, static_cast<size_t>(tc_smem(S, ks).total), pdl, s));
 }
 
+// One GEMV on int8 codes; N outputs per token (a gated linear: 2N weight
+// rows' worth of parameters, rows paired per tile), epilogue fusions in fz.
 w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bias, const int8_t* qx,
-                      const float* sx, int M, int N, int K, float* y, cudaStream_t s, bool pdl = false)
+                      const float* sx, int M, int N, int K, float* y, cudaStream_t s, bool pdl = false,
+                      const Fuse& fz = Fuse())
 {
     w4_status st = check_mk(M, K);
     if (st != W4_OK) return st;
@@ -279,10 +316,12 @@ w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bia
     if (!aligned(w, 16) || !aligned(qx, 16) || !aligned(sx, 4) || !aligned(y, 4) || (s_w && !aligned(s_w, 4)) ||
         (bias && !aligned(bias, 4)))
         return W4_ERR_MISALIGNED;
-    if (use_tc(fmt, M)) return run_gemv_tc(w, s_w, bias, qx, sx, M, N, K, y, pdl, s);
+    if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
+    const int Nw = weight_rows(N, fz.glu);
+    if (use_tc(fmt, M)) return run_gemv_tc(w, s_w, bias, qx, sx, M, Nw, K, y, pdl, s, N, fz.glu, fz.residual);
     GemvArgs a = {};
     a.w = static_cast<const uint8_t*>(w);
-    const size_t units = tiles(N) * kRows * (K / 32);
+    const size_t units = tiles(Nw) * kRows * (K / 32);
     a.whi = fmt_hi_bytes(fmt) > 0 ? a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)) : nullptr;
     a.wscale = fmt == FMT_W4 ? nullptr
                              : reinterpret_cast<const uint16_t*>(
@@ -292,34 +331,47 @@ w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bia
     a.qx_in = qx;
     a.sx_in = sx;
     a.y = y;
+    a.glu = fz.glu;
+    a.residual = fz.residual;
+    a.n_out = N;
     a.M = M;
-    a.N = N;
+    a.N = Nw;
     a.K = K;
     return run_gemv(fmt, a, false, pdl ? W4_FLAG_PDL : 0u, s);
 }
 
 w4_status linear_common(int fmt, const void* w, const float* s_w, const float* bias, const float* x, int M, int N,
-                        int K, float* y, int8_t* qx, float* sx, unsigned flags, cudaStream_t s)
+                        int K, float* y, int8_t* qx, float* sx, unsigned flags, cudaStream_t s,
+                        const w4_fusion* f = nullptr)
 {
     w4_status st = check_mk(M, K);
     if (st != W4_OK) return st;
     if (N < 0 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_INVALID_ARG;
+    Fuse fz;
+    st = check_fusion(fmt, f, fz);
+    if (st != W4_OK) return st;
     if (M == 0) return W4_OK;
     if (!x || !qx || !sx) return W4_ERR_INVALID_ARG;
     if (N > 0 && (!w || !y || (fmt == FMT_W4 && !s_w))) return W4_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(qx, 16) || !aligned(sx, 4) || (w && !aligned(w, 16)) || (y && !aligned(y, 4)) ||
         (s_w && !aligned(s_w, 4)) || (bias && !aligned(bias, 4)))
         return W4_ERR_MISALIGNED;
-    if (N == 0 || use_tc(fmt, M) || !fused_fits(fmt, M, K)) {
-        // quantize into the caller's qx/sx once, then the GEMV on int8 codes
-        // (tensor cores for many tokens), chained by programmatic dependent launch
-        st = cuda_status(launch_a8_quantize(x, M, K, qx, sx, (flags & W4_FLAG_PDL) != 0, s));
+    if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
+    const bool norm = fz.gamma != nullptr;
+    const bool pdl = (flags & W4_FLAG_PDL) != 0;
+    if (N == 0 || use_tc(fmt, M) || !fused_fits(fmt, M, K, norm)) {
+        // quantize (normalize first if asked) into the caller's qx/sx once, then
+        // the GEMV on int8 codes (tensor cores for many tokens), chained by
+        // programmatic dependent launch
+        st = cuda_status(norm ? launch_rms_a8_quantize(x, fz.gamma, fz.eps, M, K, qx, sx, pdl, s)
+                              : launch_a8_quantize(x, M, K, qx, sx, pdl, s));
         if (st != W4_OK || N == 0) return st;
-        return gemv_common(fmt, w, s_w, bias, qx, sx, M, N, K, y, s, true);
+        return gemv_common(fmt, w, s_w, bias, qx, sx, M, N, K, y, s, true, fz);
     }
+    const int Nw = weight_rows(N, fz.glu);
     GemvArgs a = {};
     a.w = static_cast<const uint8_t*>(w);
-    const size_t units = tiles(N) * kRows * (K / 32);
+    const size_t units = tiles(Nw) * kRows * (K / 32);
     a.whi = fmt_hi_bytes(fmt) > 0 ? a.w + units * static_cast<size_t>(fmt_unit_bytes(fmt)) : nullptr;
     a.wscale = fmt == FMT_W4 ? nullptr
                              : reinterpret_cast<const uint16_t*>(
@@ -330,8 +382,13 @@ w4_status linear_common(int fmt, const void* w, const float* s_w, const float* b
     a.qx_out = qx;
     a.sx_out = sx;
     a.y = y;
+    a.gamma = fz.gamma;
+    a.eps = fz.eps;
+    a.glu = fz.glu;
+    a.residual = fz.residual;
+    a.n_out = N;
     a.M = M;
-    a.N = N;
+    a.N = Nw;
     a.K = K;
     return run_gemv(fmt, a, true, flags, s);
 }
@@ -502,6 +559,61 @@ w4_status q6g32_repack(const int8_t* const* shard_q, const uint16_t* const* shar
     return cuda_status(launch_q6g32_repack(st, N, K, out, reinterpret_cast<cudaStream_t>(s)));
 }
 
+size_t w4_glu_repacked_bytes(int I, int K)
+{
+    if (I < 0 || I > (1 << 29) || K <= 0 || K % 32 != 0) return 0;
+    return w4_repacked_bytes(8 * ((I + 3) / 4), K);
+}
+
+size_t q4_0_glu_repacked_bytes(int I, int K)
+{
+    if (I < 0 || I > (1 << 29) || K <= 0 || K % 32 != 0) return 0;
+    return q4_0_repacked_bytes(8 * ((I + 3) / 4), K);
+}
+
+namespace {
+// Two shards (gate, up) of I rows each, paired per tile by the repack.
+w4_status glu_shards(const void* gate, const void* up, int I, int K, ShardTable& st, int& Nw)
+{
+    if (K <= 0 || I < 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0 || K > W4_MAX_K || I > (1 << 29)) return W4_ERR_UNSUPPORTED_SHAPE;
+    const void* p[2] = {gate, up};
+    const int rows[2] = {I, I};
+    int N = 0;
+    w4_status r = build_shards(p, nullptr, rows, 2, st, N);
+    if (r != W4_OK) return r;
+    st.glu_rows = I;
+    Nw = I > 0 ? 8 * ((I + 3) / 4) : 0;
+    return W4_OK;
+}
+}  // namespace
+
+w4_status w4_repack_glu(const uint32_t* gate, const uint32_t* up, int I, int K, void* out, size_t out_bytes,
+                        w4_stream_t s)
+{
+    ShardTable st;
+    int Nw = 0;
+    w4_status r = glu_shards(gate, up, I, K, st, Nw);
+    if (r != W4_OK || Nw == 0) return r;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (out_bytes < w4_glu_repacked_bytes(I, K)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16) || !aligned(gate, 16) || !aligned(up, 16)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_w4_repack(st, Nw, K, out, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status q4_0_repack_glu(const uint8_t* gate, const uint8_t* up, int I, int K, void* out, size_t out_bytes,
+                          w4_stream_t s)
+{
+    ShardTable st;
+    int Nw = 0;
+    w4_status r = glu_shards(gate, up, I, K, st, Nw);
+    if (r != W4_OK || Nw == 0) return r;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (out_bytes < q4_0_glu_repacked_bytes(I, K)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_q4_0_repack(st, Nw, K, out, reinterpret_cast<cudaStream_t>(s)));
+}
+
 w4_status w4_concat_f32(const float* const* parts, const int* lens, int n_parts, float* out, w4_stream_t s)
 {
     if (n_parts < 0 || (n_parts > 0 && (!parts || !lens))) return W4_ERR_INVALID_ARG;
@@ -576,6 +688,91 @@ w4_status i8g32_linear(const void* w, const float* bias, const float* x, int M, 
 {
     return linear_common(FMT_I8G32, w, nullptr, bias, x, M, N, K, y, qx, sx, flags,
                          reinterpret_cast<cudaStream_t>(s));
+}
+
+// ------------------------------------------------ fusions around the linear
+w4_status w4a8_linear_fused(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,
+                            float* y, int8_t* qx, float* sx, const w4_fusion* f, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_W4, w, s_w, bias, x, M, N, K, y, qx, sx, flags, reinterpret_cast<cudaStream_t>(s), f);
+}
+
+w4_status q4_0_linear_fused(const void* w, const float* bias, const float* x, int M, int N, int K, float* y,
+                            int8_t* qx, float* sx, const w4_fusion* f, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_Q4_0, w, nullptr, bias, x, M, N, K, y, qx, sx, flags,
+                         reinterpret_cast<cudaStream_t>(s), f);
+}
+
+w4_status i8g32_linear_fused(const void* w, const float* bias, const float* x, int M, int N, int K, float* y,
+                             int8_t* qx, float* sx, const w4_fusion* f, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_I8G32, w, nullptr, bias, x, M, N, K, y, qx, sx, flags,
+                         reinterpret_cast<cudaStream_t>(s), f);
+}
+
+w4_status q6g32_linear_fused(const void* w, const float* bias, const float* x, int M, int N, int K, float* y,
+                             int8_t* qx, float* sx, const w4_fusion* f, unsigned flags, w4_stream_t s)
+{
+    return linear_common(FMT_Q6G32, w, nullptr, bias, x, M, N, K, y, qx, sx, flags,
+                         reinterpret_cast<cudaStream_t>(s), f);
+}
+
+namespace {
+w4_status check_norm_args(const float* x, const float* g, float eps, int M, int K)
+{
+    w4_status st = check_mk(M, K);
+    if (st != W4_OK) return st;
+    if (M == 0) return W4_OK;
+    if (!x || !g || !(eps > 0.0f) || !(eps < 3.0e38f)) return W4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(g, 16)) return W4_ERR_MISALIGNED;
+    return W4_OK;
+}
+}  // namespace
+
+w4_status rms_a8_quantize(const float* x, const float* norm_weight, float eps, int M, int K, int8_t* qx, float* sx,
+                          unsigned flags, w4_stream_t s)
+{
+    if ((flags & ~W4_FLAG_PDL) != 0) return W4_ERR_INVALID_ARG;
+    w4_status st = check_norm_args(x, norm_weight, eps, M, K);
+    if (st != W4_OK || M == 0) return st;
+    if (!qx || !sx) return W4_ERR_INVALID_ARG;
+    if (!aligned(qx, 16) || !aligned(sx, 4)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_rms_a8_quantize(x, norm_weight, eps, M, K, qx, sx, (flags & W4_FLAG_PDL) != 0,
+                                              reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status w4_rmsnorm(const float* x, const float* norm_weight, float eps, int M, int K, float* out, unsigned flags,
+                     w4_stream_t s)
+{
+    if ((flags & ~W4_FLAG_PDL) != 0) return W4_ERR_INVALID_ARG;
+    w4_status st = check_norm_args(x, norm_weight, eps, M, K);
+    if (st != W4_OK || M == 0) return st;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_rmsnorm(x, norm_weight, eps, M, K, out, (flags & W4_FLAG_PDL) != 0,
+                                      reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status w4_glu(const float* gu, int kind, int M, int I, float* out, unsigned flags, w4_stream_t s)
+{
+    if ((flags & ~W4_FLAG_PDL) != 0 || M < 0 || I < 0) return W4_ERR_INVALID_ARG;
+    if (kind != W4_GLU_SILU && kind != W4_GLU_GELU_TANH) return W4_ERR_INVALID_ARG;
+    if (M > W4_MAX_M || I > (1 << 30)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || I == 0) return W4_OK;
+    if (!gu || !out) return W4_ERR_INVALID_ARG;
+    if (!aligned(gu, 4) || !aligned(out, 4)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_glu(gu, kind, M, I, out, (flags & W4_FLAG_PDL) != 0, reinterpret_cast<cudaStream_t>(s)));
+}
+
+w4_status w4_add(const float* a, const float* b, long long n, float* out, unsigned flags, w4_stream_t s)
+{
+    if ((flags & ~W4_FLAG_PDL) != 0 || n < 0) return W4_ERR_INVALID_ARG;
+    if (n > (1LL << 31) * 255) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0) return W4_OK;
+    if (!a || !b || !out) return W4_ERR_INVALID_ARG;
+    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_add(a, b, n, out, (flags & W4_FLAG_PDL) != 0, reinterpret_cast<cudaStream_t>(s)));
 }
 
 // ----------------------------------------------------------------- chains

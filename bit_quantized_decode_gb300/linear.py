@@ -3,7 +3,9 @@
 `QuantLinear.from_float` quantizes float weight shards on the GPU with the
 library's kernels, fuses the shards (q/k/v, gate/up) into one repacked
 matrix, and keeps it resident; `QuantLinear.__call__` runs the fused
-quantize + GEMV launch.  Buffers are torch tensors (device memory only).
+quantize + GEMV launch, optionally with RMSNorm in front, the gated MLP
+activation (gate/up weights paired per tile, `glu_pairs=True`) or the
+residual add behind it.  Buffers are torch tensors (device memory only).
 """
 from __future__ import annotations
 
@@ -15,10 +17,12 @@ FORMATS = ("w4", "q4_0", "i8g32", "q6g32")
 
 
 class QuantLinear:
-    def __init__(self, fmt: str, N: int, K: int, w: torch.Tensor, s_w=None, bias=None, canonical=None):
+    def __init__(self, fmt: str, N: int, K: int, w: torch.Tensor, s_w=None, bias=None, canonical=None,
+                 glu_pairs: bool = False):
         if fmt not in FORMATS:
             raise ValueError(fmt)
-        self.fmt, self.N, self.K = fmt, N, K
+        self.fmt, self.N, self.K = fmt, N, K   # N: outputs per token (a paired gate/up linear: I)
+        self.glu_pairs = glu_pairs
         self.w = w                  # repacked device layout, uint8
         self.s_w = s_w              # float32 [N] (w4 only)
         self.bias = bias            # float32 [N] or None
@@ -26,9 +30,14 @@ class QuantLinear:
 
     # ------------------------------------------------------------- building
     @classmethod
-    def from_float(cls, fmt: str, shards, biases=None, keep_canonical: bool = False) -> "QuantLinear":
-        """shards: float32 CUDA tensors [rows_s][K] concatenated by rows; biases: matching [rows_s] or None."""
+    def from_float(cls, fmt: str, shards, biases=None, keep_canonical: bool = False,
+                   glu_pairs: bool = False) -> "QuantLinear":
+        """shards: float32 CUDA tensors [rows_s][K] concatenated by rows; biases: matching [rows_s] or None.
+        glu_pairs: shards are [gate, up] of a gated MLP (W4 or Q4_0), repacked paired per tile for the
+        GLU epilogue; the linear then has I = rows outputs and must be called with glu=..."""
         shards = [s.contiguous() for s in shards]
+        if glu_pairs and (fmt not in ("w4", "q4_0") or len(shards) != 2 or shards[0].shape != shards[1].shape):
+            raise ValueError("glu_pairs needs W4 or Q4_0 gate and up shards of equal shape")
         K = shards[0].shape[1]
         dev = shards[0].device
         N = sum(s.shape[0] for s in shards)
@@ -50,12 +59,12 @@ class QuantLinear:
                 d = torch.empty((n, K // 32), dtype=torch.int16, device=dev)
                 _lib.i8g32_quantize(W, q, d)
                 canon.append((q, d))
-        w, s_w = cls._repack(fmt, canon, scales, N, K, dev)
+        w, s_w = cls._repack(fmt, canon, scales, N, K, dev, glu_pairs)
         bias = None
         if biases is not None:
             bias = torch.empty(N, dtype=torch.float32, device=dev)
             _lib.w4_concat_f32([b.contiguous() for b in biases], bias)
-        return cls(fmt, N, K, w, s_w, bias, canon if keep_canonical else None)
+        return cls(fmt, N // 2 if glu_pairs else N, K, w, s_w, bias, canon if keep_canonical else None, glu_pairs)
 
     @classmethod
     def from_canonical(cls, fmt: str, canon, K: int, scales=None, biases=None) -> "QuantLinear":
@@ -71,8 +80,19 @@ class QuantLinear:
         return cls(fmt, N, K, w, s_w, bias, canon)
 
     @staticmethod
-    def _repack(fmt, canon, scales, N, K, dev):
+    def _repack(fmt, canon, scales, N, K, dev, glu_pairs=False):
         s_w = None
+        if glu_pairs:
+            I = N // 2
+            if fmt == "w4":
+                w = torch.empty(_lib.w4_glu_repacked_bytes(I, K), dtype=torch.uint8, device=dev)
+                _lib.w4_repack_glu(canon[0], canon[1], K, w)
+                s_w = torch.empty(N, dtype=torch.float32, device=dev)
+                _lib.w4_concat_f32(scales, s_w)
+            else:
+                w = torch.empty(_lib.q4_0_glu_repacked_bytes(I, K), dtype=torch.uint8, device=dev)
+                _lib.q4_0_repack_glu(canon[0], canon[1], K, w)
+            return w, s_w
         if fmt == "w4":
             w = torch.empty(_lib.w4_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
             _lib.w4_repack(canon, K, w)
@@ -96,14 +116,26 @@ class QuantLinear:
                 torch.empty((M, self.K), dtype=torch.int8, device=dev),
                 torch.empty(M, dtype=torch.float32, device=dev))
 
-    def __call__(self, x, y=None, qx=None, sx=None, flags: int = 0, stream=None):
-        """Quantize x [M][K] and compute y [M][N] (one fused launch when it fits)."""
+    def __call__(self, x, y=None, qx=None, sx=None, flags: int = 0, stream=None, norm=None, eps: float = 1e-6,
+                 glu: int = _lib.W4_GLU_NONE, residual=None):
+        """Quantize x [M][K] and compute y [M][N] (one fused launch when it fits).
+        norm: RMSNorm weight [K] applied to x first (with eps); glu: W4_GLU_SILU or W4_GLU_GELU_TANH
+        (paired gate/up weights only); residual [M][N]: added to y last (may be y itself)."""
         M = x.shape[0]
         if y is None or qx is None or sx is None:
             y2, q2, s2 = self.buffers(M)
             y = y if y is not None else y2
             qx = qx if qx is not None else q2
             sx = sx if sx is not None else s2
+        if self.glu_pairs != (glu != _lib.W4_GLU_NONE):
+            raise ValueError("glu is taken exactly by linears built with glu_pairs=True")
+        if norm is not None or glu != _lib.W4_GLU_NONE or residual is not None:
+            fz = _lib.fusion(norm, eps, glu, residual)
+            if self.fmt == "w4":
+                _lib.w4a8_linear_fused(self.w, self.s_w, self.bias, x, y, qx, sx, fz, flags, stream)
+            else:
+                getattr(_lib, f"{self.fmt}_linear_fused")(self.w, self.bias, x, y, qx, sx, fz, flags, stream)
+            return y
         if self.fmt == "w4":
             _lib.w4a8_linear(self.w, self.s_w, self.bias, x, y, qx, sx, flags, stream)
         elif self.fmt == "q4_0":

@@ -141,6 +141,21 @@ def bias(g: np.random.Generator, N: int) -> np.ndarray:
     return (g.standard_normal(N, dtype=np.float64) * 0.01).astype(np.float32)
 
 
+def norm_weight(g: np.random.Generator, K: int) -> np.ndarray:
+    """RMSNorm weight: 1 + N(0, 0.1) per channel, with 0.5% of the channels
+    scaled by 8 (trained norm weights carry a few large channels)."""
+    w = 1.0 + 0.1 * g.standard_normal(K, dtype=np.float64)
+    idx = g.choice(K, size=max(1, K // 200), replace=False)
+    w[idx] *= 8.0
+    return w.astype(np.float32)
+
+
+def residual_stream(g: np.random.Generator, M: int, K: int, scale: float = 4.0) -> np.ndarray:
+    """Decoder residual stream h: N(0, scale^2), the magnitude a few dozen
+    residual adds leave it at."""
+    return (g.standard_normal((M, K), dtype=np.float64) * scale).astype(np.float32)
+
+
 def int_codes(g: np.random.Generator, shape, lo: int, hi: int) -> np.ndarray:
     """Uniform integers in [lo, hi], int8."""
     return g.integers(lo, hi + 1, size=shape, dtype=np.int64).astype(np.int8)

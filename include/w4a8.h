@@ -161,6 +161,19 @@ size_t q6g32_repacked_bytes(int N, int K);
 w4_status q6g32_repack(const int8_t* const* shard_q, const uint16_t* const* shard_d, const int* shard_rows,
                        int n_shards, int K, void* out, size_t out_bytes, w4_stream_t s);
 
+/* Gate/up weights of a gated MLP, paired for the GLU epilogue of the
+ * *_linear_fused calls: row tile t holds gate rows 4t..4t+3 and then up rows
+ * 4t..4t+3 (8 ceil(I/4) rows in all, padding past I zero), so one thread
+ * block sees both halves of every output.  gate and up: canonical [I][..]
+ * device arrays (W4: uint32 [I][K/8]; Q4_0: 18-byte blocks [I][K/32]).
+ * out: *_glu_repacked_bytes(I, K) bytes, 16-byte aligned. */
+size_t w4_glu_repacked_bytes(int I, int K);
+w4_status w4_repack_glu(const uint32_t* gate, const uint32_t* up, int I, int K, void* out, size_t out_bytes,
+                        w4_stream_t s);
+size_t q4_0_glu_repacked_bytes(int I, int K);
+w4_status q4_0_repack_glu(const uint8_t* gate, const uint8_t* up, int I, int K, void* out, size_t out_bytes,
+                          w4_stream_t s);
+
 /* Concatenate per-shard float vectors (per-row scales s_w, bias) into `out`
  * in shard order.  parts: HOST array of device pointers; lens: HOST array. */
 w4_status w4_concat_f32(const float* const* parts, const int* lens, int n_parts, float* out, w4_stream_t s);
@@ -214,6 +227,67 @@ w4_status i8g32_linear(const void* w, const float* bias, const float* x, int M, 
                        float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
 w4_status q6g32_linear(const void* w, const float* bias, const float* x, int M, int N, int K,
                        float* y, int8_t* qx, float* sx, unsigned flags, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * The decode linear with its neighbouring operators fused in.
+ * [Orin-INT4] §"后续还能继续优化什么" item 1 names the kernel boundaries
+ * between RMSNorm, quantization, linear, SwiGLU and the residual add;
+ * [310B-Gemma4] §4.2 names add+rmsnorm and gelu+mul fusions.  With f:
+ *   - f->norm_weight != NULL: x is first normalized per token,
+ *       r = 1 / sqrt(S / K + eps),  x'_i = (x_i * r) * g_i,
+ *     with S = sum_i x_i^2 rounded once to fp32 and every other step an IEEE
+ *     fp32 operation; x' is then quantized (qx, sx hold its codes).
+ *     norm_weight: float [K], 16-byte aligned; norm_eps > 0 and finite.
+ *   - f->glu = W4_GLU_SILU or W4_GLU_GELU_TANH: w comes from *_repack_glu
+ *     (I = N gate rows and N up rows); s_w and bias hold 2N values, the gate
+ *     rows' then the up rows'; the linear's gate and up outputs g, u (each
+ *     exactly as the plain linear makes them) become
+ *       SiLU:      y = fl(fl(g / fl(1 + expf(-g))) * u)
+ *       GELU tanh: y = (g / 2)(1 + tanhf(sqrt(2/pi)(g + 0.044715 g^3))) u,
+ *     y: float [M][N].  Only W4 and Q4_0 take a GLU.
+ *   - f->residual != NULL: float [M][N], added last, y = residual + out (fp32);
+ *     it may be y itself (the in-place residual update) but must not
+ *     otherwise overlap y.
+ * f = NULL or all fields zero is exactly the *_linear call.  x must not
+ * overlap y.  Many tokens (the tensor-core path) or a long x run the
+ * normalize+quantize as its own kernel (rms_a8_quantize) ahead of the GEMV;
+ * the results are the same.
+ * ------------------------------------------------------------------------ */
+#define W4_GLU_NONE 0
+#define W4_GLU_SILU 1
+#define W4_GLU_GELU_TANH 2
+typedef struct {
+    const float* norm_weight;
+    float norm_eps;
+    int glu;
+    const float* residual;
+} w4_fusion;
+
+w4_status w4a8_linear_fused(const void* w, const float* s_w, const float* bias, const float* x, int M, int N,
+                            int K, float* y, int8_t* qx, float* sx, const w4_fusion* f, unsigned flags,
+                            w4_stream_t s);
+w4_status q4_0_linear_fused(const void* w, const float* bias, const float* x, int M, int N, int K, float* y,
+                            int8_t* qx, float* sx, const w4_fusion* f, unsigned flags, w4_stream_t s);
+w4_status i8g32_linear_fused(const void* w, const float* bias, const float* x, int M, int N, int K, float* y,
+                             int8_t* qx, float* sx, const w4_fusion* f, unsigned flags, w4_stream_t s);
+w4_status q6g32_linear_fused(const void* w, const float* bias, const float* x, int M, int N, int K, float* y,
+                             int8_t* qx, float* sx, const w4_fusion* f, unsigned flags, w4_stream_t s);
+
+/* RMSNorm (as above) then the activation quantizer, one kernel: qx, sx of
+ * the normalized tokens.  x: float [M][K]; norm_weight: float [K]. */
+w4_status rms_a8_quantize(const float* x, const float* norm_weight, float eps, int M, int K, int8_t* qx, float* sx,
+                          unsigned flags, w4_stream_t s);
+
+/* The same operators as separate kernels (what a decoder runs without the
+ * fusions), fp32 in and out, flags 0 or W4_FLAG_PDL:
+ *   w4_rmsnorm: out[M][K] = RMSNorm(x) exactly as above (out may not overlap x);
+ *   w4_glu:     out[M][I] = act(gu[m][j]) * gu[m][I + j] for a [M][2I] gate|up
+ *               output (kind W4_GLU_SILU or W4_GLU_GELU_TANH), as above;
+ *   w4_add:     out[i] = a[i] + b[i], i < n (out may be a or b). */
+w4_status w4_rmsnorm(const float* x, const float* norm_weight, float eps, int M, int K, float* out, unsigned flags,
+                     w4_stream_t s);
+w4_status w4_glu(const float* gu, int kind, int M, int I, float* out, unsigned flags, w4_stream_t s);
+w4_status w4_add(const float* a, const float* b, long long n, float* out, unsigned flags, w4_stream_t s);
 
 /* ------------------------------------------------------------------------
  * A chain of per-row INT4 decode linears in one launch (a decode step's

@@ -70,6 +70,8 @@ def _load():
                 "orc_quantize_i8g32": [P, I, I, P, P],
                 "orc_gemv_i8g32": [P, P, P, P, P, I, I, I, P, P],
                 "orc_glu": [P, P, I, I, P],
+                "orc_quantize_rows_int8": [P, I, I, P, P],
+                "orc_gemv_weight_only": [P, P, P, P, I, I, I, P],
             }.items():
                 f = getattr(lib, name)
                 f.argtypes = args
@@ -289,3 +291,29 @@ def rmsnorm_w4a8_linear(packed, sw, x, g, eps, bias=None):
     xn = rmsnorm_f32(x, g, eps)
     y, qx, sx, acc = w4a8_linear(packed, sw, xn, bias)
     return y, qx, sx, acc, xn
+
+
+# -------------------------------------- weight-only paths (float activations)
+def quantize_rows_int8(W):
+    """Per-row symmetric INT8: returns (q int8 [N][K] in [-127,127], s_w f32 [N])."""
+    W = _c(W, np.float32)
+    N, K = W.shape
+    q = np.zeros((N, K), np.int8)
+    sw = np.zeros(N, np.float32)
+    _check(_load().orc_quantize_rows_int8(_ptr(W), N, K, _ptr(q), _ptr(sw)), "quantize_rows_int8")
+    return q, sw
+
+
+def gemv_weight_only(q, sw, x, bias=None):
+    """y = s_w[j] * sum_i q[j,i] x[m,i] + b[j] in fp64, activations not quantized."""
+    q = _c(q, np.int8)
+    sw = _c(sw, np.float32)
+    x = _c(np.atleast_2d(x), np.float32)
+    M, K = x.shape
+    N = q.shape[0]
+    assert q.shape[1] == K
+    b = None if bias is None else _c(bias, np.float32)
+    y = np.zeros((M, N), np.float64)
+    _check(_load().orc_gemv_weight_only(_ptr(q), _ptr(sw), _ptr(x), _ptr(b), M, N, K, _ptr(y)),
+           "gemv_weight_only")
+    return y

@@ -457,3 +457,56 @@ int orc_glu(const double* gate, const double* up, int n, int kind, double* out)
     }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The two paths [Orin-INT4] §"为什么 INT4 float 解包不快" measures against    */
+/* INT4 DP4A: weight-only INT8 (int8 weights, float activations, float       */
+/* multiply-add) and INT4 with float unpacking (each 4-bit weight unpacked,  */
+/* sign-extended, converted to float and multiply-added with the float      */
+/* activation).  Neither quantizes the activations.                         */
+/* ------------------------------------------------------------------------ */
+
+/* Per-row symmetric INT8 weights for the weight-only path.  The page gives  */
+/* no formula; the reading mirrors the per-row INT4 one with 127 in place of */
+/* 7: s^W_j = max_i |W_{j,i}| / 127, q = clip(round(W / s^W_j), -127, 127), */
+/* round half to even.  An all-zero row gives s = 0, q = 0.                  */
+int orc_quantize_rows_int8(const float* W, int N, int K, int8_t* q, float* sw)
+{
+    if (N < 0 || K < 0 || !W || !q || !sw) return ORC_ERR_ARG;
+    for (int j = 0; j < N; ++j) {
+        const float* wr = W + (size_t)j * K;
+        float amax = 0.0f;
+        for (int i = 0; i < K; ++i) {
+            float a = fabsf(wr[i]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / 127.0f;
+        sw[j] = s;
+        for (int i = 0; i < K; ++i) {
+            int v = 0;
+            if (s != 0.0f) {
+                v = (int)rintf(wr[i] / s);
+                if (v > 127) v = 127;
+                if (v < -127) v = -127;
+            }
+            q[(size_t)j * K + i] = (int8_t)v;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Weight-only linear on float activations (both paths above):              */
+/*   y[m][j] = s^W_j sum_i q_{j,i} x[m][i] + b_j, formed in fp64.           */
+/* q: int8 [N][K] (INT4 codes in [-8, 7] or INT8 codes); x: fp32 [M][K].    */
+int orc_gemv_weight_only(const int8_t* q, const float* sw, const float* x, const float* bias, int M, int N, int K,
+                         double* y)
+{
+    if (M < 0 || N < 0 || K < 0 || (M && N && (!q || !sw || !x || !y))) return ORC_ERR_ARG;
+    for (int m = 0; m < M; ++m)
+        for (int j = 0; j < N; ++j) {
+            double s = 0.0;
+            for (int i = 0; i < K; ++i) s += (double)q[(size_t)j * K + i] * (double)x[(size_t)m * K + i];
+            y[(size_t)m * N + j] = (double)sw[j] * s + (bias ? (double)bias[j] : 0.0);
+        }
+    return ORC_OK;
+}

@@ -487,3 +487,61 @@ def test_gelu_tanh_against_erf_gelu():
     assert err.max() > 4e-4
     u = np.full_like(v, -3.0)
     assert np.allclose(oracle.glu(v, u, oracle.GLU_GELU_TANH), -3.0 * a, rtol=1e-15, atol=0)
+
+
+# -------------------------------------- weight-only paths (float activations)
+# [Orin-INT4] §"为什么 INT4 float 解包不快": weight-only INT8 and INT4 with float
+# unpacking, the two paths the page measures against INT4 DP4A.
+
+def test_quantize_rows_int8_exact_grid_and_extremes():
+    """Rows on the grid k * s (k in [-127, 127]) with the absmax at 127 s
+    quantize exactly; the absmax maps to +-127; an all-zero row gives s = 0."""
+    g = wl.rng(21)
+    s = np.float32(2.0 ** -7)
+    k = g.integers(-127, 128, size=(4, 256))
+    k[:, 0] = 127
+    k[1, 0] = -127
+    W = (k * s).astype(np.float32)
+    q, sw = oracle.quantize_rows_int8(W)
+    assert np.all(sw == s)
+    assert np.array_equal(q.astype(int), k)
+    q0, s0 = oracle.quantize_rows_int8(np.zeros((1, 64), np.float32))
+    assert s0[0] == 0 and not q0.any()
+    Wr = wl.weights(g, 8, 512)
+    qr, swr = oracle.quantize_rows_int8(Wr)
+    assert np.all(np.abs(qr.astype(int)).max(axis=1) == 127)
+    assert np.all(np.abs(Wr - qr * swr[:, None]) <= swr[:, None] / 2 * (1 + 1e-6))
+
+
+def test_gemv_weight_only_against_numpy():
+    """The weight-only linear against numpy's float64 matmul (a library routine)
+    on the same integer codes, scales and bias."""
+    g = wl.rng(22)
+    M, N, K = 3, 40, 640
+    q = g.integers(-127, 128, size=(N, K)).astype(np.int8)
+    sw = wl.positive_scales(g, N)
+    x = wl.activations(g, M, K, outliers=True)
+    b = wl.bias(g, N)
+    y = oracle.gemv_weight_only(q, sw, x, b)
+    ref = (x.astype(np.float64) @ q.astype(np.float64).T) * sw.astype(np.float64)[None, :] + b[None, :]
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    # a single term: catches a swapped operand or a dropped scale or bias
+    q1 = np.zeros((2, 32), np.int8)
+    q1[1, 5] = -3
+    x1 = np.zeros((1, 32), np.float32)
+    x1[0, 5] = 0.5
+    y1 = oracle.gemv_weight_only(q1, np.array([1.0, 0.25], np.float32), x1, np.array([0.0, 2.0], np.float32))
+    assert y1[0, 0] == 0.0 and y1[0, 1] == 0.25 * -1.5 + 2.0
+
+
+def test_weight_only_int4_equals_float_reconstruction():
+    """INT4 codes through the weight-only linear equal the float GEMV of the
+    reconstructed weights s_w q (exact products in fp64): the float-unpack
+    path computes the dequantized weights' product with unquantized x."""
+    g = wl.rng(23)
+    W = wl.weights(g, 16, 256)
+    q, sw = oracle.quantize_rows_int4(W)
+    x = wl.activations(g, 2, 256)
+    y = oracle.gemv_weight_only(q, sw, x)
+    Wd = q.astype(np.float64) * sw.astype(np.float64)[:, None]
+    assert np.allclose(y, x.astype(np.float64) @ Wd.T, rtol=1e-12, atol=1e-12)

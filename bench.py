@@ -60,6 +60,10 @@ def parse_args(argv=None):
                         "workloads on its own, then the full step at M = 1, 2, 4, 8, 16 (one JSON line each)")
     p.add_argument("--suite-ms", default="1,2,4,8,16", help="token counts of the suite's full-step lines")
     p.add_argument("--suite-only-steps", action="store_true", help="suite: skip the single-GEMV lines")
+    p.add_argument("--suite-ablation-ms", default="1",
+                   help="token counts of the suite's weight-only ablation lines (INT4 DP4A, INT4 float unpack, "
+                        "INT8 weight-only; at most 2 tokens: the float activations of the K = 18944 linear "
+                        "live in shared memory)")
     p.add_argument("--suite-decoder-ms", default="1,16",
                    help="token counts of the suite's decoder-step lines (operators unfused, then fused)")
     p.add_argument("--independent-x", action="store_true",
@@ -90,8 +94,10 @@ def algorithmic_bytes(lin, M: int) -> int:
     (per-row INT4: 0.5 B a weight + a 4-byte scale a row; Q4_0: 18 B per 32
     weights; i8g32: 1 B a weight + 2 B per 32; q6g32: 26 B per 32), the bias,
     fp32 x and fp32 y."""
-    if lin.fmt == "w4":
+    if lin.fmt in ("w4", "w4a32"):
         w = lin.N * lin.K // 2 + 4 * lin.N
+    elif lin.fmt == "w8a32":
+        w = lin.N * lin.K + 4 * lin.N
     elif lin.fmt == "q4_0":
         w = lin.N * (lin.K // 32) * 18
     elif lin.fmt == "q6g32":
@@ -283,21 +289,24 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------- our arm
-def build_weights(args, device):
+def build_weights(args, device, fmt: str = "w4"):
     """The step's linears with resident repacked weights: [(layer, lin, QuantLinear)]."""
+    import dataclasses
+
     import torch
 
     from bit_quantized_decode_gb300 import QuantLinear
     out = []
     seed = 1000
     for layer, lin in step_linears(args.layers, not args.no_lm_head):
+        lin = dataclasses.replace(lin, fmt=fmt)
         shards = []
         for rows in lin.shards:
             shards.append(wl.torch_normal((rows, lin.K), lin.sigma, seed, device))
             seed += 1
         biases = [wl.torch_normal((rows,), 0.01, seed + i, device) for i, rows in enumerate(lin.shards)]
         seed += len(lin.shards)
-        out.append((layer, lin, QuantLinear.from_float("w4", shards, biases)))
+        out.append((layer, lin, QuantLinear.from_float(fmt, shards, biases)))
         del shards
     torch.cuda.synchronize()
     return out
@@ -777,7 +786,7 @@ def run_suite(args, local_rank):
     for kv in args.tune:
         k, v = kv.split("=")
         _lib.set_tuning(k, int(v))
-    for M in (int(m) for m in args.suite_ms.split(",")):
+    for M in (int(m) for m in args.suite_ms.split(",") if m):
         items, _, _ = make_buffers(weights, M, args.independent_x, dev)
 
         def step():
@@ -809,6 +818,26 @@ def run_suite(args, local_rank):
                               "ms_per_step": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
                               "bytes": b}), flush=True)
             del ops
+            torch.cuda.empty_cache()
+    # [Orin-INT4] §"为什么 INT4 float 解包不快": the same step on the weight-only
+    # paths with float activations (INT4 unpacked to float, INT8 weight-only)
+    for M in (int(m) for m in args.suite_ablation_ms.split(",") if m):
+        for fmt, label in (("w4", "int4_dp4a_int8_activations"), ("w4a32", "int4_float_unpack"),
+                           ("w8a32", "int8_weight_only")):
+            weights = build_weights(args, dev, fmt)
+            items, _, _ = make_buffers(weights, M, args.independent_x, dev)
+
+            def astep(items=items):
+                for i, (_, lin, ql, x, y, qx, sx) in enumerate(items):
+                    ql(x, y, qx, sx, flags=W4_FLAG_PDL if i else 0)
+
+            ms = _timed_graph(astep, stream, max(3, min(args.steps, 400)), args.warmup)
+            b = sum(algorithmic_bytes(lin, M) for _, lin, *_ in items)
+            gbs = b / (ms / 1e3) / 1e9
+            print(json.dumps({"suite": "qwen7b_step_ablation", "path": label, "M": M, "ms_per_step": round(ms, 5),
+                              "steps_per_s": round(1e3 / ms, 1), "GB/s": round(gbs, 1),
+                              "frac": round(gbs / peak, 4), "bytes": b}), flush=True)
+            del items, weights
             torch.cuda.empty_cache()
     err = _lib.device_error()
     if err:

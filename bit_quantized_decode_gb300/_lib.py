@@ -94,6 +94,11 @@ SIGNATURES.update({
     "w4_rmsnorm": ([_P, _P, _F, _I, _I, _P, _U, _P], _I),
     "w4_glu": ([_P, _I, _I, _I, _P, _U, _P], _I),
     "w4_add": ([_P, _P, _LL, _P, _U, _P], _I),
+    "w8_quantize_rows": ([_P, _I, _I, _P, _P, _P], _I),
+    "w8_repacked_bytes": ([_I, _I], _SZ),
+    "w8_repack": ([_PP, _PI, _I, _I, _P, _SZ, _P], _I),
+    "w4a32_gemv": ([_P, _P, _P, _P, _I, _I, _I, _P, _U, _P], _I),
+    "w8a32_gemv": ([_P, _P, _P, _P, _I, _I, _I, _P, _U, _P], _I),
 })
 
 
@@ -438,6 +443,45 @@ def w4_add(a, b, out, flags: int = 0, stream=None):
     _dev(a, b, out)
     assert a.numel() == b.numel() == out.numel()
     _check("w4_add", load().w4_add(_ptr(a), _ptr(b), a.numel(), _ptr(out), flags, _stream(stream)))
+
+
+# ------------------------------------- weight-only paths on float activations
+def w8_quantize_rows(W, q, s_w, stream=None):
+    """W float32 [N][K] -> q int8 [N][K] (per-row INT8), s_w float32 [N]."""
+    _dev(W, q, s_w)
+    N, K = W.shape
+    _check("w8_quantize_rows", load().w8_quantize_rows(_ptr(W), N, K, _ptr(q), _ptr(s_w), _stream(stream)))
+
+
+def w8_repacked_bytes(N: int, K: int) -> int:
+    return int(load().w8_repacked_bytes(N, K))
+
+
+def w8_repack(shards, K, out, stream=None):
+    """shards: int8 [rows_s][K] per-row INT8 codes; out: uint8 buffer of w8_repacked_bytes."""
+    _dev(out, *shards)
+    pp, keep = _ptr_array(shards)
+    rows, keep2 = _int_array([s.shape[0] for s in shards])
+    _check("w8_repack", load().w8_repack(pp, rows, len(shards), K, _ptr(out), out.numel() * out.element_size(),
+                                         _stream(stream)))
+
+
+def w4a32_gemv(w, s_w, bias, x, y, flags: int = 0, stream=None):
+    """Weight-only per-row INT4 (w4_repack layout) on float x [M][K], M <= 4; y[M][N]."""
+    _dev(w, s_w, bias, x, y)
+    M, K = x.shape
+    N = y.shape[1]
+    _check("w4a32_gemv", load().w4a32_gemv(_ptr(w), _ptr(s_w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), flags,
+                                           _stream(stream)))
+
+
+def w8a32_gemv(w, s_w, bias, x, y, flags: int = 0, stream=None):
+    """Weight-only per-row INT8 (w8_repack layout) on float x [M][K], M <= 4; y[M][N]."""
+    _dev(w, s_w, bias, x, y)
+    M, K = x.shape
+    N = y.shape[1]
+    _check("w8a32_gemv", load().w8a32_gemv(_ptr(w), _ptr(s_w), _ptr(bias), _ptr(x), M, N, K, _ptr(y), flags,
+                                           _stream(stream)))
 
 
 # ---------------------------------------------------------------- chains

@@ -30,8 +30,8 @@ NVCC_FLAGS = [
     "-Xptxas", "-v",
     "-I", INCLUDE,
 ]
-SOURCES = ["gemv_w4.cu", "gemv_q4_0.cu", "gemv_q6g32.cu", "gemv_i8g32.cu", "w4a8_api.cu", "prep_kernels.cu",
-           "gemv_tc.cu"]
+SOURCES = ["gemv_w4.cu", "gemv_q4_0.cu", "gemv_q6g32.cu", "gemv_i8g32.cu", "gemv_a32.cu", "w4a8_api.cu",
+           "prep_kernels.cu", "gemv_tc.cu"]
 
 
 def nvcc() -> str:

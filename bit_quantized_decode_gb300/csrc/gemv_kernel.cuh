@@ -91,6 +91,27 @@ __device__ __forceinline__ int unit4_signed16(const uint4 w, const uint4 x0, con
     return g;
 }
 
+// Weight-only formats on float activations: four weights from the four bytes
+// of `b` (each 0..255, the weight plus an offset) as fp32, exactly: the byte
+// is placed in the mantissa of 2^23 (PRMT with 0x4B000000 gives 2^23 + byte),
+// then 2^23 + offset is subtracted (negb, both halves).  Pairs in f32x2.
+__device__ __forceinline__ void byte_floats(uint32_t b, uint64_t negb, uint64_t& q01, uint64_t& q23)
+{
+    const float f0 = __int_as_float(static_cast<int>(__byte_perm(b, 0x4B000000u, 0x7440)));
+    const float f1 = __int_as_float(static_cast<int>(__byte_perm(b, 0x4B000000u, 0x7441)));
+    const float f2 = __int_as_float(static_cast<int>(__byte_perm(b, 0x4B000000u, 0x7442)));
+    const float f3 = __int_as_float(static_cast<int>(__byte_perm(b, 0x4B000000u, 0x7443)));
+    q01 = f2_add(f2_pack(f0, f1), negb);
+    q23 = f2_add(f2_pack(f2, f3), negb);
+}
+
+// acc2 += q . x for four weights against one float4 of x (f32x2 pairs).
+__device__ __forceinline__ uint64_t fma4(uint64_t q01, uint64_t q23, const float4& x, uint64_t acc2)
+{
+    acc2 = f2_fma(q01, f2_pack(x.x, x.y), acc2);
+    return f2_fma(q23, f2_pack(x.z, x.w), acc2);
+}
+
 // Fused prologue for large M*K: a first pass over x for the absmax, a second
 // to quantize, each in batches of 16 float4 per thread spread over the
 // tokens (all loads of a batch in flight at once).  One block barrier.
@@ -536,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
             const int prow = ra.glu != GLU_NONE ? glu_param_row(row, ra.n_out) : (row < ra.N ? row : -1);
             if (prow >= 0) {
                 if (ra.bias != nullptr) cp_async4(b_s + i, ra.bias + prow); else b_s[i] = 0.0f;
-                if constexpr (FMT == FMT_W4) cp_async4(w_s + i, ra.s_w + prow);
+                if constexpr (fmt_row_scale(FMT)) cp_async4(w_s + i, ra.s_w + prow);
             }
         }
     };
@@ -612,6 +633,31 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
             }
         }
         if (normed) {
+        } else if constexpr (XM == X_F32) {
+            // float activations, not quantized: into shared memory with each
+            // 32-value chunk's eight float4 XOR-swizzled by (chunk & 7), so the
+            // 16 lines of a pass read 8 distinct bank groups
+            float4* xs4 = reinterpret_cast<float4*>(xs);
+            const float4* xg = reinterpret_cast<const float4*>(a.x);
+            const int n4 = M * K4;
+            for (int i0 = tid; i0 < n4; i0 += 4 * kThreads) {
+                float4 t[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kThreads;
+                    t[u] = i < n4 ? __ldcg(xg + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kThreads;
+                    if (i < n4) {
+                        const int m = i / K4;
+                        const int f = i - m * K4;
+                        const int c = f >> 3;
+                        xs4[m * K4 + (c << 3) + ((f & 7) ^ (c & 7))] = t[u];
+                    }
+                }
+            }
         } else if constexpr (XM == X_FUSED) {
             constexpr int kRegF4 = 20;                  // float4 of x held per thread
             constexpr int kIt = kRegF4 / MT;            // per token
@@ -726,7 +772,63 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
                         if (line < n) {
                             const int chunk = c + line;
                             const uint8_t* ub = sw + (line * kRows + 4 * h) * kUnit;
-                            if constexpr (FMT == FMT_Q6G32) {
+                            if constexpr (fmt_float_x(FMT)) {
+                                // weight-only on float x: every weight unpacked to fp32 and
+                                // multiply-added (the pages' float path), f32x2 pairs
+                                const float4* xs4 = reinterpret_cast<const float4*>(xs);
+                                const int swz = chunk & 7;
+                                uint4 w0[4], w1[4];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    if constexpr (FMT == FMT_W4F) {
+                                        w0[j] = *reinterpret_cast<const uint4*>(ub + ((j ^ pp) << 4));
+                                    } else {
+                                        const uint8_t* u = ub + ((j ^ pp) << 5);
+                                        const uint4 first = *reinterpret_cast<const uint4*>(u + (h << 4));
+                                        const uint4 second = *reinterpret_cast<const uint4*>(u + ((h ^ 1) << 4));
+                                        w0[j] = h ? second : first;
+                                        w1[j] = h ? first : second;
+                                    }
+                                }
+#pragma unroll
+                                for (int m = 0; m < MT; ++m) {
+                                    if (MT == 1 || m < M) {
+                                        float4 xv[8];
+                                        const float4* xp = xs4 + static_cast<size_t>(m) * (K >> 2) + chunk * 8;
+#pragma unroll
+                                        for (int k = 0; k < 8; ++k) xv[k] = xp[k ^ swz];
+#pragma unroll
+                                        for (int j = 0; j < 4; ++j) {
+                                            uint64_t a2 = 0;
+                                            uint64_t q01, q23;
+                                            if constexpr (FMT == FMT_W4F) {
+                                                // byte b of word w: weight 8w+b (low nibble), 8w+4+b (high)
+                                                const uint64_t negb = f2_pack(-8388616.0f, -8388616.0f);
+                                                const uint32_t wd[4] = {w0[j].x, w0[j].y, w0[j].z, w0[j].w};
+#pragma unroll
+                                                for (int w = 0; w < 4; ++w) {
+                                                    byte_floats(wd[w] & 0x0F0F0F0Fu, negb, q01, q23);
+                                                    a2 = fma4(q01, q23, xv[2 * w], a2);
+                                                    byte_floats((wd[w] >> 4) & 0x0F0F0F0Fu, negb, q01, q23);
+                                                    a2 = fma4(q01, q23, xv[2 * w + 1], a2);
+                                                }
+                                            } else {
+                                                // byte i: weight i as int8; biased by 128 to 1..255
+                                                const uint64_t negb = f2_pack(-8388736.0f, -8388736.0f);
+                                                const uint32_t wd[8] = {w0[j].x, w0[j].y, w0[j].z, w0[j].w,
+                                                                        w1[j].x, w1[j].y, w1[j].z, w1[j].w};
+#pragma unroll
+                                                for (int k = 0; k < 8; ++k) {
+                                                    byte_floats(wd[k] ^ 0x80808080u, negb, q01, q23);
+                                                    a2 = fma4(q01, q23, xv[k], a2);
+                                                }
+                                            }
+                                            acc[m][j] = __fadd_rn(acc[m][j], __fadd_rn(__uint_as_float(f2_lo(a2)),
+                                                                                       __uint_as_float(f2_hi(a2))));
+                                        }
+                                    }
+                                }
+                            } else if constexpr (FMT == FMT_Q6G32) {
                                 // n = q + 32 = lo + 16 hi: sum n x from the two planes,
                                 // minus 32 sum x, is the exact group sum of q x
                                 const uint8_t* hb = sw + kSlotW + (line * kRows + 4 * h) * kHi;
@@ -925,6 +1027,9 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
                     const int accv = v - 8 * xsum;          // remove the +8 nibble bias
                     const float swr = rows_cached ? sw_s[ci] : a.s_w[prow];
                     return __fmaf_rn(__fmul_rn(swr, sx_s[m]), __int2float_rn(accv), b);
+                } else if constexpr (fmt_row_scale(FMT)) {
+                    const float swr = rows_cached ? sw_s[ci] : a.s_w[prow];
+                    return __fmaf_rn(swr, v, b);
                 } else {
                     return __fmaf_rn(sx_s[m], v, b);
                 }

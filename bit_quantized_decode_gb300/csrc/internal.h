@@ -7,7 +7,11 @@
 
 namespace w4k {
 
-enum FmtId { FMT_W4 = 0, FMT_Q4_0 = 1, FMT_I8G32 = 2, FMT_Q6G32 = 3 };
+// Weight formats.  W4F and W8F are the weight-only paths on float
+// activations that "Jetson Orin AGX INT4 推理优化实践" §"为什么 INT4 float
+// 解包不快" measures against INT4 DP4A: per-row INT4 in the W4 layout
+// unpacked to float, and per-row INT8 (32-byte units, no scale plane).
+enum FmtId { FMT_W4 = 0, FMT_Q4_0 = 1, FMT_I8G32 = 2, FMT_Q6G32 = 3, FMT_W4F = 4, FMT_W8F = 5 };
 
 constexpr int kRows = 8;                 // weight rows per tile
 constexpr int kWarps = 8;                // warps per GEMV thread block
@@ -16,11 +20,11 @@ constexpr int kMaxStages = 8;            // ring slots per warp, upper bound
 constexpr int kAccWords = 64;            // round_tiles * MT, bounds the per-round accumulator
 constexpr int kRowCache = 1024;          // rows per block whose s_w / bias are staged in shared memory
 
-// How a GEMV block obtains its int8 activations.
 // Activation source of a GEMV: quantized in the prologue (from x, or from
 // RMSNorm(x) when GemvArgs::gamma is set), int8 codes copied into shared
-// memory, or codes read from global memory in the inner loop.
-enum XMode { X_FUSED = 0, X_SMEM = 1, X_GLOBAL = 2 };
+// memory, codes read from global memory in the inner loop, or (the
+// weight-only formats) fp32 x copied into shared memory unquantized.
+enum XMode { X_FUSED = 0, X_SMEM = 1, X_GLOBAL = 2, X_F32 = 3 };
 
 // Gated MLP activation applied by the epilogue (fusion.cuh).
 enum GluKind { GLU_NONE = 0, GLU_SILU = 1, GLU_GELU_TANH = 2 };
@@ -38,10 +42,17 @@ __host__ __device__ inline int glu_param_row(int R, int n_out)
 // Lines (8 rows x one 32-weight chunk) per ring slot and bytes per unit.
 // Q6G32 keeps each unit in two planes: 16 bytes of low nibbles and 8 bytes
 // of 2-bit high parts (fmt_hi_bytes).
-__host__ __device__ constexpr int fmt_unit_bytes(int fmt) { return fmt == FMT_I8G32 ? 32 : 16; }
+__host__ __device__ constexpr int fmt_unit_bytes(int fmt) { return fmt == FMT_I8G32 || fmt == FMT_W8F ? 32 : 16; }
 __host__ __device__ constexpr int fmt_hi_bytes(int fmt) { return fmt == FMT_Q6G32 ? 8 : 0; }
-__host__ __device__ constexpr bool fmt_group(int fmt) { return fmt != FMT_W4; }
-__host__ __device__ constexpr int fmt_slice_lines(int fmt) { return fmt == FMT_I8G32 || fmt == FMT_Q6G32 ? 16 : 32; }
+__host__ __device__ constexpr bool fmt_group(int fmt) { return fmt == FMT_Q4_0 || fmt == FMT_I8G32 || fmt == FMT_Q6G32; }
+// Formats with one float scale per row (s_w).
+__host__ __device__ constexpr bool fmt_row_scale(int fmt) { return fmt == FMT_W4 || fmt == FMT_W4F || fmt == FMT_W8F; }
+// Formats on unquantized float activations.
+__host__ __device__ constexpr bool fmt_float_x(int fmt) { return fmt == FMT_W4F || fmt == FMT_W8F; }
+__host__ __device__ constexpr int fmt_slice_lines(int fmt)
+{
+    return fmt == FMT_I8G32 || fmt == FMT_Q6G32 || fmt == FMT_W8F ? 16 : 32;
+}
 __host__ __device__ constexpr int fmt_slot_w_bytes(int fmt) { return fmt_slice_lines(fmt) * kRows * fmt_unit_bytes(fmt); }
 __host__ __device__ constexpr int fmt_slot_h_bytes(int fmt) { return fmt_slice_lines(fmt) * kRows * fmt_hi_bytes(fmt); }
 __host__ __device__ constexpr int fmt_slot_s_bytes(int fmt) { return fmt_group(fmt) ? fmt_slice_lines(fmt) * kRows * 2 : 0; }
@@ -106,7 +117,7 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, in
     L.acc = o;   o = align_up(o + 2 * round_tiles * kRows * MT * 4, 16);
     L.bnd = o;   o = align_up(o + 2 * kWarps * 2 * kRows * MT * 4, 128);
     L.ring = o;  o = align_up(o + kWarps * stages * fmt_slot_bytes(fmt), 128);
-    L.xs = o;    o += xmode != X_GLOBAL ? MT * K : 0;
+    L.xs = o;    o += xmode == X_F32 ? MT * K * 4 : (xmode != X_GLOBAL ? MT * K : 0);
     L.total = o;
     return L;
 }
@@ -127,6 +138,9 @@ cudaError_t launch_gemv_q6g32(const ChainParams<1>& p, int MT, int xmode, int gr
 // Largest x float4 per thread and token the RMSNorm prologue holds in
 // registers (x and the norm weight together).
 __host__ __device__ constexpr int norm_max_nit(int MT) { return MT >= 4 ? 4 : 20 / (MT + 1); }
+// Weight-only GEMVs on float activations (W4F, W8F; xmode X_F32; MT in {1, 2, 4}).
+cudaError_t launch_gemv_a32(int fmt, const ChainParams<1>& p, int MT, int grid, size_t smem, bool pdl,
+                            cudaStream_t s);
 // Chains of per-row INT4 linears (cooperative launch, fused quantization).
 cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
 
@@ -204,6 +218,8 @@ cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int M,
 cudaError_t launch_glu(const float* gu, int kind, int M, int I, float* out, bool pdl, cudaStream_t s);
 cudaError_t launch_add(const float* a, const float* b, long long n, float* out, bool pdl, cudaStream_t s);
 cudaError_t launch_w4_quantize_rows(const float* W, int N, int K, uint32_t* packed, float* s_w, cudaStream_t s);
+cudaError_t launch_w8_quantize_rows(const float* W, int N, int K, int8_t* q, float* s_w, cudaStream_t s);
+cudaError_t launch_w8_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);
 cudaError_t launch_q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, cudaStream_t s);
 cudaError_t launch_i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, cudaStream_t s);
 cudaError_t launch_w4_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s);

@@ -298,6 +298,38 @@ cudaError_t launch_w4_quantize_rows(const float* W, int N, int K, uint32_t* pack
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------ per-row INT8 weights
+// The weight-only INT8 path ("Jetson Orin AGX INT4 推理优化实践", §"为什么 INT4
+// float 解包不快"): s^W_j = max|W_j| / 127, q = clip(rint(W / s^W_j), -127, 127),
+// one int8 per weight [N][K].  One warp per row.
+__global__ void __launch_bounds__(256) w8_quantize_rows_kernel(const float* __restrict__ W, int N, int K,
+                                                              int8_t* __restrict__ q, float* __restrict__ sw)
+{
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const float4* wr = reinterpret_cast<const float4*>(W + static_cast<size_t>(row) * K);
+    float mx = 0.0f;
+    for (int i = lane; i < K / 4; i += 32) mx = fmaxf(mx, abs_max4(wr[i]));
+    mx = warp_max(mx);
+    const float s = __fdiv_rn(mx, 127.0f);
+    if (lane == 0) sw[row] = s;
+    uint32_t* out = reinterpret_cast<uint32_t*>(q + static_cast<size_t>(row) * K);
+    for (int i = lane; i < K / 4; i += 32) {
+        const float4 v = wr[i];
+        out[i] = (static_cast<uint32_t>(quant_code(v.x, s, -127, 127)) & 0xffu) |
+                 ((static_cast<uint32_t>(quant_code(v.y, s, -127, 127)) & 0xffu) << 8) |
+                 ((static_cast<uint32_t>(quant_code(v.z, s, -127, 127)) & 0xffu) << 16) |
+                 ((static_cast<uint32_t>(quant_code(v.w, s, -127, 127)) & 0xffu) << 24);
+    }
+}
+
+cudaError_t launch_w8_quantize_rows(const float* W, int N, int K, int8_t* q, float* s_w, cudaStream_t s)
+{
+    w8_quantize_rows_kernel<<<(N + 7) / 8, 256, 0, s>>>(W, N, K, q, s_w);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- Q4_0
 // "在香橙派上跑 Gemma4", §3.1: 32 weights per block, 16 bytes of nibbles and an
 // fp16 scale; d = fp16(max|w| / 8), n = clip(rint(w / d), -8, 7) + 8.  Block
@@ -505,11 +537,11 @@ __global__ void i8g32_repack_kernel(const ShardTable st, int N, int K, long long
                                                           static_cast<size_t>(local) * K + c * 32);
         o0 = src[0];
         o1 = src[1];
-        dbits = static_cast<const uint16_t*>(st.p2[s])[static_cast<size_t>(local) * C + c];
+        if (plane != nullptr) dbits = static_cast<const uint16_t*>(st.p2[s])[static_cast<size_t>(local) * C + c];
     }
     out[2 * u] = o0;
     out[2 * u + 1] = o1;
-    plane[u] = dbits;
+    if (plane != nullptr) plane[u] = dbits;     // per-row INT8 (W8F) has no scale plane
 }
 
 // Q6G32: the i8g32 codes q in [-32, 31], biased n = q + 32 (6 bits), packed
@@ -593,6 +625,15 @@ cudaError_t launch_i8g32_repack(const ShardTable& st, int N, int K, void* out, c
     uint4* o = static_cast<uint4*>(out);
     uint16_t* plane = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + units * 32);
     i8g32_repack_kernel<<<blocks_for(units, 256), 256, 0, s>>>(st, N, K, units, o, plane);
+    return cudaGetLastError();
+}
+
+// Per-row INT8 weights: the I8G32 unit layout without its scale plane.
+cudaError_t launch_w8_repack(const ShardTable& st, int N, int K, void* out, cudaStream_t s)
+{
+    const long long T = (N + kRows - 1) / kRows;
+    const long long units = T * (K / 32) * kRows;
+    i8g32_repack_kernel<<<blocks_for(units, 256), 256, 0, s>>>(st, N, K, units, static_cast<uint4*>(out), nullptr);
     return cudaGetLastError();
 }
 

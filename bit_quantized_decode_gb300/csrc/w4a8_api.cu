@@ -116,7 +116,11 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
     const int whole = d.smem_optin;
     int bps = g_tune[W4_TUNE_BLOCKS_PER_SM];
     if (bps == 0 && MT > 1) bps = 1;
-    const int modes[2] = {fused ? X_FUSED : X_SMEM, fused ? -1 : X_GLOBAL};
+    int modes[2] = {fused ? X_FUSED : X_SMEM, fused ? -1 : X_GLOBAL};
+    if (fmt_float_x(fmt)) {
+        modes[0] = X_F32;
+        modes[1] = -1;
+    }
     for (int pass = 0; pass < 2; ++pass) {
         // pass 0: co-resident budget (unless forced to one block per SM)
         if (pass == 0 && bps == 1) continue;
@@ -161,7 +165,8 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     if (a.T < grid) grid = a.T;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
     cudaError_t e;
-    if (fmt == FMT_W4) e = launch_gemv_w4(cp, MT, p.xmode, grid, p.smem, pdl, s);
+    if (fmt_float_x(fmt)) e = launch_gemv_a32(fmt, cp, MT, grid, p.smem, pdl, s);
+    else if (fmt == FMT_W4) e = launch_gemv_w4(cp, MT, p.xmode, grid, p.smem, pdl, s);
     else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(cp, MT, p.xmode, grid, p.smem, pdl, s);
     else if (fmt == FMT_I8G32) e = launch_gemv_i8g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
     else e = launch_gemv_q6g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
@@ -773,6 +778,79 @@ w4_status w4_add(const float* a, const float* b, long long n, float* out, unsign
     if (!a || !b || !out) return W4_ERR_INVALID_ARG;
     if (!aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4)) return W4_ERR_MISALIGNED;
     return cuda_status(launch_add(a, b, n, out, (flags & W4_FLAG_PDL) != 0, reinterpret_cast<cudaStream_t>(s)));
+}
+
+// ------------------------------------- weight-only paths on float activations
+w4_status w8_quantize_rows(const float* W, int N, int K, int8_t* q, float* s_w, w4_stream_t s)
+{
+    if (N < 0 || K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 4 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!W || !q || !s_w) return W4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(q, 4) || !aligned(s_w, 4)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_w8_quantize_rows(W, N, K, q, s_w, reinterpret_cast<cudaStream_t>(s)));
+}
+
+size_t w8_repacked_bytes(int N, int K)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0) return 0;
+    return tiles(N) * kRows * static_cast<size_t>(K);
+}
+
+w4_status w8_repack(const int8_t* const* shard_q, const int* shard_rows, int n_shards, int K, void* out,
+                    size_t out_bytes, w4_stream_t s)
+{
+    if (K <= 0) return W4_ERR_INVALID_ARG;
+    if (K % 32 != 0 || K > W4_MAX_K) return W4_ERR_UNSUPPORTED_SHAPE;
+    ShardTable st;
+    int N = 0;
+    w4_status r = build_shards(reinterpret_cast<const void* const*>(shard_q), nullptr, shard_rows, n_shards, st, N);
+    if (r != W4_OK) return r;
+    if (N == 0) return W4_OK;
+    if (!out) return W4_ERR_INVALID_ARG;
+    if (out_bytes < w8_repacked_bytes(N, K)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(out, 16)) return W4_ERR_MISALIGNED;
+    for (int i = 0; i < n_shards; ++i)
+        if (st.p[i] && !aligned(st.p[i], 16)) return W4_ERR_MISALIGNED;
+    return cuda_status(launch_w8_repack(st, N, K, out, reinterpret_cast<cudaStream_t>(s)));
+}
+
+namespace {
+w4_status a32_common(int fmt, const void* w, const float* s_w, const float* bias, const float* x, int M, int N,
+                     int K, float* y, unsigned flags, cudaStream_t s)
+{
+    w4_status st = check_mk(M, K);
+    if (st != W4_OK) return st;
+    if (N < 0 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_INVALID_ARG;
+    if (M > 4 || N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!w || !s_w || !x || !y) return W4_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(s_w, 4) || (bias && !aligned(bias, 4)))
+        return W4_ERR_MISALIGNED;
+    GemvArgs a = {};
+    a.w = static_cast<const uint8_t*>(w);
+    a.s_w = s_w;
+    a.bias = bias;
+    a.x = x;
+    a.y = y;
+    a.n_out = N;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    return run_gemv(fmt, a, false, flags, s);
+}
+}  // namespace
+
+w4_status w4a32_gemv(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,
+                     float* y, unsigned flags, w4_stream_t s)
+{
+    return a32_common(FMT_W4F, w, s_w, bias, x, M, N, K, y, flags, reinterpret_cast<cudaStream_t>(s));
+}
+
+w4_status w8a32_gemv(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,
+                     float* y, unsigned flags, w4_stream_t s)
+{
+    return a32_common(FMT_W8F, w, s_w, bias, x, M, N, K, y, flags, reinterpret_cast<cudaStream_t>(s));
 }
 
 // ----------------------------------------------------------------- chains

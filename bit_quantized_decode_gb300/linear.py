@@ -13,7 +13,9 @@ import torch
 
 from . import _lib
 
-FORMATS = ("w4", "q4_0", "i8g32", "q6g32")
+# "w4a32" and "w8a32" are the weight-only paths on float activations (per-row
+# INT4 unpacked to float, per-row INT8); their calls ignore qx and sx.
+FORMATS = ("w4", "q4_0", "i8g32", "q6g32", "w4a32", "w8a32")
 
 
 class QuantLinear:
@@ -44,7 +46,13 @@ class QuantLinear:
         canon, scales = [], []
         for W in shards:
             n = W.shape[0]
-            if fmt == "w4":
+            if fmt == "w8a32":
+                q = torch.empty((n, K), dtype=torch.int8, device=dev)
+                sw = torch.empty(n, dtype=torch.float32, device=dev)
+                _lib.w8_quantize_rows(W, q, sw)
+                canon.append(q)
+                scales.append(sw)
+            elif fmt in ("w4", "w4a32"):
                 p = torch.empty((n, K // 8), dtype=torch.int32, device=dev)
                 sw = torch.empty(n, dtype=torch.float32, device=dev)
                 _lib.w4_quantize_rows(W, p, sw)
@@ -93,9 +101,14 @@ class QuantLinear:
                 w = torch.empty(_lib.q4_0_glu_repacked_bytes(I, K), dtype=torch.uint8, device=dev)
                 _lib.q4_0_repack_glu(canon[0], canon[1], K, w)
             return w, s_w
-        if fmt == "w4":
+        if fmt in ("w4", "w4a32"):
             w = torch.empty(_lib.w4_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
             _lib.w4_repack(canon, K, w)
+            s_w = torch.empty(N, dtype=torch.float32, device=dev)
+            _lib.w4_concat_f32(scales, s_w)
+        elif fmt == "w8a32":
+            w = torch.empty(_lib.w8_repacked_bytes(N, K), dtype=torch.uint8, device=dev)
+            _lib.w8_repack(canon, K, w)
             s_w = torch.empty(N, dtype=torch.float32, device=dev)
             _lib.w4_concat_f32(scales, s_w)
         elif fmt == "q4_0":
@@ -129,6 +142,12 @@ class QuantLinear:
             sx = sx if sx is not None else s2
         if self.glu_pairs != (glu != _lib.W4_GLU_NONE):
             raise ValueError("glu is taken exactly by linears built with glu_pairs=True")
+        if self.fmt in ("w4a32", "w8a32"):
+            if norm is not None or glu != _lib.W4_GLU_NONE or residual is not None:
+                raise ValueError("the weight-only paths take no fused operators")
+            fn = _lib.w4a32_gemv if self.fmt == "w4a32" else _lib.w8a32_gemv
+            fn(self.w, self.s_w, self.bias, x, y, flags, stream)
+            return y
         if norm is not None or glu != _lib.W4_GLU_NONE or residual is not None:
             fz = _lib.fusion(norm, eps, glu, residual)
             if self.fmt == "w4":

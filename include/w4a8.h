@@ -290,6 +290,33 @@ w4_status w4_glu(const float* gu, int kind, int M, int I, float* out, unsigned f
 w4_status w4_add(const float* a, const float* b, long long n, float* out, unsigned flags, w4_stream_t s);
 
 /* ------------------------------------------------------------------------
+ * Weight-only paths on float activations: the two paths [Orin-INT4]
+ * §"为什么 INT4 float 解包不快" measures INT4 DP4A against (weight-only INT8,
+ * and INT4 unpacked to float).  The activations are not quantized:
+ *   y[m][j] = fmaf(s_w[j], sum_i q_w[j][i] * x[m][i], b[j]),
+ * every weight converted to fp32 and multiply-added in fp32 (summation order
+ * unspecified).
+ *   w4a32_gemv: per-row INT4 weights in the w4_repack layout (the bytes the
+ *     DP4A path reads), unpacked to float.
+ *   w8a32_gemv: per-row INT8 weights from w8_quantize_rows (s_w = max|W|/127,
+ *     q = clip(rint(W / s_w), -127, 127), int8 [N][K]) in the w8_repack
+ *     layout: 32-byte units holding a row's 32 int8 weights of a chunk in
+ *     order, in the (t, c, r) order of the other formats, no scale plane.
+ * x: float [M][K], 16-byte aligned; 1 <= M <= 4; flags: 0 or W4_FLAG_PDL.
+ * x is staged in shared memory as fp32 beside a weight ring of at least two
+ * stages, so M*K is limited to about 40000 values (W4_ERR_UNSUPPORTED_SHAPE
+ * beyond: K = 18944 takes at most two tokens).
+ * ------------------------------------------------------------------------ */
+w4_status w8_quantize_rows(const float* W, int N, int K, int8_t* q, float* s_w, w4_stream_t s);
+size_t w8_repacked_bytes(int N, int K);
+w4_status w8_repack(const int8_t* const* shard_q, const int* shard_rows, int n_shards, int K, void* out,
+                    size_t out_bytes, w4_stream_t s);
+w4_status w4a32_gemv(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,
+                     float* y, unsigned flags, w4_stream_t s);
+w4_status w8a32_gemv(const void* w, const float* s_w, const float* bias, const float* x, int M, int N, int K,
+                     float* y, unsigned flags, w4_stream_t s);
+
+/* ------------------------------------------------------------------------
  * A chain of per-row INT4 decode linears in one launch (a decode step's
  * linear set).  Linear i computes exactly what w4a8_linear computes for
  * descs[i]; linear i+1 reads its x only after every output of linear i is

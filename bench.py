@@ -52,6 +52,9 @@ def parse_args(argv=None):
     p.add_argument("--chain", action="store_true",
                    help="one chained launch per step (w4a8_linear_chain) instead of one PDL launch per linear")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--weights", choices=("w4", "w4a32", "w8a32"), default="w4",
+                   help="the step's linear path: per-row INT4 x INT8 activations on DP4A (default), or a "
+                        "weight-only path on float activations (INT4 unpacked to float, per-row INT8; M <= 2)")
     p.add_argument("--decoder", choices=("off", "fused", "unfused"), default="off",
                    help="run the step with the RMSNorm, SwiGLU and residual adds of a decoder layer around "
                         "the linears: fused into them, or as separate kernels")
@@ -112,7 +115,10 @@ def workload_config(args, n_gpus):
         "workload": (f"qwen2-7b decode-step linear set: {args.layers} layers x (fused QKV 4608x3584, "
                      f"O 3584x3584, fused gate/up 37888x3584, down 3584x18944)"
                      + ("" if args.no_lm_head else " + lm_head 152064x3584")
-                     + f", per-row INT4 weights, INT8 per-token activations, M={args.M}"),
+                     + {"w4": ", per-row INT4 weights, INT8 per-token activations",
+                        "w4a32": ", per-row INT4 weights unpacked to float, float activations",
+                        "w8a32": ", per-row INT8 weights, float activations"}[args.weights]
+                     + f", M={args.M}"),
         "M": args.M,
         "layers": args.layers,
         "lm_head": not args.no_lm_head,
@@ -351,7 +357,7 @@ def make_buffers(weights, M: int, independent_x: bool, device, seed: int = 5000)
 
 
 def build_step(args, device):
-    return make_buffers(build_weights(args, device), args.M, args.independent_x, device)
+    return make_buffers(build_weights(args, device, args.weights), args.M, args.independent_x, device)
 
 
 NORM_EPS = 1e-6
@@ -509,7 +515,7 @@ def run_ours(args, rank, world, local_rank):
 
     # one chained launch per step (at most W4_MAX_CHAIN linears per launch)
     chains = []
-    if args.chain and args.decoder == "off":
+    if args.chain and args.decoder == "off" and args.weights == "w4":
         try:
             for c0 in range(0, len(items), _lib.W4_MAX_CHAIN):
                 part = items[c0: c0 + _lib.W4_MAX_CHAIN]
@@ -664,7 +670,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int32 (int4 x int8 dp4a)",
+        "dtype": {"w4": "int32 (int4 x int8 dp4a)", "w4a32": "f32 (int4 weights unpacked to float)",
+                  "w8a32": "f32 (int8 weights, float activations)"}[args.weights],
         "data": "synthetic",
         "config": workload_config(args, world),
         "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",

@@ -90,4 +90,8 @@ __device__ __forceinline__ float glu_act(int kind, float g, float u)
     return __fmul_rn(__fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, t)), u);
 }
 
+// The same, out of line: the GEMV epilogues run it once per output, and its
+// library calls stay out of the kernels' instruction footprint.
+static __device__ __noinline__ float glu_act_call(int kind, float g, float u) { return glu_act(kind, g, u); }
+
 }  // namespace w4k

@@ -193,7 +193,7 @@ __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float*
                         uint32_t ok = 0xffffffffu;
                         uint32_t q = a8_pack4_fast2(v[m][u], rr, ok);
                         // rare: a possible tie (or a tiny scale): the exact quotient decides
-                        if (all_exact || (ok >> 31) == 0u) q = a8_pack4(v[m][u], ks[m]);
+                        if (all_exact || (ok >> 31) == 0u) q = a8_pack4_exact(v[m][u], ks[m]);
                         dst[i] = q;
                         if (gout) gout[i] = q;
                         if constexpr (kCodeSums) tsum[m] += bytesum(q);
@@ -315,7 +315,7 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
                 if (need) {
 #pragma unroll
                     for (int u = 0; u < kG; ++u)
-                        if (g0 + u < NIT && ((need >> u) & 1u)) qw[u] = a8_pack4(v[m][g0 + u], ks);
+                        if (g0 + u < NIT && ((need >> u) & 1u)) qw[u] = a8_pack4_exact(v[m][g0 + u], ks);
                 }
 #pragma unroll
                 for (int u = 0; u < kG; ++u) {
@@ -335,17 +335,18 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
 }
 
 // Tile range of this block in one linear: an even split of the T tiles over
-// the grid, processed in rounds of at most RT tiles.
+// the grid (the host passes T = tq * grid + tr, so no division here),
+// processed in rounds of at most RT tiles.
 struct BlockRange {
     int t0, ntiles, nrounds;
 };
 
-__device__ __forceinline__ BlockRange block_range(int T, int RT)
+template <int RT>
+__device__ __forceinline__ BlockRange block_range(const GemvArgs& a)
 {
-    const long long G = gridDim.x;
-    const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * T) / G);
-    const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * T) / G);
-    return BlockRange{t0, t1 - t0, (t1 - t0 + RT - 1) / RT};
+    const int b = static_cast<int>(blockIdx.x);
+    const int n = a.tq + (b < a.tr ? 1 : 0);
+    return BlockRange{b * a.tq + min(b, a.tr), n, (n + RT - 1) / RT};
 }
 
 // Warp w's line range [lo, hi) within a round of nt tiles of C lines: an even
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = P.stages;
-    const int RT = P.round_tiles;
+    constexpr int RT = kAccWords / MT;               // tiles per round (the host sets P.round_tiles to this)
     const int NL = NCH == 1 ? 1 : P.n;
     const int M = P.lin[0].M;
     const SmemLayout L = smem_layout(FMT, MT, XM, P.kmax, S, RT, kRowBufs, kRowCap);
@@ -474,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
         k.lin = 0;
         k.round = 0;
         k.done = false;
-        k.r = block_range(P.lin[0].T, RT);
+        k.r = block_range<RT>(P.lin[0]);
         if (k.r.nrounds > 0) enter_round(k);
     };
     // Next slice of the cursor: linear index, first unit, lines.  False at the end.
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
                     k.done = true;
                     return false;
                 }
-                k.r = block_range(P.lin[k.lin].T, RT);
+                k.r = block_range<RT>(P.lin[k.lin]);
                 k.round = 0;
             }
             enter_round(k);
@@ -547,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
     // asynchronous 4-byte copies, complete after cp_async_wait_all().
     auto stage_rows = [&](int li) {
         const GemvArgs& ra = P.lin[li];
-        const BlockRange rr = block_range(ra.T, RT);
+        const BlockRange rr = block_range<RT>(ra);
         if (rr.ntiles * kRows > kRowCap) return;
         float* b_s = rowp_s + (li & (kRowBufs - 1)) * 2 * kRowCap;
         float* w_s = b_s + kRowCap;
@@ -578,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
         const GemvArgs& a = P.lin[li];
         const int C = a.C;
         const int K = a.K;
-        const BlockRange br = block_range(a.T, RT);
+        const BlockRange br = block_range<RT>(a);
         const int t0 = br.t0;
         const int ntiles = br.ntiles;
         const int nrounds = br.nrounds;
@@ -1057,7 +1058,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
                     const int rlg = (jo >> 2) * kRows + (jo & 3);
                     const float g = lin_out(m, rlg, row_base + rlg);
                     const float u = lin_out(m, rlg + 4, row_base + rlg + 4);
-                    float out = glu_act(a.glu, g, u);
+                    float out = glu_act_call(a.glu, g, u);
                     const size_t o = static_cast<size_t>(m) * a.n_out + j;
                     if (a.residual != nullptr) out = __fadd_rn(a.residual[o], out);
                     a.y[o] = out;

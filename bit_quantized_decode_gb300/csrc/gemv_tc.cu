@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             const float u = __shfl_down_sync(0xffffffffu, v, 4);
             if (have && (row & 4) == 0 && n < A.M) {
                 const size_t o = static_cast<size_t>(n) * A.n_out + j;
-                float out = glu_act(A.glu, v, u);
+                float out = glu_act_call(A.glu, v, u);
                 if (A.residual != nullptr) out = __fadd_rn(A.residual[o], out);
                 A.y[o] = out;
             }

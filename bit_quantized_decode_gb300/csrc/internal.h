@@ -82,6 +82,7 @@ struct GemvArgs {
     int M, N, K;             // N: weight rows (a gated linear: 8 ceil(I / 4))
     int C;                   // K / 32
     int T;                   // ceil(N / 8)
+    int tq, tr;              // T = tq * grid + tr: block b owns tq (+1 if b < tr) tiles, from b tq + min(b, tr)
 };
 
 // Kernel parameters: up to NCH linears computed in order by one launch.

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float*
     auto code = [&](float4 f) -> uint32_t {
         uint32_t ok = 0xffffffffu;
         const uint32_t q = a8_pack4_fast2(f, rr, ok);
-        return (all_exact || (ok >> 31) == 0) ? a8_pack4(f, ks) : q;
+        return (all_exact || (ok >> 31) == 0) ? a8_pack4_exact(f, ks) : q;
     };
     if constexpr (kRegs) {
 #pragma unroll
@@ -179,7 +179,9 @@ cudaError_t launch_quant(const float* x, const float* gamma, float eps, int M, i
     if (nit <= 2) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<2, kNorm>, x, gamma, eps, K, qx, sx);
     if (nit <= 4) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<4, kNorm>, x, gamma, eps, K, qx, sx);
     if (nit <= 10) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<10, kNorm>, x, gamma, eps, K, qx, sx);
-    if (!kNorm && nit <= 16) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<16, kNorm>, x, gamma, eps, K, qx, sx);
+    if constexpr (!kNorm) {
+        if (nit <= 16) return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<16, kNorm>, x, gamma, eps, K, qx, sx);
+    }
     return cudaLaunchKernelEx(&cfg, a8_quantize_kernel<0, kNorm>, x, gamma, eps, K, qx, sx);
 }
 
@@ -227,7 +229,7 @@ __global__ void glu_kernel(const float* __restrict__ gu, int kind, int I, long l
     const long long m = k / I;
     const long long j = k - m * I;
     const float* row = gu + m * 2 * I;
-    out[k] = glu_act(kind, __ldcg(row + j), __ldcg(row + I + j));
+    out[k] = glu_act_call(kind, __ldcg(row + j), __ldcg(row + I + j));
 }
 
 __global__ void add_kernel(const float* __restrict__ a, const float* __restrict__ b, long long n,

@@ -21,7 +21,9 @@ struct A8Scale {
     float r;   // fl(1 / s), or 0 when the exact path must be used throughout
 };
 
-__device__ __forceinline__ A8Scale a8_scale(float amax)
+// Out of line: once per token, and its IEEE division need not sit in every
+// quantizer's instruction stream.
+static __device__ __noinline__ A8Scale a8_scale(float amax)
 {
     A8Scale k;
     k.s = __fdiv_rn(amax, 127.0f);
@@ -123,6 +125,12 @@ __device__ __forceinline__ uint32_t a8_pack4_fast2(float4 v, uint64_t rr, uint32
                        0x5410);
 }
 
+// The exact path for one word, out of line: it runs for about one word in
+// 10^4 (possible ties, tiny scales), and inlined into every unrolled group of
+// the quantizers its IEEE divisions would crowd the hot loop out of the
+// instruction cache.
+static __device__ __noinline__ uint32_t a8_pack4_exact(float4 v, A8Scale k);
+
 // True when the fast path may not be used at all for this scale.
 __device__ __forceinline__ bool a8_needs_exact(const A8Scale& k) { return k.s != 0.0f && k.r == 0.0f; }
 
@@ -132,5 +140,7 @@ __device__ __forceinline__ uint32_t a8_pack4(float4 v, const A8Scale& k)
            ((static_cast<uint32_t>(a8_code(v.z, k)) & 0xffu) << 16) |
            ((static_cast<uint32_t>(a8_code(v.w, k)) & 0xffu) << 24);
 }
+
+static __device__ __noinline__ uint32_t a8_pack4_exact(float4 v, A8Scale k) { return a8_pack4(v, k); }
 
 }  // namespace w4k

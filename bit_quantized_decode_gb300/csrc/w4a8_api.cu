@@ -163,6 +163,8 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     int grid = dev->sms;
     if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
     if (a.T < grid) grid = a.T;
+    cp.lin[0].tq = a.T / grid;
+    cp.lin[0].tr = a.T % grid;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
     cudaError_t e;
     if (fmt_float_x(fmt)) e = launch_gemv_a32(fmt, cp, MT, grid, p.smem, pdl, s);
@@ -212,6 +214,10 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
     const int smem = smem_layout(FMT_W4, MT, X_FUSED, kmax, s_max, cp.round_tiles, 2, kRowCache / 2).total;
     int grid = dev->sms;
     if (g_tune[W4_TUNE_GRID_BLOCKS] > 0 && g_tune[W4_TUNE_GRID_BLOCKS] < grid) grid = g_tune[W4_TUNE_GRID_BLOCKS];
+    for (int i = 0; i < n; ++i) {
+        cp.lin[i].tq = cp.lin[i].T / grid;
+        cp.lin[i].tr = cp.lin[i].T % grid;
+    }
     return cuda_status(launch_chain_w4(cp, MT, grid, static_cast<size_t>(smem), s));
 }
 

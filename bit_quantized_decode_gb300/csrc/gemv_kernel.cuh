@@ -541,6 +541,9 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
     const int ahead = S < kAhead ? S : kAhead;
     int consumed = 0;
 
+    // one copy of the issue code (not unrolled): it runs once per launch,
+    // before the dependency wait, and its footprint costs instruction fetch
+#pragma unroll 1
     for (int s = 0; s < ahead; ++s)
         if (!issue_next()) break;
 

@@ -164,3 +164,55 @@ def test_product_never_imports_the_oracle():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 assert not pat.search(open(os.path.join(dirpath, f)).read()), f
+
+
+def test_fusion_and_weight_only_argument_checks(lib):
+    """The fused-operator and weight-only entry points reject bad arguments on
+    the host, before any device query or launch."""
+    from bit_quantized_decode_gb300 import _lib
+    F = _lib.Fusion
+    by = ctypes.byref
+    args = (FAKE, FAKE, None, FAKE, 1, 8, 64, FAKE, FAKE, FAKE)
+    bad_glu = F(None, 0.0, 3, None)
+    assert lib.w4a8_linear_fused(*args, by(bad_glu), 0, None) == 1               # unknown GLU kind
+    glu = F(None, 0.0, 1, None)
+    assert lib.i8g32_linear_fused(FAKE, None, FAKE, 1, 8, 64, FAKE, FAKE, FAKE, by(glu), 0, None) == 2
+    assert lib.q6g32_linear_fused(FAKE, None, FAKE, 1, 8, 64, FAKE, FAKE, FAKE, by(glu), 0, None) == 2
+    no_eps = F(0x1000, 0.0, 0, None)
+    assert lib.w4a8_linear_fused(*args, by(no_eps), 0, None) == 1                # RMSNorm needs eps > 0
+    inf_eps = F(0x1000, float("inf"), 0, None)
+    assert lib.w4a8_linear_fused(*args, by(inf_eps), 0, None) == 1
+    odd_norm = F(0x1004, 1e-6, 0, None)
+    assert lib.w4a8_linear_fused(*args, by(odd_norm), 0, None) == 3             # norm weight 16-B aligned
+    odd_res = F(None, 0.0, 0, 0x1002)
+    assert lib.w4a8_linear_fused(*args, by(odd_res), 0, None) == 3
+    assert lib.w4a8_linear_fused(*args, by(glu), 2, None) == 1                   # unknown flag
+    assert lib.w4a8_linear_fused(None, None, None, None, 0, 8, 64, None, None, None, None, 0, None) == 0
+    # normalize + quantize, and the separate operators
+    assert lib.rms_a8_quantize(FAKE, FAKE, 0.0, 1, 64, FAKE, FAKE, 0, None) == 1
+    assert lib.rms_a8_quantize(FAKE, ODD, 1e-6, 1, 64, FAKE, FAKE, 0, None) == 3
+    assert lib.rms_a8_quantize(FAKE, FAKE, 1e-6, 0, 64, None, None, 0, None) == 0
+    assert lib.w4_rmsnorm(FAKE, FAKE, 1e-6, 1, 48, FAKE, 0, None) == 2
+    assert lib.w4_rmsnorm(FAKE, FAKE, 1e-6, 1, 64, None, 0, None) == 1
+    assert lib.w4_glu(FAKE, 0, 1, 8, FAKE, 0, None) == 1
+    assert lib.w4_glu(FAKE, 1, 17, 8, FAKE, 0, None) == 2
+    assert lib.w4_glu(None, 2, 1, 0, None, 0, None) == 0
+    assert lib.w4_add(FAKE, FAKE, -1, FAKE, 0, None) == 1
+    assert lib.w4_add(None, None, 0, None, 0, None) == 0
+    # paired gate/up layout sizes and checks
+    assert lib.w4_glu_repacked_bytes(3, 64) == 8 * 64 // 2
+    assert lib.w4_glu_repacked_bytes(8, 64) == 16 * 64 // 2
+    assert lib.q4_0_glu_repacked_bytes(5, 64) == 16 * 64 * 18 // 32
+    assert lib.w4_glu_repacked_bytes(8, 48) == 0
+    assert lib.w4_repack_glu(FAKE, None, 8, 64, FAKE, 1 << 20, None) == 1
+    assert lib.w4_repack_glu(FAKE, FAKE, 8, 64, FAKE, 16, None) == 2
+    assert lib.w4_repack_glu(FAKE, FAKE, 8, 64, ODD, 1 << 20, None) == 3
+    assert lib.w4_repack_glu(FAKE, FAKE, 0, 64, None, 0, None) == 0
+    # weight-only paths on float activations
+    assert lib.w4a32_gemv(FAKE, FAKE, None, FAKE, 5, 8, 64, FAKE, 0, None) == 2  # at most four tokens
+    assert lib.w8a32_gemv(FAKE, None, None, FAKE, 1, 8, 64, FAKE, 0, None) == 1
+    assert lib.w8a32_gemv(FAKE, FAKE, None, ODD, 1, 8, 64, FAKE, 0, None) == 3
+    assert lib.w4a32_gemv(None, None, None, None, 1, 0, 64, None, 0, None) == 0
+    assert lib.w8_repacked_bytes(13, 64) == 16 * 64
+    assert lib.w8_quantize_rows(FAKE, 4, 6, FAKE, FAKE, None) == 2
+    assert lib.w8_quantize_rows(ODD, 4, 64, FAKE, FAKE, None) == 3

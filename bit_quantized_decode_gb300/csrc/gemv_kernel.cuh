@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
     constexpr int kSlotH = fmt_slot_h_bytes(FMT);
     constexpr bool kCodeSums = FMT == FMT_W4;        // activation code sums for the nibble bias
     constexpr int kPassLines = 16;
+    constexpr int kPassUnroll = MT == 1 ? kSL / kPassLines : 1;
     constexpr int kRowBufs = NCH == 1 ? 1 : 2;       // per-row parameter buffers (by linear parity)
     constexpr int kRowCap = NCH == 1 ? kRowCache : kRowCache / 2;   // rows per buffer
     // single linears with up to four tokens take the RMSNorm prologue when
@@ -770,7 +771,9 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
                 if (!dead) {
                     const uint8_t* sw = my_ring + static_cast<size_t>(slot) * kSlot;
                     const __half* sd = reinterpret_cast<const __half*>(sw + kSlotW + kSlotH);
-#pragma unroll
+                    // several tokens: the passes of a slice share one loop body (unrolled,
+                    // their bodies outgrow the instruction cache); one token: unrolled
+#pragma unroll kPassUnroll
                     for (int pass = 0; pass < kSL / kPassLines; ++pass) {
                         const int line = pass * kPassLines + pl;
                         if (line < n) {

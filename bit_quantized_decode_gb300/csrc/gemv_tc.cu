@@ -9,20 +9,23 @@
 //
 // How (GB300 design): the product is a GEMM of N x K by K x 16, so it runs on
 // tcgen05.mma (kind::f16, M = 128 rows, N = 16 tokens, K = 16 per
-// instruction).  int4 weights and int8 codes are exact in fp16, each product
-// |q_w q_x| <= 1016 is exact, and every partial sum is an integer below 2^24
-// in magnitude (a split covers at most 16384 K), so the fp32 accumulator in
-// tensor memory holds the exact integer sum.
+// instruction).  A weight enters as its biased nibble n = q + 8 placed in the
+// mantissa of an fp16 subnormal, n 2^-24 exactly (one mask per pair, no
+// conversion arithmetic); the int8 codes are exact fp16 integers.  Each
+// product n x 2^-24 is exact, and every partial sum is a multiple of 2^-24
+// below 1 in magnitude (|n x| <= 1905 and a split covers at most 8192 K), so
+// the fp32 accumulator in tensor memory holds sum n x 2^-24 exactly; the
+// epilogue scales by 2^24 and removes the bias, sum q x = sum n x - 8 sum x,
+// with each token's code sum over the split's K range.
 //   * One block of six warps per (128-row group, K split).  K splits of a row
 //     group form one thread-block cluster and add their partial sums in the
 //     leader's shared memory (distributed shared memory), which writes y.
 //   * Packed weights stream through a ring of stages (512 K x 128 rows,
 //     32 KB: one 2 KB bulk copy per 8-row tile) issued before the dependency
 //     wait; the operand pipeline steps through 128-K blocks of a stage.
-//   * Warps 0-3 (thread t: row t) turn their row's nibbles into fp16 pairs
-//     with one LOP3 and one HSUB2 per pair (0x6400 | n is 1024 + n; minus
-//     1032 gives q) and store them into tensor memory as the MMA's A operand
-//     (three buffers).  The pairs come out in the K order (0,2), (1,3),
+//   * Warps 0-3 (thread t: row t) mask their row's nibbles into fp16 subnormal
+//     pairs (one shift and one LOP3 per pair) and store them into tensor
+//     memory as the MMA's A operand (three buffers).  The pairs come out in the K order (0,2), (1,3),
 //     (4,6), (5,7) within each 8 weights; the same warps write the fp16
 //     activation tile (B, shared memory, K-major, no swizzle) in that order,
 //     so the sum is unchanged.
@@ -59,23 +62,19 @@ constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcTok >> 3) <<
 constexpr uint32_t kTcBsbo = 128;
 constexpr uint32_t kTcBlbo = 256;
 
-// 32 biased nibbles (n = q + 8) of one row -> 16 fp16 pairs q, in the K order
-// (8w+0, 8w+2), (8w+1, 8w+3), (8w+4, 8w+6), (8w+5, 8w+7) for word w.
+// 32 biased nibbles (n = q + 8) of one row -> 16 fp16 pairs n 2^-24 (fp16
+// subnormals: the nibble is the mantissa), in the K order (8w+0, 8w+2),
+// (8w+1, 8w+3), (8w+4, 8w+6), (8w+5, 8w+7) for word w.
 __device__ __forceinline__ void tc_dequant_unit(const uint4 u, uint32_t (&h)[16])
 {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6408u), __ushort_as_half(0x6408u));   // 1032
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t v = w[i];
-        const uint32_t p[4] = {(v & 0x000F000Fu) | 0x64006400u, ((v >> 8) & 0x000F000Fu) | 0x64006400u,
-                               ((v >> 4) & 0x000F000Fu) | 0x64006400u, ((v >> 12) & 0x000F000Fu) | 0x64006400u};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            __half2 x = *reinterpret_cast<const __half2*>(&p[e]);
-            x = __hsub2(x, bias);
-            h[4 * i + e] = *reinterpret_cast<const uint32_t*>(&x);
-        }
+        h[4 * i + 0] = v & 0x000F000Fu;
+        h[4 * i + 1] = (v >> 8) & 0x000F000Fu;
+        h[4 * i + 2] = (v >> 4) & 0x000F000Fu;
+        h[4 * i + 3] = (v >> 12) & 0x000F000Fu;
     }
 }
 
@@ -128,6 +127,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     };
     static_assert(kTcBufs == 3, "one named barrier per operand buffer");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem);   // [0] base address, [1] stop flag
+    int* xsum_s = reinterpret_cast<int*>(smem + L.xsum);                 // [kTcTok] code sums of the split
     volatile uint32_t* dead_s = tmem_slot + 1;
 
     constexpr int kSubs = kTcStageChunks / kTcChunks;      // K blocks per ring stage
@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
         // and writes them to B as fp16.
         const int cn = tid >> 3;
         const int cpart = tid & 7;
+        int xsum = 0;       // this thread's code sum (token cn) over the split's K range
         auto fetch_codes = [&](int b) {
             uint8_t* dst = codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + tid * 16;
             const int kofs = (cb + b * kTcChunks) * 32 + cpart * 16;
@@ -311,12 +312,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             uint8_t* bt = bbuf + j * kTcBBytes + (cn >> 3) * kTcBsbo + (cn & 7) * 16;
             *reinterpret_cast<uint4*>(bt + (2 * cpart) * kTcBlbo) = tc_codes8(c.x, c.y);
             *reinterpret_cast<uint4*>(bt + (2 * cpart + 1) * kTcBlbo) = tc_codes8(c.z, c.w);
+            xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
+            xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
+            xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
+            xsum = __dp4a(static_cast<int>(c.w), 0x01010101, xsum);
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             ready_arrive(j);
         }
         cp_async_wait_group<0>();
+        // token cn's code sum: its eight threads are lanes 8k..8k+7 of one warp
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) xsum += __shfl_xor_sync(0xffffffffu, xsum, off);
+        if (cpart == 0) xsum_s[cn] = xsum;
     }
     __syncthreads();
 
@@ -327,15 +336,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
     if (!control && !dead && nb > 0) {
         // the control warp saw the last commit complete before the barrier above;
-        // each accumulator holds an exact integer, so their sum is exact in int
+        // each accumulator holds sum n x 2^-24 exactly: times 2^24 it is an exact
+        // integer, and the sum of the four, less 8 sum x, is the exact sum q x
         tc_fence_after();
         const int used = min(kTcAccs, 2 * min(kTcChunks, ce - cb));   // accumulators written at all
         for (int q = 0; q < used; ++q) {
             uint32_t d[kTcTok];
             tmem_ld16(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcTok, d);
 #pragma unroll
-            for (int n = 0; n < kTcTok; ++n) acc[n] += __float2int_rn(__uint_as_float(d[n]));
+            for (int n = 0; n < kTcTok; ++n) acc[n] += __float2int_rn(__fmul_rn(__uint_as_float(d[n]), 16777216.0f));
         }
+#pragma unroll
+        for (int n = 0; n < kTcTok; ++n) acc[n] -= 8 * xsum_s[n];
     }
     tc_fence_before();
     __syncthreads();

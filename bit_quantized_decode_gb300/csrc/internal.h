@@ -160,7 +160,7 @@ constexpr int kTcBBytes = kTcTok * kTcKb * 2;    // fp16 activation tile per K b
 constexpr int kTcCodeRing = 4;                   // K blocks of int8 codes in flight
 constexpr int kTcBufs = 3;                       // A (tensor memory) / B (shared memory) operand buffers
 constexpr int kTcMaxSplit = 8;                   // K splits (cluster size) at most
-constexpr int kTcMaxSplitK = 16384;              // K per split at most: partial sums stay below 2^24
+constexpr int kTcMaxSplitK = 8192;               // K per split at most: |sum n x| stays below 2^24 (n <= 15)
 
 struct TcArgs {
     const uint8_t* w;       // repacked per-row INT4 (8-row tiles)
@@ -179,7 +179,7 @@ struct TcArgs {
 };
 
 struct TcSmem {
-    int ring, bbuf, codes, red, bars, tmem, total;
+    int ring, bbuf, codes, red, bars, tmem, xsum, total;
 };
 
 __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
@@ -192,6 +192,7 @@ __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
     L.red = L.ring;   // K-split partial sums reuse the ring once every block is past its K loop
     L.bars = o;  o += (2 * stages + 2 * kTcBufs) * 8;
     L.tmem = o;  o += 16;
+    L.xsum = o;  o += kTcTok * 4;
     L.total = o;
     return L;
 }

@@ -261,11 +261,12 @@ w4_status check_fusion(int fmt, const w4_fusion* f, Fuse& z)
 // Weight rows behind n outputs: a gated linear pairs 4 gate and 4 up rows per tile.
 inline int weight_rows(int n, int glu) { return glu != GLU_NONE ? 8 * ((n + 3) / 4) : n; }
 
-// Per-row INT4 with this many tokens runs on the tensor cores (gemv_tc.cu).
-bool use_tc(int fmt, int M)
+// Per-row INT4 with this many tokens runs on the tensor cores (gemv_tc.cu),
+// up to kTcMaxSplit K splits of kTcMaxSplitK.
+bool use_tc(int fmt, int M, int K)
 {
     const int lo = g_tune[W4_TUNE_TC_MIN_M] > 0 ? g_tune[W4_TUNE_TC_MIN_M] : 8;
-    return fmt == FMT_W4 && M >= lo && M <= kTcTok;
+    return fmt == FMT_W4 && M >= lo && M <= kTcTok && K <= kTcMaxSplit * kTcMaxSplitK;
 }
 
 // Tensor-core GEMV: one block per (128-row group, K split); enough splits to
@@ -329,7 +330,7 @@ w4_status gemv_common(int fmt, const void* w, const float* s_w, const float* bia
         return W4_ERR_MISALIGNED;
     if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
     const int Nw = weight_rows(N, fz.glu);
-    if (use_tc(fmt, M)) return run_gemv_tc(w, s_w, bias, qx, sx, M, Nw, K, y, pdl, s, N, fz.glu, fz.residual);
+    if (use_tc(fmt, M, K)) return run_gemv_tc(w, s_w, bias, qx, sx, M, Nw, K, y, pdl, s, N, fz.glu, fz.residual);
     GemvArgs a = {};
     a.w = static_cast<const uint8_t*>(w);
     const size_t units = tiles(Nw) * kRows * (K / 32);
@@ -370,7 +371,7 @@ w4_status linear_common(int fmt, const void* w, const float* s_w, const float* b
     if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
     const bool norm = fz.gamma != nullptr;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
-    if (N == 0 || use_tc(fmt, M) || !fused_fits(fmt, M, K, norm)) {
+    if (N == 0 || use_tc(fmt, M, K) || !fused_fits(fmt, M, K, norm)) {
         // quantize (normalize first if asked) into the caller's qx/sx once, then
         // the GEMV on int8 codes (tensor cores for many tokens), chained by
         // programmatic dependent launch

@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
         // Every K block is synchronised (named barrier) and committed even after a
         // failure, so that warps 0-3, which arrive once per block and wait for each
         // buffer's commit in order, never block on a missing step.
+        const uint32_t dcol = tbase + kTcColD;
         for (int b = 0; b < nb; ++b) {
             const int j = b % kTcBufs;
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
@@ -209,12 +210,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                     tc_fence_after();
                     const uint64_t bdesc = smem_desc_noswizzle(smem_u32(bbuf + j * kTcBBytes), kTcBlbo, kTcBsbo);
                     const uint32_t acol = tbase + kTcColA + j * 64;
+                    static_assert(kTcAccs == 4 && 2 * kTcChunks == 8, "eight MMAs per block into four accumulators");
+                    if (nch == kTcChunks) {
+                        tc_mma_f16_ts_x8(dcol, dcol + kTcTok, dcol + 2 * kTcTok, dcol + 3 * kTcTok, acol, bdesc, kTcIdesc,
+                                         b > 0 ? 1u : 0u);
+                    } else {
 #pragma unroll
-                    for (int kk = 0; kk < 2 * kTcChunks; ++kk)
-                        if (kk < 2 * nch)
-                            tc_mma_f16_ts(tbase + kTcColD + (kk % kTcAccs) * kTcTok, acol + kk * 8,
-                                          bdesc + static_cast<uint64_t>(kk * 32), kTcIdesc,
-                                          (b > 0 || kk >= kTcAccs) ? 1u : 0u);
+                        for (int kk = 0; kk < 2 * kTcChunks; ++kk)
+                            if (kk < 2 * nch)
+                                tc_mma_f16_ts(dcol + (kk % kTcAccs) * kTcTok, acol + kk * 8,
+                                              bdesc + static_cast<uint64_t>(kk * 32), kTcIdesc,
+                                              (b > 0 || kk >= kTcAccs) ? 1u : 0u);
+                    }
                 }
                 tc_commit(free_b + 8 * j);
             }

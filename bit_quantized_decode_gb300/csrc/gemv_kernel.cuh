@@ -38,6 +38,18 @@
 //     butterfly at the end of each tile.
 //   * Tiles split between warps are merged in shared memory in warp order
 //     (deterministic); the epilogue writes y coalesced.
+//   * Operators around the linear (fusion.cuh) are runtime branches of the
+//     same instantiation: RMSNorm in the quantize prologue (one to four
+//     tokens), the gated activation over gate/up rows paired per tile, and the
+//     residual add in the epilogue.  One instantiation keeps consecutive
+//     launches on the same instruction-cache lines.
+//   * Code that runs once per launch (prologue, epilogue) is on the critical
+//     path and meets cold instruction-cache lines, so rare paths (the
+//     quantizer's exact tie path, the token scale, the gated activation) are
+//     out-of-line functions, and tile ranges come from the host without a
+//     division.
+//   * FMT_W4F / FMT_W8F (xmode X_F32) are the weight-only baselines on float
+//     activations: the same streaming, with every weight unpacked to fp32.
 #pragma once
 #include <cuda_fp16.h>
 

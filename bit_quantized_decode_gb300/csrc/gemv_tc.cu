@@ -8,36 +8,37 @@
 // scales come from the activation quantizer launched before this kernel.
 //
 // How (GB300 design): the product is a GEMM of N x K by K x 16, so it runs on
-// tcgen05.mma (kind::f16, M = 128 rows, N = 16 tokens, K = 16 per
-// instruction).  A weight enters as its biased nibble n = q + 8 placed in the
-// mantissa of an fp16 subnormal, n 2^-24 exactly (one mask per pair, no
-// conversion arithmetic); the int8 codes are exact fp16 integers.  Each
-// product n x 2^-24 is exact, and every partial sum is a multiple of 2^-24
-// below 1 in magnitude (|n x| <= 1905 and a split covers at most 8192 K), so
-// the fp32 accumulator in tensor memory holds sum n x 2^-24 exactly; the
-// epilogue scales by 2^24 and removes the bias, sum q x = sum n x - 8 sum x,
-// with each token's code sum over the split's K range.
+// tcgen05.mma (kind::f8f6f4, e4m3 operands, M = 128 rows, K = 32 per
+// instruction).  e4m3 bytes 0x00..0x0F are exactly n 2^-9 (subnormals below
+// 8, the first binade above), so a weight enters as its biased nibble
+// n = q + 8 masked into a byte: two masks give eight weights, in order.  An
+// int8 code x = 16 h + l is split into h = x >> 4 in [-8, 7] (e4m3
+// sign-magnitude) and l = x & 15, both exact, laid side by side in N = 32
+// (columns 0-15 the tokens' h, 16-31 their l): one MMA covers 32 K for all
+// sixteen tokens.  Products n h 2^-18 and n l 2^-18 are exact and every
+// partial sum is a multiple of 2^-18 below 64 in magnitude (|n l| <= 225 and a
+// split covers at most 16384 K), so the fp32 accumulators hold the sums
+// exactly; the epilogue forms sum n x = 16 S_h + S_l and removes the bias,
+// sum q x = sum n x - 8 sum x, with each token's code sum over the split.
 //   * One block of six warps per (128-row group, K split).  K splits of a row
 //     group form one thread-block cluster and add their partial sums in the
 //     leader's shared memory (distributed shared memory), which writes y.
 //   * Packed weights stream through a ring of stages (512 K x 128 rows,
 //     32 KB: one 2 KB bulk copy per 8-row tile) issued before the dependency
 //     wait; the operand pipeline steps through 128-K blocks of a stage.
-//   * Warps 0-3 (thread t: row t) mask their row's nibbles into fp16 subnormal
-//     pairs (one shift and one LOP3 per pair) and store them into tensor
-//     memory as the MMA's A operand (three buffers).  The pairs come out in the K order (0,2), (1,3),
-//     (4,6), (5,7) within each 8 weights; the same warps write the fp16
-//     activation tile (B, shared memory, K-major, no swizzle) in that order,
-//     so the sum is unchanged.
-//   * Lane 0 of warp 4 issues a block's MMAs (K slice kk into accumulator
-//     kk % 4, so consecutive MMAs are independent; the four exact partial sums
-//     are added at the end) and commits them; warp 5 issues the weight copies.
+//   * Warps 0-3 (thread t: row t) mask their row's nibbles into e4m3 bytes
+//     (two LOP3 and a shift per 8 weights) and store them into tensor memory
+//     as the MMA's A operand (three buffers); the same warps write the split
+//     activation tile (B, shared memory, K-major, no swizzle).
+//   * Lane 0 of warp 4 issues a block's four MMAs (K slice kk into accumulator
+//     kk, so consecutive MMAs are independent; the four exact partial sums are
+//     added at the end) and commits them; warp 5 issues the weight copies.
 //     "Operands written" is a named barrier per buffer (warps 0-4), "operands
 //     read" the MMA commit's mbarrier, and the ring has full / empty
 //     mbarriers: no block-wide barrier sits in the K loop.
-//   * What bounds it is the MMA issue inside this pipeline (one block's eight
-//     128 x 16 x 16 MMAs take 900-1900 cycles to issue, against about 45 per
-//     MMA in an isolated loop), not HBM and not the tensor cores' arithmetic.
+//   * What bounds it is the MMA issue inside this pipeline (about 100 cycles
+//     per MMA after the first, against about 45 in an isolated loop), not HBM
+//     and not the tensor cores' arithmetic: hence few, wide MMAs.
 #include <cuda_fp16.h>
 
 #include "fusion.cuh"
@@ -48,54 +49,42 @@ namespace w4k {
 namespace {
 
 constexpr uint64_t kTcWaitNs = 250ull * 1000ull * 1000ull;
-constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 3 (64 each), D x 4 (16 each)
+constexpr int kTcN = 2 * kTcTok;      // MMA N: each token's high and low code halves
+constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 3 (32 each), D x 4 (32 each)
 constexpr uint32_t kTcColA = 0;
-constexpr uint32_t kTcColD = 192;
+constexpr uint32_t kTcColD = 128;
 constexpr int kTcAccs = 4;            // independent accumulators: consecutive MMAs do not wait on each other
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+// Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3
 // (bits 7-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcTok >> 3) << 17) |
+constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcN >> 3) << 17) |
                               (static_cast<uint32_t>(kTcRows >> 4) << 24);
-// B tile: core matrices of 8 tokens x 8 K (16 B rows), token groups 128 B
-// apart, K groups 256 B apart.
+// B tile: core matrices of 8 columns x 16 K (16 B rows), column groups 128 B
+// apart, K groups 512 B apart (four column groups); one MMA's 32 K is 1024 B.
 constexpr uint32_t kTcBsbo = 128;
-constexpr uint32_t kTcBlbo = 256;
+constexpr uint32_t kTcBlbo = 512;
 
-// 32 biased nibbles (n = q + 8) of one row -> 16 fp16 pairs n 2^-24 (fp16
-// subnormals: the nibble is the mantissa), in the K order (8w+0, 8w+2),
-// (8w+1, 8w+3), (8w+4, 8w+6), (8w+5, 8w+7) for word w.
-__device__ __forceinline__ void tc_dequant_unit(const uint4 u, uint32_t (&h)[16])
+// 32 biased nibbles (n = q + 8) of one row -> 32 e4m3 bytes n 2^-9 in K
+// order: byte b of word w holds weight 8w+b (low nibble) and 8w+4+b (high).
+__device__ __forceinline__ void tc_unit_e4m3(const uint4 u, uint32_t* h)
 {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t v = w[i];
-        h[4 * i + 0] = v & 0x000F000Fu;
-        h[4 * i + 1] = (v >> 8) & 0x000F000Fu;
-        h[4 * i + 2] = (v >> 4) & 0x000F000Fu;
-        h[4 * i + 3] = (v >> 12) & 0x000F000Fu;
+        h[2 * i] = w[i] & 0x0F0F0F0Fu;
+        h[2 * i + 1] = (w[i] >> 4) & 0x0F0F0F0Fu;
     }
 }
 
-// Eight int8 codes at K offsets 0..7 (words lo, hi) -> eight fp16 in the A
-// operand's K order: 0x6400 | (c + 128) is 1024 + c + 128 in fp16, minus 1152
-// gives c; byte permutes pick the pairs (0,2), (1,3), (4,6), (5,7).
-__device__ __forceinline__ uint4 tc_codes8(uint32_t lo, uint32_t hi)
+// Four int8 codes x -> the e4m3 bytes of h = x >> 4 (sign-magnitude, |h| <= 8)
+// and of l = x & 15, each exactly its value times 2^-9.
+__device__ __forceinline__ void tc_split4(uint32_t c, uint32_t& hi, uint32_t& lo)
 {
-    const __half2 off = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));   // 1152
-    const uint32_t ul = lo ^ 0x80808080u;
-    const uint32_t uh = hi ^ 0x80808080u;
-    const uint32_t p[4] = {__byte_perm(ul, 0x64646464u, 0x4240), __byte_perm(ul, 0x64646464u, 0x4341),
-                           __byte_perm(uh, 0x64646464u, 0x4240), __byte_perm(uh, 0x64646464u, 0x4341)};
-    uint32_t r[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __half2 x = *reinterpret_cast<const __half2*>(&p[e]);
-        x = __hsub2(x, off);
-        r[e] = *reinterpret_cast<const uint32_t*>(&x);
-    }
-    return make_uint4(r[0], r[1], r[2], r[3]);
+    lo = c & 0x0F0F0F0Fu;
+    const uint32_t u = (c >> 4) & 0x0F0F0F0Fu;              // h + 16 for negative h
+    const uint32_t bm = ((u & 0x08080808u) >> 3) * 0xFFu;    // 0xFF in the bytes of negative h
+    const uint32_t m = (u ^ (bm & 0x0F0F0F0Fu)) + (bm & 0x01010101u);   // |h| = 16 - u there
+    hi = m | (bm & 0x80808080u);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_constant__ TcArgs A)
@@ -204,23 +193,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             ready_sync(j);                           // A[j] and B[j] written by warps 0-3
             if (lane == 0) {
                 if (!*dead_s) {
-                    // K slice kk (16 K: 8 tensor-memory columns of A, 512 B of B, which is
-                    // 32 in the descriptor's address field and cannot carry) accumulates
-                    // into D[kk % 4]; the first use of each overwrites.
+                    // K slice kk (32 K: 8 tensor-memory columns of A, 1024 B of B, which is
+                    // 64 in the descriptor's address field and cannot carry) accumulates
+                    // into D[kk]; the first block overwrites.
                     tc_fence_after();
                     const uint64_t bdesc = smem_desc_noswizzle(smem_u32(bbuf + j * kTcBBytes), kTcBlbo, kTcBsbo);
-                    const uint32_t acol = tbase + kTcColA + j * 64;
-                    static_assert(kTcAccs == 4 && 2 * kTcChunks == 8, "eight MMAs per block into four accumulators");
+                    const uint32_t acol = tbase + kTcColA + j * 32;
+                    static_assert(kTcAccs == 4 && kTcChunks == 4, "four MMAs per block, one per accumulator");
                     if (nch == kTcChunks) {
-                        tc_mma_f16_ts_x8(dcol, dcol + kTcTok, dcol + 2 * kTcTok, dcol + 3 * kTcTok, acol, bdesc, kTcIdesc,
-                                         b > 0 ? 1u : 0u);
+                        tc_mma_f8_ts_x4(dcol, dcol + kTcN, dcol + 2 * kTcN, dcol + 3 * kTcN, acol, bdesc, kTcIdesc,
+                                        b > 0 ? 1u : 0u);
                     } else {
 #pragma unroll
-                        for (int kk = 0; kk < 2 * kTcChunks; ++kk)
-                            if (kk < 2 * nch)
-                                tc_mma_f16_ts(dcol + (kk % kTcAccs) * kTcTok, acol + kk * 8,
-                                              bdesc + static_cast<uint64_t>(kk * 32), kTcIdesc,
-                                              (b > 0 || kk >= kTcAccs) ? 1u : 0u);
+                        for (int kk = 0; kk < kTcChunks; ++kk)
+                            if (kk < nch)
+                                tc_mma_f8_ts(dcol + kk * kTcN, acol + kk * 8, bdesc + static_cast<uint64_t>(kk * 64),
+                                             kTcIdesc, b > 0 ? 1u : 0u);
                     }
                 }
                 tc_commit(free_b + 8 * j);
@@ -305,20 +293,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // the stage's bytes are in registers
             }
+            {
+                // the block's 128 K as e4m3: 32 columns, stored as two 16-column halves
+                uint32_t h[2][16];
 #pragma unroll
-            for (int cl = 0; cl < kTcChunks; ++cl) {
-                if (cl < nch) {
-                    uint32_t h[16];
-                    tc_dequant_unit(u[cl], h);
-                    tmem_st16(tbase + tlane + kTcColA + j * 64 + cl * 16, h);
+                for (int cl = 0; cl < kTcChunks; ++cl) {
+                    if (cl < nch) {
+                        tc_unit_e4m3(u[cl], &h[cl >> 1][(cl & 1) * 8]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) h[cl >> 1][(cl & 1) * 8 + e] = 0u;
+                    }
                 }
+                tmem_st16(tbase + tlane + kTcColA + j * 32, h[0]);
+                tmem_st16(tbase + tlane + kTcColA + j * 32 + 16, h[1]);
             }
-            // B: token cn, K positions 16 cpart .. +15 of the block, fp16 in A's order
+            // B: token cn, K positions 16 cpart .. +15 of the block (K group cpart):
+            // the high halves in column cn, the low halves in column 16 + cn
             cp_async_wait_group<kTcCodeRing - 1>();
             const uint4 c = *reinterpret_cast<const uint4*>(codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + tid * 16);
-            uint8_t* bt = bbuf + j * kTcBBytes + (cn >> 3) * kTcBsbo + (cn & 7) * 16;
-            *reinterpret_cast<uint4*>(bt + (2 * cpart) * kTcBlbo) = tc_codes8(c.x, c.y);
-            *reinterpret_cast<uint4*>(bt + (2 * cpart + 1) * kTcBlbo) = tc_codes8(c.z, c.w);
+            uint4 hv, lv;
+            tc_split4(c.x, hv.x, lv.x);
+            tc_split4(c.y, hv.y, lv.y);
+            tc_split4(c.z, hv.z, lv.z);
+            tc_split4(c.w, hv.w, lv.w);
+            uint8_t* bt = bbuf + j * kTcBBytes + cpart * kTcBlbo + (cn & 7) * 16;
+            *reinterpret_cast<uint4*>(bt + (cn >> 3) * kTcBsbo) = hv;
+            *reinterpret_cast<uint4*>(bt + (2 + (cn >> 3)) * kTcBsbo) = lv;
             xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
             xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
             xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
@@ -343,15 +344,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
     if (!control && !dead && nb > 0) {
         // the control warp saw the last commit complete before the barrier above;
-        // each accumulator holds sum n x 2^-24 exactly: times 2^24 it is an exact
-        // integer, and the sum of the four, less 8 sum x, is the exact sum q x
+        // each accumulator holds sum n h 2^-18 (columns 0-15) and sum n l 2^-18
+        // (16-31) exactly: times 2^18 they are exact integers, and over the
+        // accumulators 16 S_h + S_l, less 8 sum x, is the exact sum q x
         tc_fence_after();
-        const int used = min(kTcAccs, 2 * min(kTcChunks, ce - cb));   // accumulators written at all
+        const int used = min(kTcAccs, min(kTcChunks, ce - cb));   // accumulators written at all
         for (int q = 0; q < used; ++q) {
-            uint32_t d[kTcTok];
-            tmem_ld16(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcTok, d);
+            uint32_t dh[kTcTok], dl[kTcTok];
+            tmem_ld16(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcN, dh);
+            tmem_ld16(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcN + kTcTok, dl);
 #pragma unroll
-            for (int n = 0; n < kTcTok; ++n) acc[n] += __float2int_rn(__fmul_rn(__uint_as_float(d[n]), 16777216.0f));
+            for (int n = 0; n < kTcTok; ++n)
+                acc[n] += 16 * __float2int_rn(__fmul_rn(__uint_as_float(dh[n]), 262144.0f)) +
+                          __float2int_rn(__fmul_rn(__uint_as_float(dl[n]), 262144.0f));
         }
 #pragma unroll
         for (int n = 0; n < kTcTok; ++n) acc[n] -= 8 * xsum_s[n];

@@ -156,11 +156,11 @@ constexpr int kTcChunks = 4;                     // 32-weight chunks per K block
 constexpr int kTcKb = 32 * kTcChunks;            // K per block: 128
 constexpr int kTcStageChunks = 16;              // chunks per weight-ring stage (4 K blocks): 2 KB copies per tile
 constexpr int kTcStageBytes = (kTcRows / kRows) * kTcStageChunks * kRows * 16;   // 32 KB of packed weights
-constexpr int kTcBBytes = kTcTok * kTcKb * 2;    // fp16 activation tile per K block
+constexpr int kTcBBytes = 2 * kTcTok * kTcKb;    // e4m3 activation tile per K block (high and low halves)
 constexpr int kTcCodeRing = 4;                   // K blocks of int8 codes in flight
 constexpr int kTcBufs = 3;                       // A (tensor memory) / B (shared memory) operand buffers
 constexpr int kTcMaxSplit = 8;                   // K splits (cluster size) at most
-constexpr int kTcMaxSplitK = 8192;               // K per split at most: |sum n x| stays below 2^24 (n <= 15)
+constexpr int kTcMaxSplitK = 16384;              // K per split at most: |sum n l| <= 225 K stays below 2^24
 
 struct TcArgs {
     const uint8_t* w;       // repacked per-row INT4 (8-row tiles)

@@ -261,6 +261,39 @@ __device__ __forceinline__ void tc_mma_f16_ts_x8(uint32_t d0, uint32_t d1, uint3
         : "memory");
 }
 
+// One MMA of kind::f8f6f4 (A in tensor memory, B from a shared-memory
+// descriptor), e4m3 operands with the types set in idesc; accumulate unless
+// `accumulate` is 0.
+__device__ __forceinline__ void tc_mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Four kind::f8f6f4 MMAs of one 128-K block in one statement: K slice kk (A
+// at a0 + 8 kk columns, B at b0 + 64 kk in the descriptor's address field,
+// i.e. 1024 bytes) into accumulator d[kk].  Each overwrites its accumulator
+// unless `accumulate`.
+__device__ __forceinline__ void tc_mma_f8_ts_x4(uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3, uint32_t a0,
+                                                uint64_t b0, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+        "setp.ne.b32 p, %7, 0;\n\t"
+        "add.u32 a1, %4, 8;\n\tadd.u32 a2, %4, 16;\n\tadd.u32 a3, %4, 24;\n\t"
+        "add.u64 b1, %5, 64;\n\tadd.u64 b2, %5, 128;\n\tadd.u64 b3, %5, 192;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %5, %6, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%1], [a1], b1, %6, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%2], [a2], b2, %6, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%3], [a3], b3, %6, p;\n\t}" ::"r"(d0),
+        "r"(d1), "r"(d2), "r"(d3), "r"(a0), "l"(b0), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // One arrival on `bar` once every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar)

@@ -87,15 +87,14 @@ __device__ __forceinline__ void tc_split4(uint32_t c, uint32_t& hi, uint32_t& lo
     hi = m | (bm & 0x80808080u);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_constant__ TcArgs A)
+__global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_constant__ TcArgs A)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const bool mma_warp = warp == 4;
-    const bool producer = warp == 5;
-    const bool control = warp >= 4;
+    const bool mma_warp = warp == kTcDqWarps;
+    const bool producer = warp == kTcDqWarps + 1;
     const int S = A.stages;
     const int ks = A.splits;
     const TcSmem L = tc_smem(S, ks);
@@ -104,10 +103,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     uint8_t* codes = smem + L.codes;
     const uint32_t bars = smem_u32(smem + L.bars);
     const uint32_t full_b = bars;                        // [S]  stage landed (1 arrival + bytes)
-    const uint32_t empty_b = bars + 8 * S;               // [S]  stage read by warps 0-3 (4 arrivals)
+    const uint32_t empty_b = bars + 8 * S;               // [S]  stage read by the dequantizing warps
     const uint32_t free_b = bars + 16 * S;               // [3]  MMAs reading an operand buffer completed
-    // operand buffer j written by warps 0-3: named barrier 1 + j (warps 0-4)
-    constexpr uint32_t kReadyCount = 5 * 32;
+    // operand buffer j written by the dequantizing warps: named barrier 1 + j
+    // (those warps and the MMA warp)
+    constexpr uint32_t kReadyCount = (kTcDqWarps + 1) * 32;
     auto ready_arrive = [](int j) {
         if (j == 0) named_arrive(1, kReadyCount); else if (j == 1) named_arrive(2, kReadyCount); else named_arrive(3, kReadyCount);
     };
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_b + 8 * s, 1);
-            mbar_init(empty_b + 8 * s, 4);
+            mbar_init(empty_b + 8 * s, kTcDqWarps);
         }
         for (int j = 0; j < kTcBufs; ++j) {
             mbar_init(free_b + 8 * j, 1);         // the MMA lane's commit
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     __syncthreads();
     pdl_launch_dependents();
 
-    // stage st of the weights into ring slot st % S (control warp: lane 0 sets
+    // stage st of the weights into ring slot st % S (copy warp: lane 0 sets
     // the byte count, lane l < 16 copies 8-row tile l: up to 16 chunks, 2 KB)
     const uint64_t pol = l2_policy_evict_first();
     auto issue = [&](int st) {
@@ -244,17 +244,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             for (int k = issued - S > 0 ? issued - S : 0; k < issued; ++k)
                 if (!mbar_wait_bounded(full_b + 8 * (k % S), static_cast<uint32_t>(k / S) & 1u, kTcWaitNs)) break;
     } else {
-        // ------------------------------------------- warps 0-3: A and B
-        const uint32_t tlane = static_cast<uint32_t>(warp * 32) << 16;
-        const uint8_t* my_units = ring + (tid >> 3) * (kTcStageChunks * kRows * 16) + (tid & 7) * 16;
-        // Activation codes: thread t copies token t / 8, 16 codes at K offset
-        // 16 (t % 8) of each K block through a small ring (its own bytes only)
-        // and writes them to B as fp16.
-        const int cn = tid >> 3;
-        const int cpart = tid & 7;
-        int xsum = 0;       // this thread's code sum (token cn) over the split's K range
+        // ------------------------------------------- warps 0-7: A and B
+        // Thread t works on row t % 128 (tensor-memory lane t % 128, which warp
+        // t / 32 reaches as warp (t / 32) % 4 does); half t / 128 stores chunks
+        // 2 half and 2 half + 1 of each K block and writes the high (half 0) or
+        // low (half 1) code halves of B.
+        const int row = tid & (kTcRows - 1);
+        const int half = tid / kTcRows;
+        const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint8_t* my_units = ring + (row >> 3) * (kTcStageChunks * kRows * 16) + (row & 7) * 16;
+        // Activation codes: thread t copies token (t % 128) / 8, 16 codes at K
+        // offset 16 (t % 8) of each K block through a small ring (its own
+        // bytes only).
+        const int cn = row >> 3;
+        const int cpart = row & 7;
+        int xsum = 0;       // this thread's code sum (token cn) over the split's K range (half 0)
         auto fetch_codes = [&](int b) {
-            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + tid * 16;
+            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * 16) + tid * 16;
             const int kofs = (cb + b * kTcChunks) * 32 + cpart * 16;
             const bool ok = b < nb && cn < A.M && kofs < ce * 32;
             cp_async16(dst, ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx, ok ? 16u : 0u);
@@ -283,47 +289,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                 continue;
             }
             tc_fence_after();
-            uint4 u[kTcChunks];
+            const int c0 = 2 * half;
+            uint4 u[2];
 #pragma unroll
-            for (int cl = 0; cl < kTcChunks; ++cl)
-                if (cl < nch)
-                    u[cl] = *reinterpret_cast<const uint4*>(my_units + static_cast<size_t>(slot) * kTcStageBytes +
-                                                            (sub * kTcChunks + cl) * kRows * 16);
+            for (int e = 0; e < 2; ++e)
+                if (c0 + e < nch)
+                    u[e] = *reinterpret_cast<const uint4*>(my_units + static_cast<size_t>(slot) * kTcStageBytes +
+                                                           (sub * kTcChunks + c0 + e) * kRows * 16);
             if (sub == kSubs - 1 || b == nb - 1) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // the stage's bytes are in registers
             }
             {
-                // the block's 128 K as e4m3: 32 columns, stored as two 16-column halves
-                uint32_t h[2][16];
+                // this half of the block's 128 K as e4m3: 16 of the buffer's 32 columns
+                uint32_t h[16];
 #pragma unroll
-                for (int cl = 0; cl < kTcChunks; ++cl) {
-                    if (cl < nch) {
-                        tc_unit_e4m3(u[cl], &h[cl >> 1][(cl & 1) * 8]);
+                for (int e = 0; e < 2; ++e) {
+                    if (c0 + e < nch) {
+                        tc_unit_e4m3(u[e], &h[e * 8]);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) h[cl >> 1][(cl & 1) * 8 + e] = 0u;
+                        for (int k = 0; k < 8; ++k) h[e * 8 + k] = 0u;
                     }
                 }
-                tmem_st16(tbase + tlane + kTcColA + j * 32, h[0]);
-                tmem_st16(tbase + tlane + kTcColA + j * 32 + 16, h[1]);
+                tmem_st16(tbase + tlane + kTcColA + j * 32 + 16 * half, h);
             }
             // B: token cn, K positions 16 cpart .. +15 of the block (K group cpart):
             // the high halves in column cn, the low halves in column 16 + cn
             cp_async_wait_group<kTcCodeRing - 1>();
-            const uint4 c = *reinterpret_cast<const uint4*>(codes + (b % kTcCodeRing) * (kTcTok * kTcKb) + tid * 16);
+            const uint4 c =
+                *reinterpret_cast<const uint4*>(codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * 16) + tid * 16);
             uint4 hv, lv;
             tc_split4(c.x, hv.x, lv.x);
             tc_split4(c.y, hv.y, lv.y);
             tc_split4(c.z, hv.z, lv.z);
             tc_split4(c.w, hv.w, lv.w);
-            uint8_t* bt = bbuf + j * kTcBBytes + cpart * kTcBlbo + (cn & 7) * 16;
-            *reinterpret_cast<uint4*>(bt + (cn >> 3) * kTcBsbo) = hv;
-            *reinterpret_cast<uint4*>(bt + (2 + (cn >> 3)) * kTcBsbo) = lv;
-            xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
-            xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
-            xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
-            xsum = __dp4a(static_cast<int>(c.w), 0x01010101, xsum);
+            uint8_t* bt = bbuf + j * kTcBBytes + cpart * kTcBlbo + (cn & 7) * 16 + (2 * half + (cn >> 3)) * kTcBsbo;
+            *reinterpret_cast<uint4*>(bt) = half == 0 ? hv : lv;
+            if (half == 0) {
+                xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
+                xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
+                xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
+                xsum = __dp4a(static_cast<int>(c.w), 0x01010101, xsum);
+            }
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
@@ -333,17 +341,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
         // token cn's code sum: its eight threads are lanes 8k..8k+7 of one warp
 #pragma unroll
         for (int off = 1; off < 8; off <<= 1) xsum += __shfl_xor_sync(0xffffffffu, xsum, off);
-        if (cpart == 0) xsum_s[cn] = xsum;
+        if (cpart == 0 && half == 0) xsum_s[cn] = xsum;
     }
     __syncthreads();
 
     // ---- the accumulator: row tid, tokens 0..15 (warps 0-3)
     const bool dead = *dead_s != 0u;
+    const bool row_thread = tid < kTcRows;
     int acc[kTcTok];
 #pragma unroll
     for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
-    if (!control && !dead && nb > 0) {
-        // the control warp saw the last commit complete before the barrier above;
+    if (row_thread && !dead && nb > 0) {
+        // the MMA warp saw the last commit complete before the barrier above;
         // each accumulator holds sum n h 2^-18 (columns 0-15) and sum n l 2^-18
         // (16-31) exactly: times 2^18 they are exact integers, and over the
         // accumulators 16 S_h + S_l, less 8 sum x, is the exact sum q x
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
     if (ks > 1) {
         int* red = reinterpret_cast<int*>(smem + L.red);
         cluster_sync();
-        if (!control) {
+        if (row_thread) {
             const uint32_t dst = mapa_shared(smem_u32(red + (split * kTcRows + tid) * kTcTok), 0);
 #pragma unroll
             for (int n = 0; n < kTcTok; n += 4)
@@ -381,7 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
                               static_cast<uint32_t>(acc[n + 2]), static_cast<uint32_t>(acc[n + 3]));
         }
         cluster_sync();
-        if (split != 0 || control) return;
+        if (split != 0 || !row_thread) return;
 #pragma unroll
         for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
         for (int r = 0; r < ks; ++r) {
@@ -396,7 +405,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_w4_tc_kernel(const __grid_
             }
         }
     }
-    if (control) return;
+    if (!row_thread) return;
 
     // ---- epilogue: y = fmaf(s_w s_x, acc, b), coalesced over rows per token
     // (a partial sum of a dead split makes the row wrong: the error word says so)

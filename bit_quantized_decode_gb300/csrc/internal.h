@@ -149,7 +149,8 @@ cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, s
 // Per-row INT4 GEMV for 8..16 tokens on the tcgen05 tensor cores
 // (gemv_tc.cu): one block of kTcThreads per (128-row group, K split), the
 // K splits of a row group forming one thread-block cluster.
-constexpr int kTcThreads = 192;                  // warps 0-3: row t = thread t (tensor-memory lane t); 4: MMA; 5: copies
+constexpr int kTcDqWarps = 8;                    // warps 0-7: A and B (rows 0-127 twice: chunks 0-1 / 2-3)
+constexpr int kTcThreads = (kTcDqWarps + 2) * 32;  // then the MMA warp and the copy warp
 constexpr int kTcRows = 128;                     // MMA M: weight rows per block
 constexpr int kTcTok = 16;                       // MMA N: tokens (fewer are zero-padded)
 constexpr int kTcChunks = 4;                     // 32-weight chunks per K block
@@ -188,7 +189,7 @@ __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
     int o = 0;
     L.ring = o;  o += stages * kTcStageBytes;
     L.bbuf = o;  o += kTcBufs * kTcBBytes;
-    L.codes = o; o += kTcCodeRing * kTcTok * kTcKb;
+    L.codes = o; o += kTcCodeRing * (kTcDqWarps * 32) * 16;   // 16 codes per dequantizing thread and K block
     L.red = L.ring;   // K-split partial sums reuse the ring once every block is past its K loop
     L.bars = o;  o += (2 * stages + 2 * kTcBufs) * 8;
     L.tmem = o;  o += 16;

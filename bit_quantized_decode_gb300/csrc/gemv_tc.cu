@@ -50,7 +50,7 @@ namespace {
 
 constexpr uint64_t kTcWaitNs = 250ull * 1000ull * 1000ull;
 constexpr int kTcN = 2 * kTcTok;      // MMA N: each token's high and low code halves
-constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 3 (32 each), D x 4 (32 each)
+constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 4 (32 each), D x 4 (32 each)
 constexpr uint32_t kTcColA = 0;
 constexpr uint32_t kTcColD = 128;
 constexpr int kTcAccs = 4;            // independent accumulators: consecutive MMAs do not wait on each other
@@ -104,17 +104,27 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
     const uint32_t bars = smem_u32(smem + L.bars);
     const uint32_t full_b = bars;                        // [S]  stage landed (1 arrival + bytes)
     const uint32_t empty_b = bars + 8 * S;               // [S]  stage read by the dequantizing warps
-    const uint32_t free_b = bars + 16 * S;               // [3]  MMAs reading an operand buffer completed
+    const uint32_t free_b = bars + 16 * S;               // [kTcBufs]  MMAs reading an operand buffer completed
     // operand buffer j written by the dequantizing warps: named barrier 1 + j
     // (those warps and the MMA warp)
     constexpr uint32_t kReadyCount = (kTcDqWarps + 1) * 32;
     auto ready_arrive = [](int j) {
-        if (j == 0) named_arrive(1, kReadyCount); else if (j == 1) named_arrive(2, kReadyCount); else named_arrive(3, kReadyCount);
+        switch (j) {
+            case 0: named_arrive(1, kReadyCount); break;
+            case 1: named_arrive(2, kReadyCount); break;
+            case 2: named_arrive(3, kReadyCount); break;
+            default: named_arrive(4, kReadyCount); break;
+        }
     };
     auto ready_sync = [](int j) {
-        if (j == 0) named_sync(1, kReadyCount); else if (j == 1) named_sync(2, kReadyCount); else named_sync(3, kReadyCount);
+        switch (j) {
+            case 0: named_sync(1, kReadyCount); break;
+            case 1: named_sync(2, kReadyCount); break;
+            case 2: named_sync(3, kReadyCount); break;
+            default: named_sync(4, kReadyCount); break;
+        }
     };
-    static_assert(kTcBufs == 3, "one named barrier per operand buffer");
+    static_assert(kTcBufs == 4, "one named barrier per operand buffer");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem);   // [0] base address, [1] stop flag
     int* xsum_s = reinterpret_cast<int*>(smem + L.xsum);                 // [kTcTok] code sums of the split
     volatile uint32_t* dead_s = tmem_slot + 1;

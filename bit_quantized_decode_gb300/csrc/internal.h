@@ -159,7 +159,7 @@ constexpr int kTcStageChunks = 16;              // chunks per weight-ring stage 
 constexpr int kTcStageBytes = (kTcRows / kRows) * kTcStageChunks * kRows * 16;   // 32 KB of packed weights
 constexpr int kTcBBytes = 2 * kTcTok * kTcKb;    // e4m3 activation tile per K block (high and low halves)
 constexpr int kTcCodeRing = 4;                   // K blocks of int8 codes in flight
-constexpr int kTcBufs = 3;                       // A (tensor memory) / B (shared memory) operand buffers
+constexpr int kTcBufs = 4;                       // A (tensor memory) / B (shared memory) operand buffers
 constexpr int kTcMaxSplit = 8;                   // K splits (cluster size) at most
 constexpr int kTcMaxSplitK = 16384;              // K per split at most: |sum n l| <= 225 K stays below 2^24
 

@@ -221,46 +221,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
                  : "memory");
 }
 
-// D[tmem] (+)= A[tmem] x B[shared memory descriptor], fp16 operands, fp32
-// accumulation; issued by one thread.
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Eight MMAs of one 128-K block in one statement: K slice kk (A at a0 + 8 kk
-// columns, B at b0 + 32 kk in the descriptor's address field) into
-// accumulator d[kk % 4].  The first four overwrite their accumulator unless
-// `accumulate`; the last four always accumulate.  The operand arithmetic
-// comes first, so the MMAs issue back to back.
-__device__ __forceinline__ void tc_mma_f16_ts_x8(uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3, uint32_t a0,
-                                                 uint64_t b0, uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
-        ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
-        "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 q, %7, %7;\n\t"
-        "add.u32 a1, %4, 8;\n\tadd.u32 a2, %4, 16;\n\tadd.u32 a3, %4, 24;\n\tadd.u32 a4, %4, 32;\n\t"
-        "add.u32 a5, %4, 40;\n\tadd.u32 a6, %4, 48;\n\tadd.u32 a7, %4, 56;\n\t"
-        "add.u64 b1, %5, 32;\n\tadd.u64 b2, %5, 64;\n\tadd.u64 b3, %5, 96;\n\tadd.u64 b4, %5, 128;\n\t"
-        "add.u64 b5, %5, 160;\n\tadd.u64 b6, %5, 192;\n\tadd.u64 b7, %5, 224;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %5, %6, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %6, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%2], [a2], b2, %6, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%3], [a3], b3, %6, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %6, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], [a5], b5, %6, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%2], [a6], b6, %6, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%3], [a7], b7, %6, q;\n\t}" ::"r"(d0),
-        "r"(d1), "r"(d2), "r"(d3), "r"(a0), "l"(b0), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // One MMA of kind::f8f6f4 (A in tensor memory, B from a shared-memory
 // descriptor), e4m3 operands with the types set in idesc; accumulate unless
 // `accumulate` is 0.

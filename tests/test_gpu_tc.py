@@ -5,7 +5,7 @@ scales), y must agree with the oracle within the per-row INT4 tolerance and
 be bit-identical to the DP4A path on the same codes (both finish with
 fmaf(s_w s_x, (float)acc, b)).  Shapes cover one and several K splits (the
 cluster reduction), a partial last 128-row group, K not a multiple of the
-128-wide K block, the split forced by K > 8192, and the largest magnitudes
+128-wide K block, the split forced by K > 16384, and the largest magnitudes
 a split may reach.
 """
 import numpy as np
@@ -64,10 +64,11 @@ def test_tc_accumulators_bit_exact(lib, M, N, K):
 
 
 def test_tc_extreme_magnitudes(lib):
-    """Every product at +-1016 over K = 32768 (four splits of 8192): the
-    tensor cores sum the biased nibbles n = q + 8, whose partial sums reach
-    15 * 127 * 8192 = 15,605,760 < 2^24; the total 33,292,288 is rounded only
-    by the final conversion, exactly as in the oracle."""
+    """Every product at +-1016 over K = 32768 (two splits of 16384): the
+    tensor cores sum the biased nibbles n = q + 8 against the codes' high and
+    low halves, whose partial sums reach 15 * 8 * 16384 and 15 * 15 * 16384,
+    below 2^24; the total 33,292,288 is rounded only by the final conversion,
+    exactly as in the oracle."""
     M, N, K = 16, 256, 32768
     q = np.full((N, K), -8, np.int8)
     q[1::2] = 7
@@ -117,7 +118,7 @@ def test_tc_linear_fused_api(lib, M, N, K):
 
 
 def test_tc_large_k_split_sampled_rows(lib):
-    """152 row groups (one block each by count) with K = 18944 > 8192: the
+    """152 row groups (one block each by count) with K = 18944 > 16384: the
     split is forced by K.  Oracle on a sample of rows."""
     M, N, K = 8, 152 * 128, 18944
     g = wl.rng(99)

@@ -129,3 +129,17 @@ def test_tc_large_k_split_sampled_rows(lib):
     rows = np.sort(g.choice(N, 64, replace=False))
     acc = oracle.gemv_w4a8_acc(oracle.pack_int4(q[rows]), qx)
     assert np.array_equal(y[:, rows].astype(np.int64), acc.astype(np.int64))
+
+
+def test_tc_largest_k_eight_splits(lib):
+    """K = 131072, the largest K the library takes: eight K splits of 16384
+    (a cluster of eight), whose partial sums fill the weight ring exactly;
+    the accumulators stay bit-exact (unit scales)."""
+    M, N, K = 8, 128, 131072
+    g = wl.rng(2024)
+    q = wl.int_codes(g, (N, K), -8, 7)
+    qx = wl.int_codes(g, (M, K), -127, 127)
+    acc = oracle.gemv_w4a8_acc(oracle.pack_int4(q), qx)
+    w = _prep(lib, q, K)
+    y = _gemv(lib, w, dev(np.ones(N, np.float32)), None, dev(qx), dev(np.ones(M, np.float32)), M, N)
+    assert np.array_equal(y.view(np.uint32), acc.astype(np.float32).view(np.uint32))

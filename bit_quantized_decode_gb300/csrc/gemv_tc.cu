@@ -4,7 +4,7 @@
 // 的数学推导"; the multi-token verify case of "在香橙派上跑 Gemma4", §五):
 //   acc[m][j] = sum_i q_w[j][i] qx[m][i]  (exact),
 //   y[m][j]   = fmaf(s_w[j] * sx[m], (float)acc[m][j], b[j])
-// for M = 8..16 tokens sharing one pass over the weights.  The int8 codes and
+// for M = 5..16 tokens sharing one pass over the weights.  The int8 codes and
 // scales come from the activation quantizer launched before this kernel.
 //
 // How (GB300 design): the product is a GEMM of N x K by K x 16, so it runs on
@@ -20,25 +20,31 @@
 // split covers at most 16384 K), so the fp32 accumulators hold the sums
 // exactly; the epilogue forms sum n x = 16 S_h + S_l and removes the bias,
 // sum q x = sum n x - 8 sum x, with each token's code sum over the split.
-//   * One block of six warps per (128-row group, K split).  K splits of a row
-//     group form one thread-block cluster and add their partial sums in the
-//     leader's shared memory (distributed shared memory), which writes y.
+//   * One block of ten warps per (128-row group, K split), two blocks per
+//     SM.  K splits of a row group form one thread-block cluster and add
+//     their partial sums in the leader's shared memory (distributed shared
+//     memory), which writes y.
 //   * Packed weights stream through a ring of stages (512 K x 128 rows,
 //     32 KB: one 2 KB bulk copy per 8-row tile) issued before the dependency
-//     wait; the operand pipeline steps through 128-K blocks of a stage.
-//   * Warps 0-3 (thread t: row t) mask their row's nibbles into e4m3 bytes
-//     (two LOP3 and a shift per 8 weights) and store them into tensor memory
-//     as the MMA's A operand (three buffers); the same warps write the split
-//     activation tile (B, shared memory, K-major, no swizzle).
-//   * Lane 0 of warp 4 issues a block's four MMAs (K slice kk into accumulator
-//     kk, so consecutive MMAs are independent; the four exact partial sums are
-//     added at the end) and commits them; warp 5 issues the weight copies.
-//     "Operands written" is a named barrier per buffer (warps 0-4), "operands
-//     read" the MMA commit's mbarrier, and the ring has full / empty
-//     mbarriers: no block-wide barrier sits in the K loop.
-//   * What bounds it is the MMA issue inside this pipeline (about 100 cycles
-//     per MMA after the first, against about 45 in an isolated loop), not HBM
-//     and not the tensor cores' arithmetic: hence few, wide MMAs.
+//     wait; the operand pipeline steps through the stage in two 256-K blocks.
+//   * Warps 0-7 (thread t: row t % 128, half t / 128) mask their row's
+//     nibbles into e4m3 bytes (two LOP3 and a shift per 8 weights; each half
+//     takes 128 of the block's 256 K) and store them into tensor memory as
+//     the MMA's A operand (three buffers of 64 columns).  The same threads copy the block's
+//     codes (a small cp.async ring), split them and write the activation
+//     tile (B, shared memory, K-major, no swizzle): half 0 the high halves,
+//     half 1 the low halves.
+//   * Lane 0 of warp 8 issues a block's eight MMAs (K slice kk into
+//     accumulator kk % 2, so consecutive MMAs are independent; the two exact
+//     partial sums are added at the end) and commits them; warp 9 issues the
+//     weight copies.  "Operands written" is a named barrier per buffer (warps
+//     0-8), "operands read" the MMA commit's mbarrier, and the ring has full /
+//     empty mbarriers: no block-wide barrier sits in the K loop.
+//   * What bounds it is the latency of the per-block hand-offs (tensor-memory
+//     store wait, the named barrier to the MMA lane, commit to mbarrier), not
+//     HBM, the weight stages or the tensor cores' arithmetic: hence K blocks
+//     of 256 (half the hand-offs of 128) and three operand buffers, which
+//     the 256 tensor-memory columns of a block allow with two accumulators.
 #include <cuda_fp16.h>
 
 #include "fusion.cuh"
@@ -50,10 +56,11 @@ namespace {
 
 constexpr uint64_t kTcWaitNs = 250ull * 1000ull * 1000ull;
 constexpr int kTcN = 2 * kTcTok;      // MMA N: each token's high and low code halves
-constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 4 (32 each), D x 4 (32 each)
+constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 3 (64 each), D x 2 (32 each)
 constexpr uint32_t kTcColA = 0;
-constexpr uint32_t kTcColD = 128;
-constexpr int kTcAccs = 4;            // independent accumulators: consecutive MMAs do not wait on each other
+constexpr uint32_t kTcAStride = kTcKb / 4;   // one K block of e4m3 A: 4 bytes per column
+constexpr uint32_t kTcColD = kTcColA + kTcBufs * kTcAStride;
+constexpr int kTcAccs = 2;            // accumulators: consecutive MMAs do not wait on each other
 // Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3
 // (bits 7-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
@@ -109,22 +116,17 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
     // (those warps and the MMA warp)
     constexpr uint32_t kReadyCount = (kTcDqWarps + 1) * 32;
     auto ready_arrive = [](int j) {
-        switch (j) {
-            case 0: named_arrive(1, kReadyCount); break;
-            case 1: named_arrive(2, kReadyCount); break;
-            case 2: named_arrive(3, kReadyCount); break;
-            default: named_arrive(4, kReadyCount); break;
-        }
+        if (j == 0) named_arrive(1, kReadyCount);
+        else if (j == 1) named_arrive(2, kReadyCount);
+        else named_arrive(3, kReadyCount);
     };
     auto ready_sync = [](int j) {
-        switch (j) {
-            case 0: named_sync(1, kReadyCount); break;
-            case 1: named_sync(2, kReadyCount); break;
-            case 2: named_sync(3, kReadyCount); break;
-            default: named_sync(4, kReadyCount); break;
-        }
+        if (j == 0) named_sync(1, kReadyCount);
+        else if (j == 1) named_sync(2, kReadyCount);
+        else named_sync(3, kReadyCount);
     };
-    static_assert(kTcBufs == 4, "one named barrier per operand buffer");
+    static_assert(kTcBufs == 3, "one named barrier per operand buffer");
+    static_assert(kTcColD + kTcAccs * kTcN <= kTcCols, "tensor-memory columns");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem);   // [0] base address, [1] stop flag
     int* xsum_s = reinterpret_cast<int*>(smem + L.xsum);                 // [kTcTok] code sums of the split
     volatile uint32_t* dead_s = tmem_slot + 1;
@@ -194,31 +196,33 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
     if (mma_warp) {
         // --------------------------------------------------------- MMA warp
         // Every K block is synchronised (named barrier) and committed even after a
-        // failure, so that warps 0-3, which arrive once per block and wait for each
+        // failure, so that warps 0-7, which arrive once per block and wait for each
         // buffer's commit in order, never block on a missing step.
         const uint32_t dcol = tbase + kTcColD;
         for (int b = 0; b < nb; ++b) {
             const int j = b % kTcBufs;
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
-            ready_sync(j);                           // A[j] and B[j] written by warps 0-3
+            ready_sync(j);                           // A[j] and B[j] written by warps 0-7
             if (lane == 0) {
                 if (!*dead_s) {
                     // K slice kk (32 K: 8 tensor-memory columns of A, 1024 B of B, which is
                     // 64 in the descriptor's address field and cannot carry) accumulates
-                    // into D[kk]; the first block overwrites.
+                    // into D[kk % 2]; the first block's first two slices overwrite.
                     tc_fence_after();
                     const uint64_t bdesc = smem_desc_noswizzle(smem_u32(bbuf + j * kTcBBytes), kTcBlbo, kTcBsbo);
-                    const uint32_t acol = tbase + kTcColA + j * 32;
-                    static_assert(kTcAccs == 4 && kTcChunks == 4, "four MMAs per block, one per accumulator");
-                    if (nch == kTcChunks) {
-                        tc_mma_f8_ts_x4(dcol, dcol + kTcN, dcol + 2 * kTcN, dcol + 3 * kTcN, acol, bdesc, kTcIdesc,
-                                        b > 0 ? 1u : 0u);
+                    const uint32_t acol = tbase + kTcColA + j * kTcAStride;
+                    static_assert(kTcAccs == 2 && kTcChunks == 8, "eight MMAs per block, four per accumulator");
+                    if (nch == kTcChunks && b > 0) {
+                        tc_mma_f8_ts_x4(dcol, dcol + kTcN, dcol, dcol + kTcN, acol, bdesc, kTcIdesc, 1u);
+                        tc_mma_f8_ts_x4(dcol, dcol + kTcN, dcol, dcol + kTcN, acol + 32, bdesc + 256,
+                                        kTcIdesc, 1u);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < kTcChunks; ++kk)
                             if (kk < nch)
-                                tc_mma_f8_ts(dcol + kk * kTcN, acol + kk * 8, bdesc + static_cast<uint64_t>(kk * 64),
-                                             kTcIdesc, b > 0 ? 1u : 0u);
+                                tc_mma_f8_ts(dcol + (kk & 1) * kTcN, acol + kk * 8,
+                                             bdesc + static_cast<uint64_t>(kk * 64), kTcIdesc,
+                                             b > 0 || kk >= kTcAccs ? 1u : 0u);
                     }
                 }
                 tc_commit(free_b + 8 * j);
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
         }
     } else if (producer) {
         // ---------------------------------------------------- producer warp
-        // refill each stage's slot once warps 0-3 have read it
+        // refill each stage's slot once warps 0-7 have read it
         for (; issued < nst; ++issued) {
             const int prev = issued - S;
             bool ok = true;
@@ -257,23 +261,26 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
         // ------------------------------------------- warps 0-7: A and B
         // Thread t works on row t % 128 (tensor-memory lane t % 128, which warp
         // t / 32 reaches as warp (t / 32) % 4 does); half t / 128 stores chunks
-        // 2 half and 2 half + 1 of each K block and writes the high (half 0) or
+        // 4 half .. 4 half + 3 of each K block and writes the high (half 0) or
         // low (half 1) code halves of B.
         const int row = tid & (kTcRows - 1);
         const int half = tid / kTcRows;
         const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint8_t* my_units = ring + (row >> 3) * (kTcStageChunks * kRows * 16) + (row & 7) * 16;
-        // Activation codes: thread t copies token (t % 128) / 8, 16 codes at K
-        // offset 16 (t % 8) of each K block through a small ring (its own
-        // bytes only).
+        // Activation codes: thread t copies token (t % 128) / 8, the 32 codes of
+        // chunk t % 8 of each K block through a small ring (its own bytes only).
         const int cn = row >> 3;
         const int cpart = row & 7;
+        constexpr int kHalfChunks = kTcChunks / 2;
         int xsum = 0;       // this thread's code sum (token cn) over the split's K range (half 0)
         auto fetch_codes = [&](int b) {
-            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * 16) + tid * 16;
-            const int kofs = (cb + b * kTcChunks) * 32 + cpart * 16;
+            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
+            const int kofs = (cb + b * kTcChunks) * 32 + cpart * kTcThreadCodes;
             const bool ok = b < nb && cn < A.M && kofs < ce * 32;
-            cp_async16(dst, ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx, ok ? 16u : 0u);
+            const int8_t* src = ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx;
+#pragma unroll
+            for (int e = 0; e < kTcThreadCodes / 16; ++e)
+                cp_async16(dst + 16 * e, ok ? src + 16 * e : A.qx, ok ? 16u : 0u);
             cp_async_commit();
         };
 #pragma unroll
@@ -285,8 +292,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
             const int j = b % kTcBufs;
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
             fetch_codes(b + kTcCodeRing - 1);
-            // buffer j is free once the commit of block b - 3 arrived (the MMA lane
-            // commits every block, failed or not, so this wait keeps its order)
+            // buffer j is free once the commit of block b - kTcBufs arrived (the MMA
+            // lane commits every block, failed or not, so this wait keeps its order)
             bool ok = b < kTcBufs ||
                       mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>((b - kTcBufs) / kTcBufs) & 1u, kTcWaitNs);
             if (ok && !*dead_s && sub == 0)
@@ -299,10 +306,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
                 continue;
             }
             tc_fence_after();
-            const int c0 = 2 * half;
-            uint4 u[2];
+            const int c0 = kHalfChunks * half;
+            uint4 u[kHalfChunks];
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
+            for (int e = 0; e < kHalfChunks; ++e)
                 if (c0 + e < nch)
                     u[e] = *reinterpret_cast<const uint4*>(my_units + static_cast<size_t>(slot) * kTcStageBytes +
                                                            (sub * kTcChunks + c0 + e) * kRows * 16);
@@ -310,37 +317,43 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // the stage's bytes are in registers
             }
-            {
-                // this half of the block's 128 K as e4m3: 16 of the buffer's 32 columns
+            // this half of the block's 256 K as e4m3: 32 of the buffer's 64 columns,
+            // sixteen at a time
+#pragma unroll
+            for (int r = 0; r < kHalfChunks / 2; ++r) {
                 uint32_t h[16];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    if (c0 + e < nch) {
-                        tc_unit_e4m3(u[e], &h[e * 8]);
+                    if (c0 + 2 * r + e < nch) {
+                        tc_unit_e4m3(u[2 * r + e], &h[e * 8]);
                     } else {
 #pragma unroll
                         for (int k = 0; k < 8; ++k) h[e * 8 + k] = 0u;
                     }
                 }
-                tmem_st16(tbase + tlane + kTcColA + j * 32 + 16 * half, h);
+                tmem_st16(tbase + tlane + kTcColA + j * kTcAStride + 32 * half + 16 * r, h);
             }
-            // B: token cn, K positions 16 cpart .. +15 of the block (K group cpart):
+            // B: token cn, K groups 2 cpart and 2 cpart + 1 (16 K each) of the block:
             // the high halves in column cn, the low halves in column 16 + cn
             cp_async_wait_group<kTcCodeRing - 1>();
-            const uint4 c =
-                *reinterpret_cast<const uint4*>(codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * 16) + tid * 16);
-            uint4 hv, lv;
-            tc_split4(c.x, hv.x, lv.x);
-            tc_split4(c.y, hv.y, lv.y);
-            tc_split4(c.z, hv.z, lv.z);
-            tc_split4(c.w, hv.w, lv.w);
-            uint8_t* bt = bbuf + j * kTcBBytes + cpart * kTcBlbo + (cn & 7) * 16 + (2 * half + (cn >> 3)) * kTcBsbo;
-            *reinterpret_cast<uint4*>(bt) = half == 0 ? hv : lv;
-            if (half == 0) {
-                xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
-                xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
-                xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
-                xsum = __dp4a(static_cast<int>(c.w), 0x01010101, xsum);
+            const uint8_t* my_codes = codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
+#pragma unroll
+            for (int e = 0; e < kTcThreadCodes / 16; ++e) {
+                const uint4 c = *reinterpret_cast<const uint4*>(my_codes + 16 * e);
+                uint4 hv, lv;
+                tc_split4(c.x, hv.x, lv.x);
+                tc_split4(c.y, hv.y, lv.y);
+                tc_split4(c.z, hv.z, lv.z);
+                tc_split4(c.w, hv.w, lv.w);
+                uint8_t* bt = bbuf + j * kTcBBytes + (2 * cpart + e) * kTcBlbo + (cn & 7) * 16 +
+                              (2 * half + (cn >> 3)) * kTcBsbo;
+                *reinterpret_cast<uint4*>(bt) = half == 0 ? hv : lv;
+                if (half == 0) {
+                    xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
+                    xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
+                    xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
+                    xsum = __dp4a(static_cast<int>(c.w), 0x01010101, xsum);
+                }
             }
             fence_proxy_async_smem();
             tmem_wait_st();

@@ -146,20 +146,21 @@ cudaError_t launch_gemv_a32(int fmt, const ChainParams<1>& p, int MT, int grid, 
 cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
 
 // ---------------------------------------------- multi-token tensor-core GEMV
-// Per-row INT4 GEMV for 8..16 tokens on the tcgen05 tensor cores
+// Per-row INT4 GEMV for 5..16 tokens on the tcgen05 tensor cores
 // (gemv_tc.cu): one block of kTcThreads per (128-row group, K split), the
 // K splits of a row group forming one thread-block cluster.
-constexpr int kTcDqWarps = 8;                    // warps 0-7: A and B (rows 0-127 twice: chunks 0-1 / 2-3)
+constexpr int kTcDqWarps = 8;                    // warps 0-7: A and B (rows 0-127 twice: chunks 0-3 / 4-7)
 constexpr int kTcThreads = (kTcDqWarps + 2) * 32;  // then the MMA warp and the copy warp
 constexpr int kTcRows = 128;                     // MMA M: weight rows per block
 constexpr int kTcTok = 16;                       // MMA N: tokens (fewer are zero-padded)
-constexpr int kTcChunks = 4;                     // 32-weight chunks per K block
-constexpr int kTcKb = 32 * kTcChunks;            // K per block: 128
-constexpr int kTcStageChunks = 16;              // chunks per weight-ring stage (4 K blocks): 2 KB copies per tile
+constexpr int kTcChunks = 8;                     // 32-weight chunks per K block
+constexpr int kTcKb = 32 * kTcChunks;            // K per block: 256
+constexpr int kTcStageChunks = 16;              // chunks per weight-ring stage (2 K blocks): 2 KB copies per tile
 constexpr int kTcStageBytes = (kTcRows / kRows) * kTcStageChunks * kRows * 16;   // 32 KB of packed weights
 constexpr int kTcBBytes = 2 * kTcTok * kTcKb;    // e4m3 activation tile per K block (high and low halves)
-constexpr int kTcCodeRing = 4;                   // K blocks of int8 codes in flight
-constexpr int kTcBufs = 4;                       // A (tensor memory) / B (shared memory) operand buffers
+constexpr int kTcThreadCodes = kTcKb / 8;        // codes a dequantizing thread copies per K block
+constexpr int kTcCodeRing = 3;                   // K blocks of int8 codes in flight
+constexpr int kTcBufs = 3;                       // A (tensor memory) / B (shared memory) operand buffers
 constexpr int kTcMaxSplit = 8;                   // K splits (cluster size) at most
 constexpr int kTcMaxSplitK = 16384;              // K per split at most: |sum n l| <= 225 K stays below 2^24
 
@@ -189,7 +190,7 @@ __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
     int o = 0;
     L.ring = o;  o += stages * kTcStageBytes;
     L.bbuf = o;  o += kTcBufs * kTcBBytes;
-    L.codes = o; o += kTcCodeRing * (kTcDqWarps * 32) * 16;   // 16 codes per dequantizing thread and K block
+    L.codes = o; o += kTcCodeRing * (kTcDqWarps * 32) * kTcThreadCodes;
     L.red = L.ring;   // K-split partial sums reuse the ring once every block is past its K loop
     L.bars = o;  o += (2 * stages + 2 * kTcBufs) * 8;
     L.tmem = o;  o += 16;

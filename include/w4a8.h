@@ -103,7 +103,7 @@ int w4_version(void);
  *   W4_TUNE_MAX_STAGES     cap on the ring depth per warp (>= 2).
  *   W4_TUNE_GRID_BLOCKS    cap on the grid size (default: the SM count).
  *   W4_TUNE_TC_MIN_M       per-row INT4 calls with at least this many tokens
- *                          run on the tensor cores (default 0: 8; 17: never).
+ *                          run on the tensor cores (default 0: 5; 17: never).
  * Returns W4_ERR_INVALID_ARG for an unknown key or an out-of-range value.
  * Not thread-safe with concurrent launches; set before launching.
  * ------------------------------------------------------------------------ */

@@ -225,7 +225,7 @@ def test_norm_linear_tensor_cores(lib):
     gam = wl.norm_weight(g, K)
     qx_ref, sx_ref = oracle.quantize_act_int8(oracle.rmsnorm_f32(x, gam, EPS))
     y, qx, sx = _bufs(M, N, K)
-    lib.set_tuning("tc_min_m", 8)
+    lib.set_tuning("tc_min_m", 1)
     L.fused(lib, dev(x), y, qx, sx, lib.fusion(norm_weight=dev(gam), eps=EPS), lib.W4_FLAG_PDL)
     lib.set_tuning("tc_min_m", 0)
     amb = _ambiguous(x, 4 * ((K // 4 + 511) // 512))
@@ -308,15 +308,15 @@ def test_glu_linear(lib, fmt, kind, M, I, K):
 
 
 def test_glu_linear_tensor_cores_and_uncached_rows(lib):
-    """W4 gated linear on the tensor cores (M = 16) and, at one token, with
+    """W4 gated linear on the tensor cores (M = 16 and 6) and, at one token, with
     more rows per block than the staged parameter cache (I = 80000)."""
     import torch
-    for M, I, K, tc in ((16, 4736, 3584, True), (1, 80000, 64, False)):
+    for M, I, K, tc in ((16, 4736, 3584, True), (6, 1000, 1536, True), (1, 80000, 64, False)):
         g = wl.rng(4000 + I)
         L = GatedLayer(lib, "w4", g, I, K)
         x = wl.activations(g, M, K)
         y, qx, sx = _bufs(M, I, K)
-        lib.set_tuning("tc_min_m", 8 if tc else 17)
+        lib.set_tuning("tc_min_m", 1 if tc else 17)
         L.run(lib, L.wp, dev(x), y, qx, sx, lib.fusion(glu=1), lib.W4_FLAG_PDL)
         lib.set_tuning("tc_min_m", 0)
         qx_ref, sx_ref = oracle.quantize_act_int8(x)
@@ -327,7 +327,7 @@ def test_glu_linear_tensor_cores_and_uncached_rows(lib):
 # ------------------------------------------------------------- residual
 @pytest.mark.parametrize("fmt,M,N,K,tc", [("w4", 1, 3584, 3584, False), ("w4", 2, 3584, 18944, False),
                                           ("q4_0", 3, 1536, 6144, False), ("w4", 16, 3584, 3584, True),
-                                          ("i8g32", 1, 200, 1536, False)])
+                                          ("i8g32", 1, 200, 1536, False), ("w4", 7, 1000, 3584, True)])
 def test_residual_linear_in_place(lib, fmt, M, N, K, tc):
     """y = residual + linear(x), with the residual buffer as the output (the
     decoder's in-place update): within the linear's tolerance plus the final
@@ -339,7 +339,7 @@ def test_residual_linear_in_place(lib, fmt, M, N, K, tc):
     h = wl.residual_stream(g, M, N)
     hd = dev(h)
     y, qx, sx = _bufs(M, N, K)
-    lib.set_tuning("tc_min_m", 8 if tc else 17)
+    lib.set_tuning("tc_min_m", 1 if tc else 17)
     L.fused(lib, dev(x), hd, qx, sx, lib.fusion(residual=hd), lib.W4_FLAG_PDL)
     L.fused(lib, dev(x), y, qx, sx, None, lib.W4_FLAG_PDL)
     lib.set_tuning("tc_min_m", 0)

@@ -1,11 +1,12 @@
-"""The multi-token per-row INT4 GEMV on the tensor cores (M = 8..16).
+"""The multi-token per-row INT4 GEMV on the tensor cores (by default M = 5..16;
+the tests force it for any M, one token included).
 
 The accumulators must be the exact integer sums (read out through unit
 scales), y must agree with the oracle within the per-row INT4 tolerance and
 be bit-identical to the DP4A path on the same codes (both finish with
 fmaf(s_w s_x, (float)acc, b)).  Shapes cover one and several K splits (the
 cluster reduction), a partial last 128-row group, K not a multiple of the
-128-wide K block, the split forced by K > 16384, and the largest magnitudes
+256-wide K block (and shorter than one), the split forced by K > 16384, and the largest magnitudes
 a split may reach.
 """
 import numpy as np
@@ -40,7 +41,7 @@ def _prep(lib, q, K):
 
 def _gemv(lib, w, sw, b, qx, sx, M, N, tc=True):
     import torch
-    lib.set_tuning("tc_min_m", 8 if tc else 17)
+    lib.set_tuning("tc_min_m", 1 if tc else 17)
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     lib.w4a8_gemv(w, sw, b, qx, sx, y)
     lib.set_tuning("tc_min_m", 0)
@@ -48,7 +49,8 @@ def _gemv(lib, w, sw, b, qx, sx, M, N, tc=True):
 
 
 @pytest.mark.parametrize("M,N,K", [(8, 256, 256), (16, 300, 3584), (12, 4608, 3584), (9, 3584, 18944),
-                                   (16, 128, 96), (10, 1000, 6144), (16, 136, 32)])
+                                   (16, 128, 96), (10, 1000, 6144), (16, 136, 32), (5, 384, 640),
+                                   (6, 200, 224), (7, 1000, 3584), (1, 264, 1088)])
 def test_tc_accumulators_bit_exact(lib, M, N, K):
     """Unit scales, no bias: y is (float)acc, exact while |acc| < 2^24."""
     g = wl.rng(3 * M + N + K)
@@ -80,7 +82,8 @@ def test_tc_extreme_magnitudes(lib):
     assert np.array_equal(y.view(np.uint32), acc.astype(np.float32).view(np.uint32))
 
 
-@pytest.mark.parametrize("M,N,K", [(8, 512, 3584), (16, 4608, 3584), (13, 3584, 18944), (16, 1000, 1536)])
+@pytest.mark.parametrize("M,N,K", [(8, 512, 3584), (16, 4608, 3584), (13, 3584, 18944), (16, 1000, 1536),
+                                   (5, 3584, 18944), (6, 4608, 3584), (7, 640, 1536), (2, 300, 3584)])
 def test_tc_matches_oracle_and_dp4a(lib, M, N, K):
     g = wl.rng(5 * M + N + K)
     W = wl.weights(g, N, K)
@@ -96,7 +99,8 @@ def test_tc_matches_oracle_and_dp4a(lib, M, N, K):
     assert np.array_equal(y_tc.view(np.uint32), y_dp.view(np.uint32))
 
 
-@pytest.mark.parametrize("M,N,K", [(8, 4608, 3584), (16, 3584, 18944), (11, 37888 // 4, 3584)])
+@pytest.mark.parametrize("M,N,K", [(8, 4608, 3584), (16, 3584, 18944), (11, 37888 // 4, 3584),
+                                   (5, 3584, 18944), (7, 4608, 3584)])
 def test_tc_linear_fused_api(lib, M, N, K):
     """w4a8_linear with many tokens: the activation quantizer, then the
     tensor-core GEMV (chained); codes and scales bit-exact."""

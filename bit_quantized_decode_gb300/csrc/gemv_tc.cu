@@ -431,39 +431,64 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
     if (!row_thread) return;
 
     // ---- epilogue: y = fmaf(s_w s_x, acc, b), coalesced over rows per token
-    // (a partial sum of a dead split makes the row wrong: the error word says so)
+    // (a partial sum of a dead split makes the row wrong: the error word says so).
+    // Every load (token scales, residuals) is issued before the first store: y
+    // may alias the residual, so a store between two loads would serialise them.
     const int row = g * kTcRows + tid;
     if (A.glu == GLU_NONE) {
         if (row < A.N && !dead) {
             const float sw = A.s_w[row];
             const float bv = A.bias != nullptr ? A.bias[row] : 0.0f;
+            float v[kTcTok];
 #pragma unroll
-            for (int n = 0; n < kTcTok; ++n) {
-                if (n < A.M) {
-                    const size_t o = static_cast<size_t>(n) * A.N + row;
-                    float out = __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv);
-                    if (A.residual != nullptr) out = __fadd_rn(A.residual[o], out);
-                    A.y[o] = out;
-                }
+            for (int n = 0; n < kTcTok; ++n)
+                v[n] = n < A.M ? __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv) : 0.0f;
+            if (A.residual != nullptr) {
+                float rv[kTcTok];
+#pragma unroll
+                for (int n = 0; n < kTcTok; ++n)
+                    rv[n] = n < A.M ? A.residual[static_cast<size_t>(n) * A.N + row] : 0.0f;
+#pragma unroll
+                for (int n = 0; n < kTcTok; ++n) v[n] = __fadd_rn(rv[n], v[n]);
             }
+#pragma unroll
+            for (int n = 0; n < kTcTok; ++n)
+                if (n < A.M) A.y[static_cast<size_t>(n) * A.N + row] = v[n];
         }
     } else {
-        // gated: this thread's row pairs with the row 4 lanes up (the up row of
-        // the same tile); the gate lanes (row % 8 < 4) write output j
+        // gated: this thread's row pairs with the row 4 lanes away (gate rows
+        // r % 8 < 4, up rows 4 below them, in the same tile).  The gate lane
+        // writes output j for the even tokens, the up lane for the odd ones.
         const int prow = glu_param_row(row, A.n_out);
         const bool have = row < A.N && prow >= 0 && !dead;
+        const bool up = (row & 4) != 0;
         const float sw = have ? A.s_w[prow] : 0.0f;
         const float bv = have && A.bias != nullptr ? A.bias[prow] : 0.0f;
         const int j = (row >> 3) * 4 + (row & 3);
+        float v[kTcTok];
 #pragma unroll
-        for (int n = 0; n < kTcTok; ++n) {
-            const float v = n < A.M ? __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv) : 0.0f;
-            const float u = __shfl_down_sync(0xffffffffu, v, 4);
-            if (have && (row & 4) == 0 && n < A.M) {
-                const size_t o = static_cast<size_t>(n) * A.n_out + j;
-                float out = glu_act_call(A.glu, v, u);
-                if (A.residual != nullptr) out = __fadd_rn(A.residual[o], out);
-                A.y[o] = out;
+        for (int n = 0; n < kTcTok; ++n)
+            v[n] = n < A.M ? __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv) : 0.0f;
+        constexpr int kHalfTok = kTcTok / 2;
+        float gv[kHalfTok], uv[kHalfTok], rv[kHalfTok];
+#pragma unroll
+        for (int k = 0; k < kHalfTok; ++k) {
+            // token 2k + up is this lane's: the partner sends its value there
+            const float other = __shfl_xor_sync(0xffffffffu, up ? v[2 * k] : v[2 * k + 1], 4);
+            gv[k] = up ? other : v[2 * k];
+            uv[k] = up ? v[2 * k + 1] : other;
+            const int n = 2 * k + (up ? 1 : 0);
+            rv[k] = (have && A.residual != nullptr && n < A.M) ? A.residual[static_cast<size_t>(n) * A.n_out + j] : 0.0f;
+        }
+        if (have) {
+#pragma unroll
+            for (int k = 0; k < kHalfTok; ++k) {
+                const int n = 2 * k + (up ? 1 : 0);
+                if (n < A.M) {
+                    float out = glu_act_call(A.glu, gv[k], uv[k]);
+                    if (A.residual != nullptr) out = __fadd_rn(rv[k], out);
+                    A.y[static_cast<size_t>(n) * A.n_out + j] = out;
+                }
             }
         }
     }

@@ -64,7 +64,8 @@ def kernel_digest(names=GEMV_W4_SOURCES) -> str:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    # the include directory is an absolute path that differs between checkouts
+    h.update(" ".join("include" if f == INCLUDE else f for f in NVCC_FLAGS).encode())
     return h.hexdigest()
 
 

@@ -75,3 +75,14 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_kernel_digest_does_not_depend_on_the_checkout_path(monkeypatch):
+    """The profile summaries name the kernel sources by digest; the same
+    sources in another directory (the GPU host's copy) give the same digest."""
+    from bit_quantized_decode_gb300 import build
+    here = build.kernel_digest()
+    elsewhere = "/some/other/checkout/include"
+    monkeypatch.setattr(build, "NVCC_FLAGS", [elsewhere if f == build.INCLUDE else f for f in build.NVCC_FLAGS])
+    monkeypatch.setattr(build, "INCLUDE", elsewhere)
+    assert build.kernel_digest() == here

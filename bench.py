@@ -63,6 +63,9 @@ def parse_args(argv=None):
                         "workloads on its own, then the full step at M = 1, 2, 4, 8, 16 (one JSON line each)")
     p.add_argument("--suite-ms", default="1,2,4,8,16", help="token counts of the suite's full-step lines")
     p.add_argument("--suite-only-steps", action="store_true", help="suite: skip the single-GEMV lines")
+    p.add_argument("--suite-gemvs", default="",
+                   help="suite: only these single GEMVs, comma-separated, each a workload (gemma_q4_0) or "
+                        "workload:linear (lm_head:lm_head_q6g32); default all")
     p.add_argument("--suite-ablation-ms", default="1",
                    help="token counts of the suite's weight-only ablation lines (INT4 DP4A, INT4 float unpack, "
                         "INT8 weight-only; at most 2 tokens: the float activations of the K = 18944 linear "
@@ -771,6 +774,13 @@ def suite_gemv(wname: str, lin, M: int, device, stream, steps: int, warmup: int,
             "bytes": b, "weight_copies": copies, "replays": reps}
 
 
+def suite_selected(spec: str, wname: str, lname: str) -> bool:
+    """--suite-gemvs: an empty list selects every GEMV; an entry is a workload
+    name or workload:linear."""
+    sel = [e.strip() for e in spec.split(",") if e.strip()]
+    return not sel or wname in sel or f"{wname}:{lname}" in sel
+
+
 def run_suite(args, local_rank):
     """Configs 1-4 GEMV by GEMV, then the full step at M = 1, 2, 4, 8, 16.
     One JSON line per entry."""
@@ -788,12 +798,14 @@ def run_suite(args, local_rank):
         if wname == "lm_head":
             lins.append(wl.gemma_lm_head_q6g32())   # the same values packed in 6 bits
         for lin in lins:
-            print(json.dumps(suite_gemv(wname, lin, 1, dev, stream, args.steps, args.warmup, peak)), flush=True)
-    weights = build_weights(args, dev)
+            if suite_selected(args.suite_gemvs, wname, lin.name):
+                print(json.dumps(suite_gemv(wname, lin, 1, dev, stream, args.steps, args.warmup, peak)), flush=True)
+    step_ms = [int(m) for m in args.suite_ms.split(",") if m]
+    weights = build_weights(args, dev) if step_ms else None
     for kv in args.tune:
         k, v = kv.split("=")
         _lib.set_tuning(k, int(v))
-    for M in (int(m) for m in args.suite_ms.split(",") if m):
+    for M in step_ms:
         items, _, _ = make_buffers(weights, M, args.independent_x, dev)
 
         def step():

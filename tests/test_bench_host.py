@@ -86,3 +86,11 @@ def test_kernel_digest_does_not_depend_on_the_checkout_path(monkeypatch):
     monkeypatch.setattr(build, "NVCC_FLAGS", [elsewhere if f == build.INCLUDE else f for f in build.NVCC_FLAGS])
     monkeypatch.setattr(build, "INCLUDE", elsewhere)
     assert build.kernel_digest() == here
+
+
+def test_suite_gemv_selection():
+    assert bench.suite_selected("", "lm_head", "lm_head_q6g32")
+    assert bench.suite_selected("gemma_q4_0", "gemma_q4_0", "qkv")
+    assert not bench.suite_selected("gemma_q4_0", "lm_head", "lm_head")
+    assert bench.suite_selected("gemma_q4_0:down, lm_head:lm_head_q6g32", "lm_head", "lm_head_q6g32")
+    assert not bench.suite_selected("lm_head:lm_head_q6g32", "lm_head", "lm_head_i8g32")

@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
     volatile uint32_t* dead_s = tmem_slot + 1;
 
     constexpr int kSubs = kTcStageChunks / kTcChunks;      // K blocks per ring stage
+    static_assert((kSubs & (kSubs - 1)) == 0, "K blocks per stage: a power of two");
     const int g = blockIdx.x / ks;                         // row group
     const int split = blockIdx.x - g * ks;                 // = rank in the cluster
     const int cb = static_cast<int>(static_cast<long long>(split) * A.C / ks);
@@ -273,8 +274,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
         const int cpart = row & 7;
         constexpr int kHalfChunks = kTcChunks / 2;
         int xsum = 0;       // this thread's code sum (token cn) over the split's K range (half 0)
-        auto fetch_codes = [&](int b) {
-            uint8_t* dst = codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
+        auto fetch_codes = [&](int b, int cs) {
+            uint8_t* dst = codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
             const int kofs = (cb + b * kTcChunks) * 32 + cpart * kTcThreadCodes;
             const bool ok = b < nb && cn < A.M && kofs < ce * 32;
             const int8_t* src = ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx;
@@ -284,20 +285,27 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
             cp_async_commit();
         };
 #pragma unroll
-        for (int i = 0; i < kTcCodeRing - 1; ++i) fetch_codes(i);
+        for (int i = 0; i < kTcCodeRing - 1; ++i) fetch_codes(i, i);
+        // ring positions kept as counters (no division in the loop): weight
+        // stage slot and its phase, operand buffer j and the phase of its
+        // previous commit, code-ring slots of this block and of the one fetched
+        int slot = 0, j = 0, cs = 0, cs_next = kTcCodeRing - 1;
+        uint32_t sph = 0u, jph = 1u;
         for (int b = 0; b < nb; ++b) {
-            const int st = b / kSubs;
-            const int sub = b - st * kSubs;
-            const int slot = st % S;
-            const int j = b % kTcBufs;
+            const int sub = b & (kSubs - 1);
+            if (b > 0) {
+                if (sub == 0 && ++slot == S) { slot = 0; sph ^= 1u; }
+                if (++j == kTcBufs) { j = 0; jph ^= 1u; }
+                if (++cs == kTcCodeRing) cs = 0;
+                if (++cs_next == kTcCodeRing) cs_next = 0;
+            }
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
-            fetch_codes(b + kTcCodeRing - 1);
+            fetch_codes(b + kTcCodeRing - 1, cs_next);
             // buffer j is free once the commit of block b - kTcBufs arrived (the MMA
             // lane commits every block, failed or not, so this wait keeps its order)
-            bool ok = b < kTcBufs ||
-                      mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>((b - kTcBufs) / kTcBufs) & 1u, kTcWaitNs);
+            bool ok = b < kTcBufs || mbar_wait_bounded(free_b + 8 * j, jph, kTcWaitNs);
             if (ok && !*dead_s && sub == 0)
-                ok = mbar_wait_bounded(full_b + 8 * slot, static_cast<uint32_t>(st / S) & 1u, kTcWaitNs);
+                ok = mbar_wait_bounded(full_b + 8 * slot, sph, kTcWaitNs);
             if (!__all_sync(0xffffffffu, ok) && lane == 0 && !*dead_s) fail();
             if (*dead_s) {
                 // stop working but keep the per-block handshake
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
             // B: token cn, K groups 2 cpart and 2 cpart + 1 (16 K each) of the block:
             // the high halves in column cn, the low halves in column 16 + cn
             cp_async_wait_group<kTcCodeRing - 1>();
-            const uint8_t* my_codes = codes + (b % kTcCodeRing) * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
+            const uint8_t* my_codes = codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
 #pragma unroll
             for (int e = 0; e < kTcThreadCodes / 16; ++e) {
                 const uint4 c = *reinterpret_cast<const uint4*>(my_codes + 16 * e);

@@ -192,8 +192,11 @@ w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_st
  * Per token: GEMV on INT8 activations.
  *
  * w4a8_gemv, [Orin-INT4] §"从 FP 线性层到 INT4 DP4A 的数学推导" and §"DP4A 做了什么":
- *   acc[m][j] = sum_i q_w[j][i] * qx[m][i]   (exact int32, DP4A),
+ *   acc[m][j] = sum_i q_w[j][i] * qx[m][i]   (exact int32),
  *   y[m][j]   = fmaf(s_w[j] * sx[m], (float)acc, b[j])   (b = 0 if bias NULL).
+ *   Up to four tokens the sums run on DP4A; from five tokens (see
+ *   W4_TUNE_TC_MIN_M) on the tensor cores, with exact fp8 products and fp32
+ *   partial sums.  y is bit-identical either way.
  * q4_0_gemv / i8g32_gemv / q6g32_gemv, [310B-Gemma4] §3.1 / §3.2:
  *   acc_g = exact int32 sum over 32-block g,
  *   y[m][j] = fmaf(sx[m], sum_g d_g * acc_g, b[j])  (fp32; group order unspecified).

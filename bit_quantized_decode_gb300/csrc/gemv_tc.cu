@@ -40,11 +40,13 @@
 //     weight copies.  "Operands written" is a named barrier per buffer (warps
 //     0-8), "operands read" the MMA commit's mbarrier, and the ring has full /
 //     empty mbarriers: no block-wide barrier sits in the K loop.
-//   * What bounds it is the latency of the per-block hand-offs (tensor-memory
-//     store wait, the named barrier to the MMA lane, commit to mbarrier), not
-//     HBM, the weight stages or the tensor cores' arithmetic: hence K blocks
-//     of 256 (half the hand-offs of 128) and three operand buffers, which
-//     the 256 tensor-memory columns of a block allow with two accumulators.
+//   * What bounds it is the latency of the dequantizing warps' per-block
+//     chain (shared-memory loads, tensor-memory stores and their wait, the
+//     named barrier to the MMA lane, the commit's mbarrier), not HBM, the
+//     weight stages or the tensor cores' arithmetic: hence K blocks of 256
+//     (half the hand-offs of 128), three operand buffers (which the 256
+//     tensor-memory columns of a block allow with two accumulators) and no
+//     division in the loop.
 #include <cuda_fp16.h>
 
 #include "fusion.cuh"

@@ -108,6 +108,24 @@ class LinearDesc(ctypes.Structure):
                 ("N", _I), ("K", _I)]
 
 
+class DeviceDesc(ctypes.Structure):
+    """w4_device_desc of include/w4a8.h."""
+    _fields_ = [("sms", _I), ("smem_per_sm", _I), ("smem_reserved", _I), ("smem_optin", _I)]
+
+
+class LaunchPlan(ctypes.Structure):
+    """w4_launch_plan of include/w4a8.h."""
+    _fields_ = [("path", _I), ("quantize_launches", _I), ("grid", _I), ("threads", _I), ("smem_bytes", _I),
+                ("stages", _I), ("k_splits", _I)]
+
+
+FORMATS = {"w4": 0, "q4_0": 1, "i8g32": 2, "q6g32": 3}
+W4_PLAN_LINEAR = 1
+W4_PLAN_NORM = 2
+W4_PLAN_GLU = 4
+PATHS = {0: "none", 1: "fused", 2: "codes_smem", 3: "codes_global", 4: "tensor_cores"}
+SIGNATURES["w4_plan"] = ([_I, _I, _I, _I, _U, ctypes.POINTER(DeviceDesc), ctypes.POINTER(LaunchPlan)], _I)
+SIGNATURES["w4_describe_device"] = ([ctypes.POINTER(DeviceDesc)], _I)
 SIGNATURES["w4_chain_workspace_bytes"] = ([], _SZ)
 SIGNATURES["w4_chain_noalloc_scratch_bytes"] = ([], _SZ)
 SIGNATURES["w4a8_linear_chain_noalloc"] = ([ctypes.POINTER(LinearDesc), _I, _I, _P], _I)
@@ -180,6 +198,26 @@ def status_str(st: int) -> str:
 
 def version() -> int:
     return load().w4_version()
+
+
+def w4_describe_device() -> dict:
+    """The current device's description (w4_device_desc) as a dict."""
+    d = DeviceDesc()
+    _check("w4_describe_device", load().w4_describe_device(ctypes.byref(d)))
+    return {f: getattr(d, f) for f, _ in DeviceDesc._fields_}
+
+
+def w4_plan(fmt: str, M: int, N: int, K: int, device: dict, linear: bool = True, norm: bool = False,
+            glu: bool = False) -> dict:
+    """The launch plan of a call (w4_plan): host computation only, no GPU
+    needed.  device: a dict with the w4_device_desc fields."""
+    d = DeviceDesc(**{f: int(device[f]) for f, _ in DeviceDesc._fields_})
+    what = (W4_PLAN_LINEAR if linear else 0) | (W4_PLAN_NORM if norm else 0) | (W4_PLAN_GLU if glu else 0)
+    p = LaunchPlan()
+    _check("w4_plan", load().w4_plan(FORMATS[fmt], M, N, K, what, ctypes.byref(d), ctypes.byref(p)))
+    out = {f: getattr(p, f) for f, _ in LaunchPlan._fields_}
+    out["path"] = PATHS[out["path"]]
+    return out
 
 
 def set_tuning(key: str, value: int):

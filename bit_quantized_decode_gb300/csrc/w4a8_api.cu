@@ -141,6 +141,15 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
     return false;
 }
 
+// Blocks of a DP4A GEMV launch over T row tiles: one per SM (or the tuned
+// cap), never more than the tiles.
+int gemv_grid(const DeviceInfo& d, int T)
+{
+    int grid = d.sms;
+    if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
+    return T < grid ? T : grid;
+}
+
 // Launch one GEMV.
 w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t s)
 {
@@ -160,9 +169,7 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     Plan p;
     if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p)) return W4_ERR_UNSUPPORTED_SHAPE;
     cp.stages = p.stages;
-    int grid = dev->sms;
-    if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
-    if (a.T < grid) grid = a.T;
+    const int grid = gemv_grid(*dev, a.T);
     cp.lin[0].tq = a.T / grid;
     cp.lin[0].tr = a.T % grid;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
@@ -221,15 +228,20 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
     return cuda_status(launch_chain_w4(cp, MT, grid, static_cast<size_t>(smem), s));
 }
 
-// Would the fused kernel (x quantized into shared memory) fit?
+// Would the fused kernel (x quantized into shared memory) fit on device d?
+bool fused_fits_on(const DeviceInfo& d, int fmt, int M, int K, bool norm)
+{
+    const int MT = round_pow2_tokens(M);
+    if (norm && (MT > 4 || (K / 4 + kThreads - 1) / kThreads > norm_max_nit(MT))) return false;
+    Plan p;
+    return plan_gemv(d, fmt, MT, true, K, kAccWords / MT, p);
+}
+
 bool fused_fits(int fmt, int M, int K, bool norm = false)
 {
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != W4_OK) return false;
-    const int MT = round_pow2_tokens(M);
-    if (norm && (MT > 4 || (K / 4 + kThreads - 1) / kThreads > norm_max_nit(MT))) return false;
-    Plan p;
-    return plan_gemv(*dev, fmt, MT, true, K, kAccWords / MT, p);
+    return fused_fits_on(*dev, fmt, M, K, norm);
 }
 
 // Operators fused around one linear (w4_fusion, checked).
@@ -269,11 +281,30 @@ bool use_tc(int fmt, int M, int K)
     return fmt == FMT_W4 && M >= lo && M <= kTcTok && K <= kTcMaxSplit * kTcMaxSplitK;
 }
 
-// Tensor-core GEMV: one block per (128-row group, K split); enough splits to
-// cover the SMs, rounded down to a power of two (clusters of 5 or 6 blocks
-// measured slower), at most kTcMaxSplit, and enough to keep every split within
-// kTcMaxSplitK; the deepest weight ring that leaves room for a second block
-// per SM.
+// Tensor-core GEMV on device d: one block per (128-row group, K split);
+// enough splits to cover the SMs, rounded down to a power of two (clusters of
+// 5 or 6 blocks measured slower), at most kTcMaxSplit, and enough to keep
+// every split within kTcMaxSplitK; the deepest weight ring that leaves room
+// for a second block per SM.  N: weight rows.
+w4_status tc_plan(const DeviceInfo& d, int N, int K, int& ks, int& S)
+{
+    const int C = K / 32;
+    const int G = (N + kTcRows - 1) / kTcRows;
+    ks = (d.sms + G - 1) / G;
+    if (ks > kTcMaxSplit) ks = kTcMaxSplit;
+    while (ks & (ks - 1)) --ks;                 // clusters of 1, 2, 4 or 8 blocks
+    const int need = (K + kTcMaxSplitK - 1) / kTcMaxSplitK;
+    if (ks < need) ks = need;
+    if (ks > C) ks = C;
+    if (ks < need || ks > kTcMaxSplit) return W4_ERR_UNSUPPORTED_SHAPE;
+    const int half = d.smem_per_sm / 2 - d.smem_reserved;
+    S = 4;
+    while (S > 2 && tc_smem(S, ks).total > half) --S;
+    if (tc_smem(S, ks).total > d.smem_optin) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (S * kTcStageBytes < ks * kTcRows * kTcTok * 4) return W4_ERR_UNSUPPORTED_SHAPE;   // partial sums fit the ring
+    return W4_OK;
+}
+
 w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx, int M,
                       int N, int K, float* y, bool pdl, cudaStream_t s, int n_out, int glu, const float* residual)
 {
@@ -297,19 +328,10 @@ w4_status run_gemv_tc(const void* w, const float* s_w, const float* bias, const 
     a.T = static_cast<int>(tiles(N));
     a.err = dev->err;
     const int G = (N + kTcRows - 1) / kTcRows;
-    int ks = (dev->sms + G - 1) / G;
-    if (ks > kTcMaxSplit) ks = kTcMaxSplit;
-    while (ks & (ks - 1)) --ks;                 // clusters of 1, 2, 4 or 8 blocks
-    const int need = (K + kTcMaxSplitK - 1) / kTcMaxSplitK;
-    if (ks < need) ks = need;
-    if (ks > a.C) ks = a.C;
-    if (ks < need || ks > kTcMaxSplit) return W4_ERR_UNSUPPORTED_SHAPE;
+    int ks = 0, S = 0;
+    st = tc_plan(*dev, N, K, ks, S);
+    if (st != W4_OK) return st;
     a.splits = ks;
-    const int half = dev->smem_per_sm / 2 - dev->smem_reserved;
-    int S = 4;
-    while (S > 2 && tc_smem(S, ks).total > half) --S;
-    if (tc_smem(S, ks).total > dev->smem_optin) return W4_ERR_UNSUPPORTED_SHAPE;
-    if (S * kTcStageBytes < ks * kTcRows * kTcTok * 4) return W4_ERR_UNSUPPORTED_SHAPE;   // partial sums fit the ring
     a.stages = S;
     return cuda_status(launch_gemv_w4_tc(a, G * ks, static_cast<size_t>(tc_smem(S, ks).total), pdl, s));
 }
@@ -423,6 +445,78 @@ const char* w4_status_str(w4_status st)
 }
 
 int w4_version(void) { return 1; }
+
+static_assert(W4_FMT_W4 == FMT_W4 && W4_FMT_Q4_0 == FMT_Q4_0 && W4_FMT_I8G32 == FMT_I8G32 &&
+                  W4_FMT_Q6G32 == FMT_Q6G32,
+              "public format codes");
+
+w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_desc* dev, w4_launch_plan* out)
+{
+    if (!dev || !out || fmt < FMT_W4 || fmt > FMT_Q6G32 ||
+        (what & ~(W4_PLAN_LINEAR | W4_PLAN_NORM | W4_PLAN_GLU)) != 0)
+        return W4_ERR_INVALID_ARG;
+    const bool linear = (what & W4_PLAN_LINEAR) != 0;
+    const bool norm = (what & W4_PLAN_NORM) != 0;
+    const bool glu = (what & W4_PLAN_GLU) != 0;
+    if ((norm && !linear) || (glu && fmt != FMT_W4 && fmt != FMT_Q4_0)) return W4_ERR_INVALID_ARG;
+    if (dev->sms <= 0 || dev->smem_per_sm <= 0 || dev->smem_reserved < 0 || dev->smem_optin <= 0)
+        return W4_ERR_INVALID_ARG;
+    w4_status st = check_mk(M, K);
+    if (st != W4_OK) return st;
+    if (N < 0) return W4_ERR_INVALID_ARG;
+    DeviceInfo d;
+    d.sms = dev->sms;
+    d.smem_per_sm = dev->smem_per_sm;
+    d.smem_reserved = dev->smem_reserved;
+    d.smem_optin = dev->smem_optin;
+    w4_launch_plan p = {};
+    p.k_splits = 1;
+    if (M > 0) {
+        const bool tc = use_tc(fmt, M, K);
+        if (linear && (N == 0 || tc || !fused_fits_on(d, fmt, M, K, norm))) p.quantize_launches = 1;
+        if (N > 0) {
+            if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
+            const int Nw = weight_rows(N, glu ? GLU_SILU : GLU_NONE);
+            if (tc) {
+                int ks = 0, S = 0;
+                st = tc_plan(d, Nw, K, ks, S);
+                if (st != W4_OK) return st;
+                p.path = W4_PATH_TENSOR_CORES;
+                p.grid = (Nw + kTcRows - 1) / kTcRows * ks;
+                p.threads = kTcThreads;
+                p.smem_bytes = tc_smem(S, ks).total;
+                p.stages = S;
+                p.k_splits = ks;
+            } else {
+                const int MT = round_pow2_tokens(M);
+                Plan q;
+                if (!plan_gemv(d, fmt, MT, linear && p.quantize_launches == 0, K, kAccWords / MT, q))
+                    return W4_ERR_UNSUPPORTED_SHAPE;
+                p.path = q.xmode == X_FUSED ? W4_PATH_FUSED : q.xmode == X_SMEM ? W4_PATH_CODES_SMEM
+                                                                                : W4_PATH_CODES_GLOBAL;
+                p.grid = gemv_grid(d, static_cast<int>(tiles(Nw)));
+                p.threads = kThreads;
+                p.smem_bytes = q.smem;
+                p.stages = q.stages;
+            }
+        }
+    }
+    *out = p;
+    return W4_OK;
+}
+
+w4_status w4_describe_device(w4_device_desc* out)
+{
+    if (!out) return W4_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    const w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    out->sms = dev->sms;
+    out->smem_per_sm = dev->smem_per_sm;
+    out->smem_reserved = dev->smem_reserved;
+    out->smem_optin = dev->smem_optin;
+    return W4_OK;
+}
 
 w4_status w4_set_tuning(int key, int value)
 {

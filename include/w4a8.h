@@ -115,6 +115,68 @@ w4_status w4_set_tuning(int key, int value);
 int w4_get_tuning(int key); /* current value, -1 for an unknown key */
 
 /* ------------------------------------------------------------------------
+ * Launch plan: what a GEMV or linear call launches on a device, computed on
+ * the host from a description of the device (no CUDA call, so it also runs
+ * without a GPU).  The launch path takes its decisions through the same
+ * functions, with the current tuning (w4_set_tuning).
+ *   fmt:  W4_FMT_W4, W4_FMT_Q4_0, W4_FMT_I8G32 or W4_FMT_Q6G32.
+ *   M, N, K: the call's shapes (N outputs; a gated call reads 2N weight rows).
+ *   what: 0 for the *_gemv call on int8 codes, or W4_PLAN_LINEAR for the
+ *         *_linear call on float x, with W4_PLAN_NORM (RMSNorm fused in, a
+ *         *_linear_fused option) and W4_PLAN_GLU (gated, W4 and Q4_0 only).
+ *   dev:  host; the device attributes of the same names (SM count, shared
+ *         memory per SM, shared memory per block reserved by the system,
+ *         opt-in maximum per block).  w4_describe_device fills it for the
+ *         current device.
+ *   out:  host; path (W4_PATH_*), quantize_launches (1 when a *_linear call
+ *         quantizes x in a kernel of its own first, else 0), and the GEMV
+ *         launch: grid, threads, smem_bytes (dynamic, per block), stages
+ *         (weight-ring depth), k_splits (tensor cores: K splits per 128-row
+ *         group, which form one thread-block cluster; 1 otherwise).
+ * Paths:
+ *   W4_PATH_NONE          nothing (M = 0, or N = 0 where only the quantizer
+ *                         of a *_linear call runs);
+ *   W4_PATH_FUSED         one DP4A GEMV launch with the activation quantizer
+ *                         (and the norm) in its prologue;
+ *   W4_PATH_CODES_SMEM    DP4A GEMV on int8 codes staged in shared memory;
+ *   W4_PATH_CODES_GLOBAL  DP4A GEMV reading the int8 codes from global memory;
+ *   W4_PATH_TENSOR_CORES  tensor-core GEMV on int8 codes (per-row INT4).
+ * Returns W4_ERR_INVALID_ARG for a null pointer, an unknown fmt or flag, a
+ * non-positive device field, W4_PLAN_NORM without W4_PLAN_LINEAR or a GLU on
+ * I8G32 / Q6G32, and otherwise the shape status the call would return.
+ * ------------------------------------------------------------------------ */
+#define W4_FMT_W4 0
+#define W4_FMT_Q4_0 1
+#define W4_FMT_I8G32 2
+#define W4_FMT_Q6G32 3
+#define W4_PLAN_LINEAR 1u
+#define W4_PLAN_NORM 2u
+#define W4_PLAN_GLU 4u
+#define W4_PATH_NONE 0
+#define W4_PATH_FUSED 1
+#define W4_PATH_CODES_SMEM 2
+#define W4_PATH_CODES_GLOBAL 3
+#define W4_PATH_TENSOR_CORES 4
+typedef struct {
+    int sms;
+    int smem_per_sm;
+    int smem_reserved;
+    int smem_optin;
+} w4_device_desc;
+typedef struct {
+    int path;
+    int quantize_launches;
+    int grid;
+    int threads;
+    int smem_bytes;
+    int stages;
+    int k_splits;
+} w4_launch_plan;
+w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_desc* dev, w4_launch_plan* out);
+/* The current device's description (W4_ERR_CUDA without a usable device). */
+w4_status w4_describe_device(w4_device_desc* out);
+
+/* ------------------------------------------------------------------------
  * Load time: quantize float weights (device kernels).
  * ------------------------------------------------------------------------ */
 

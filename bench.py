@@ -37,6 +37,8 @@ from bit_quantized_decode_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "W4A8 GEMV achieved HBM GB/s (% of GB300 peak); 7B decode-step linear ms"
 FALLBACK_PEAK_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0          # GB300 HBM3e, nominal (~8 TB/s)
+READ_PEAK_BYTES = 4 << 30         # the pure-read probe streams this many bytes per launch
 
 
 def parse_args(argv=None):
@@ -146,6 +148,44 @@ def measured_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_PEAK_GBS, "fallback"
+
+
+def read_peak(device, stream, reps: int = 10):
+    """Pure-read HBM bandwidth of this device, GB/s: the best of `reps`
+    launches of the library's read probe (w4_hbm_read) over a 4 GiB buffer,
+    timed with CUDA events on `stream`.  [310B-Gemma4] §4.1 bounds a weight
+    stream by the measured pure read bandwidth, which differs from a copy."""
+    import torch
+
+    from bit_quantized_decode_gb300 import _lib
+    buf = torch.empty(READ_PEAK_BYTES, dtype=torch.uint8, device=device)
+    sink = torch.zeros(1, dtype=torch.int32, device=device)
+    best = 0.0
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            _lib.hbm_read(buf, sink, stream)
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            _lib.hbm_read(buf, sink, stream)
+            e1.record(stream)
+            e1.synchronize()
+            best = max(best, READ_PEAK_BYTES / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del buf
+    return best
+
+
+def roofline_fracs(achieved: float, peak_copy: float, peak_read) -> dict:
+    """The achieved rate against the three denominators: the driver's measured
+    copy peak (read+write bytes), the pure-read peak measured in this run, and
+    the nominal HBM rate."""
+    out = {"frac": round(achieved / peak_copy, 4), "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+           "nominal": NOMINAL_HBM_GBS}
+    if peak_read:
+        out["peak_read"] = round(peak_read, 1)
+        out["frac_read"] = round(achieved / peak_read, 4)
+    return out
 
 
 def profiled_traffic(alg_bytes_per_launch: float, chain: bool):
@@ -261,6 +301,59 @@ def time_oracle(layer, M: int, min_seconds: float, row_fraction: float = 1.0):
         if dt >= min_seconds:
             break
     return nbytes * reps / dt / 1e9, dt, reps
+
+
+def oracle_gemv_baseline(lin, M: int, seconds: float = 1.5, seed: int = 3) -> dict:
+    """The oracle (single-threaded C) on a row slice of one decode linear of
+    the suite: N(0, sigma) weights drawn on the host and quantized by the
+    oracle in the linear's format, x ~ N(0, 1); the timed work is the whole
+    linear (activation quantization, integer GEMV, epilogue).  GB/s counts the
+    slice's algorithmic bytes.  A baseline only."""
+    import dataclasses
+
+    import oracle
+    g = wl.rng(seed)
+    n = min(lin.N, 256)
+    while True:
+        sl = dataclasses.replace(lin, shards=(n,))
+        W = wl.weights(g, n, lin.K, lin.sigma)
+        x = wl.activations(g, M, lin.K)
+        b = wl.bias(g, n) if lin.bias else None
+        if lin.fmt == "w4":
+            q, sw = oracle.quantize_rows_int4(W)
+            packed = oracle.pack_int4(q)
+
+            def run():
+                oracle.w4a8_linear(packed, sw, x, b)
+        elif lin.fmt == "q4_0":
+            blocks = oracle.quantize_q4_0(W)
+
+            def run():
+                qx, sx = oracle.quantize_act_int8(x)
+                oracle.gemv_q4_0(blocks, qx, sx, b)
+        else:                            # i8g32, and q6g32 (the same values and arithmetic)
+            qi, d = oracle.quantize_i8g32(W)
+
+            def run():
+                qx, sx = oracle.quantize_act_int8(x)
+                oracle.gemv_i8g32(qi, d, qx, sx, b)
+        t0 = time.perf_counter()
+        run()
+        dt = time.perf_counter() - t0
+        cap = min(lin.N, max(256, (1 << 25) // lin.K))     # at most ~32 M weights drawn on the host
+        if dt * 4 >= seconds or n >= cap:
+            break
+        n = min(cap, n * min(16, max(2, int(seconds / 4 / max(dt, 1e-6)))))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    gbs = algorithmic_bytes(sl, M) * reps / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "host_cpus": os.cpu_count(), "kind": "oracle",
+            "sample": f"rows 0..{n} of {lin.N} ({lin.fmt}, K={lin.K}), M={M}, {reps} passes in {dt:.2f} s"}
 
 
 def run_reference(args, rank, world):
@@ -656,12 +749,15 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         layer = oracle_layer_sample(M)
         gbs, dt, reps = time_oracle(layer, M, 10.0)
-        cpu_baseline = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        cpu_baseline = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "host_cpus": os.cpu_count(),
+                        "kind": "oracle",
                         "sample": (f"one Qwen2-7B layer (QKV, O, gate/up, down; N(0,0.02) weights drawn on the "
                                    f"host and quantized by the oracle), M={M}, single-threaded C oracle, "
                                    f"{reps} passes in {dt:.1f} s")}
 
     peak, peak_kind = measured_peak()
+    peak_rd = read_peak(dev, stream)
+    achieved = value / world
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -677,13 +773,14 @@ def run_ours(args, rank, world, local_rank):
                   "w8a32": "f32 (int8 weights, float activations)"}[args.weights],
         "data": "synthetic",
         "config": workload_config(args, world),
-        "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     **roofline_fracs(achieved, peak, peak_rd),
                      "traffic": profiled_traffic(bytes_per_step / launches, bool(chains)),
                      "peak_kind": peak_kind,
-                     "kernel": ("gemv_kernel<W4, M, fused, chain> (one launch per step: the whole linear set)"
+                     "peak_read_kind": "measured in this run: best of 10 w4_hbm_read launches over 4 GiB",
+                     "kernel": ("stream_linear_kernel<W4, M, fused, chain> (one launch per step: the whole linear set)"
                                 if chains else
-                                "gemv_kernel<W4, M, fused> (one launch per linear; bytes and time per launch "
+                                "stream_linear_kernel<W4, M, fused> (one launch per linear; bytes and time per launch "
                                 "averaged over the step)")},
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
@@ -730,7 +827,8 @@ def _timed_graph(fn, stream, steps: int, warmup: int) -> float:
     return e0.elapsed_time(e1) / steps
 
 
-def suite_gemv(wname: str, lin, M: int, device, stream, steps: int, warmup: int, peak: float) -> dict:
+def suite_gemv(wname: str, lin, M: int, device, stream, steps: int, warmup: int, peak: float,
+               peak_read=None) -> dict:
     """One decode linear timed on its own: back-to-back fused launches (PDL)
     rotating over enough distinct weight copies (>= 4, > 2.5x L2 in all)
     that L2 cannot serve the weights."""
@@ -770,7 +868,7 @@ def suite_gemv(wname: str, lin, M: int, device, stream, steps: int, warmup: int,
     del qls
     torch.cuda.synchronize()
     return {"suite": wname, "linear": lin.name, "fmt": lin.fmt, "N": lin.N, "K": lin.K, "M": M,
-            "us_per_gemv": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "us_per_gemv": round(us, 3), "GB/s": round(gbs, 1), **roofline_fracs(gbs, peak, peak_read),
             "bytes": b, "weight_copies": copies, "replays": reps}
 
 
@@ -793,13 +891,22 @@ def run_suite(args, local_rank):
     _lib.clear_device_error()
     peak, _ = measured_peak()
     stream = torch.cuda.Stream(device=dev)
+    peak_rd = read_peak(dev, stream)
+    print(json.dumps({"suite": "hbm_read_peak", "GB/s": round(peak_rd, 1), "bytes": READ_PEAK_BYTES,
+                      "copy_peak": peak, "nominal": NOMINAL_HBM_GBS}), flush=True)
+
+    def baseline(lin, M):
+        return None if args.no_cpu_baseline else oracle_gemv_baseline(lin, M)
+
     for wname in (() if args.suite_only_steps else ("w4a8_single", "qwen7b_layer", "gemma_q4_0", "lm_head")):
         lins = list(wl.workload(wname).linears)
         if wname == "lm_head":
             lins.append(wl.gemma_lm_head_q6g32())   # the same values packed in 6 bits
         for lin in lins:
             if suite_selected(args.suite_gemvs, wname, lin.name):
-                print(json.dumps(suite_gemv(wname, lin, 1, dev, stream, args.steps, args.warmup, peak)), flush=True)
+                line = suite_gemv(wname, lin, 1, dev, stream, args.steps, args.warmup, peak, peak_rd)
+                line["cpu_baseline"] = baseline(lin, 1)
+                print(json.dumps(line), flush=True)
     step_ms = [int(m) for m in args.suite_ms.split(",") if m]
     weights = build_weights(args, dev) if step_ms else None
     for kv in args.tune:
@@ -815,9 +922,16 @@ def run_suite(args, local_rank):
         ms = _timed_graph(step, stream, max(3, min(args.steps, 400)), args.warmup)
         b = sum(algorithmic_bytes(lin, M) for _, lin, *_ in items)
         gbs = b / (ms / 1e3) / 1e9
+        cpu = None
+        if not args.no_cpu_baseline:
+            layer = oracle_layer_sample(M, row_fraction=0.02)
+            cgbs, cdt, creps = time_oracle(layer, M, 2.0, row_fraction=0.02)
+            cpu = {"value": round(cgbs, 4), "unit": "GB/s", "cores": 1, "host_cpus": os.cpu_count(),
+                   "kind": "oracle", "sample": f"rows 0..0.02*N of each linear of one Qwen2-7B layer, M={M}, "
+                                               f"{creps} passes in {cdt:.2f} s"}
         print(json.dumps({"suite": "qwen7b_step", "M": M, "linears": len(items), "ms_per_step": round(ms, 5),
-                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "bytes": b,
-                          "ms_per_token": round(ms / M, 5)}), flush=True)
+                          "GB/s": round(gbs, 1), **roofline_fracs(gbs, peak, peak_rd), "bytes": b,
+                          "ms_per_token": round(ms / M, 5), "cpu_baseline": cpu}), flush=True)
         del items
     del weights
     # the decoder step: RMSNorm / SwiGLU / residual as separate kernels, then fused
@@ -834,8 +948,8 @@ def run_suite(args, local_rank):
             ms = _timed_graph(dstep, stream, max(3, min(args.steps, 400)), args.warmup)
             gbs = b / (ms / 1e3) / 1e9
             print(json.dumps({"suite": "qwen7b_decoder_step", "operators": mode, "M": M, "launches": len(ops),
-                              "ms_per_step": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                              "bytes": b}), flush=True)
+                              "ms_per_step": round(ms, 5), "GB/s": round(gbs, 1),
+                              **roofline_fracs(gbs, peak, peak_rd), "bytes": b}), flush=True)
             del ops
             torch.cuda.empty_cache()
     # [Orin-INT4] §"为什么 INT4 float 解包不快": the same step on the weight-only
@@ -855,7 +969,7 @@ def run_suite(args, local_rank):
             gbs = b / (ms / 1e3) / 1e9
             print(json.dumps({"suite": "qwen7b_step_ablation", "path": label, "M": M, "ms_per_step": round(ms, 5),
                               "steps_per_s": round(1e3 / ms, 1), "GB/s": round(gbs, 1),
-                              "frac": round(gbs / peak, 4), "bytes": b}), flush=True)
+                              **roofline_fracs(gbs, peak, peak_rd), "bytes": b}), flush=True)
             del items, weights
             torch.cuda.empty_cache()
     err = _lib.device_error()

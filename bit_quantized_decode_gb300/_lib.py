@@ -130,6 +130,12 @@ SIGNATURES["w4_chain_workspace_bytes"] = ([], _SZ)
 SIGNATURES["w4_chain_noalloc_scratch_bytes"] = ([], _SZ)
 SIGNATURES["w4a8_linear_chain_noalloc"] = ([ctypes.POINTER(LinearDesc), _I, _I, _P], _I)
 SIGNATURES["w4a8_linear_chain"] = ([ctypes.POINTER(LinearDesc), _I, _I, _P, _SZ, _P], _I)
+SIGNATURES["w4_workspace_bytes"] = ([_I, _I, _I], _SZ)
+SIGNATURES["w4_quantize_rows_host"] = ([_P, _I, _I, _P, _P], _I)
+SIGNATURES["q4_0_quantize_host"] = ([_P, _I, _I, _P], _I)
+SIGNATURES["i8g32_quantize_host"] = ([_P, _I, _I, _P, _P], _I)
+SIGNATURES["w4_last_device_error"] = ([ctypes.POINTER(ctypes.c_uint)], _I)
+SIGNATURES["w4_hbm_read"] = ([_P, _SZ, _P, _P], _I)
 W4_MAX_CHAIN = 128
 
 _lib = None
@@ -265,6 +271,51 @@ def i8g32_quantize(W, q, d, stream=None):
     _dev(W, q, d)
     N, K = W.shape
     _check("i8g32_quantize", load().i8g32_quantize(_ptr(W), N, K, _ptr(q), _ptr(d), _stream(stream)))
+
+
+# ------------------------------------------------- quantizers on the host
+def _host_arr(a, dtype):
+    """A C-contiguous numpy array of `dtype` (the host entry points take host memory)."""
+    import numpy as np
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags.c_contiguous:
+        raise ValueError(f"expected a C-contiguous numpy array of {np.dtype(dtype)}")
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def w4_quantize_rows_host(W):
+    """Host numpy float32 [N][K] -> (packed uint32 [N][K/8], s_w float32 [N]), by the library's host code."""
+    import numpy as np
+    N, K = W.shape
+    packed = np.zeros((N, K // 8), np.uint32)
+    sw = np.zeros(N, np.float32)
+    _check("w4_quantize_rows_host", load().w4_quantize_rows_host(_host_arr(W, np.float32), N, K,
+                                                                 _host_arr(packed, np.uint32), _host_arr(sw, np.float32)))
+    return packed, sw
+
+
+def q4_0_quantize_host(W):
+    """Host numpy float32 [N][K] -> Q4_0 blocks uint8 [N][K/32][18], by the library's host code."""
+    import numpy as np
+    N, K = W.shape
+    blocks = np.zeros((N, K // 32, 18), np.uint8)
+    _check("q4_0_quantize_host", load().q4_0_quantize_host(_host_arr(W, np.float32), N, K,
+                                                           _host_arr(blocks, np.uint8)))
+    return blocks
+
+
+def i8g32_quantize_host(W):
+    """Host numpy float32 [N][K] -> (q int8 [N][K], d fp16 bits uint16 [N][K/32]), by the library's host code."""
+    import numpy as np
+    N, K = W.shape
+    q = np.zeros((N, K), np.int8)
+    d = np.zeros((N, K // 32), np.uint16)
+    _check("i8g32_quantize_host", load().i8g32_quantize_host(_host_arr(W, np.float32), N, K, _host_arr(q, np.int8),
+                                                             _host_arr(d, np.uint16)))
+    return q, d
+
+
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4_workspace_bytes(M, N, K))
 
 
 # ---------------------------------------------------------------- repack
@@ -560,6 +611,23 @@ def device_error() -> int:
     if st not in (W4_OK, 5):
         raise W4Error("w4_device_error", st)
     return int(code.value)
+
+
+def last_device_error() -> int:
+    """w4_last_device_error: the same word as device_error()."""
+    code = ctypes.c_uint(0)
+    st = load().w4_last_device_error(ctypes.byref(code))
+    if st not in (W4_OK, 5):
+        raise W4Error("w4_last_device_error", st)
+    return int(code.value)
+
+
+def hbm_read(buf, sink, stream=None):
+    """Stream every byte of the device tensor `buf` once (w4_hbm_read); sink:
+    a device int32 [1] that receives the XOR of all 32-bit words."""
+    _dev(buf, sink)
+    _check("w4_hbm_read", load().w4_hbm_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                             _stream(stream)))
 
 
 def clear_device_error():

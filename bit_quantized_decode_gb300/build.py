@@ -31,7 +31,10 @@ NVCC_FLAGS = [
     "-I", INCLUDE,
 ]
 SOURCES = ["gemv_w4.cu", "gemv_q4_0.cu", "gemv_q6g32.cu", "gemv_i8g32.cu", "gemv_a32.cu", "w4a8_api.cu",
-           "prep_kernels.cu", "gemv_tc.cu"]
+           "prep_kernels.cu", "gemv_tc.cu", "hbm_read.cu", "host_quant.cpp"]
+# host-only C++ (the host quantizers): IEEE arithmetic as written, no FMA contraction
+HOST_FLAGS = ["-O2", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
+              "-Xcompiler", "-fno-fast-math", "-I", INCLUDE]
 
 
 def nvcc() -> str:
@@ -45,15 +48,15 @@ def _inputs_digest() -> str:
     h = hashlib.sha256()
     for d in (CSRC, INCLUDE):
         for name in sorted(os.listdir(d)):
-            if name.endswith((".cu", ".cuh", ".h")):
+            if name.endswith((".cu", ".cuh", ".h", ".cpp")):
                 with open(os.path.join(d, name), "rb") as f:
                     h.update(name.encode())
                     h.update(f.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(" ".join(NVCC_FLAGS + HOST_FLAGS).encode())
     return h.hexdigest()
 
 
-# Sources that define the one-token decode GEMV (gemv_kernel<W4, 1, fused>):
+# Sources that define the one-token decode GEMV (stream_linear_kernel<W4, 1, fused>):
 # a profile summary taken on them stays valid while they are unchanged.
 GEMV_W4_SOURCES = ("gemv_kernel.cuh", "quant_a8.cuh", "fusion.cuh", "ptx.cuh", "internal.h", "gemv_w4.cu")
 
@@ -82,7 +85,8 @@ def up_to_date() -> bool:
 
 def _compile(src: str, log: list) -> str:
     obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    flags = HOST_FLAGS if src.endswith(".cpp") else NVCC_FLAGS
+    cmd = [nvcc(), *flags, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     log.append((src, r.stdout + r.stderr))
     if r.returncode != 0:

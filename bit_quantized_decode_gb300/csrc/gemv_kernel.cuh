@@ -417,7 +417,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned* count, unsigned target
 // has written the outputs of linear i, while each warp's ring keeps streaming
 // the next linear's weights across that barrier.
 template <int FMT, int MT, int XM, int NCH>
-__global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ ChainParams<NCH> P)
+__global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kernel(const __grid_constant__ ChainParams<NCH> P)
 {
     using Acc = typename std::conditional<FMT == FMT_W4, int, float>::type;
     constexpr int kUnit = fmt_unit_bytes(FMT);
@@ -1104,16 +1104,10 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) gemv_kernel(const 
 template <int FMT, int MT, int XM, int NCH>
 cudaError_t launch_gemv_t(const ChainParams<NCH>& p, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-    auto kern = gemv_kernel<FMT, MT, XM, NCH>;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    auto kern = stream_linear_kernel<FMT, MT, XM, NCH>;
+    static SmemLimit limit;
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), limit, smem);
     if (e != cudaSuccess) return e;
-    static int configured[64] = {0};
-    if (dev < 64 && configured[dev] < static_cast<int>(smem)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured[dev] = static_cast<int>(smem);
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);

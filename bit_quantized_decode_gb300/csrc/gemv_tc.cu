@@ -96,7 +96,7 @@ __device__ __forceinline__ void tc_split4(uint32_t c, uint32_t& hi, uint32_t& lo
     hi = m | (bm & 0x80808080u);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_constant__ TcArgs A)
+__global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_constant__ TcArgs A)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
@@ -508,16 +508,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) gemv_w4_tc_kernel(const __grid_
 
 cudaError_t launch_gemv_w4_tc(const TcArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-    auto kern = gemv_w4_tc_kernel;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    auto kern = tc_linear_kernel;
+    static SmemLimit limit;
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), limit, smem);
     if (e != cudaSuccess) return e;
-    static int configured[64] = {0};
-    if (dev < 64 && configured[dev] < static_cast<int>(smem)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured[dev] = static_cast<int>(smem);
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kTcThreads);

@@ -1,5 +1,6 @@
 // Declarations shared by the host API and the kernel translation units.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -127,6 +128,15 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, in
 constexpr unsigned kErrWaitTimeout = 0x57414954u;     // "WAIT": an mbarrier wait ran out
 constexpr unsigned kErrBarrierTimeout = 0x42415252u;  // "BARR": a grid barrier wait ran out
 
+// Dynamic shared-memory limit set so far for one kernel, per device.
+// raise_smem_limit (w4a8_api.cu) raises it under a lock, so host threads
+// launching the same kernel concurrently never lower another's setting.
+constexpr int kMaxDevices = 64;
+struct SmemLimit {
+    std::atomic<int> bytes[kMaxDevices];
+};
+cudaError_t raise_smem_limit(const void* kern, SmemLimit& rec, size_t smem);
+
 // Kernel launchers, one translation unit per format.
 cudaError_t launch_gemv_w4(const ChainParams<1>& p, int MT, int xmode, int grid, size_t smem, bool pdl,
                            cudaStream_t s);
@@ -200,6 +210,11 @@ __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
 }
 
 cudaError_t launch_gemv_w4_tc(const TcArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s);
+
+// Pure-read bandwidth probe (hbm_read.cu): one block per SM streams `bytes`
+// bytes once and XORs every 32-bit word into *sink (cleared first).
+cudaError_t launch_hbm_read(const void* buf, unsigned long long bytes, unsigned* sink, unsigned* err, int sms,
+                            cudaStream_t s);
 
 // Load-time and activation kernels (prep_kernels.cu).
 constexpr int kMaxShards = 8;

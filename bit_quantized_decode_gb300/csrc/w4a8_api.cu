@@ -3,8 +3,10 @@
 // memory or synchronises, except the two device-error-word calls.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/w4a8.h"
 #include "internal.h"
@@ -16,8 +18,6 @@ __device__ unsigned g_w4_error_word;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
     int sms = 0;
     int smem_optin = 0;       // largest dynamic shared memory one block may use
@@ -27,6 +27,10 @@ struct DeviceInfo {
     bool ready = false;
 };
 DeviceInfo g_dev[kMaxDevices];
+// Guards the one-time set-up of g_dev (and of the no-alloc scratch address):
+// host threads may call the library concurrently, each on its own stream.
+std::mutex g_setup_mutex;
+std::atomic<bool> g_dev_ready[kMaxDevices];
 
 // Launch tuning set by w4_set_tuning (0 = automatic).
 int g_tune[4] = {0, 0, 0, 0};
@@ -36,7 +40,12 @@ w4_status device_info(DeviceInfo** out)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W4_ERR_CUDA;
     DeviceInfo& d = g_dev[dev];
-    if (!d.ready) {
+    if (!g_dev_ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        if (g_dev_ready[dev].load(std::memory_order_relaxed)) {
+            *out = &d;
+            return W4_OK;
+        }
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return W4_ERR_CUDA;
         if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return W4_ERR_CUDA;
@@ -48,10 +57,32 @@ w4_status device_info(DeviceInfo** out)
         if (cudaGetSymbolAddress(&p, g_w4_error_word) != cudaSuccess) return W4_ERR_CUDA;
         d.err = static_cast<unsigned*>(p);
         d.ready = true;
+        g_dev_ready[dev].store(true, std::memory_order_release);
     }
     *out = &d;
     return W4_OK;
 }
+
+}  // namespace
+
+namespace w4k {
+cudaError_t raise_smem_limit(const void* kern, SmemLimit& rec, size_t smem)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const int want = static_cast<int>(smem);
+    if (rec.bytes[dev].load(std::memory_order_acquire) >= want) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (rec.bytes[dev].load(std::memory_order_relaxed) >= want) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e == cudaSuccess) rec.bytes[dev].store(want, std::memory_order_release);
+    return e;
+}
+}  // namespace w4k
+
+namespace {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -189,7 +220,9 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
     w4_status st = device_info(&dev);
     if (st != W4_OK) return st;
     const int MT = round_pow2_tokens(M);
-    static ChainParams<kMaxChain> cp;     // host staging only; copied into the launch
+    // host staging only, copied into the launch; one per host thread, so
+    // threads launching chains on their own streams do not share it
+    thread_local ChainParams<kMaxChain> cp;
     std::memset(&cp, 0, sizeof(cp));
     int kmax = 32;
     for (int i = 0; i < n; ++i) {
@@ -954,18 +987,31 @@ w4_status w8a32_gemv(const void* w, const float* s_w, const float* bias, const f
     return a32_common(FMT_W8F, w, s_w, bias, x, M, N, K, y, flags, reinterpret_cast<cudaStream_t>(s));
 }
 
+// The single-linear calls keep nothing between launches: K is never split
+// across blocks through global memory, so no call needs a workspace.
+size_t w4_workspace_bytes(int M, int N, int K)
+{
+    (void)M;
+    (void)N;
+    (void)K;
+    return 0;
+}
+
 // ----------------------------------------------------------------- chains
 size_t w4_chain_workspace_bytes(void) { return 256; }
 
-w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* workspace, size_t ws_bytes,
-                            w4_stream_t s)
+namespace {
+// Checks of a chain's descriptors shared by both chain entry points; W4_OK
+// with nothing to launch sets *empty.
+w4_status check_chain(const w4_linear_desc* descs, int n, int M, bool* empty)
 {
+    *empty = false;
     if (n < 0 || M < 0 || (n > 0 && descs == nullptr)) return W4_ERR_INVALID_ARG;
     if (n > W4_MAX_CHAIN || M > W4_MAX_M) return W4_ERR_UNSUPPORTED_SHAPE;
-    if (n == 0 || M == 0) return W4_OK;
-    if (workspace == nullptr) return W4_ERR_INVALID_ARG;
-    if (ws_bytes < w4_chain_workspace_bytes()) return W4_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(workspace, 16)) return W4_ERR_MISALIGNED;
+    if (n == 0 || M == 0) {
+        *empty = true;
+        return W4_OK;
+    }
     for (int i = 0; i < n; ++i) {
         const w4_linear_desc& d = descs[i];
         w4_status st = check_mk(M, d.K);
@@ -976,6 +1022,19 @@ w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* wor
             (d.bias && !aligned(d.bias, 4)) || (d.qx && !aligned(d.qx, 16)) || (d.sx && !aligned(d.sx, 4)))
             return W4_ERR_MISALIGNED;
     }
+    return W4_OK;
+}
+}  // namespace
+
+w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* workspace, size_t ws_bytes,
+                            w4_stream_t s)
+{
+    bool empty = false;
+    w4_status st = check_chain(descs, n, M, &empty);
+    if (st != W4_OK || empty) return st;
+    if (workspace == nullptr) return W4_ERR_INVALID_ARG;
+    if (ws_bytes < w4_chain_workspace_bytes()) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(workspace, 16)) return W4_ERR_MISALIGNED;
     return run_chain(descs, n, M, static_cast<unsigned*>(workspace), reinterpret_cast<cudaStream_t>(s));
 }
 
@@ -988,19 +1047,27 @@ constexpr size_t kChainScratchBytes = 256;
 static __device__ __align__(256) unsigned char g_chain_scratch[kChainScratchBytes];
 
 namespace {
-unsigned* g_chain_scratch_ptr[kMaxDevices] = {nullptr};
+// Device address of the scratch array per device, looked up once.  The
+// look-up runs under the set-up lock, so threads calling at once for the
+// first time store the same address once.
+std::atomic<unsigned*> g_chain_scratch_ptr[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once per device.
 w4_status chain_scratch(unsigned** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W4_ERR_CUDA;
-    if (g_chain_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_chain_scratch) != cudaSuccess || p == nullptr) return W4_ERR_CUDA;
-        g_chain_scratch_ptr[dev] = static_cast<unsigned*>(p);
+    unsigned* p = g_chain_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        p = g_chain_scratch_ptr[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            void* a = nullptr;
+            if (cudaGetSymbolAddress(&a, g_chain_scratch) != cudaSuccess || a == nullptr) return W4_ERR_CUDA;
+            p = static_cast<unsigned*>(a);
+            g_chain_scratch_ptr[dev].store(p, std::memory_order_release);
+        }
     }
-    *out = g_chain_scratch_ptr[dev];
+    *out = p;
     return W4_OK;
 }
 }  // namespace
@@ -1010,16 +1077,17 @@ size_t w4_chain_noalloc_scratch_bytes(void) { return kChainScratchBytes; }
 w4_status w4a8_linear_chain_noalloc(const w4_linear_desc* descs, int n, int M, w4_stream_t s)
 {
     if (w4_chain_workspace_bytes() > kChainScratchBytes) return W4_ERR_UNSUPPORTED_SHAPE;
-    if (n < 0 || M < 0 || (n > 0 && descs == nullptr)) return W4_ERR_INVALID_ARG;
-    if (n > W4_MAX_CHAIN || M > W4_MAX_M) return W4_ERR_UNSUPPORTED_SHAPE;
-    if (n == 0 || M == 0) return W4_OK;
+    // every check first: a call that fails them enqueues nothing, not even the clear below
+    bool empty = false;
+    w4_status st = check_chain(descs, n, M, &empty);
+    if (st != W4_OK || empty) return st;
     unsigned* scratch = nullptr;
-    w4_status st = chain_scratch(&scratch);
+    st = chain_scratch(&scratch);
     if (st != W4_OK) return st;
     // the array keeps the previous call's contents: the barrier count must start at zero
     if (cudaMemsetAsync(scratch, 0, w4_chain_workspace_bytes(), reinterpret_cast<cudaStream_t>(s)) != cudaSuccess)
         return W4_ERR_CUDA;
-    return w4a8_linear_chain(descs, n, M, scratch, kChainScratchBytes, s);
+    return run_chain(descs, n, M, scratch, reinterpret_cast<cudaStream_t>(s));
 }
 
 // ------------------------------------------------------ device error word
@@ -1034,6 +1102,20 @@ w4_status w4_device_error(unsigned* code)
     if (cudaMemcpy(&v, dev->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return W4_ERR_CUDA;
     *code = v;
     return v ? W4_ERR_DEVICE_TIMEOUT : W4_OK;
+}
+
+w4_status w4_last_device_error(unsigned* code) { return w4_device_error(code); }
+
+// ------------------------------------------------------ pure-read probe
+w4_status w4_hbm_read(const void* buf, size_t bytes, unsigned* sink, w4_stream_t s)
+{
+    if (!sink || (bytes > 0 && !buf)) return W4_ERR_INVALID_ARG;
+    if (bytes % 16 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(sink, 4) || (buf && !aligned(buf, 16))) return W4_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    const w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    return cuda_status(launch_hbm_read(buf, bytes, sink, dev->err, dev->sms, reinterpret_cast<cudaStream_t>(s)));
 }
 
 w4_status w4_clear_device_error(void)

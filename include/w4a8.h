@@ -196,6 +196,20 @@ w4_status q4_0_quantize(const float* W, int N, int K, uint8_t* blocks, w4_stream
 w4_status i8g32_quantize(const float* W, int N, int K, int8_t* q, uint16_t* d, w4_stream_t s);
 
 /* ------------------------------------------------------------------------
+ * Load time on the host: the same three quantizers as plain C++ over host
+ * memory, for loaders that hold float weights on the host.  Outputs are
+ * bit-identical to the device calls above (IEEE fp32 division,
+ * round-half-to-even to an integer, fp16 round-to-nearest-even).  All
+ * pointers are HOST pointers (no alignment rule); the call is synchronous,
+ * makes no CUDA call and keeps no state, so it is safe from any thread.
+ * Same shapes and checks as the device calls: N >= 0, K > 0, and K % 8 == 0
+ * (w4_quantize_rows_host) or K % 32 == 0 (the group formats).
+ * ------------------------------------------------------------------------ */
+w4_status w4_quantize_rows_host(const float* W, int N, int K, uint32_t* packed, float* s_w);
+w4_status q4_0_quantize_host(const float* W, int N, int K, uint8_t* blocks);
+w4_status i8g32_quantize_host(const float* W, int N, int K, int8_t* q, uint16_t* d);
+
+/* ------------------------------------------------------------------------
  * Load time: repack canonical weights into the device layout, fusing shards.
  * [310B-Gemma4] §3.1 (load-time reorder; q/k/v and gate/up concatenated by
  * rows into one matrix, one repack, one matmul per token).
@@ -267,6 +281,11 @@ w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_st
  * ------------------------------------------------------------------------ */
 w4_status w4a8_gemv(const void* w, const float* s_w, const float* bias, const int8_t* qx, const float* sx,
                     int M, int N, int K, float* y, w4_stream_t s);
+/* Device scratch a GEMV or linear call of this shape needs from its caller:
+ * always 0.  Where K is split over several blocks (W4_PATH_* plans with
+ * k_splits > 1) the partial sums merge on chip, in the shared memory of one
+ * thread-block cluster, so no call takes a workspace. */
+size_t w4_workspace_bytes(int M, int N, int K);
 w4_status q4_0_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx,
                     int M, int N, int K, float* y, w4_stream_t s);
 w4_status i8g32_gemv(const void* w, const float* bias, const int8_t* qx, const float* sx,
@@ -397,6 +416,8 @@ w4_status w8a32_gemv(const void* w, const float* s_w, const float* bias, const f
  * zero-filled before its first use; each call leaves it zero again, ready for
  * the next.  Calls that share a workspace must not overlap on the GPU.  After
  * a call that reported W4_ERR_DEVICE_TIMEOUT, zero the workspace again.
+ * Host threads may call the chain entry points at the same time, each with
+ * its own workspace and stream: the launch parameters are staged per thread. 
  * ------------------------------------------------------------------------ */
 #define W4_MAX_CHAIN 128
 typedef struct {
@@ -434,7 +455,9 @@ w4_status w4a8_linear_chain(const w4_linear_desc* descs, int n, int M, void* wor
  *     streams, other threads) race on it and must be serialised by the caller.
  *   - A workspace need above the array's size is rejected with
  *     W4_ERR_UNSUPPORTED_SHAPE; all other arguments are checked as in
- *     w4a8_linear_chain.
+ *     w4a8_linear_chain, before anything is enqueued: a call that fails a
+ *     check does not touch the array (no clear), so it cannot disturb a
+ *     chain already in flight.
  * ------------------------------------------------------------------------ */
 size_t w4_chain_noalloc_scratch_bytes(void);
 w4_status w4a8_linear_chain_noalloc(const w4_linear_desc* descs, int n, int M, w4_stream_t s);
@@ -447,7 +470,20 @@ w4_status w4a8_linear_chain_noalloc(const w4_linear_desc* descs, int n, int M, w
  * nonzero, else W4_OK.  w4_clear_device_error zeroes it (synchronous).
  * ------------------------------------------------------------------------ */
 w4_status w4_device_error(unsigned* code);
+w4_status w4_last_device_error(unsigned* code); /* the same call under a second name */
 w4_status w4_clear_device_error(void);
+
+/* ------------------------------------------------------------------------
+ * Pure-read HBM bandwidth probe: the roofline denominator for a kernel that
+ * only reads.  [310B-Gemma4] §4.1 measures the device's pure read bandwidth
+ * (distinct from a read+write copy) as the bound of a weight-streaming decode;
+ * this is the same measurement on this device.  The kernel streams `bytes`
+ * bytes of `buf` (16-byte aligned; bytes a multiple of 16) once through the
+ * same per-warp bulk-copy rings as the GEMVs (one block per SM, evict-first)
+ * and writes the XOR of all its 32-bit words to *sink (device, 4 bytes), so
+ * that no read is dead.  bytes = 0 writes 0.  Time it with events on `s`.
+ * ------------------------------------------------------------------------ */
+w4_status w4_hbm_read(const void* buf, size_t bytes, unsigned* sink, w4_stream_t s);
 
 #ifdef __cplusplus
 }

@@ -216,3 +216,47 @@ def test_fusion_and_weight_only_argument_checks(lib):
     assert lib.w8_repacked_bytes(13, 64) == 16 * 64
     assert lib.w8_quantize_rows(FAKE, 4, 6, FAKE, FAKE, None) == 2
     assert lib.w8_quantize_rows(ODD, 4, 64, FAKE, FAKE, None) == 3
+
+
+def test_noalloc_chain_checks_run_before_any_device_work(lib):
+    """A bad descriptor is rejected before the scratch is looked up or
+    cleared: without a GPU a CUDA call would fail with W4_ERR_CUDA (4), so
+    the argument statuses here show that nothing reached the device."""
+    from bit_quantized_decode_gb300 import _lib
+    d = (_lib.LinearDesc * 2)()
+    for i in range(2):
+        d[i] = _lib.LinearDesc(0x1000, 0x1000, None, 0x1000, 0x1000, None, None, 8, 64)
+    assert lib.w4a8_linear_chain_noalloc(d, 0, 1, None) == 0                   # empty chain
+    assert lib.w4a8_linear_chain_noalloc(d, 129, 1, None) == 2
+    d[1] = _lib.LinearDesc(0x1000, 0x1000, None, 0x1000, 0x1000, None, None, 8, 48)
+    assert lib.w4a8_linear_chain_noalloc(d, 2, 1, None) == 2                   # K % 32 != 0
+    d[1] = _lib.LinearDesc(0x1000, None, None, 0x1000, 0x1000, None, None, 8, 64)
+    assert lib.w4a8_linear_chain_noalloc(d, 2, 1, None) == 1                   # no s_w
+    d[1] = _lib.LinearDesc(0x1004, 0x1000, None, 0x1000, 0x1000, None, None, 8, 64)
+    assert lib.w4a8_linear_chain_noalloc(d, 2, 1, None) == 3                   # misaligned weights
+
+
+def test_workspace_query_and_error_word_alias(lib):
+    for M, N, K in ((1, 512, 3584), (16, 152064, 3584), (4, 8, 32)):
+        assert lib.w4_workspace_bytes(M, N, K) == 0
+    assert hasattr(lib, "w4_last_device_error")
+    assert lib.w4_last_device_error(None) == 1          # null output pointer, checked before any device call
+
+
+def test_hbm_read_argument_checks(lib):
+    assert lib.w4_hbm_read(FAKE, 1 << 20, None, None) == 1     # no sink
+    assert lib.w4_hbm_read(None, 64, FAKE, None) == 1          # no buffer
+    assert lib.w4_hbm_read(FAKE, 40, FAKE, None) == 2          # not a multiple of 16 bytes
+    assert lib.w4_hbm_read(ODD, 64, FAKE, None) == 3
+    assert lib.w4_hbm_read(FAKE, 64, ctypes.c_void_p(0x1002), None) == 3
+
+
+def test_host_quantizer_argument_checks(lib):
+    assert lib.w4_quantize_rows_host(FAKE, 4, 12, FAKE, FAKE) == 2
+    assert lib.w4_quantize_rows_host(FAKE, -1, 64, FAKE, FAKE) == 1
+    assert lib.w4_quantize_rows_host(None, 4, 64, FAKE, FAKE) == 1
+    assert lib.w4_quantize_rows_host(None, 0, 64, None, None) == 0
+    assert lib.q4_0_quantize_host(FAKE, 4, 48, FAKE) == 2
+    assert lib.q4_0_quantize_host(FAKE, 4, 64, None) == 1
+    assert lib.i8g32_quantize_host(FAKE, 4, 0, FAKE, FAKE) == 1
+    assert lib.i8g32_quantize_host(FAKE, 4, 64, FAKE, None) == 1

@@ -31,7 +31,7 @@ NVCC_FLAGS = [
     "-I", INCLUDE,
 ]
 SOURCES = ["gemv_w4.cu", "gemv_q4_0.cu", "gemv_q6g32.cu", "gemv_i8g32.cu", "gemv_a32.cu", "w4a8_api.cu",
-           "prep_kernels.cu", "gemv_tc.cu", "hbm_read.cu", "host_quant.cpp"]
+           "prep_kernels.cu", "gemv_tc.cu", "gemv_chain.cu", "hbm_read.cu", "host_quant.cpp"]
 # host-only C++ (the host quantizers): IEEE arithmetic as written, no FMA contraction
 HOST_FLAGS = ["-O2", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
               "-Xcompiler", "-fno-fast-math", "-I", INCLUDE]

@@ -89,6 +89,23 @@ __device__ __forceinline__ void unit4(const uint4 w, const uint4 x0, const uint4
     A = dp4a_us(w.w & 0xF0F0F0F0u, x1.w, A);
 }
 
+// unit4 accumulated in place: B += sum n x (low nibbles), A += sum 16 n x
+// (high nibbles), each a chain of four DP4A through its accumulator, so a
+// line costs no separate adds; the row's sum n x is B + (A >> 4), formed once
+// per tile (A stays a multiple of 16 and, over a row of K weights, within
+// 16 * 15 * 127 * K / 2 < 2^31 for K <= 131072).
+__device__ __forceinline__ void unit4_acc(const uint4 w, const uint4 x0, const uint4 x1, int& B, int& A)
+{
+    B = dp4a_us(w.x & 0x0F0F0F0Fu, x0.x, B);
+    A = dp4a_us(w.x & 0xF0F0F0F0u, x0.y, A);
+    B = dp4a_us(w.y & 0x0F0F0F0Fu, x0.z, B);
+    A = dp4a_us(w.y & 0xF0F0F0F0u, x0.w, A);
+    B = dp4a_us(w.z & 0x0F0F0F0Fu, x1.x, B);
+    A = dp4a_us(w.z & 0xF0F0F0F0u, x1.y, A);
+    B = dp4a_us(w.w & 0x0F0F0F0Fu, x1.z, B);
+    A = dp4a_us(w.w & 0xF0F0F0F0u, x1.w, A);
+}
+
 // Signed 4-bit units (Q4_0): 16 * sum q x over one 16-byte unit.
 __device__ __forceinline__ int unit4_signed16(const uint4 w, const uint4 x0, const uint4 x1)
 {
@@ -124,10 +141,23 @@ __device__ __forceinline__ uint64_t fma4(uint64_t q01, uint64_t q23, const float
     return f2_fma(q23, f2_pack(x.z, x.w), acc2);
 }
 
+// Barrier of the kThreads threads that run a linear's prologue and
+// epilogue: the whole block (kBar = 0), or named barrier kBar when the block
+// has further warps (a weight-producer warp) that stay out of it.
+template <int kBar, int NT = kThreads>
+__device__ __forceinline__ void block_sync()
+{
+    if constexpr (kBar == 0) {
+        __syncthreads();
+    } else {
+        named_sync(kBar, NT);
+    }
+}
+
 // Fused prologue for large M*K: a first pass over x for the absmax, a second
 // to quantize, each in batches of 16 float4 per thread spread over the
 // tokens (all loads of a batch in flight at once).  One block barrier.
-template <int MT, bool kCodeSums>
+template <int MT, bool kCodeSums, int kBar = 0, int NT = kThreads>
 __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float* red_s, float* sx_s, int8_t* xs,
                                                        int (&tsum)[MT])
 {
@@ -141,14 +171,14 @@ __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float*
     float mx[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) mx[m] = 0.0f;
-    for (int i0 = 0; i0 < K4; i0 += kB * kThreads) {
+    for (int i0 = 0; i0 < K4; i0 += kB * NT) {
         float4 v[MT][kB];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
 #pragma unroll
             for (int u = 0; u < kB; ++u) {
-                const int i = i0 + u * kThreads + tid;
+                const int i = i0 + u * NT + tid;
                 v[m][u] = (m < M && i < K4) ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
@@ -165,27 +195,27 @@ __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float*
         for (int off = 16; off > 0; off >>= 1) mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], off));
         if (lane == 0) red_s[warp * MT + m] = mx[m];
     }
-    __syncthreads();
+    block_sync<kBar, NT>();
     A8Scale ks[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         float amax = red_s[m];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
+        for (int w = 1; w < (NT / 32); ++w) amax = fmaxf(amax, red_s[w * MT + m]);
         ks[m] = a8_scale(m < M ? amax : 0.0f);
         if (tid == m) {
             sx_s[m] = m < M ? ks[m].s : 0.0f;
             if (m < M && blockIdx.x == 0 && a.sx_out != nullptr) a.sx_out[m] = ks[m].s;
         }
     }
-    for (int i0 = 0; i0 < K4; i0 += kB * kThreads) {
+    for (int i0 = 0; i0 < K4; i0 += kB * NT) {
         float4 v[MT][kB];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
 #pragma unroll
             for (int u = 0; u < kB; ++u) {
-                const int i = i0 + u * kThreads + tid;
+                const int i = i0 + u * NT + tid;
                 v[m][u] = (m < M && i < K4) ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
@@ -200,7 +230,7 @@ __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float*
                 const uint64_t rr = f2_pack(ks[m].r, ks[m].r);
 #pragma unroll
                 for (int u = 0; u < kB; ++u) {
-                    const int i = i0 + u * kThreads + tid;
+                    const int i = i0 + u * NT + tid;
                     if (i < K4) {
                         uint32_t ok = 0xffffffffu;
                         uint32_t q = a8_pack4_fast2(v[m][u], rr, ok);
@@ -226,9 +256,9 @@ __device__ __forceinline__ void fused_prologue_twopass(const GemvArgs& a, float*
 // does not depend on the previous kernel: it is loaded first and the
 // dependency wait (griddepcontrol.wait) is taken here, after those loads are
 // in flight and before x is read.  Each token's compensated sum of squares is
-// reduced over the block through nrm_s (2 kWarps MT floats, free until the
+// reduced over the block through nrm_s (2 * (NT / 32) * MT floats, free until the
 // first merge), then x is normalized in registers.  One more block barrier.
-template <int MT, int NIT, bool kCodeSums, bool kNorm = false>
+template <int MT, int NIT, bool kCodeSums, bool kNorm = false, int kBar = 0, int NT = kThreads>
 __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, float* red_s, float* sx_s,
                                                     int8_t* xs, int (&tsum)[MT], float* nrm_s = nullptr)
 {
@@ -243,7 +273,7 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
         const float4* gr = reinterpret_cast<const float4*>(a.gamma);
 #pragma unroll
         for (int it = 0; it < NIT; ++it) {
-            const int i = tid + it * kThreads;
+            const int i = tid + it * NT;
             gv[it] = (it < nit && i < K4) ? __ldg(gr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         pdl_wait();
@@ -254,7 +284,7 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
         const float4* xr = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(m) * K);
 #pragma unroll
         for (int it = 0; it < NIT; ++it) {
-            const int i = tid + it * kThreads;
+            const int i = tid + it * NT;
             v[m][it] = (m < M && it < nit && i < K4) ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
@@ -270,12 +300,12 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
                 nrm_s[(warp * MT + m) * 2 + 1] = lo;
             }
         }
-        __syncthreads();
+        block_sync<kBar, NT>();
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             float hi = nrm_s[m * 2], lo = nrm_s[m * 2 + 1];
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) pair_merge(hi, lo, nrm_s[(w * MT + m) * 2], nrm_s[(w * MT + m) * 2 + 1]);
+            for (int w = 1; w < (NT / 32); ++w) pair_merge(hi, lo, nrm_s[(w * MT + m) * 2], nrm_s[(w * MT + m) * 2 + 1]);
             const float r = rms_scale(hi, lo, K, a.eps);
 #pragma unroll
             for (int it = 0; it < NIT; ++it) v[m][it] = rms_apply(v[m][it], r, gv[it]);
@@ -291,13 +321,13 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         if (lane == 0) red_s[warp * MT + m] = mx;
     }
-    __syncthreads();
+    block_sync<kBar, NT>();
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         if (m < M) {
             float amax = red_s[m];
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red_s[w * MT + m]);
+            for (int w = 1; w < (NT / 32); ++w) amax = fmaxf(amax, red_s[w * MT + m]);
             const A8Scale ks = a8_scale(amax);
             if (tid == m) {
                 sx_s[m] = ks.s;
@@ -332,7 +362,7 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
 #pragma unroll
                 for (int u = 0; u < kG; ++u) {
                     const int it = g0 + u;
-                    const int i = tid + it * kThreads;
+                    const int i = tid + it * NT;
                     if (it < NIT && it < nit && i < K4) {
                         dst[i] = qw[u];
                         if (gout) gout[i] = qw[u];
@@ -356,18 +386,19 @@ struct BlockRange {
 template <int RT>
 __device__ __forceinline__ BlockRange block_range(const GemvArgs& a)
 {
-    const int b = static_cast<int>(blockIdx.x);
+    int b = static_cast<int>(blockIdx.x) + a.rot;
+    if (b >= static_cast<int>(gridDim.x)) b -= static_cast<int>(gridDim.x);
     const int n = a.tq + (b < a.tr ? 1 : 0);
     return BlockRange{b * a.tq + min(b, a.tr), n, (n + RT - 1) / RT};
 }
 
 // Warp w's line range [lo, hi) within a round of nt tiles of C lines: an even
 // split, boundaries rounded down to whole 16-line passes.
-__device__ __forceinline__ void warp_lines(int warp, int nt, int C, int& lo, int& hi)
+__device__ __forceinline__ void warp_lines(int warp, int nt, int C, int& lo, int& hi, int nw = kWarps)
 {
     const long long nL = static_cast<long long>(nt) * C;
-    lo = static_cast<int>((warp * nL / kWarps) & ~15LL);
-    hi = warp == kWarps - 1 ? static_cast<int>(nL) : static_cast<int>(((warp + 1) * nL / kWarps) & ~15LL);
+    lo = static_cast<int>((warp * nL / nw) & ~15LL);
+    hi = warp == nw - 1 ? static_cast<int>(nL) : static_cast<int>(((warp + 1) * nL / nw) & ~15LL);
 }
 
 // Grid-wide barrier between the linears of a chain (cooperative launch, so
@@ -744,12 +775,19 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
             }
         };
 
-        // acc[m][j]: row 4h + (j ^ pp) of the current tile, token m
+        // acc[m][j]: row 4h + (j ^ pp) of the current tile, token m (W4: the
+        // low-nibble sums; accA the high-nibble sums, folded in at tile end)
+        // (up to four tokens; more keep one sum per row and token)
+        constexpr bool kSplitAcc = FMT == FMT_W4 && MT <= 4;
         Acc acc[MT][4];
+        int accA[kSplitAcc ? MT : 1][4];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
+            for (int j = 0; j < 4; ++j) {
+                acc[m][j] = Acc(0);
+                if constexpr (kSplitAcc) accA[m][j] = 0;
+            }
 
         if (NCH > 1 && nrounds == 0 && !dead)
             while (issued - consumed < S && issue_next()) {
@@ -934,7 +972,9 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
                                         load_x(m, chunk, x0, x1);
 #pragma unroll
                                         for (int j = 0; j < 4; ++j) {
-                                            if constexpr (FMT == FMT_W4) {
+                                            if constexpr (kSplitAcc) {
+                                                unit4_acc(wv[j], x0, x1, acc[m][j], accA[m][j]);
+                                            } else if constexpr (FMT == FMT_W4) {
                                                 int B, A;
                                                 unit4(wv[j], x0, x1, B, A);
                                                 acc[m][j] += B + (A >> 4);
@@ -967,6 +1007,10 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             if constexpr (FMT == FMT_W4) {
+                                if constexpr (kSplitAcc) {
+                                    acc[m][j] += accA[m][j] >> 4;
+                                    accA[m][j] = 0;
+                                }
                                 acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 8);
                                 acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], 16);
                             } else {
@@ -1146,19 +1190,6 @@ cudaError_t launch_gemv_fmt(const ChainParams<1>& p, int MT, int xmode, int grid
             return cudaErrorInvalidValue;
     }
 #undef W4_CASE
-}
-
-template <int FMT>
-cudaError_t launch_chain_fmt(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s)
-{
-    switch (MT) {
-        case 1: return launch_gemv_t<FMT, 1, X_FUSED, kMaxChain>(p, grid, smem, false, s);
-        case 2: return launch_gemv_t<FMT, 2, X_FUSED, kMaxChain>(p, grid, smem, false, s);
-        case 4: return launch_gemv_t<FMT, 4, X_FUSED, kMaxChain>(p, grid, smem, false, s);
-        case 8: return launch_gemv_t<FMT, 8, X_FUSED, kMaxChain>(p, grid, smem, false, s);
-        case 16: return launch_gemv_t<FMT, 16, X_FUSED, kMaxChain>(p, grid, smem, false, s);
-        default: return cudaErrorInvalidValue;
-    }
 }
 
 }  // namespace w4k

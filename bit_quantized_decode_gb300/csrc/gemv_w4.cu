@@ -10,9 +10,4 @@ cudaError_t launch_gemv_w4(const ChainParams<1>& p, int MT, int xmode, int grid,
     return launch_gemv_fmt<FMT_W4>(p, MT, xmode, grid, smem, pdl, s);
 }
 
-cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s)
-{
-    return launch_chain_fmt<FMT_W4>(p, MT, grid, smem, s);
-}
-
 }  // namespace w4k

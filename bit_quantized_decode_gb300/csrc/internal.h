@@ -84,6 +84,7 @@ struct GemvArgs {
     int C;                   // K / 32
     int T;                   // ceil(N / 8)
     int tq, tr;              // T = tq * grid + tr: block b owns tq (+1 if b < tr) tiles, from b tq + min(b, tr)
+    int rot;                 // block b takes the range of block (b + rot) % grid (balances chains over linears)
 };
 
 // Kernel parameters: up to NCH linears computed in order by one launch.
@@ -97,6 +98,7 @@ struct ChainParams {
     int round_tiles;         // tiles per accumulation round
     unsigned* barrier;       // grid barrier state [2] (chains only)
     unsigned* err;           // device error word
+    int prefetch_slices;     // chains: slices per ring prefetched into L2 ahead of the copies
 };
 
 struct SmemLayout {
@@ -120,6 +122,37 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, in
     L.bnd = o;   o = align_up(o + 2 * kWarps * 2 * kRows * MT * 4, 128);
     L.ring = o;  o = align_up(o + kWarps * stages * fmt_slot_bytes(fmt), 128);
     L.xs = o;    o += xmode == X_F32 ? MT * K * 4 : (xmode != X_GLOBAL ? MT * K : 0);
+    L.total = o;
+    return L;
+}
+
+// Persistent chain (gemv_chain.cu): fifteen consumer warps plus one warp
+// that streams the weights of every linear in order into the consumers'
+// rings.  Shared memory: full and empty barriers per slot, then the
+// consumer areas (two per-row parameter buffers), the rings and the codes.
+constexpr int kChainWarps = 15;                          // consumer warps (with the producer: 16, 128 registers each)
+constexpr int kChainConsumers = kChainWarps * 32;
+constexpr int kChainThreads = (kChainWarps + 1) * 32;
+
+struct ChainLayout {
+    int full, empty, sx, red, xsum, rowp, meta, acc, bnd, ring, xs, total;
+};
+
+__host__ __device__ inline ChainLayout chain_layout(int MT, int K, int stages, int round_tiles)
+{
+    ChainLayout L;
+    int o = 0;
+    L.full = o;  o += kChainWarps * stages * 8;
+    L.empty = o; o = align_up(o + kChainWarps * stages * 8, 16);
+    L.sx = o;    o = align_up(o + MT * 4, 16);
+    L.red = o;   o = align_up(o + kChainWarps * MT * 4, 16);
+    L.xsum = o;  o = align_up(o + kChainWarps * MT * 4, 16);
+    L.rowp = o;  o = align_up(o + 2 * 2 * (kRowCache / 2) * 4, 16);
+    L.meta = o;  o = align_up(o + 2 * kChainWarps * 2 * 4, 16);
+    L.acc = o;   o = align_up(o + 2 * round_tiles * kRows * MT * 4, 16);
+    L.bnd = o;   o = align_up(o + 2 * kChainWarps * 2 * kRows * MT * 4, 128);
+    L.ring = o;  o = align_up(o + kChainWarps * stages * fmt_slot_bytes(FMT_W4), 128);
+    L.xs = o;    o += MT * K;
     L.total = o;
     return L;
 }
@@ -152,7 +185,8 @@ __host__ __device__ constexpr int norm_max_nit(int MT) { return MT >= 4 ? 4 : 20
 // Weight-only GEMVs on float activations (W4F, W8F; xmode X_F32; MT in {1, 2, 4}).
 cudaError_t launch_gemv_a32(int fmt, const ChainParams<1>& p, int MT, int grid, size_t smem, bool pdl,
                             cudaStream_t s);
-// Chains of per-row INT4 linears (cooperative launch, fused quantization).
+// Chains of per-row INT4 linears (cooperative launch, fused quantization,
+// a producer warp streaming the weights; gemv_chain.cu).
 cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
 
 // ---------------------------------------------- multi-token tensor-core GEMV

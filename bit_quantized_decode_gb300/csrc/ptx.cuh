@@ -51,6 +51,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (mbarrier.try_wait may suspend the
+// thread for a while when the phase is incomplete; a thread polling several
+// barriers uses this instead).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
@@ -96,6 +112,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Bring `bytes` bytes at src (16-byte aligned, a multiple of 16) into L2
+// ahead of a later bulk copy; no completion is tracked.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 4-byte asynchronous copy global -> shared (cp.async), and its completion.
 __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src)
 {
@@ -115,6 +138,12 @@ __device__ __forceinline__ unsigned atom_add_release_gpu(unsigned* p, unsigned v
     unsigned old;
     asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+// Reduction (no return value) with release semantics at GPU scope.
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Acquire load at GPU scope (pairs with __threadfence + atomics on the writer).

@@ -33,7 +33,10 @@ std::mutex g_setup_mutex;
 std::atomic<bool> g_dev_ready[kMaxDevices];
 
 // Launch tuning set by w4_set_tuning (0 = automatic).
-int g_tune[4] = {0, 0, 0, 0};
+int g_tune[5] = {0, 0, 0, 0, 0};
+// Weight bytes a chain block prefetches into L2 ahead of its ring copies (KB):
+// none by default (measured slower: the prefetches slowed the stream they lead).
+constexpr int kChainPrefetchKB = 0;
 
 w4_status device_info(DeviceInfo** out)
 {
@@ -247,16 +250,28 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
     cp.round_tiles = kAccWords / MT;
     cp.barrier = barrier;
     cp.err = dev->err;
-    // one block per SM with the whole shared memory, the x buffer sized for the largest K
-    const int s_max = stages_for(FMT_W4, MT, X_FUSED, kmax, cp.round_tiles, dev->smem_optin, 2, kRowCache / 2);
-    if (s_max < 2) return W4_ERR_UNSUPPORTED_SHAPE;
-    cp.stages = s_max;
-    const int smem = smem_layout(FMT_W4, MT, X_FUSED, kmax, s_max, cp.round_tiles, 2, kRowCache / 2).total;
+    // one block per SM with the whole shared memory: the x buffer sized for
+    // the largest K, then the deepest ring (at most the tuned cap) that fits
+    const int cap_s = g_tune[W4_TUNE_MAX_STAGES] > 0 && g_tune[W4_TUNE_MAX_STAGES] < kMaxStages
+                          ? g_tune[W4_TUNE_MAX_STAGES] : kMaxStages;
+    int S = cap_s;
+    while (S >= 2 && chain_layout(MT, kmax, S, cp.round_tiles).total > dev->smem_optin) --S;
+    if (S < 2) return W4_ERR_UNSUPPORTED_SHAPE;
+    cp.stages = S;
+    const int smem = chain_layout(MT, kmax, S, cp.round_tiles).total;
+    // L2 lookahead per block, spread over the eight rings in 4 KB slices
+    const int la_kb = g_tune[W4_TUNE_CHAIN_PREFETCH_KB] > 0 ? g_tune[W4_TUNE_CHAIN_PREFETCH_KB] : kChainPrefetchKB;
+    cp.prefetch_slices = la_kb / (kChainWarps * 4);
     int grid = dev->sms;
     if (g_tune[W4_TUNE_GRID_BLOCKS] > 0 && g_tune[W4_TUNE_GRID_BLOCKS] < grid) grid = g_tune[W4_TUNE_GRID_BLOCKS];
+    // the blocks holding a linear's remainder tiles move on from linear to
+    // linear, so no block carries an extra tile in every linear of the chain
+    int rot = 0;
     for (int i = 0; i < n; ++i) {
         cp.lin[i].tq = cp.lin[i].T / grid;
         cp.lin[i].tr = cp.lin[i].T % grid;
+        cp.lin[i].rot = rot;
+        rot = (rot + cp.lin[i].tr) % grid;
     }
     return cuda_status(launch_chain_w4(cp, MT, grid, static_cast<size_t>(smem), s));
 }
@@ -553,7 +568,8 @@ w4_status w4_describe_device(w4_device_desc* out)
 
 w4_status w4_set_tuning(int key, int value)
 {
-    if (key < 0 || key > W4_TUNE_TC_MIN_M || value < 0) return W4_ERR_INVALID_ARG;
+    if (key < 0 || key > W4_TUNE_CHAIN_PREFETCH_KB || value < 0) return W4_ERR_INVALID_ARG;
+    if (key == W4_TUNE_CHAIN_PREFETCH_KB && value > 4096) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_TC_MIN_M && value > W4_MAX_M + 1) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_BLOCKS_PER_SM && value > 2) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_MAX_STAGES && value == 1) return W4_ERR_INVALID_ARG;
@@ -563,7 +579,7 @@ w4_status w4_set_tuning(int key, int value)
 
 int w4_get_tuning(int key)
 {
-    if (key < 0 || key > W4_TUNE_TC_MIN_M) return -1;
+    if (key < 0 || key > W4_TUNE_CHAIN_PREFETCH_KB) return -1;
     return g_tune[key];
 }
 

@@ -104,6 +104,10 @@ int w4_version(void);
  *   W4_TUNE_GRID_BLOCKS    cap on the grid size (default: the SM count).
  *   W4_TUNE_TC_MIN_M       per-row INT4 calls with at least this many tokens
  *                          run on the tensor cores (default 0: 5; 17: never).
+ *   W4_TUNE_CHAIN_PREFETCH_KB  w4a8_linear_chain: weight bytes (KB, at most
+ *                          4096) each block prefetches into L2 ahead of the
+ *                          weights it copies into shared memory (default
+ *                          0: none; below 32 none).
  * Returns W4_ERR_INVALID_ARG for an unknown key or an out-of-range value.
  * Not thread-safe with concurrent launches; set before launching.
  * ------------------------------------------------------------------------ */
@@ -111,6 +115,7 @@ int w4_version(void);
 #define W4_TUNE_MAX_STAGES 1
 #define W4_TUNE_GRID_BLOCKS 2
 #define W4_TUNE_TC_MIN_M 3
+#define W4_TUNE_CHAIN_PREFETCH_KB 4
 w4_status w4_set_tuning(int key, int value);
 int w4_get_tuning(int key); /* current value, -1 for an unknown key */
 

@@ -83,3 +83,36 @@ def test_true_chain_aliasing_outputs_as_inputs(lib, M):
         y_ref, _, sx_ref, acc = oracle.w4a8_linear(oracle.pack_int4(q), sw, host(x), b)
         check_close(host(y1), y_ref, w4_scale(acc, sw, sx_ref, b), RTOL_W4, f"link {i}")
         x = y1
+
+
+@pytest.mark.parametrize("prefetch_kb,stages", [(1, 2), (64, 3), (4096, 0)])
+def test_chain_producer_limits(lib, prefetch_kb, stages):
+    """The weight stream of the chain with two ring slots per warp and no L2
+    prefetch, with a short lookahead, and with a 4 MB lookahead per block
+    (past the end of the chain): the outputs stay bit-identical to single
+    launches.  A linear with 80000 rows takes two rounds per block and more
+    rows than the staged per-row parameters."""
+    import torch
+    lib.set_tuning("chain_prefetch_kb", prefetch_kb)
+    lib.set_tuning("max_stages", stages)
+    try:
+        M = 1
+        g = wl.rng(300 + prefetch_kb + stages)
+        shapes = [(80000, 64), (3584, 18944), (13, 64), (4608, 3584)]
+        lins = [_linear(lib, g, N, K) for N, K in shapes]
+        xs = [dev(wl.activations(g, M, K)) for _, K in shapes]
+        ys = [torch.full((M, N), float("nan"), device="cuda") for N, _ in shapes]
+        descs = lib.make_chain_descs([(L[3], L[4], L[5], x, y, None, None) for L, x, y in zip(lins, xs, ys)])
+        ws = torch.zeros(lib.chain_workspace_bytes(), dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            lib.w4a8_linear_chain(descs, M, ws)
+        torch.cuda.synchronize()
+        for (q, sw, b, w, swd, bd), x, y, (N, K) in zip(lins, xs, ys, shapes):
+            y1 = torch.empty((M, N), device="cuda")
+            lib.w4a8_linear(w, swd, bd, x, y1, torch.empty((M, K), dtype=torch.int8, device="cuda"),
+                            torch.empty(M, device="cuda"))
+            assert np.array_equal(host(y).view(np.uint32), host(y1).view(np.uint32)), (N, K)
+        assert host(ws.view(torch.int32)).tolist() == [0] * (ws.numel() // 4)
+    finally:
+        lib.set_tuning("chain_prefetch_kb", 0)
+        lib.set_tuning("max_stages", 0)

@@ -810,8 +810,10 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
                 const int n = min(min(hi - p, C - c), kSL);
                 const int slot = cslot;
                 if (!dead) {
-                    const bool ok = mbar_wait_bounded(my_bars + 8 * slot, cphase, kWaitTimeoutNs);
-                    if (__all_sync(0xffffffffu, ok)) {
+                    // a non-blocking test first: the slot has usually landed already
+                    bool ok = __all_sync(0xffffffffu, mbar_test_wait(my_bars + 8 * slot, cphase));
+                    if (!ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(my_bars + 8 * slot, cphase, kWaitTimeoutNs));
+                    if (ok) {
                         ++observed;
                     } else {
                         dead = true;   // warp-uniform from here on

@@ -195,7 +195,7 @@ def profiled_traffic(alg_bytes_per_launch: float, chain: bool):
     try:
         from bit_quantized_decode_gb300 import build
         digest = build.kernel_digest()
-        name = "gemv_w4_chain_qwen7b_step.md" if chain else "gemv_w4_fused_qwen7b_step.md"
+        name = "stream_chain_w4_qwen7b_step.md" if chain else "stream_linear_w4_fused_qwen7b_step.md"
         vals = {}
         with open(os.path.join(ROOT, "profiles", name)) as f:
             for line in f:

@@ -12,9 +12,9 @@ template <int FMT>
 cudaError_t launch_a32_fmt(const ChainParams<1>& p, int MT, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
     switch (MT) {
-        case 1: return launch_gemv_t<FMT, 1, X_F32, 1>(p, grid, smem, pdl, s);
-        case 2: return launch_gemv_t<FMT, 2, X_F32, 1>(p, grid, smem, pdl, s);
-        case 4: return launch_gemv_t<FMT, 4, X_F32, 1>(p, grid, smem, pdl, s);
+        case 1: return launch_gemv_t<FMT, 1, X_F32>(p, grid, smem, pdl, s);
+        case 2: return launch_gemv_t<FMT, 2, X_F32>(p, grid, smem, pdl, s);
+        case 4: return launch_gemv_t<FMT, 4, X_F32>(p, grid, smem, pdl, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -401,54 +401,11 @@ __device__ __forceinline__ void warp_lines(int warp, int nt, int C, int& lo, int
     hi = warp == nw - 1 ? static_cast<int>(nL) : static_cast<int>(((warp + 1) * nL / nw) & ~15LL);
 }
 
-// Grid-wide barrier between the linears of a chain (cooperative launch, so
-// every block is resident), split into arrive and wait so that independent
-// work can run in between.  state[0] counts arrivals over the whole launch:
-// before linear li a block waits until li * gridDim.x blocks have arrived.
-// After the last linear every block arrives once more; the block that makes
-// the count n * gridDim.x is the last one to touch it and resets it to zero,
-// leaving the state ready for the next launch.  Waits are bounded: after
-// kBarrierTimeoutNs the block records an error and goes on.
-constexpr uint64_t kBarrierTimeoutNs = 500ull * 1000ull * 1000ull;
-
-// All of this block's writes before the call are published to the grid.
-__device__ __forceinline__ unsigned grid_arrive(unsigned* count)
-{
-    __syncthreads();
-    unsigned prev = 0;
-    if (threadIdx.x == 0) prev = atom_add_release_gpu(count, 1u);
-    return prev;   // meaningful in thread 0 only
-}
-
-__device__ __forceinline__ bool grid_wait(const unsigned* count, unsigned target, unsigned* err, int* flag_s)
-{
-    if (threadIdx.x == 0) {
-        bool ok = true;
-        if (ld_acquire_gpu(count) < target) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(count) < target) {
-                if (globaltimer_ns() - t0 > kBarrierTimeoutNs) {
-                    ok = false;
-                    break;
-                }
-            }
-        }
-        __threadfence();
-        if (!ok && err != nullptr) atomicExch(err, kErrBarrierTimeout);
-        *flag_s = ok ? 1 : 0;
-    }
-    __syncthreads();
-    return *flag_s != 0;
-}
-
-// One launch computes a chain of NCH-at-most linears in order.  NCH == 1 is a
-// single linear (launched with programmatic dependent launch, two blocks per
-// SM); larger NCH is the persistent chain (cooperative launch, one block per
-// SM), where linear i+1 starts reading its activations only after every block
-// has written the outputs of linear i, while each warp's ring keeps streaming
-// the next linear's weights across that barrier.
-template <int FMT, int MT, int XM, int NCH>
-__global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kernel(const __grid_constant__ ChainParams<NCH> P)
+// One linear per launch, launched with programmatic dependent launch: two
+// blocks per SM, so the next GEMV's blocks become resident beside this one's
+// and fill their rings before the dependency resolves.
+template <int FMT, int MT, int XM>
+__global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid_constant__ ChainParams<1> P)
 {
     using Acc = typename std::conditional<FMT == FMT_W4, int, float>::type;
     constexpr int kUnit = fmt_unit_bytes(FMT);
@@ -462,16 +419,16 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
     constexpr bool kCodeSums = FMT == FMT_W4;        // activation code sums for the nibble bias
     constexpr int kPassLines = 16;
     constexpr int kPassUnroll = MT == 1 ? kSL / kPassLines : 1;
-    constexpr int kRowBufs = NCH == 1 ? 1 : 2;       // per-row parameter buffers (by linear parity)
-    constexpr int kRowCap = NCH == 1 ? kRowCache : kRowCache / 2;   // rows per buffer
-    // single linears with up to four tokens take the RMSNorm prologue when
-    // a.gamma is set (one kernel for both, so alternating launches share code)
-    constexpr bool kNormable = NCH == 1 && XM == X_FUSED && MT <= 4;
+    constexpr int kRowBufs = 1;                      // per-row parameter buffers
+    constexpr int kRowCap = kRowCache;               // rows per buffer
+    // up to four tokens take the RMSNorm prologue when a.gamma is set (one
+    // kernel for both, so alternating launches share code)
+    constexpr bool kNormable = XM == X_FUSED && MT <= 4;
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = P.stages;
     constexpr int RT = kAccWords / MT;               // tiles per round (the host sets P.round_tiles to this)
-    const int NL = NCH == 1 ? 1 : P.n;
+    constexpr int NL = 1;
     const int M = P.lin[0].M;
     const SmemLayout L = smem_layout(FMT, MT, XM, P.kmax, S, RT, kRowBufs, kRowCap);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -484,7 +441,6 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
     Acc* bnd_s = reinterpret_cast<Acc*>(smem + L.bnd);
     uint8_t* ring = smem + L.ring;
     int8_t* xs = reinterpret_cast<int8_t*>(smem + L.xs);
-    __shared__ int flag_s;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -498,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
         fence_mbar_init();
     }
     __syncwarp();
-    if (NCH == 1) pdl_launch_dependents();   // the next kernel may become resident beside this one
+    pdl_launch_dependents();   // the next kernel may become resident beside this one
     const uint64_t pol = l2_policy_evict_first();
 
     // Slice cursor over this warp's work: linear, round, line position in the
@@ -577,12 +533,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
         if (++islot == S) islot = 0;
         return true;
     };
-    // In chains the ring runs at most kAhead slices ahead inside a linear and is
-    // topped up to all S slots when the warp finishes its part of a linear, so
-    // the extra slots are requested during the dependency wait (not before it)
-    // and HBM keeps streaming through it.
-    constexpr int kAhead = NCH > 1 ? 3 : kMaxStages;
-    const int ahead = S < kAhead ? S : kAhead;
+    const int ahead = S;
     int consumed = 0;
 
     // one copy of the issue code (not unrolled): it runs once per launch,
@@ -631,26 +582,17 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
         const int ntiles = br.ntiles;
         const int nrounds = br.nrounds;
 
-        // outputs of the previous linear are written: let the grid know
-        if (NCH > 1 && li > 0) grid_arrive(P.barrier);
-
         // this linear's per-row parameters were staged one linear ahead
         float* bias_s = rowp_s + (li & (kRowBufs - 1)) * 2 * kRowCap;
         float* sw_s = bias_s + kRowCap;
         const int row0 = t0 * kRows;
         const bool rows_cached = ntiles * kRows <= kRowCap;
 
-        // ---- inputs produced before this linear are read only from here on
-        if (li == 0) {
-            // with the RMSNorm prologue the wait is taken inside it, after the norm weight loads
-            if (!(kNormable && a.gamma != nullptr)) pdl_wait();
-        } else if (!grid_wait(P.barrier, static_cast<unsigned>(li) * gridDim.x, P.err, &flag_s)) {
-            dead = true;
-        }
-        // the next linear's per-row parameters go to the other buffer (its last
-        // reader, linear li-1's epilogue, finished before the barrier above)
+        // ---- inputs produced by earlier kernels are read only from here on
+        // (with the RMSNorm prologue the wait is taken inside it, after the
+        // norm weight loads)
+        if (!(kNormable && a.gamma != nullptr)) pdl_wait();
         cp_async_wait_all();
-        if (li + 1 < NL) stage_rows(li + 1);
 
         // ---- activation prologue: int8 codes into shared memory (fused: quantize
         // here) and, for W4, per-thread code sums that the epilogue reduces.  All
@@ -789,9 +731,6 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
                 if constexpr (kSplitAcc) accA[m][j] = 0;
             }
 
-        if (NCH > 1 && nrounds == 0 && !dead)
-            while (issued - consumed < S && issue_next()) {
-            }
         for (int round = 0; round < nrounds; ++round, ++round_count) {
             const int buf = round_count & 1;
             int lo, hi;
@@ -1053,11 +992,6 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
                 }
             }
 
-            // last round of a chained linear: fill the whole ring for the dependency wait
-            if (NCH > 1 && round == nrounds - 1 && !dead)
-                while (issued - consumed < S && issue_next()) {
-                }
-
             __syncthreads();
 
             // ---- epilogue for this round's rows (coalesced over rows)
@@ -1132,12 +1066,6 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
         }
     }
 
-    // ---- chains: the final arrival; the block that completes the count resets it
-    if (NCH > 1) {
-        const unsigned prev = grid_arrive(P.barrier);
-        if (threadIdx.x == 0 && prev + 1u == static_cast<unsigned>(NL) * gridDim.x) atomicExch(P.barrier, 0u);
-    }
-
     // ---- after a timeout: wait (bounded) for copies still in flight into this warp's ring
     if (dead) {
         for (int k = observed; k < issued; ++k) {
@@ -1147,10 +1075,10 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 2 : 1) stream_linear_kern
     }
 }
 
-template <int FMT, int MT, int XM, int NCH>
-cudaError_t launch_gemv_t(const ChainParams<NCH>& p, int grid, size_t smem, bool pdl, cudaStream_t s)
+template <int FMT, int MT, int XM>
+cudaError_t launch_gemv_t(const ChainParams<1>& p, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-    auto kern = stream_linear_kernel<FMT, MT, XM, NCH>;
+    auto kern = stream_linear_kernel<FMT, MT, XM>;
     static SmemLimit limit;
     cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), limit, smem);
     if (e != cudaSuccess) return e;
@@ -1160,16 +1088,10 @@ cudaError_t launch_gemv_t(const ChainParams<NCH>& p, int grid, size_t smem, bool
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    if (NCH == 1) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-    } else {
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-    }
-    const bool use_attr = NCH != 1 || pdl;
-    cfg.attrs = use_attr ? attr : nullptr;
-    cfg.numAttrs = use_attr ? 1 : 0;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -1179,9 +1101,9 @@ cudaError_t launch_gemv_fmt(const ChainParams<1>& p, int MT, int xmode, int grid
 {
 #define W4_CASE(mt)                                                                               \
     case mt:                                                                                      \
-        return xmode == X_FUSED  ? launch_gemv_t<FMT, mt, X_FUSED, 1>(p, grid, smem, pdl, s)      \
-               : xmode == X_SMEM ? launch_gemv_t<FMT, mt, X_SMEM, 1>(p, grid, smem, pdl, s)       \
-                                 : launch_gemv_t<FMT, mt, X_GLOBAL, 1>(p, grid, smem, pdl, s);
+        return xmode == X_FUSED  ? launch_gemv_t<FMT, mt, X_FUSED>(p, grid, smem, pdl, s)         \
+               : xmode == X_SMEM ? launch_gemv_t<FMT, mt, X_SMEM>(p, grid, smem, pdl, s)          \
+                                 : launch_gemv_t<FMT, mt, X_GLOBAL>(p, grid, smem, pdl, s);
     switch (MT) {
         W4_CASE(1)
         W4_CASE(2)

@@ -889,6 +889,9 @@ def run_suite(args, local_rank):
     torch.cuda.set_device(dev)
     _lib.load()
     _lib.clear_device_error()
+    for kv in args.tune:                       # launch tuning applies to every line of the suite
+        k, v = kv.split("=")
+        _lib.set_tuning(k, int(v))
     peak, _ = measured_peak()
     stream = torch.cuda.Stream(device=dev)
     peak_rd = read_peak(dev, stream)
@@ -909,9 +912,6 @@ def run_suite(args, local_rank):
                 print(json.dumps(line), flush=True)
     step_ms = [int(m) for m in args.suite_ms.split(",") if m]
     weights = build_weights(args, dev) if step_ms else None
-    for kv in args.tune:
-        k, v = kv.split("=")
-        _lib.set_tuning(k, int(v))
     for M in step_ms:
         items, _, _ = make_buffers(weights, M, args.independent_x, dev)
 

@@ -27,7 +27,7 @@ STATUS = {
     5: "W4_ERR_DEVICE_TIMEOUT",
 }
 W4_FLAG_PDL = 1
-TUNE_KEYS = {"blocks_per_sm": 0, "max_stages": 1, "grid_blocks": 2, "tc_min_m": 3, "chain_prefetch_kb": 4}
+TUNE_KEYS = {"blocks_per_sm": 0, "max_stages": 1, "grid_blocks": 2, "tc_min_m": 3, "chain_prefetch_kb": 4, "k_splits": 5}
 W4_MAX_M = 16
 W4_MAX_K = 131072
 W4_MAX_SHARDS = 8

@@ -377,17 +377,19 @@ __device__ __forceinline__ void fused_prologue_regs(const GemvArgs& a, int nit, 
 }
 
 // Tile range of this block in one linear: an even split of the T tiles over
-// the grid (the host passes T = tq * grid + tr, so no division here),
-// processed in rounds of at most RT tiles.
+// the grid's clusters of ks blocks (ks = 1 without K splits; the host passes
+// T = tq * clusters + tr), processed in rounds of at most RT tiles.
 struct BlockRange {
     int t0, ntiles, nrounds;
 };
 
-template <int RT>
+template <int RT, bool KS = false>
 __device__ __forceinline__ BlockRange block_range(const GemvArgs& a)
 {
-    int b = static_cast<int>(blockIdx.x) + a.rot;
-    if (b >= static_cast<int>(gridDim.x)) b -= static_cast<int>(gridDim.x);
+    const int ks = KS ? a.ks : 1;                    // K splits share their cluster's range
+    const int nb = static_cast<int>(gridDim.x) / ks;
+    int b = static_cast<int>(blockIdx.x) / ks + a.rot;
+    if (b >= nb) b -= nb;
     const int n = a.tq + (b < a.tr ? 1 : 0);
     return BlockRange{b * a.tq + min(b, a.tr), n, (n + RT - 1) / RT};
 }
@@ -404,7 +406,10 @@ __device__ __forceinline__ void warp_lines(int warp, int nt, int C, int& lo, int
 // One linear per launch, launched with programmatic dependent launch: two
 // blocks per SM, so the next GEMV's blocks become resident beside this one's
 // and fill their rings before the dependency resolves.
-template <int FMT, int MT, int XM>
+//
+// KS: K split over a cluster of P.lin[0].ks blocks (a separate instantiation,
+// so the unsplit kernel keeps none of the split's bookkeeping).
+template <int FMT, int MT, int XM, bool KS>
 __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid_constant__ ChainParams<1> P)
 {
     using Acc = typename std::conditional<FMT == FMT_W4, int, float>::type;
@@ -430,7 +435,12 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
     constexpr int RT = kAccWords / MT;               // tiles per round (the host sets P.round_tiles to this)
     constexpr int NL = 1;
     const int M = P.lin[0].M;
-    const SmemLayout L = smem_layout(FMT, MT, XM, P.kmax, S, RT, kRowBufs, kRowCap);
+    // K split: this block's rank in its cluster and its chunk range [c0, c0 + Cr)
+    const int kspl = KS ? P.lin[0].ks : 1;
+    const int krank = KS ? static_cast<int>(blockIdx.x) % kspl : 0;
+    const int c0 = KS ? static_cast<int>(static_cast<long long>(krank) * P.lin[0].C / kspl) : 0;
+    const int Cr = KS ? static_cast<int>(static_cast<long long>(krank + 1) * P.lin[0].C / kspl) - c0 : P.lin[0].C;
+    const SmemLayout L = smem_layout(FMT, MT, XM, P.kmax, S, RT, kRowBufs, kRowCap, kspl);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     float* sx_s = reinterpret_cast<float*>(smem + L.sx);
     float* red_s = reinterpret_cast<float*>(smem + L.red);
@@ -439,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
     int* meta_s = reinterpret_cast<int*>(smem + L.meta);
     Acc* acc_s = reinterpret_cast<Acc*>(smem + L.acc);
     Acc* bnd_s = reinterpret_cast<Acc*>(smem + L.bnd);
+    Acc* mrg_s = reinterpret_cast<Acc*>(smem + L.merge);       // [kspl][MT][RT rows]: own sums, then other ranks'
     uint8_t* ring = smem + L.ring;
     int8_t* xs = reinterpret_cast<int8_t*>(smem + L.xs);
 
@@ -465,17 +476,17 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
         BlockRange r;
         bool done;
     };
+    // (lines of a tile: this block's Cr chunks of it)
     auto enter_round = [&](Cursor& k) {
-        const int C = P.lin[k.lin].C;
-        warp_lines(warp, min(RT, k.r.ntiles - k.round * RT), C, k.p, k.hi);
-        k.tl = k.p / C;
-        k.c = k.p - k.tl * C;
+        warp_lines(warp, min(RT, k.r.ntiles - k.round * RT), Cr, k.p, k.hi);
+        k.tl = k.p / Cr;
+        k.c = k.p - k.tl * Cr;
     };
     auto cursor_start = [&](Cursor& k) {
         k.lin = 0;
         k.round = 0;
         k.done = false;
-        k.r = block_range<RT>(P.lin[0]);
+        k.r = block_range<RT, KS>(P.lin[0]);
         if (k.r.nrounds > 0) enter_round(k);
     };
     // Next slice of the cursor: linear index, first unit, lines.  False at the end.
@@ -483,12 +494,12 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
         while (!k.done) {
             if (k.round < k.r.nrounds && k.p < k.hi) {
                 const int C = P.lin[k.lin].C;
-                n = min(min(k.hi - k.p, C - k.c), kSL);
+                n = min(min(k.hi - k.p, Cr - k.c), kSL);
                 lin = k.lin;
-                unit0 = (static_cast<size_t>(k.r.t0 + k.round * RT + k.tl) * C + k.c) * kRows;
+                unit0 = (static_cast<size_t>(k.r.t0 + k.round * RT + k.tl) * C + c0 + k.c) * kRows;
                 k.p += n;
                 k.c += n;
-                if (k.c == C) {
+                if (k.c == Cr) {
                     k.c = 0;
                     ++k.tl;
                 }
@@ -501,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
                     k.done = true;
                     return false;
                 }
-                k.r = block_range<RT>(P.lin[k.lin]);
+                k.r = block_range<RT, KS>(P.lin[k.lin]);
                 k.round = 0;
             }
             enter_round(k);
@@ -546,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
     // asynchronous 4-byte copies, complete after cp_async_wait_all().
     auto stage_rows = [&](int li) {
         const GemvArgs& ra = P.lin[li];
-        const BlockRange rr = block_range<RT>(ra);
+        const BlockRange rr = block_range<RT, KS>(ra);
         if (rr.ntiles * kRows > kRowCap) return;
         float* b_s = rowp_s + (li & (kRowBufs - 1)) * 2 * kRowCap;
         float* w_s = b_s + kRowCap;
@@ -575,9 +586,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
 
     for (int li = 0; li < NL; ++li) {
         const GemvArgs& a = P.lin[li];
-        const int C = a.C;
         const int K = a.K;
-        const BlockRange br = block_range<RT>(a);
+        const BlockRange br = block_range<RT, KS>(a);
         const int t0 = br.t0;
         const int ntiles = br.ntiles;
         const int nrounds = br.nrounds;
@@ -704,14 +714,18 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
         }
         __syncthreads();
 
-        // Activation chunk (32 int8) of token m at chunk c.
+        // Activation chunk (32 int8) of token m at chunk c of this block's K
+        // range (the bases start at its first chunk, c0, so the loop keeps no
+        // offset of its own).
+        const int8_t* xs_k = xs + c0 * 32;
+        const int8_t* qg_k = XM == X_GLOBAL ? a.qx_in + c0 * 32 : nullptr;
         auto load_x = [&](int m, int c, uint4& x0, uint4& x1) {
             if constexpr (XM == X_GLOBAL) {
-                const uint4* p = reinterpret_cast<const uint4*>(a.qx_in + static_cast<size_t>(m) * K + c * 32);
+                const uint4* p = reinterpret_cast<const uint4*>(qg_k + static_cast<size_t>(m) * K + c * 32);
                 x0 = __ldg(p);
                 x1 = __ldg(p + 1);
             } else {
-                const uint4* p = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * K + c * 32);
+                const uint4* p = reinterpret_cast<const uint4*>(xs_k + static_cast<size_t>(m) * K + c * 32);
                 x0 = p[0];
                 x1 = p[1];
             }
@@ -734,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
         for (int round = 0; round < nrounds; ++round, ++round_count) {
             const int buf = round_count & 1;
             int lo, hi;
-            warp_lines(warp, min(RT, ntiles - round * RT), C, lo, hi);
+            warp_lines(warp, min(RT, ntiles - round * RT), Cr, lo, hi);
             int* meta = meta_s + (buf * kWarps + warp) * 2;
             if (lane == 0) {
                 meta[0] = -1;
@@ -743,10 +757,10 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
             __syncwarp();
 
             int p = lo;
-            int tl = lo / C;
-            int c = lo - tl * C;
+            int tl = lo / Cr;
+            int c = lo - tl * Cr;
             while (p < hi) {
-                const int n = min(min(hi - p, C - c), kSL);
+                const int n = min(min(hi - p, Cr - c), kSL);
                 const int slot = cslot;
                 if (!dead) {
                     // a non-blocking test first: the slot has usually landed already
@@ -768,7 +782,9 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
                     for (int pass = 0; pass < kSL / kPassLines; ++pass) {
                         const int line = pass * kPassLines + pl;
                         if (line < n) {
-                            const int chunk = c + line;
+                            // chunk within this block's K range (absolute for the float-x
+                            // formats, whose x layout swizzles by chunk; they never split K)
+                            const int chunk = (fmt_float_x(FMT) ? c0 : 0) + c + line;
                             const uint8_t* ub = sw + (line * kRows + 4 * h) * kUnit;
                             if constexpr (fmt_float_x(FMT)) {
                                 // weight-only on float x: every weight unpacked to fp32 and
@@ -940,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
 
                 p += n;
                 c += n;
-                if (c == C || p == hi) {
+                if (c == Cr || p == hi) {
                     // tile done for this warp: reduce lanes of equal (h, pp), then undo
                     // the read permutation with a two-step butterfly
 #pragma unroll
@@ -967,14 +983,14 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
                         const Acc v = __shfl_xor_sync(0xffffffffu, acc[m][1], 2);
                         if constexpr (FMT == FMT_W4) acc[m][0] += v; else acc[m][0] = __fadd_rn(acc[m][0], v);
                     }
-                    const int tstart = tl * C;
+                    const int tstart = tl * Cr;
                     if (lane < kRows) {
-                        const bool full = lo <= tstart && hi >= tstart + C;
+                        const bool full = lo <= tstart && hi >= tstart + Cr;
                         Acc* dst;
                         if (full) {
                             dst = acc_s + (static_cast<size_t>(buf) * RT * kRows + tl * kRows + my_row) * MT;
                         } else {
-                            const int which = (lo >= tstart && lo < tstart + C) ? 0 : 1;
+                            const int which = (lo >= tstart && lo < tstart + Cr) ? 0 : 1;
                             dst = bnd_s + (((buf * kWarps + warp) * 2 + which) * kRows + my_row) * MT;
                             if (lane == 0) meta[which] = tl;
                         }
@@ -985,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
                     for (int m = 0; m < MT; ++m)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) acc[m][j] = Acc(0);
-                    if (c == C) {
+                    if (c == Cr) {
                         c = 0;
                         ++tl;
                     }
@@ -999,7 +1015,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
             const int nrows = min(RT, ntiles - rt0) * kRows;
             const int row_base = (t0 + rt0) * kRows;
             // linear output of round row rl (kernel row `row`), token m
-            auto lin_out = [&](int m, int rl, int row) -> float {
+            // this block's sum for round row rl, token m (its warps' tiles merged in order)
+            auto own_sum = [&](int m, int rl) -> Acc {
                 const int tile = rl >> 3;
                 const int rr = rl & 7;
                 Acc v = Acc(0);
@@ -1016,6 +1033,43 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
                     }
                 }
                 if (!part) v = acc_s[(static_cast<size_t>(buf) * RT * kRows + rl) * MT + m];
+                return v;
+            };
+            // K splits: every rank writes its sums into the leader (rank 0), which adds
+            // them in rank order; only the leader writes the outputs.
+            constexpr int kRR = RT * kRows;                       // rows of a round, at most
+            if constexpr (KS) {
+                const uint32_t mrg_u = smem_u32(mrg_s);
+                for (int idx = tid; idx < M * nrows; idx += kThreads) {
+                    const int m = idx / nrows;
+                    const int rl = idx - m * nrows;
+                    const Acc v = own_sum(m, rl);
+                    const int o = (krank * MT + m) * kRR + rl;
+                    if (krank == 0) {
+                        mrg_s[o] = v;
+                    } else {
+                        uint32_t bits;
+                        if constexpr (FMT == FMT_W4) bits = static_cast<uint32_t>(v); else bits = __float_as_uint(v);
+                        st_cluster_u32(mapa_shared(mrg_u + 4u * static_cast<uint32_t>(o), 0u), bits);
+                    }
+                }
+                cluster_sync();
+                if (krank == 0)
+                    for (int idx = tid; idx < M * nrows; idx += kThreads) {
+                        const int m = idx / nrows;
+                        const int rl = idx - m * nrows;
+                        Acc v = mrg_s[m * kRR + rl];
+                        for (int r = 1; r < kspl; ++r) {
+                            const Acc pv = mrg_s[(r * MT + m) * kRR + rl];
+                            if constexpr (FMT == FMT_W4) v += pv; else v = __fadd_rn(v, pv);
+                        }
+                        mrg_s[m * kRR + rl] = v;
+                    }
+                cluster_sync();                                   // the ranks' buffers are free again
+            }
+            // linear output of round row rl (kernel row `row`), token m
+            auto lin_out = [&](int m, int rl, int row) -> float {
+                const Acc v = KS ? mrg_s[m * kRR + rl] : own_sum(m, rl);
                 const int ci = row - row0;
                 const int prow = a.glu != GLU_NONE ? glu_param_row(row, a.n_out) : row;
                 const float b = rows_cached ? bias_s[ci] : (a.bias != nullptr ? a.bias[prow] : 0.0f);
@@ -1033,7 +1087,9 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
                     return __fmaf_rn(sx_s[m], v, b);
                 }
             };
-            if (a.glu == GLU_NONE) {
+            if (KS && krank != 0) {
+                // another rank writes the outputs
+            } else if (a.glu == GLU_NONE) {
                 for (int idx = tid; idx < M * nrows; idx += kThreads) {
                     const int m = idx / nrows;
                     const int rl = idx - m * nrows;
@@ -1075,10 +1131,10 @@ __global__ void __launch_bounds__(kThreads, 2) stream_linear_kernel(const __grid
     }
 }
 
-template <int FMT, int MT, int XM>
+template <int FMT, int MT, int XM, bool KS = false>
 cudaError_t launch_gemv_t(const ChainParams<1>& p, int grid, size_t smem, bool pdl, cudaStream_t s)
 {
-    auto kern = stream_linear_kernel<FMT, MT, XM>;
+    auto kern = stream_linear_kernel<FMT, MT, XM, KS>;
     static SmemLimit limit;
     cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), limit, smem);
     if (e != cudaSuccess) return e;
@@ -1087,11 +1143,22 @@ cudaError_t launch_gemv_t(const ChainParams<1>& p, int grid, size_t smem, bool p
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = pdl ? attr : nullptr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (KS) {                            // K splits: clusters of ks blocks
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(p.lin[0].ks);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = static_cast<unsigned>(na);
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -1104,6 +1171,20 @@ cudaError_t launch_gemv_fmt(const ChainParams<1>& p, int MT, int xmode, int grid
         return xmode == X_FUSED  ? launch_gemv_t<FMT, mt, X_FUSED>(p, grid, smem, pdl, s)         \
                : xmode == X_SMEM ? launch_gemv_t<FMT, mt, X_SMEM>(p, grid, smem, pdl, s)          \
                                  : launch_gemv_t<FMT, mt, X_GLOBAL>(p, grid, smem, pdl, s);
+#define W4_SPLIT_CASE(mt)                                                                         \
+    case mt:                                                                                      \
+        return xmode == X_FUSED  ? launch_gemv_t<FMT, mt, X_FUSED, true>(p, grid, smem, pdl, s)   \
+               : xmode == X_SMEM ? launch_gemv_t<FMT, mt, X_SMEM, true>(p, grid, smem, pdl, s)    \
+                                 : launch_gemv_t<FMT, mt, X_GLOBAL, true>(p, grid, smem, pdl, s);
+    // K splits: one and two tokens (kMaxSplitTokens)
+    if (p.lin[0].ks > 1) {
+        switch (MT) {
+            W4_SPLIT_CASE(1)
+            W4_SPLIT_CASE(2)
+            default:
+                return cudaErrorInvalidValue;
+        }
+    }
     switch (MT) {
         W4_CASE(1)
         W4_CASE(2)
@@ -1114,6 +1195,7 @@ cudaError_t launch_gemv_fmt(const ChainParams<1>& p, int MT, int xmode, int grid
             return cudaErrorInvalidValue;
     }
 #undef W4_CASE
+#undef W4_SPLIT_CASE
 }
 
 }  // namespace w4k

@@ -20,6 +20,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxStages = 8;            // ring slots per warp, upper bound
 constexpr int kAccWords = 64;            // round_tiles * MT, bounds the per-round accumulator
 constexpr int kRowCache = 1024;          // rows per block whose s_w / bias are staged in shared memory
+constexpr int kMaxSplitTokens = 2;       // DP4A GEMVs split K for at most this many tokens
 
 // Activation source of a GEMV: quantized in the prologue (from x, or from
 // RMSNorm(x) when GemvArgs::gamma is set), int8 codes copied into shared
@@ -85,6 +86,8 @@ struct GemvArgs {
     int T;                   // ceil(N / 8)
     int tq, tr;              // T = tq * grid + tr: block b owns tq (+1 if b < tr) tiles, from b tq + min(b, tr)
     int rot;                 // block b takes the range of block (b + rot) % grid (balances chains over linears)
+    int ks;                  // K splits: clusters of ks blocks share a tile range, block rank r
+                             // takes chunks [r C / ks, (r + 1) C / ks) (0 or 1: no split)
 };
 
 // Kernel parameters: up to NCH linears computed in order by one launch.
@@ -102,13 +105,13 @@ struct ChainParams {
 };
 
 struct SmemLayout {
-    int bars, sx, red, xsum, rowp, meta, acc, bnd, ring, xs, total;
+    int bars, sx, red, xsum, rowp, meta, acc, bnd, merge, ring, xs, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, int K, int stages, int round_tiles,
-                                                  int row_bufs = 1, int row_cap = kRowCache)
+                                                  int row_bufs = 1, int row_cap = kRowCache, int ks = 1)
 {
     SmemLayout L;
     int o = 0;
@@ -119,7 +122,10 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, int MT, int xmode, in
     L.rowp = o;  o = align_up(o + row_bufs * 2 * row_cap * 4, 16);
     L.meta = o;  o = align_up(o + 2 * kWarps * 2 * 4, 16);
     L.acc = o;   o = align_up(o + 2 * round_tiles * kRows * MT * 4, 16);
-    L.bnd = o;   o = align_up(o + 2 * kWarps * 2 * kRows * MT * 4, 128);
+    L.bnd = o;   o = align_up(o + 2 * kWarps * 2 * kRows * MT * 4, 16);
+    // K splits: the round's per-row sums of this block, then (in the leader)
+    // one buffer per other rank that rank writes through the cluster
+    L.merge = o; o = align_up(o + (ks > 1 ? ks * round_tiles * kRows * MT * 4 : 0), 128);
     L.ring = o;  o = align_up(o + kWarps * stages * fmt_slot_bytes(fmt), 128);
     L.xs = o;    o += xmode == X_F32 ? MT * K * 4 : (xmode != X_GLOBAL ? MT * K : 0);
     L.total = o;

@@ -189,6 +189,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                  : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Cluster-wide barrier: every thread of every block in the cluster arrives
 // (release) and waits (acquire); shared-memory stores to any block of the
 // cluster made before it are visible after it.  All threads must execute it.

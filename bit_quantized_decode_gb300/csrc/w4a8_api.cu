@@ -33,7 +33,7 @@ std::mutex g_setup_mutex;
 std::atomic<bool> g_dev_ready[kMaxDevices];
 
 // Launch tuning set by w4_set_tuning (0 = automatic).
-int g_tune[5] = {0, 0, 0, 0, 0};
+int g_tune[6] = {0, 0, 0, 0, 0, 0};
 // Weight bytes a chain block prefetches into L2 ahead of its ring copies (KB):
 // none by default (measured slower: the prefetches slowed the stream they lead).
 constexpr int kChainPrefetchKB = 0;
@@ -131,11 +131,11 @@ struct Plan {
 };
 
 // Largest ring (at most the cap) whose layout fits `budget`; 0 if fewer than 2 stages fit.
-int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget, int row_bufs = 1, int row_cap = kRowCache)
+int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget, int ks = 1)
 {
     const int cap = g_tune[W4_TUNE_MAX_STAGES] > 0 ? g_tune[W4_TUNE_MAX_STAGES] : kMaxStages;
     int s = cap < kMaxStages ? cap : kMaxStages;
-    while (s >= 2 && smem_layout(fmt, MT, xmode, K, s, RT, row_bufs, row_cap).total > budget) --s;
+    while (s >= 2 && smem_layout(fmt, MT, xmode, K, s, RT, 1, kRowCache, ks).total > budget) --s;
     return s >= 2 ? s : 0;
 }
 
@@ -144,7 +144,7 @@ int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget, int row_bu
 // budget.  Several tokens: the whole-block budget (a deeper ring pays more
 // than the early start of the next GEMV once the inner loop does M times the
 // DP4A work).  `fused` asks for the quantize prologue.
-bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p)
+bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p, int ks = 1)
 {
     const int half = d.smem_per_sm / 2 - d.smem_reserved;
     const int whole = d.smem_optin;
@@ -163,11 +163,11 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
         for (int mi = 0; mi < 2; ++mi) {
             const int xm = modes[mi];
             if (xm < 0) continue;
-            const int s = stages_for(fmt, MT, xm, K, RT, budget);
+            const int s = stages_for(fmt, MT, xm, K, RT, budget, ks);
             if (s >= 2) {
                 p.xmode = xm;
                 p.stages = s;
-                p.smem = smem_layout(fmt, MT, xm, K, s, RT).total;
+                p.smem = smem_layout(fmt, MT, xm, K, s, RT, 1, kRowCache, ks).total;
                 return true;
             }
         }
@@ -176,12 +176,37 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
 }
 
 // Blocks of a DP4A GEMV launch over T row tiles: one per SM (or the tuned
-// cap), never more than the tiles.
-int gemv_grid(const DeviceInfo& d, int T)
+// cap), never more than the tiles; with K splits, clusters of ks blocks each
+// take a tile range (grid = clusters * ks).
+int gemv_grid(const DeviceInfo& d, int T, int ks = 1)
 {
     int grid = d.sms;
     if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
-    return T < grid ? T : grid;
+    int clusters = grid / ks;
+    if (clusters < 1) clusters = 1;
+    return (T < clusters ? T : clusters) * ks;
+}
+
+// K splits of a DP4A GEMV with C chunks per row over T tiles: clusters of ks
+// blocks share a tile range, block r taking chunks [r C / ks, (r + 1) C / ks),
+// and add their per-row sums in the leader's shared memory (exact integers for
+// per-row INT4; fp32 group sums in rank order otherwise).  Measured on GB300
+// at one token, every split was slower than none, also where the tiles are
+// too few for the SMs (the 512-row GEMV: 2.68 us unsplit, 3.77 / 4.05 us in
+// two / four; the Gemma Q4_0 down projection: 4.06 against 5.17 / 5.44 us):
+// these GEMVs are latency-bound, and the cluster launch and the merge's two
+// cluster barriers per round cost more than the shorter loop saves.  So a
+// split is never chosen on its own; W4_TUNE_K_SPLITS forces one where each
+// rank keeps at least 16 chunks (one pass) per tile, for one or two tokens.
+int choose_splits(const DeviceInfo& d, int fmt, int MT, int T, int C)
+{
+    (void)T;
+    if (fmt_float_x(fmt) || MT > kMaxSplitTokens) return 1;
+    int grid = d.sms;
+    if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
+    const int forced = g_tune[W4_TUNE_K_SPLITS];
+    if (forced > 1 && C / forced >= 16 && grid / forced >= 1) return forced;
+    return 1;
 }
 
 // Launch one GEMV.
@@ -193,6 +218,7 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     const int MT = round_pow2_tokens(a.M);
     a.C = a.K / 32;
     a.T = static_cast<int>(tiles(a.N));
+    a.ks = choose_splits(*dev, fmt, MT, a.T, a.C);
     ChainParams<1> cp;
     std::memset(&cp, 0, sizeof(cp));
     cp.lin[0] = a;
@@ -201,11 +227,14 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     cp.round_tiles = kAccWords / MT;
     cp.err = dev->err;
     Plan p;
-    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (a.ks > 1 && !plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) a.ks = 1;   // no room to merge
+    cp.lin[0].ks = a.ks;
+    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) return W4_ERR_UNSUPPORTED_SHAPE;
     cp.stages = p.stages;
-    const int grid = gemv_grid(*dev, a.T);
-    cp.lin[0].tq = a.T / grid;
-    cp.lin[0].tr = a.T % grid;
+    const int grid = gemv_grid(*dev, a.T, a.ks);
+    const int clusters = grid / a.ks;
+    cp.lin[0].tq = a.T / clusters;
+    cp.lin[0].tr = a.T % clusters;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
     cudaError_t e;
     if (fmt_float_x(fmt)) e = launch_gemv_a32(fmt, cp, MT, grid, p.smem, pdl, s);
@@ -537,12 +566,15 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
                 p.k_splits = ks;
             } else {
                 const int MT = round_pow2_tokens(M);
+                const int T = static_cast<int>(tiles(Nw));
+                const int ks = choose_splits(d, fmt, MT, T, K / 32);
                 Plan q;
-                if (!plan_gemv(d, fmt, MT, linear && p.quantize_launches == 0, K, kAccWords / MT, q))
+                if (!plan_gemv(d, fmt, MT, linear && p.quantize_launches == 0, K, kAccWords / MT, q, ks))
                     return W4_ERR_UNSUPPORTED_SHAPE;
                 p.path = q.xmode == X_FUSED ? W4_PATH_FUSED : q.xmode == X_SMEM ? W4_PATH_CODES_SMEM
                                                                                 : W4_PATH_CODES_GLOBAL;
-                p.grid = gemv_grid(d, static_cast<int>(tiles(Nw)));
+                p.grid = gemv_grid(d, T, ks);
+                p.k_splits = ks;
                 p.threads = kThreads;
                 p.smem_bytes = q.smem;
                 p.stages = q.stages;
@@ -568,7 +600,9 @@ w4_status w4_describe_device(w4_device_desc* out)
 
 w4_status w4_set_tuning(int key, int value)
 {
-    if (key < 0 || key > W4_TUNE_CHAIN_PREFETCH_KB || value < 0) return W4_ERR_INVALID_ARG;
+    if (key < 0 || key > W4_TUNE_K_SPLITS || value < 0) return W4_ERR_INVALID_ARG;
+    if (key == W4_TUNE_K_SPLITS && value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
+        return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_CHAIN_PREFETCH_KB && value > 4096) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_TC_MIN_M && value > W4_MAX_M + 1) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_BLOCKS_PER_SM && value > 2) return W4_ERR_INVALID_ARG;
@@ -579,7 +613,7 @@ w4_status w4_set_tuning(int key, int value)
 
 int w4_get_tuning(int key)
 {
-    if (key < 0 || key > W4_TUNE_CHAIN_PREFETCH_KB) return -1;
+    if (key < 0 || key > W4_TUNE_K_SPLITS) return -1;
     return g_tune[key];
 }
 

@@ -104,6 +104,11 @@ int w4_version(void);
  *   W4_TUNE_GRID_BLOCKS    cap on the grid size (default: the SM count).
  *   W4_TUNE_TC_MIN_M       per-row INT4 calls with at least this many tokens
  *                          run on the tensor cores (default 0: 5; 17: never).
+ *   W4_TUNE_K_SPLITS       DP4A GEMVs of one or two tokens: K split over a
+ *                          cluster of 2, 4 or 8 blocks sharing a tile range
+ *                          (where each split keeps at least 16 chunks of 32 K);
+ *                          0 or 1: no split, the default (a split measured
+ *                          slower on every shape tried, see DESIGN notes).
  *   W4_TUNE_CHAIN_PREFETCH_KB  w4a8_linear_chain: weight bytes (KB, at most
  *                          4096) each block prefetches into L2 ahead of the
  *                          weights it copies into shared memory (default
@@ -116,6 +121,7 @@ int w4_version(void);
 #define W4_TUNE_GRID_BLOCKS 2
 #define W4_TUNE_TC_MIN_M 3
 #define W4_TUNE_CHAIN_PREFETCH_KB 4
+#define W4_TUNE_K_SPLITS 5
 w4_status w4_set_tuning(int key, int value);
 int w4_get_tuning(int key); /* current value, -1 for an unknown key */
 
@@ -136,8 +142,9 @@ int w4_get_tuning(int key); /* current value, -1 for an unknown key */
  *   out:  host; path (W4_PATH_*), quantize_launches (1 when a *_linear call
  *         quantizes x in a kernel of its own first, else 0), and the GEMV
  *         launch: grid, threads, smem_bytes (dynamic, per block), stages
- *         (weight-ring depth), k_splits (tensor cores: K splits per 128-row
- *         group, which form one thread-block cluster; 1 otherwise).
+ *         (weight-ring depth), k_splits (K splits per tile range, which form
+ *         one thread-block cluster: per 128-row group on the tensor cores, per
+ *         range of 8-row tiles on DP4A; 1 without a split).
  * Paths:
  *   W4_PATH_NONE          nothing (M = 0, or N = 0 where only the quantizer
  *                         of a *_linear call runs);

@@ -135,9 +135,10 @@ def test_invariants_over_a_shape_sweep(lib):
                     assert p["stages"] * 32768 >= ks * 128 * 16 * 4  # partial sums fit the ring
                 else:
                     assert p["path"] in ("fused", "codes_smem", "codes_global")
-                    assert p["grid"] == min(152, math.ceil(N / 8))
+                    ks = p["k_splits"]                                # DP4A: clusters of ks blocks
+                    assert ks in (1, 2, 4) and (ks == 1 or (M <= 2 and K // 32 // ks >= 16))
+                    assert p["grid"] == min(152 // ks, math.ceil(N / 8)) * ks
                     assert 2 <= p["stages"] and p["smem_bytes"] <= GB300["smem_optin"]
-                    assert p["k_splits"] == 1
 
 
 def test_describe_device_without_a_gpu_is_an_error(lib):
@@ -151,3 +152,22 @@ def test_describe_device_without_a_gpu_is_an_error(lib):
         with pytest.raises(_lib.W4Error) as e:
             lib.w4_describe_device()
         assert e.value.status == 4
+
+
+def test_k_splits_only_when_forced(lib):
+    """DP4A GEMVs split K over a cluster only when W4_TUNE_K_SPLITS asks for it
+    (a split measured slower on every shape tried, the few-tile GEMVs
+    included), for one or two tokens and where every split keeps at least 16
+    chunks; the grid is then a cluster per tile range."""
+    for fmt, N, K in (("w4", 512, 3584), ("q4_0", 1536, 6144), ("q4_0", 2560, 1536), ("w4", 152064, 3584)):
+        assert plan(lib, fmt, 1, N, K)["k_splits"] == 1
+    lib.set_tuning("k_splits", 4)
+    try:
+        p = plan(lib, "w4", 1, 512, 3584)
+        assert (p["k_splits"], p["grid"]) == (4, 38 * 4)
+        assert plan(lib, "w4", 2, 4608, 3584)["k_splits"] == 4
+        assert plan(lib, "w4", 3, 4608, 3584)["k_splits"] == 1       # four tokens' kernel: no split
+        assert plan(lib, "w4", 1, 8, 64)["k_splits"] == 1            # two chunks: nothing to split
+    finally:
+        lib.set_tuning("k_splits", 0)
+    assert lib.load().w4_set_tuning(5, 3) == 1                      # splits: 0, 1, 2, 4 or 8

@@ -31,9 +31,10 @@
 //     nibbles into e4m3 bytes (two LOP3 and a shift per 8 weights; each half
 //     takes 128 of the block's 256 K) and store them into tensor memory as
 //     the MMA's A operand (three buffers of 64 columns).  The same threads copy the block's
-//     codes (a small cp.async ring), split them and write the activation
-//     tile (B, shared memory, K-major, no swizzle): half 0 the high halves,
-//     half 1 the low halves.
+//     codes (a small cp.async ring), split each code once and write both
+//     halves into the activation tile (B, shared memory, K-major, no
+//     swizzle): thread t takes token t % 16 in one 16-K group, so eight
+//     consecutive threads store 128 contiguous bytes.
 //   * Lane 0 of warp 8 issues a block's eight MMAs (K slice kk into
 //     accumulator kk % 2, so consecutive MMAs are independent; the two exact
 //     partial sums are added at the end) and commits them; warp 9 issues the
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     const int ntl = min(kTcRows / kRows, A.T - tile0);     // 8-row tiles present
 
     if (tid == 0) {
+        for (int n = 0; n < kTcTok; ++n) xsum_s[n] = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(full_b + 8 * s, 1);
             mbar_init(empty_b + 8 * s, kTcDqWarps);
@@ -270,20 +272,21 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         const int half = tid / kTcRows;
         const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint8_t* my_units = ring + (row >> 3) * (kTcStageChunks * kRows * 16) + (row & 7) * 16;
-        // Activation codes: thread t copies token (t % 128) / 8, the 32 codes of
-        // chunk t % 8 of each K block through a small ring (its own bytes only).
-        const int cn = row >> 3;
-        const int cpart = row & 7;
+        // Activation codes: thread t copies the 16 codes of token t % 16 in K
+        // group kg = (t % 128) / 16 + 8 half (16 K of each block's 256) through a
+        // small ring (its own bytes only).
+        const int cn = row & (kTcTok - 1);
+        const int kg = (row >> 4) + 8 * half;
         constexpr int kHalfChunks = kTcChunks / 2;
-        int xsum = 0;       // this thread's code sum (token cn) over the split's K range (half 0)
+        static_assert(kTcThreadCodes == 16 && kTcRows / kTcTok * 2 * kTcThreadCodes == kTcKb,
+                      "each dequantizing thread copies one 16-K group of one token");
+        int xsum = 0;       // this thread's code sum (token cn, K group kg) over the split's K range
         auto fetch_codes = [&](int b, int cs) {
             uint8_t* dst = codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
-            const int kofs = (cb + b * kTcChunks) * 32 + cpart * kTcThreadCodes;
+            const int kofs = (cb + b * kTcChunks) * 32 + kg * kTcThreadCodes;
             const bool ok = b < nb && cn < A.M && kofs < ce * 32;
             const int8_t* src = ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx;
-#pragma unroll
-            for (int e = 0; e < kTcThreadCodes / 16; ++e)
-                cp_async16(dst + 16 * e, ok ? src + 16 * e : A.qx, ok ? 16u : 0u);
+            cp_async16(dst, src, ok ? 16u : 0u);
             cp_async_commit();
         };
 #pragma unroll
@@ -343,27 +346,24 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
                 }
                 tmem_st16(tbase + tlane + kTcColA + j * kTcAStride + 32 * half + 16 * r, h);
             }
-            // B: token cn, K groups 2 cpart and 2 cpart + 1 (16 K each) of the block:
-            // the high halves in column cn, the low halves in column 16 + cn
+            // B: token cn, K group kg of the block: the high halves in column cn,
+            // the low halves in column 16 + cn
             cp_async_wait_group<kTcCodeRing - 1>();
-            const uint8_t* my_codes = codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
-#pragma unroll
-            for (int e = 0; e < kTcThreadCodes / 16; ++e) {
-                const uint4 c = *reinterpret_cast<const uint4*>(my_codes + 16 * e);
+            {
+                const uint4 c = *reinterpret_cast<const uint4*>(codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) +
+                                                                tid * kTcThreadCodes);
                 uint4 hv, lv;
                 tc_split4(c.x, hv.x, lv.x);
                 tc_split4(c.y, hv.y, lv.y);
                 tc_split4(c.z, hv.z, lv.z);
                 tc_split4(c.w, hv.w, lv.w);
-                uint8_t* bt = bbuf + j * kTcBBytes + (2 * cpart + e) * kTcBlbo + (cn & 7) * 16 +
-                              (2 * half + (cn >> 3)) * kTcBsbo;
-                *reinterpret_cast<uint4*>(bt) = half == 0 ? hv : lv;
-                if (half == 0) {
-                    xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
-                    xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
-                    xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
-                    xsum = __dp4a(static_cast<int>(c.w), 0x01010101, xsum);
-                }
+                uint8_t* bt = bbuf + j * kTcBBytes + kg * kTcBlbo + (cn & 7) * 16 + (cn >> 3) * kTcBsbo;
+                *reinterpret_cast<uint4*>(bt) = hv;
+                *reinterpret_cast<uint4*>(bt + 2 * kTcBsbo) = lv;
+                xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);
+                xsum = __dp4a(static_cast<int>(c.y), 0x01010101, xsum);
+                xsum = __dp4a(static_cast<int>(c.z), 0x01010101, xsum);
+                xsum = __dp4a(static_cast<int>(c.w), 0x01010101, xsum);
             }
             fence_proxy_async_smem();
             tmem_wait_st();
@@ -371,10 +371,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
             ready_arrive(j);
         }
         cp_async_wait_group<0>();
-        // token cn's code sum: its eight threads are lanes 8k..8k+7 of one warp
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) xsum += __shfl_xor_sync(0xffffffffu, xsum, off);
-        if (cpart == 0 && half == 0) xsum_s[cn] = xsum;
+        // token cn's code sum: lanes cn and cn + 16 of each of the eight warps
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 16);
+        if (lane < kTcTok) atomicAdd(xsum_s + cn, xsum);
     }
     __syncthreads();
 

@@ -27,14 +27,14 @@
 //   * Packed weights stream through a ring of stages (512 K x 128 rows,
 //     32 KB: one 2 KB bulk copy per 8-row tile) issued before the dependency
 //     wait; the operand pipeline steps through the stage in two 256-K blocks.
-//   * Warps 0-7 (thread t: row t % 128, half t / 128) mask their row's
-//     nibbles into e4m3 bytes (two LOP3 and a shift per 8 weights; each half
-//     takes 128 of the block's 256 K) and store them into tensor memory as
-//     the MMA's A operand (three buffers of 64 columns).  The same threads copy the block's
-//     codes (a small cp.async ring), split each code once and write both
-//     halves into the activation tile (B, shared memory, K-major, no
-//     swizzle): thread t takes token t % 16 in one 16-K group, so eight
-//     consecutive threads store 128 contiguous bytes.
+//   * Warps 0-7 form two groups that take alternate K blocks.  Thread t of a
+//     group masks row t % 128's nibbles into e4m3 bytes (two LOP3 and a shift
+//     per 8 weights, the block's whole 256 K) and stores them into tensor
+//     memory as the MMA's A operand (three buffers of 64 columns).  The same
+//     threads copy the block's codes (a small cp.async ring), split each code
+//     once and write both halves into the activation tile (B, shared memory,
+//     K-major, no swizzle): thread t takes token t % 16 in two 16-K groups,
+//     so eight consecutive threads store 128 contiguous bytes.
 //   * Lane 0 of warp 8 issues a block's eight MMAs (K slice kk into
 //     accumulator kk % 2, so consecutive MMAs are independent; the two exact
 //     partial sums are added at the end) and commits them; warp 9 issues the
@@ -92,7 +92,7 @@ __device__ __forceinline__ void tc_split4(uint32_t c, uint32_t& hi, uint32_t& lo
 {
     lo = c & 0x0F0F0F0Fu;
     const uint32_t u = (c >> 4) & 0x0F0F0F0Fu;              // h + 16 for negative h
-    const uint32_t bm = ((u & 0x08080808u) >> 3) * 0xFFu;    // 0xFF in the bytes of negative h
+    const uint32_t bm = prmt_sign_bytes(c);                  // 0xFF in the bytes of negative x (so of h)
     const uint32_t m = (u ^ (bm & 0x0F0F0F0Fu)) + (bm & 0x01010101u);   // |h| = 16 - u there
     hi = m | (bm & 0x80808080u);
 }
@@ -115,9 +115,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     const uint32_t full_b = bars;                        // [S]  stage landed (1 arrival + bytes)
     const uint32_t empty_b = bars + 8 * S;               // [S]  stage read by the dequantizing warps
     const uint32_t free_b = bars + 16 * S;               // [kTcBufs]  MMAs reading an operand buffer completed
-    // operand buffer j written by the dequantizing warps: named barrier 1 + j
-    // (those warps and the MMA warp)
-    constexpr uint32_t kReadyCount = (kTcDqWarps + 1) * 32;
+    // operand buffer j written by one group of four dequantizing warps: named
+    // barrier 1 + j (that group and the MMA warp)
+    constexpr uint32_t kReadyCount = (kTcDqWarps / 2 + 1) * 32;
     auto ready_arrive = [](int j) {
         if (j == 0) named_arrive(1, kReadyCount);
         else if (j == 1) named_arrive(2, kReadyCount);
@@ -264,53 +264,58 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
                 if (!mbar_wait_bounded(full_b + 8 * (k % S), static_cast<uint32_t>(k / S) & 1u, kTcWaitNs)) break;
     } else {
         // ------------------------------------------- warps 0-7: A and B
-        // Thread t works on row t % 128 (tensor-memory lane t % 128, which warp
-        // t / 32 reaches as warp (t / 32) % 4 does); half t / 128 stores chunks
-        // 4 half .. 4 half + 3 of each K block and writes the high (half 0) or
-        // low (half 1) code halves of B.
+        // Two warp groups take alternate K blocks: group g = warp / 4 the blocks
+        // b = g, g + 2, ..., i.e. sub-block g of every weight stage.  Thread t
+        // works on row t % 128 (tensor-memory lane t % 128, which warp t / 32
+        // reaches as warp (t / 32) % 4 does) over the whole 256 K of its blocks,
+        // and splits the codes of token t % 16 in K groups (t % 128) / 16 and
+        // that + 8 (16 K each) into both halves of the activation tile B.  A
+        // group's per-block chain (waits, stores, fences, the hand-off) thus has
+        // two block periods to run while the other group fills the next buffer.
+        static_assert(kSubs == 2 && kTcDqWarps == 8, "two groups of four warps, one K block of a stage each");
         const int row = tid & (kTcRows - 1);
-        const int half = tid / kTcRows;
+        const int grp = warp >> 2;
         const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint8_t* my_units = ring + (row >> 3) * (kTcStageChunks * kRows * 16) + (row & 7) * 16;
-        // Activation codes: thread t copies the 16 codes of token t % 16 in K
-        // group kg = (t % 128) / 16 + 8 half (16 K of each block's 256) through a
-        // small ring (its own bytes only).
+        const uint8_t* my_units =
+            ring + (row >> 3) * (kTcStageChunks * kRows * 16) + (grp * kTcChunks) * kRows * 16 + (row & 7) * 16;
         const int cn = row & (kTcTok - 1);
-        const int kg = (row >> 4) + 8 * half;
-        constexpr int kHalfChunks = kTcChunks / 2;
-        static_assert(kTcThreadCodes == 16 && kTcRows / kTcTok * 2 * kTcThreadCodes == kTcKb,
-                      "each dequantizing thread copies one 16-K group of one token");
-        int xsum = 0;       // this thread's code sum (token cn, K group kg) over the split's K range
+        const int kg = row >> 4;
+        static_assert(kTcThreadCodes == 32 && kTcRows * kTcThreadCodes == kTcTok * kTcKb,
+                      "each dequantizing thread copies two 16-K groups of one token per block");
+        int xsum = 0;       // this thread's code sum (token cn, its K groups) over the split's K range
         auto fetch_codes = [&](int b, int cs) {
             uint8_t* dst = codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
-            const int kofs = (cb + b * kTcChunks) * 32 + kg * kTcThreadCodes;
-            const bool ok = b < nb && cn < A.M && kofs < ce * 32;
-            const int8_t* src = ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx;
-            cp_async16(dst, src, ok ? 16u : 0u);
+            const int kbase = (cb + b * kTcChunks) * 32;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int kofs = kbase + (kg + 8 * e) * 16;
+                const bool ok = b < nb && cn < A.M && kofs < ce * 32;
+                cp_async16(dst + 16 * e, ok ? A.qx + static_cast<size_t>(cn) * A.K + kofs : A.qx, ok ? 16u : 0u);
+            }
             cp_async_commit();
         };
 #pragma unroll
-        for (int i = 0; i < kTcCodeRing - 1; ++i) fetch_codes(i, i);
+        for (int i = 0; i < kTcCodeRing - 1; ++i) fetch_codes(grp + 2 * i, i);
         // ring positions kept as counters (no division in the loop): weight
-        // stage slot and its phase, operand buffer j and the phase of its
-        // previous commit, code-ring slots of this block and of the one fetched
-        int slot = 0, j = 0, cs = 0, cs_next = kTcCodeRing - 1;
-        uint32_t sph = 0u, jph = 1u;
-        for (int b = 0; b < nb; ++b) {
-            const int sub = b & (kSubs - 1);
-            if (b > 0) {
-                if (sub == 0 && ++slot == S) { slot = 0; sph ^= 1u; }
-                if (++j == kTcBufs) { j = 0; jph ^= 1u; }
+        // stage slot and its phase, operand buffer j = b % 3 and q = b / 3 (the
+        // previous commit on buffer j is that of block b - 3, phase (q - 1) & 1),
+        // code-ring slots of this block and of the one fetched
+        int slot = 0, j = grp, q = 0, cs = 0, cs_next = kTcCodeRing - 1;
+        uint32_t sph = 0u;
+        for (int b = grp; b < nb; b += 2) {
+            if (b > grp) {
+                if (++slot == S) { slot = 0; sph ^= 1u; }
+                j += 2;
+                if (j >= kTcBufs) { j -= kTcBufs; ++q; }
                 if (++cs == kTcCodeRing) cs = 0;
                 if (++cs_next == kTcCodeRing) cs_next = 0;
             }
             const int nch = min(kTcChunks, ce - (cb + b * kTcChunks));
-            fetch_codes(b + kTcCodeRing - 1, cs_next);
+            fetch_codes(b + 2 * (kTcCodeRing - 1), cs_next);
             // buffer j is free once the commit of block b - kTcBufs arrived (the MMA
             // lane commits every block, failed or not, so this wait keeps its order)
-            bool ok = b < kTcBufs || mbar_wait_bounded(free_b + 8 * j, jph, kTcWaitNs);
-            if (ok && !*dead_s && sub == 0)
-                ok = mbar_wait_bounded(full_b + 8 * slot, sph, kTcWaitNs);
+            bool ok = b < kTcBufs || mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>(q - 1) & 1u, kTcWaitNs);
+            if (ok && !*dead_s) ok = mbar_wait_bounded(full_b + 8 * slot, sph, kTcWaitNs);
             if (!__all_sync(0xffffffffu, ok) && lane == 0 && !*dead_s) fail();
             if (*dead_s) {
                 // stop working but keep the per-block handshake
@@ -319,45 +324,48 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
                 continue;
             }
             tc_fence_after();
-            const int c0 = kHalfChunks * half;
-            uint4 u[kHalfChunks];
+            // the block's 256 K of this row as e4m3 (the buffer's 64 columns) in two
+            // halves of four chunks, sixteen columns per store
+            const uint8_t* units = my_units + static_cast<size_t>(slot) * kTcStageBytes;
 #pragma unroll
-            for (int e = 0; e < kHalfChunks; ++e)
-                if (c0 + e < nch)
-                    u[e] = *reinterpret_cast<const uint4*>(my_units + static_cast<size_t>(slot) * kTcStageBytes +
-                                                           (sub * kTcChunks + c0 + e) * kRows * 16);
-            if (sub == kSubs - 1 || b == nb - 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // the stage's bytes are in registers
-            }
-            // this half of the block's 256 K as e4m3: 32 of the buffer's 64 columns,
-            // sixteen at a time
+            for (int hf = 0; hf < 2; ++hf) {
+                constexpr int kQ = kTcChunks / 2;
+                uint4 u[kQ];
 #pragma unroll
-            for (int r = 0; r < kHalfChunks / 2; ++r) {
-                uint32_t h[16];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    if (c0 + 2 * r + e < nch) {
-                        tc_unit_e4m3(u[2 * r + e], &h[e * 8]);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) h[e * 8 + k] = 0u;
-                    }
+                for (int e = 0; e < kQ; ++e)
+                    if (kQ * hf + e < nch) u[e] = *reinterpret_cast<const uint4*>(units + (kQ * hf + e) * kRows * 16);
+                if (hf == 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // this group's block of the stage is read
                 }
-                tmem_st16(tbase + tlane + kTcColA + j * kTcAStride + 32 * half + 16 * r, h);
+#pragma unroll
+                for (int r = 0; r < kQ / 2; ++r) {
+                    uint32_t h[16];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (kQ * hf + 2 * r + e < nch) {
+                            tc_unit_e4m3(u[2 * r + e], &h[e * 8]);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) h[e * 8 + k] = 0u;
+                        }
+                    }
+                    tmem_st16(tbase + tlane + kTcColA + j * kTcAStride + 32 * hf + 16 * r, h);
+                }
             }
-            // B: token cn, K group kg of the block: the high halves in column cn,
-            // the low halves in column 16 + cn
+            // B: token cn, K groups kg and kg + 8 of the block: the high halves in
+            // column cn, the low halves in column 16 + cn
             cp_async_wait_group<kTcCodeRing - 1>();
-            {
-                const uint4 c = *reinterpret_cast<const uint4*>(codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) +
-                                                                tid * kTcThreadCodes);
+            const uint8_t* mc = codes + cs * (kTcDqWarps * 32 * kTcThreadCodes) + tid * kTcThreadCodes;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint4 c = *reinterpret_cast<const uint4*>(mc + 16 * e);
                 uint4 hv, lv;
                 tc_split4(c.x, hv.x, lv.x);
                 tc_split4(c.y, hv.y, lv.y);
                 tc_split4(c.z, hv.z, lv.z);
                 tc_split4(c.w, hv.w, lv.w);
-                uint8_t* bt = bbuf + j * kTcBBytes + kg * kTcBlbo + (cn & 7) * 16 + (cn >> 3) * kTcBsbo;
+                uint8_t* bt = bbuf + j * kTcBBytes + (kg + 8 * e) * kTcBlbo + (cn & 7) * 16 + (cn >> 3) * kTcBsbo;
                 *reinterpret_cast<uint4*>(bt) = hv;
                 *reinterpret_cast<uint4*>(bt + 2 * kTcBsbo) = lv;
                 xsum = __dp4a(static_cast<int>(c.x), 0x01010101, xsum);

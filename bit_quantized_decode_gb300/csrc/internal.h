@@ -199,7 +199,7 @@ cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, s
 // Per-row INT4 GEMV for 5..16 tokens on the tcgen05 tensor cores
 // (gemv_tc.cu): one block of kTcThreads per (128-row group, K split), the
 // K splits of a row group forming one thread-block cluster.
-constexpr int kTcDqWarps = 8;                    // warps 0-7: A (rows 0-127 twice: chunks 0-3 / 4-7) and B
+constexpr int kTcDqWarps = 8;                    // warps 0-7: A and B, two groups of four on alternate K blocks
 constexpr int kTcThreads = (kTcDqWarps + 2) * 32;  // then the MMA warp and the copy warp
 constexpr int kTcRows = 128;                     // MMA M: weight rows per block
 constexpr int kTcTok = 16;                       // MMA N: tokens (fewer are zero-padded)
@@ -208,7 +208,7 @@ constexpr int kTcKb = 32 * kTcChunks;            // K per block: 256
 constexpr int kTcStageChunks = 16;              // chunks per weight-ring stage (2 K blocks): 2 KB copies per tile
 constexpr int kTcStageBytes = (kTcRows / kRows) * kTcStageChunks * kRows * 16;   // 32 KB of packed weights
 constexpr int kTcBBytes = 2 * kTcTok * kTcKb;    // e4m3 activation tile per K block (high and low halves)
-constexpr int kTcThreadCodes = kTcKb / 16;       // codes a dequantizing thread copies per K block
+constexpr int kTcThreadCodes = kTcKb / 8;        // codes a dequantizing thread copies per K block (its group's)
 constexpr int kTcCodeRing = 3;                   // K blocks of int8 codes in flight
 constexpr int kTcBufs = 3;                       // A (tensor memory) / B (shared memory) operand buffers
 constexpr int kTcMaxSplit = 8;                   // K splits (cluster size) at most

@@ -316,6 +316,16 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
 }
 
 // --------------------------------------------------------------- integer
+// 0xFF in each byte of c whose sign bit is set, 0x00 in the others: prmt in
+// its default mode with selector bit 3 set replicates the selected byte's
+// sign bit over the result byte (__byte_perm keeps only the low 3 bits).
+__device__ __forceinline__ uint32_t prmt_sign_bytes(uint32_t c)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(r) : "r"(c));
+    return r;
+}
+
 // DP4A: c + sum_k a_k * b_k over the four signed bytes of a and b.
 __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
 {

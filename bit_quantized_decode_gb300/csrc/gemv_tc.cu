@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     const uint32_t full_b = bars;                        // [S]  stage landed (1 arrival + bytes)
     const uint32_t empty_b = bars + 8 * S;               // [S]  stage read by the dequantizing warps
     const uint32_t free_b = bars + 16 * S;               // [kTcBufs]  MMAs reading an operand buffer completed
+    const uint32_t red_b = bars + 8 * (2 * S + 2 * kTcBufs);   // the leader's: every other split's sums added
     // operand buffer j written by one group of four dequantizing warps: named
     // barrier 1 + j (that group and the MMA warp)
     constexpr uint32_t kReadyCount = (kTcDqWarps / 2 + 1) * 32;
@@ -154,9 +155,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         for (int j = 0; j < kTcBufs; ++j) {
             mbar_init(free_b + 8 * j, 1);         // the MMA lane's commit
         }
+        if (ks > 1 && split == 0) mbar_init(red_b, static_cast<uint32_t>((ks - 1) * kTcRows));
         fence_mbar_init();
         *dead_s = 0u;
     }
+    // the leader's K-split sums start at zero: the other splits add into them
+    int* red = reinterpret_cast<int*>(smem + L.red);
+    if (ks > 1 && split == 0)
+        for (int i = tid; i < kTcRows * kTcTok; i += kTcThreads) red[i] = 0;
     __syncthreads();
     pdl_launch_dependents();
 
@@ -181,13 +187,25 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     int issued = 0;      // stages whose weights were requested (producer warp)
     if (producer)
         for (; issued < S && issued < nst; ++issued) issue(issued);
-
-    // ---- inputs produced by earlier kernels (codes, scales) from here on
-    pdl_wait();
+    // the leader's zeroed sums and its barrier are visible to the whole cluster
+    // (all of this runs before the dependency wait, beside the previous kernel)
+    if (ks > 1) cluster_sync();
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTcCols);
         tmem_relinquish();
     }
+    // this row's output parameters do not depend on the previous kernel
+    const bool row_thread = tid < kTcRows;
+    const int row = g * kTcRows + tid;
+    const int prow = A.glu == GLU_NONE ? (row < A.N ? row : -1) : glu_param_row(row, A.n_out);
+    float sw_r = 0.0f, bv_r = 0.0f;
+    if (row_thread && split == 0 && prow >= 0) {
+        sw_r = A.s_w[prow];
+        bv_r = A.bias != nullptr ? A.bias[prow] : 0.0f;
+    }
+
+    // ---- inputs produced by earlier kernels (codes, scales) from here on
+    pdl_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -387,7 +405,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
 
     // ---- the accumulator: row tid, tokens 0..15 (warps 0-3)
     const bool dead = *dead_s != 0u;
-    const bool row_thread = tid < kTcRows;
     int acc[kTcTok];
 #pragma unroll
     for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
@@ -417,33 +434,25 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         tmem_dealloc(tbase, kTcCols);
     }
 
-    // ---- K splits: partial sums into the leader's ring (every block of the
-    // cluster is past its K loop after the first cluster barrier)
+    // ---- K splits: every other split adds its exact integer sums into the
+    // leader's (red[n][row], integer adds in any order give the same sums),
+    // arrives once per row thread on the leader's barrier and exits; only the
+    // leader waits, for the last of them.
     if (ks > 1) {
-        int* red = reinterpret_cast<int*>(smem + L.red);
-        cluster_sync();
-        if (row_thread) {
-            const uint32_t dst = mapa_shared(smem_u32(red + (split * kTcRows + tid) * kTcTok), 0);
+        if (split != 0) {
+            if (row_thread) {
+                const uint32_t dst = mapa_shared(smem_u32(red + tid), 0);
 #pragma unroll
-            for (int n = 0; n < kTcTok; n += 4)
-                st_cluster_v4(dst + 4 * n, static_cast<uint32_t>(acc[n]), static_cast<uint32_t>(acc[n + 1]),
-                              static_cast<uint32_t>(acc[n + 2]), static_cast<uint32_t>(acc[n + 3]));
-        }
-        cluster_sync();
-        if (split != 0 || !row_thread) return;
-#pragma unroll
-        for (int n = 0; n < kTcTok; ++n) acc[n] = 0;
-        for (int r = 0; r < ks; ++r) {
-            const int4* p = reinterpret_cast<const int4*>(red + (r * kTcRows + tid) * kTcTok);
-#pragma unroll
-            for (int q = 0; q < kTcTok / 4; ++q) {
-                const int4 v = p[q];
-                acc[4 * q] += v.x;
-                acc[4 * q + 1] += v.y;
-                acc[4 * q + 2] += v.z;
-                acc[4 * q + 3] += v.w;
+                for (int n = 0; n < kTcTok; ++n)
+                    red_add_cluster_u32(dst + 4 * n * kTcRows, static_cast<uint32_t>(acc[n]));
+                mbar_arrive_remote_release(mapa_shared(red_b, 0));
             }
+            return;
         }
+        if (!row_thread) return;
+        if (!mbar_wait_cluster_bounded(red_b, 0u, kTcWaitNs) && !dead) fail();
+#pragma unroll
+        for (int n = 0; n < kTcTok; ++n) acc[n] += red[n * kTcRows + tid];
     }
     if (!row_thread) return;
 
@@ -451,11 +460,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     // (a partial sum of a dead split makes the row wrong: the error word says so).
     // Every load (token scales, residuals) is issued before the first store: y
     // may alias the residual, so a store between two loads would serialise them.
-    const int row = g * kTcRows + tid;
+    const bool dead_out = *dead_s != 0u;
     if (A.glu == GLU_NONE) {
-        if (row < A.N && !dead) {
-            const float sw = A.s_w[row];
-            const float bv = A.bias != nullptr ? A.bias[row] : 0.0f;
+        if (row < A.N && !dead_out) {
+            const float sw = sw_r;
+            const float bv = bv_r;
             float v[kTcTok];
 #pragma unroll
             for (int n = 0; n < kTcTok; ++n)
@@ -476,11 +485,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         // gated: this thread's row pairs with the row 4 lanes away (gate rows
         // r % 8 < 4, up rows 4 below them, in the same tile).  The gate lane
         // writes output j for the even tokens, the up lane for the odd ones.
-        const int prow = glu_param_row(row, A.n_out);
-        const bool have = row < A.N && prow >= 0 && !dead;
+        const bool have = row < A.N && prow >= 0 && !dead_out;
         const bool up = (row & 4) != 0;
-        const float sw = have ? A.s_w[prow] : 0.0f;
-        const float bv = have && A.bias != nullptr ? A.bias[prow] : 0.0f;
+        const float sw = have ? sw_r : 0.0f;
+        const float bv = have ? bv_r : 0.0f;
         const int j = (row >> 3) * 4 + (row & 3);
         float v[kTcTok];
 #pragma unroll

@@ -209,7 +209,7 @@ constexpr int kTcStageChunks = 16;              // chunks per weight-ring stage 
 constexpr int kTcStageBytes = (kTcRows / kRows) * kTcStageChunks * kRows * 16;   // 32 KB of packed weights
 constexpr int kTcBBytes = 2 * kTcTok * kTcKb;    // e4m3 activation tile per K block (high and low halves)
 constexpr int kTcThreadCodes = kTcKb / 8;        // codes a dequantizing thread copies per K block (its group's)
-constexpr int kTcCodeRing = 3;                   // K blocks of int8 codes in flight
+constexpr int kTcCodeRing = 2;                   // K blocks of int8 codes in flight per warp group
 constexpr int kTcBufs = 3;                       // A (tensor memory) / B (shared memory) operand buffers
 constexpr int kTcMaxSplit = 8;                   // K splits (cluster size) at most
 constexpr int kTcMaxSplitK = 16384;              // K per split at most: |sum n l| <= 225 K stays below 2^24
@@ -241,8 +241,8 @@ __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
     L.ring = o;  o += stages * kTcStageBytes;
     L.bbuf = o;  o += kTcBufs * kTcBBytes;
     L.codes = o; o += kTcCodeRing * (kTcDqWarps * 32) * kTcThreadCodes;
-    L.red = L.ring;   // K-split partial sums reuse the ring once every block is past its K loop
-    L.bars = o;  o += (2 * stages + 2 * kTcBufs) * 8;
+    L.red = o;   o += splits > 1 ? kTcRows * kTcTok * 4 : 0;   // the leader's K-split sums
+    L.bars = o;  o += (2 * stages + 2 * kTcBufs + 1) * 8;
     L.tmem = o;  o += 16;
     L.xsum = o;  o += kTcTok * 4;
     L.total = o;

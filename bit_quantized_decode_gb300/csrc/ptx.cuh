@@ -194,6 +194,42 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// Atomic add of v to the 32-bit word at `addr` in the cluster shared window
+// (another block's shared memory); no result.
+__device__ __forceinline__ void red_add_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// One arrival on the mbarrier at `addr` in the cluster shared window, with
+// release semantics at cluster scope: this thread's earlier writes (remote
+// ones included) are visible to a thread whose cluster-scope acquire wait
+// observes the phase completing.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// Wait for phase `parity` of a local mbarrier with acquire semantics at
+// cluster scope (arrivals from other blocks of the cluster), giving up after
+// `timeout_ns`.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.b32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
 // Cluster-wide barrier: every thread of every block in the cluster arrives
 // (release) and waits (acquire); shared-memory stores to any block of the
 // cluster made before it are visible after it.  All threads must execute it.

@@ -378,7 +378,6 @@ w4_status tc_plan(const DeviceInfo& d, int N, int K, int& ks, int& S)
     S = 4;
     while (S > 2 && tc_smem(S, ks).total > half) --S;
     if (tc_smem(S, ks).total > d.smem_optin) return W4_ERR_UNSUPPORTED_SHAPE;
-    if (S * kTcStageBytes < ks * kTcRows * kTcTok * 4) return W4_ERR_UNSUPPORTED_SHAPE;   // partial sums fit the ring
     return W4_OK;
 }
 

@@ -209,6 +209,9 @@ __device__ __forceinline__ bool chain_wait(const unsigned* count, unsigned targe
         if (!ok && err != nullptr) atomicExch(err, kErrBarrierTimeout);
         *flag_s = ok ? 1 : 0;
     }
+    // thread 0's spin is divergent: reconverge warp 0 before the barrier
+    // (bar.sync is the aligned form, which assumes a converged warp)
+    __syncwarp();
     block_sync<kConsumerBar, kChainConsumers>();
     return *flag_s != 0;
 }

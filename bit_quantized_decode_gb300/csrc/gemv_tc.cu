@@ -35,12 +35,14 @@
 //     once and write both halves into the activation tile (B, shared memory,
 //     K-major, no swizzle): thread t takes token t % 16 in two 16-K groups,
 //     so eight consecutive threads store 128 contiguous bytes.
-//   * Lane 0 of warp 8 issues a block's eight MMAs (K slice kk into
-//     accumulator kk % 2, so consecutive MMAs are independent; the two exact
-//     partial sums are added at the end) and commits them; warp 9 issues the
-//     weight copies.  "Operands written" is a named barrier per buffer (warps
-//     0-8), "operands read" the MMA commit's mbarrier, and the ring has full /
-//     empty mbarriers: no block-wide barrier sits in the K loop.
+//   * Lane 0 of warp 8 issues a block's eight MMAs into one accumulator (a
+//     second one, alternating, made the K loop no faster and doubled the
+//     tensor-memory reads at the end) and commits them; warp 9 issues the
+//     weight copies.  "Operands written" is a named barrier per buffer (one
+//     warp group and warp 8), "operands read" the MMA commit's mbarrier, and
+//     the ring has full / empty mbarriers: no block-wide barrier sits in the
+//     K loop.  Warp 8 also allocates and frees the tensor memory, so warps
+//     0-3 go from the accumulator read straight to the epilogue.
 //   * What bounds it is the latency of the dequantizing warps' per-block
 //     chain (shared-memory loads, tensor-memory stores and their wait, the
 //     named barrier to the MMA lane, the commit's mbarrier), not HBM, the
@@ -63,7 +65,7 @@ constexpr uint32_t kTcCols = 256;     // tensor-memory columns: A x 3 (64 each),
 constexpr uint32_t kTcColA = 0;
 constexpr uint32_t kTcAStride = kTcKb / 4;   // one K block of e4m3 A: 4 bytes per column
 constexpr uint32_t kTcColD = kTcColA + kTcBufs * kTcAStride;
-constexpr int kTcAccs = 2;            // accumulators: consecutive MMAs do not wait on each other
+constexpr int kTcAccs = 1;            // accumulators (K slice kk into D[kk % kTcAccs])
 // Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3
 // (bits 7-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     static_assert(kTcColD + kTcAccs * kTcN <= kTcCols, "tensor-memory columns");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem);   // [0] base address, [1] stop flag
     int* xsum_s = reinterpret_cast<int*>(smem + L.xsum);                 // [kTcTok] code sums of the split
+    float* sx_s = reinterpret_cast<float*>(smem + L.sx);                 // [kTcTok] token scales
     volatile uint32_t* dead_s = tmem_slot + 1;
 
     constexpr int kSubs = kTcStageChunks / kTcChunks;      // K blocks per ring stage
@@ -190,7 +193,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     // the leader's zeroed sums and its barrier are visible to the whole cluster
     // (all of this runs before the dependency wait, beside the previous kernel)
     if (ks > 1) cluster_sync();
-    if (warp == 0) {
+    // the MMA warp holds the tensor memory (it frees it while warps 0-3 write y)
+    if (mma_warp) {
         tmem_alloc(smem_u32(tmem_slot), kTcCols);
         tmem_relinquish();
     }
@@ -206,6 +210,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
 
     // ---- inputs produced by earlier kernels (codes, scales) from here on
     pdl_wait();
+    // token scales for the epilogue, fetched while the K loop runs (the MMA
+    // warp waits for them before the block barrier that ends the loop)
+    if (mma_warp) {
+        if (lane < kTcTok) cp_async4(sx_s + lane, lane < A.M ? A.sx + lane : A.sx, lane < A.M ? 4u : 0u);
+        cp_async_commit();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -230,20 +240,21 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
                 if (!*dead_s) {
                     // K slice kk (32 K: 8 tensor-memory columns of A, 1024 B of B, which is
                     // 64 in the descriptor's address field and cannot carry) accumulates
-                    // into D[kk % 2]; the first block's first two slices overwrite.
+                    // into D[kk % kTcAccs]; the first block's first slice per accumulator
+                    // overwrites.
                     tc_fence_after();
                     const uint64_t bdesc = smem_desc_noswizzle(smem_u32(bbuf + j * kTcBBytes), kTcBlbo, kTcBsbo);
                     const uint32_t acol = tbase + kTcColA + j * kTcAStride;
-                    static_assert(kTcAccs == 2 && kTcChunks == 8, "eight MMAs per block, four per accumulator");
+                    static_assert((kTcAccs == 1 || kTcAccs == 2) && kTcChunks == 8, "eight MMAs per block");
+                    constexpr uint32_t d1 = (1 % kTcAccs) * kTcN;
                     if (nch == kTcChunks && b > 0) {
-                        tc_mma_f8_ts_x4(dcol, dcol + kTcN, dcol, dcol + kTcN, acol, bdesc, kTcIdesc, 1u);
-                        tc_mma_f8_ts_x4(dcol, dcol + kTcN, dcol, dcol + kTcN, acol + 32, bdesc + 256,
-                                        kTcIdesc, 1u);
+                        tc_mma_f8_ts_x4(dcol, dcol + d1, dcol, dcol + d1, acol, bdesc, kTcIdesc, 1u);
+                        tc_mma_f8_ts_x4(dcol, dcol + d1, dcol, dcol + d1, acol + 32, bdesc + 256, kTcIdesc, 1u);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < kTcChunks; ++kk)
                             if (kk < nch)
-                                tc_mma_f8_ts(dcol + (kk & 1) * kTcN, acol + kk * 8,
+                                tc_mma_f8_ts(dcol + (kk % kTcAccs) * kTcN, acol + kk * 8,
                                              bdesc + static_cast<uint64_t>(kk * 64), kTcIdesc,
                                              b > 0 || kk >= kTcAccs ? 1u : 0u);
                     }
@@ -262,6 +273,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
             }
             if (committed < nb && !*dead_s) fail();
         }
+        // lane 0's wait above is a divergent loop: reconverge the warp before the
+        // block barrier (bar.sync is the aligned form, which assumes a converged
+        // warp), so the barrier follows the last MMA's completion
+        __syncwarp();
+        cp_async_wait_group<0>();   // the token scales
     } else if (producer) {
         // ---------------------------------------------------- producer warp
         // refill each stage's slot once warps 0-7 have read it
@@ -280,6 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         if (lane == 0 && *dead_s)
             for (int k = issued - S > 0 ? issued - S : 0; k < issued; ++k)
                 if (!mbar_wait_bounded(full_b + 8 * (k % S), static_cast<uint32_t>(k / S) & 1u, kTcWaitNs)) break;
+        __syncwarp();
     } else {
         // ------------------------------------------- warps 0-7: A and B
         // Two warp groups take alternate K blocks: group g = warp / 4 the blocks
@@ -400,6 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         // token cn's code sum: lanes cn and cn + 16 of each of the eight warps
         xsum += __shfl_xor_sync(0xffffffffu, xsum, 16);
         if (lane < kTcTok) atomicAdd(xsum_s + cn, xsum);
+        __syncwarp();
     }
     __syncthreads();
 
@@ -417,8 +435,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         const int used = min(kTcAccs, min(kTcChunks, ce - cb));   // accumulators written at all
         for (int q = 0; q < used; ++q) {
             uint32_t dh[kTcTok], dl[kTcTok];
-            tmem_ld16(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcN, dh);
-            tmem_ld16(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcN + kTcTok, dl);
+            const uint32_t da = tbase + (static_cast<uint32_t>(warp * 32) << 16) + kTcColD + q * kTcN;
+            tmem_ld16x2(da, dh, da + kTcTok, dl);
 #pragma unroll
             for (int n = 0; n < kTcTok; ++n)
                 acc[n] += 16 * __float2int_rn(__fmul_rn(__uint_as_float(dh[n]), 262144.0f)) +
@@ -429,7 +447,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (mma_warp) {
         tc_fence_after();
         tmem_dealloc(tbase, kTcCols);
     }
@@ -468,7 +486,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
             float v[kTcTok];
 #pragma unroll
             for (int n = 0; n < kTcTok; ++n)
-                v[n] = n < A.M ? __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv) : 0.0f;
+                v[n] = n < A.M ? __fmaf_rn(__fmul_rn(sw, sx_s[n]), __int2float_rn(acc[n]), bv) : 0.0f;
             if (A.residual != nullptr) {
                 float rv[kTcTok];
 #pragma unroll
@@ -493,7 +511,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         float v[kTcTok];
 #pragma unroll
         for (int n = 0; n < kTcTok; ++n)
-            v[n] = n < A.M ? __fmaf_rn(__fmul_rn(sw, A.sx[n]), __int2float_rn(acc[n]), bv) : 0.0f;
+            v[n] = n < A.M ? __fmaf_rn(__fmul_rn(sw, sx_s[n]), __int2float_rn(acc[n]), bv) : 0.0f;
         constexpr int kHalfTok = kTcTok / 2;
         float gv[kHalfTok], uv[kHalfTok], rv[kHalfTok];
 #pragma unroll

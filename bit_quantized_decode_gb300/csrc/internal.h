@@ -231,7 +231,7 @@ struct TcArgs {
 };
 
 struct TcSmem {
-    int ring, bbuf, codes, red, bars, tmem, xsum, total;
+    int ring, bbuf, codes, red, bars, tmem, xsum, sx, total;
 };
 
 __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
@@ -245,6 +245,7 @@ __host__ __device__ inline TcSmem tc_smem(int stages, int splits)
     L.bars = o;  o += (2 * stages + 2 * kTcBufs + 1) * 8;
     L.tmem = o;  o += 16;
     L.xsum = o;  o += kTcTok * 4;
+    L.sx = o;    o += kTcTok * 4;
     L.total = o;
     return L;
 }

@@ -4,7 +4,7 @@
 // 的数学推导"; the multi-token verify case of "在香橙派上跑 Gemma4", §五):
 //   acc[m][j] = sum_i q_w[j][i] qx[m][i]  (exact),
 //   y[m][j]   = fmaf(s_w[j] * sx[m], (float)acc[m][j], b[j])
-// for M = 5..16 tokens sharing one pass over the weights.  The int8 codes and
+// for M = 3..16 tokens sharing one pass over the weights.  The int8 codes and
 // scales come from the activation quantizer launched before this kernel.
 //
 // How (GB300 design): the product is a GEMM of N x K by K x 16, so it runs on

@@ -196,7 +196,7 @@ cudaError_t launch_gemv_a32(int fmt, const ChainParams<1>& p, int MT, int grid, 
 cudaError_t launch_chain_w4(const ChainParams<kMaxChain>& p, int MT, int grid, size_t smem, cudaStream_t s);
 
 // ---------------------------------------------- multi-token tensor-core GEMV
-// Per-row INT4 GEMV for 5..16 tokens on the tcgen05 tensor cores
+// Per-row INT4 GEMV for 3..16 tokens on the tcgen05 tensor cores
 // (gemv_tc.cu): one block of kTcThreads per (128-row group, K split), the
 // K splits of a row group forming one thread-block cluster.
 constexpr int kTcDqWarps = 8;                    // warps 0-7: A and B, two groups of four on alternate K blocks

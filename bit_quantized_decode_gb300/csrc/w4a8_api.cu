@@ -354,7 +354,7 @@ inline int weight_rows(int n, int glu) { return glu != GLU_NONE ? 8 * ((n + 3) /
 // up to kTcMaxSplit K splits of kTcMaxSplitK.
 bool use_tc(int fmt, int M, int K)
 {
-    const int lo = g_tune[W4_TUNE_TC_MIN_M] > 0 ? g_tune[W4_TUNE_TC_MIN_M] : 5;
+    const int lo = g_tune[W4_TUNE_TC_MIN_M] > 0 ? g_tune[W4_TUNE_TC_MIN_M] : 3;
     return fmt == FMT_W4 && M >= lo && M <= kTcTok && K <= kTcMaxSplit * kTcMaxSplitK;
 }
 

@@ -103,7 +103,7 @@ int w4_version(void);
  *   W4_TUNE_MAX_STAGES     cap on the ring depth per warp (>= 2).
  *   W4_TUNE_GRID_BLOCKS    cap on the grid size (default: the SM count).
  *   W4_TUNE_TC_MIN_M       per-row INT4 calls with at least this many tokens
- *                          run on the tensor cores (default 0: 5; 17: never).
+ *                          run on the tensor cores (default 0: 3; 17: never).
  *   W4_TUNE_K_SPLITS       DP4A GEMVs of one or two tokens: K split over a
  *                          cluster of 2, 4 or 8 blocks sharing a tile range
  *                          (where each split keeps at least 16 chunks of 32 K);
@@ -282,7 +282,7 @@ w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_st
  * w4a8_gemv, [Orin-INT4] §"从 FP 线性层到 INT4 DP4A 的数学推导" and §"DP4A 做了什么":
  *   acc[m][j] = sum_i q_w[j][i] * qx[m][i]   (exact int32),
  *   y[m][j]   = fmaf(s_w[j] * sx[m], (float)acc, b[j])   (b = 0 if bias NULL).
- *   Up to four tokens the sums run on DP4A; from five tokens (see
+ *   Up to two tokens the sums run on DP4A; from three tokens (see
  *   W4_TUNE_TC_MIN_M) on the tensor cores, with exact fp8 products and fp32
  *   partial sums.  y is bit-identical either way.
  * q4_0_gemv / i8g32_gemv / q6g32_gemv, [310B-Gemma4] §3.1 / §3.2:

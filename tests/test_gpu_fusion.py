@@ -327,7 +327,8 @@ def test_glu_linear_tensor_cores_and_uncached_rows(lib):
 # ------------------------------------------------------------- residual
 @pytest.mark.parametrize("fmt,M,N,K,tc", [("w4", 1, 3584, 3584, False), ("w4", 2, 3584, 18944, False),
                                           ("q4_0", 3, 1536, 6144, False), ("w4", 16, 3584, 3584, True),
-                                          ("i8g32", 1, 200, 1536, False), ("w4", 7, 1000, 3584, True)])
+                                          ("i8g32", 1, 200, 1536, False), ("w4", 7, 1000, 3584, True),
+                                          ("w4", 4, 264, 3584, False), ("w4", 3, 520, 6144, False)])
 def test_residual_linear_in_place(lib, fmt, M, N, K, tc):
     """y = residual + linear(x), with the residual buffer as the output (the
     decoder's in-place update): within the linear's tolerance plus the final

@@ -228,6 +228,34 @@ def test_w4a8_linear_fused(lib, M, N, K):
     check_close(host(y), y_ref, w4_scale(acc, sw, sx_ref, b), RTOL_W4, "w4a8_linear")
 
 
+@pytest.mark.parametrize("M,N,K", [(3, 77, 3584), (4, 600, 18944), (3, 129, 18944), (4, 1000, 3584)])
+def test_w4a8_dp4a_three_and_four_tokens(lib, M, N, K):
+    """Three and four tokens run on the tensor cores by default; the DP4A
+    kernels for them (fused prologue, codes in shared or global memory) stay
+    reachable through W4_TUNE_TC_MIN_M and are checked here the same way."""
+    torch = _torch()
+    g = wl.rng(13 * M + N + K)
+    W = wl.weights(g, N, K)
+    x = wl.activations(g, M, K)
+    b = wl.bias(g, N)
+    q, sw = oracle.quantize_rows_int4(W)
+    y_ref, qx_ref, sx_ref, acc = oracle.w4a8_linear(oracle.pack_int4(q), sw, x, b)
+    w, swd, bd = _prep_w4(lib, [q], sw, b, K)
+    lib.set_tuning("tc_min_m", 17)
+    try:
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        qx = torch.empty((M, K), dtype=torch.int8, device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        lib.w4a8_linear(w, swd, bd, dev(x), y, qx, sx)
+        y2 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        lib.w4a8_gemv(w, swd, bd, qx, sx, y2)
+    finally:
+        lib.set_tuning("tc_min_m", 0)
+    assert np.array_equal(host(qx), qx_ref)
+    check_close(host(y), y_ref, w4_scale(acc, sw, sx_ref, b), RTOL_W4, "dp4a linear")
+    check_close(host(y2), y_ref, w4_scale(acc, sw, sx_ref, b), RTOL_W4, "dp4a gemv")
+
+
 def test_w4a8_linear_deterministic_and_pdl(lib):
     torch = _torch()
     M, N, K = 1, 37888, 3584

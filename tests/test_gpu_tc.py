@@ -1,4 +1,4 @@
-"""The multi-token per-row INT4 GEMV on the tensor cores (by default M = 5..16;
+"""The multi-token per-row INT4 GEMV on the tensor cores (by default M = 3..16;
 the tests force it for any M, one token included).
 
 The accumulators must be the exact integer sums (read out through unit

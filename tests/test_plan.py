@@ -3,8 +3,9 @@
 The expected grids, shared-memory sizes, stages and K splits are those of the
 launches measured on a GB300 (ncu launch lists and -Xptxas/launch attributes of
 the 7B decode step): the one-token DP4A GEMV at 115,712 B (98,176 B at
-K = 18944) on 152 blocks, and the tensor-core GEMV at 114,848 B with clusters
-of 4 for QKV, O and down.  The launch path takes its decisions through the same
+K = 18944) on 152 blocks, and the tensor-core GEMV at 114,920 B with clusters
+of 4 for QKV, O and down (106,728 B for gate/up, whose K is not split: no
+buffer for the other splits' sums).  The launch path takes its decisions through the same
 functions, so these checks cover the host side of every GEMV launch.
 """
 import math
@@ -49,7 +50,8 @@ def test_sixteen_tokens_run_on_the_tensor_cores(lib, name, grid, splits):
     lin = {l.name: l for l in wl.qwen7b_layer()}[name]
     p = plan(lib, "w4", 16, lin.N, lin.K)
     assert p["path"] == "tensor_cores" and p["quantize_launches"] == 1
-    assert (p["grid"], p["k_splits"], p["threads"], p["smem_bytes"], p["stages"]) == (grid, splits, 320, 114848, 2)
+    smem = 114920 if splits > 1 else 106728
+    assert (p["grid"], p["k_splits"], p["threads"], p["smem_bytes"], p["stages"]) == (grid, splits, 320, smem, 2)
 
 
 def test_lm_head_and_largest_k_on_the_tensor_cores(lib):
@@ -60,8 +62,10 @@ def test_lm_head_and_largest_k_on_the_tensor_cores(lib):
 
 
 def test_token_threshold_and_formats(lib):
-    assert plan(lib, "w4", 4, 4608, 3584)["path"] == "fused"
-    for M in (5, 6, 7):
+    # measured: two tokens are faster on DP4A (1.39 against 1.43 ms per 7B step),
+    # three and four on the tensor cores (1.46 / 1.49 against 1.80 / 2.05 ms)
+    assert plan(lib, "w4", 2, 4608, 3584)["path"] == "fused"
+    for M in (3, 4, 5, 6, 7):
         assert plan(lib, "w4", M, 4608, 3584)["path"] == "tensor_cores"
     for fmt in ("q4_0", "i8g32", "q6g32"):        # the tensor-core path is per-row INT4 only
         assert plan(lib, fmt, 16, 2560, 1536)["path"] != "tensor_cores"
@@ -132,7 +136,6 @@ def test_invariants_over_a_shape_sweep(lib):
                     assert ks & (ks - 1) == 0 or ks == math.ceil(K / 16384) or ks == C
                     assert p["grid"] == math.ceil(N / 128) * ks
                     assert p["smem_bytes"] <= HALF                  # two blocks per SM
-                    assert p["stages"] * 32768 >= ks * 128 * 16 * 4  # partial sums fit the ring
                 else:
                     assert p["path"] in ("fused", "codes_smem", "codes_global")
                     ks = p["k_splits"]                                # DP4A: clusters of ks blocks
@@ -166,7 +169,7 @@ def test_k_splits_only_when_forced(lib):
         p = plan(lib, "w4", 1, 512, 3584)
         assert (p["k_splits"], p["grid"]) == (4, 38 * 4)
         assert plan(lib, "w4", 2, 4608, 3584)["k_splits"] == 4
-        assert plan(lib, "w4", 3, 4608, 3584)["k_splits"] == 1       # four tokens' kernel: no split
+        assert plan(lib, "q4_0", 3, 1536, 6144)["k_splits"] == 1     # three tokens' DP4A kernel: no split
         assert plan(lib, "w4", 1, 8, 64)["k_splits"] == 1            # two chunks: nothing to split
     finally:
         lib.set_tuning("k_splits", 0)

@@ -154,6 +154,72 @@ __global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float*
     if (tid == 0) sx[m] = ks.s;
 }
 
+// Long tokens (8192 <= K <= 32768): kQuantCluster blocks per token, in one
+// thread-block cluster.  Block r reads quarter r of the token's float4 words
+// into registers and takes its absmax; the blocks read one another's maxima
+// through distributed shared memory, so each holds the token's absmax, and
+// each quantizes its own quarter with a8_scale of that absmax: the codes and
+// the scale are the single-block kernel's, bit for bit (a maximum does not
+// depend on its order).  A block leaves only after every block has read its
+// maximum (the second half of the last cluster barrier).
+constexpr int kQuantCluster = 4;
+
+template <int NIT>
+__global__ void __launch_bounds__(kQuantThreads) a8_quantize_cluster_kernel(const float* __restrict__ x, int K,
+                                                                            int8_t* __restrict__ qx,
+                                                                            float* __restrict__ sx)
+{
+    __shared__ float red[kQuantWarps];
+    __shared__ float part;
+    const int m = blockIdx.x / kQuantCluster;
+    const int r = blockIdx.x - m * kQuantCluster;           // = rank in the cluster
+    const int tid = threadIdx.x;
+    const int K4 = K >> 2;
+    const int q0 = r * K4 / kQuantCluster;
+    const int q1 = (r + 1) * K4 / kQuantCluster;
+    const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K);
+    pdl_launch_dependents();
+    pdl_wait();
+    float4 v[NIT];
+    float mx = 0.0f;
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int i = q0 + tid + it * kQuantThreads;
+        v[it] = i < q1 ? __ldcg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        mx = fmaxf(mx, abs_max4(v[it]));
+    }
+    mx = warp_max(mx);
+    if ((tid & 31) == 0) red[tid >> 5] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kQuantWarps; ++w) a = fmaxf(a, red[w]);
+        part = a;
+    }
+    cluster_sync();                       // every block's maximum is written
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kQuantCluster; ++c)
+        amax = fmaxf(amax, __uint_as_float(ld_cluster_u32(mapa_shared(smem_u32(&part), static_cast<uint32_t>(c)))));
+    cluster_arrive_release();             // done with the other blocks' shared memory
+    const A8Scale ks = a8_scale(amax);
+    const bool all_exact = a8_needs_exact(ks);
+    const uint64_t rr = f2_pack(ks.r, ks.r);
+    uint32_t* out = reinterpret_cast<uint32_t*>(qx + static_cast<size_t>(m) * K);
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int i = q0 + tid + it * kQuantThreads;
+        if (i < q1) {
+            uint32_t ok = 0xffffffffu;
+            const uint32_t q = a8_pack4_fast2(v[it], rr, ok);
+            out[i] = (all_exact || (ok >> 31) == 0) ? a8_pack4_exact(v[it], ks) : q;
+        }
+    }
+    if (r == 0 && tid == 0) sx[m] = ks.s;
+    cluster_wait_acquire();
+}
+
 namespace {
 
 cudaLaunchConfig_t token_launch(int M, bool pdl, cudaStream_t s, cudaLaunchAttribute* attr)
@@ -189,6 +255,21 @@ cudaError_t launch_quant(const float* x, const float* gamma, float eps, int M, i
 
 cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, bool pdl, cudaStream_t s)
 {
+    const int per_block = (K / 4 + kQuantCluster - 1) / kQuantCluster;     // float4 words of a quarter
+    if (M > 0 && K >= 8192 && per_block <= 4 * kQuantThreads) {
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = token_launch(M, pdl, s, attr);
+        cfg.gridDim = dim3(static_cast<unsigned>(M * kQuantCluster));
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = kQuantCluster;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        ++cfg.numAttrs;
+        if (per_block <= 2 * kQuantThreads)
+            return cudaLaunchKernelEx(&cfg, a8_quantize_cluster_kernel<2>, x, K, qx, sx);
+        return cudaLaunchKernelEx(&cfg, a8_quantize_cluster_kernel<4>, x, K, qx, sx);
+    }
     return launch_quant<false>(x, nullptr, 0.0f, M, K, qx, sx, pdl, s);
 }
 

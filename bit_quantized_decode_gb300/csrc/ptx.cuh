@@ -230,6 +230,26 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
     }
 }
 
+// 32-bit load from the cluster shared window (another block's shared memory).
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// The two halves of a cluster-wide barrier, for work between them: arrive
+// (release: this thread's earlier writes are visible to a thread whose wait
+// completes) and wait (acquire).  Every thread executes both, in order.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Cluster-wide barrier: every thread of every block in the cluster arrives
 // (release) and waits (acquire); shared-memory stores to any block of the
 // cluster made before it are visible after it.  All threads must execute it.

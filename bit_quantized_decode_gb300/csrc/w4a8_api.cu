@@ -367,9 +367,18 @@ w4_status tc_plan(const DeviceInfo& d, int N, int K, int& ks, int& S)
 {
     const int C = K / 32;
     const int G = (N + kTcRows - 1) / kTcRows;
-    ks = (d.sms + G - 1) / G;
-    if (ks > kTcMaxSplit) ks = kTcMaxSplit;
-    while (ks & (ks - 1)) --ks;                 // clusters of 1, 2, 4 or 8 blocks
+    auto fill = [&](int blocks) {
+        int k = (blocks + G - 1) / G;
+        if (k > kTcMaxSplit) k = kTcMaxSplit;
+        while (k & (k - 1)) --k;                // clusters of 1, 2, 4 or 8 blocks
+        return k;
+    };
+    // Both block slots of every SM when the splits stay long (at least four
+    // K blocks each: the 7B down projection, 1-2% faster per step); otherwise
+    // one: with shorter splits (QKV, O) the second slot is worth more to the
+    // next linear, whose blocks become resident there and fetch their weights.
+    ks = fill(d.sms);
+    if (G * 2 <= d.sms && C / fill(2 * d.sms) >= 4 * kTcChunks) ks = fill(2 * d.sms);
     const int need = (K + kTcMaxSplitK - 1) / kTcMaxSplitK;
     if (ks < need) ks = need;
     if (ks > C) ks = C;

@@ -4,8 +4,9 @@ The expected grids, shared-memory sizes, stages and K splits are those of the
 launches measured on a GB300 (ncu launch lists and -Xptxas/launch attributes of
 the 7B decode step): the one-token DP4A GEMV at 115,712 B (98,176 B at
 K = 18944) on 152 blocks, and the tensor-core GEMV at 114,920 B with clusters
-of 4 for QKV, O and down (106,728 B for gate/up, whose K is not split: no
-buffer for the other splits' sums).  The launch path takes its decisions through the same
+of 4 for QKV and O and of 8 for down (its splits keep at least four K blocks,
+so it fills both block slots of every SM), and 106,728 B for gate/up, whose K
+is not split (no buffer for the other splits' sums).  The launch path takes its decisions through the same
 functions, so these checks cover the host side of every GEMV launch.
 """
 import math
@@ -45,7 +46,7 @@ def test_one_token_step_is_one_fused_launch_per_linear(lib):
     assert plan(lib, "w4", 1, 152064, 3584)["smem_bytes"] == HALF
 
 
-@pytest.mark.parametrize("name,grid,splits", [("qkv", 144, 4), ("o", 112, 4), ("gate_up", 296, 1), ("down", 112, 4)])
+@pytest.mark.parametrize("name,grid,splits", [("qkv", 144, 4), ("o", 112, 4), ("gate_up", 296, 1), ("down", 224, 8)])
 def test_sixteen_tokens_run_on_the_tensor_cores(lib, name, grid, splits):
     lin = {l.name: l for l in wl.qwen7b_layer()}[name]
     p = plan(lib, "w4", 16, lin.N, lin.K)

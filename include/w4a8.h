@@ -429,7 +429,12 @@ w4_status w8a32_gemv(const void* w, const float* s_w, const float* bias, const f
  * the next.  Calls that share a workspace must not overlap on the GPU.  After
  * a call that reported W4_ERR_DEVICE_TIMEOUT, zero the workspace again.
  * Host threads may call the chain entry points at the same time, each with
- * its own workspace and stream: the launch parameters are staged per thread. 
+ * its own workspace and stream: the launch parameters are staged per thread.
+ * The chain runs its linears on DP4A whatever M is.  Per-row INT4 calls of
+ * three or more tokens are faster through the per-linear entry points
+ * (w4a8_linear with W4_FLAG_PDL, on the tensor cores), which need the qx / sx
+ * buffers the chain may leave out: measured on the 7B step, a chain of 113
+ * linears runs best at one or two tokens. 
  * ------------------------------------------------------------------------ */
 #define W4_MAX_CHAIN 128
 typedef struct {

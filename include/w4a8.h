@@ -433,8 +433,9 @@ w4_status w8a32_gemv(const void* w, const float* s_w, const float* bias, const f
  * The chain runs its linears on DP4A whatever M is.  Per-row INT4 calls of
  * three or more tokens are faster through the per-linear entry points
  * (w4a8_linear with W4_FLAG_PDL, on the tensor cores), which need the qx / sx
- * buffers the chain may leave out: measured on the 7B step, a chain of 113
- * linears runs best at one or two tokens. 
+ * buffers the chain may leave out.  On the 7B step the per-linear launches
+ * chained with W4_FLAG_PDL are also faster at one token (0.874 against
+ * 1.03-1.07 ms); the chain is the single-launch alternative. 
  * ------------------------------------------------------------------------ */
 #define W4_MAX_CHAIN 128
 typedef struct {

@@ -136,6 +136,7 @@ SIGNATURES["q4_0_quantize_host"] = ([_P, _I, _I, _P], _I)
 SIGNATURES["i8g32_quantize_host"] = ([_P, _I, _I, _P, _P], _I)
 SIGNATURES["w4_last_device_error"] = ([ctypes.POINTER(ctypes.c_uint)], _I)
 SIGNATURES["w4_hbm_read"] = ([_P, _SZ, _P, _P], _I)
+SIGNATURES["w4_selftest_wait_timeout"] = ([_I, ctypes.c_uint, _P], _I)
 W4_MAX_CHAIN = 128
 
 _lib = None
@@ -628,6 +629,16 @@ def hbm_read(buf, sink, stream=None):
     _dev(buf, sink)
     _check("w4_hbm_read", load().w4_hbm_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
                                              _stream(stream)))
+
+
+def selftest_wait_timeout(cluster: bool, timeout_us: int, stream=None):
+    """A kernel whose bounded wait nothing completes: it gives up after
+    timeout_us and sets the device error word to the wait-timeout code."""
+    _check("w4_selftest_wait_timeout", load().w4_selftest_wait_timeout(1 if cluster else 0, int(timeout_us),
+                                                                        _stream(stream)))
+
+
+WAIT_TIMEOUT_CODE = 0x57414954
 
 
 def clear_device_error():

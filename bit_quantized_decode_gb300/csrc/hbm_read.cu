@@ -124,4 +124,47 @@ cudaError_t launch_hbm_read(const void* buf, unsigned long long bytes, unsigned*
     return cudaGetLastError();
 }
 
+// ------------------------------------------------- the timeout path, tested
+// A wait that nothing completes: thread 0 of block 0 waits (bounded) for phase
+// 0 of an mbarrier on which no thread arrives, and records the timeout in the
+// device error word as every kernel's bounded waits do.  With `cluster`, two
+// blocks form a cluster and block 0 waits with cluster-scope acquire (the
+// K-split leader's wait) while block 1 leaves, as the other splits do.  The
+// kernel always ends after `timeout_ns`: the error path of the waits runs on
+// the GPU without a fault, and the context stays usable.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int cluster, unsigned long long timeout_ns, unsigned* err)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (cluster) cluster_sync();
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        const bool ok = cluster ? mbar_wait_cluster_bounded(b, 0u, timeout_ns) : mbar_wait_bounded(b, 0u, timeout_ns);
+        if (!ok && err != nullptr) atomicExch(err, kErrWaitTimeout);
+    }
+    __syncwarp();
+}
+
+cudaError_t launch_wait_selftest(int cluster, unsigned long long timeout_ns, unsigned* err, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster ? 2u : 1u);
+    cfg.blockDim = dim3(32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (cluster) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, wait_selftest_kernel, cluster, timeout_ns, err);
+}
+
 }  // namespace w4k

@@ -254,6 +254,9 @@ cudaError_t launch_gemv_w4_tc(const TcArgs& a, int grid, size_t smem, bool pdl, 
 
 // Pure-read bandwidth probe (hbm_read.cu): one block per SM streams `bytes`
 // bytes once and XORs every 32-bit word into *sink (cleared first).
+// A bounded wait that nothing completes (hbm_read.cu): it must end and set
+// the device error word.
+cudaError_t launch_wait_selftest(int cluster, unsigned long long timeout_ns, unsigned* err, cudaStream_t s);
 cudaError_t launch_hbm_read(const void* buf, unsigned long long bytes, unsigned* sink, unsigned* err, int sms,
                             cudaStream_t s);
 

@@ -1176,6 +1176,15 @@ w4_status w4_hbm_read(const void* buf, size_t bytes, unsigned* sink, w4_stream_t
     return cuda_status(launch_hbm_read(buf, bytes, sink, dev->err, dev->sms, reinterpret_cast<cudaStream_t>(s)));
 }
 
+w4_status w4_selftest_wait_timeout(int cluster, unsigned timeout_us, w4_stream_t s)
+{
+    if ((cluster != 0 && cluster != 1) || timeout_us == 0 || timeout_us > 1000000u) return W4_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    const w4_status st = device_info(&dev);
+    if (st != W4_OK) return st;
+    return cuda_status(launch_wait_selftest(cluster, 1000ull * timeout_us, dev->err, reinterpret_cast<cudaStream_t>(s)));
+}
+
 w4_status w4_clear_device_error(void)
 {
     DeviceInfo* dev = nullptr;

@@ -491,6 +491,16 @@ w4_status w4_device_error(unsigned* code);
 w4_status w4_last_device_error(unsigned* code); /* the same call under a second name */
 w4_status w4_clear_device_error(void);
 
+/* Self-test of the timeout path: launches a kernel whose bounded wait nothing
+ * completes (an mbarrier on which no thread arrives), so it gives up after
+ * timeout_us microseconds (1..1000000) and sets the device error word to the
+ * wait-timeout code (0x57414954, "WAIT"), as a GEMV's waits do.  cluster = 1
+ * waits as the K-split leader does (two blocks in a cluster, cluster-scope
+ * acquire, the other block leaving); 0 waits as every other ring does.  The
+ * kernel always finishes and faults nothing; clear the word afterwards.
+ * W4_ERR_INVALID_ARG for other arguments. */
+w4_status w4_selftest_wait_timeout(int cluster, unsigned timeout_us, w4_stream_t s);
+
 /* ------------------------------------------------------------------------
  * Pure-read HBM bandwidth probe: the roofline denominator for a kernel that
  * only reads.  [310B-Gemma4] §4.1 measures the device's pure read bandwidth

@@ -255,6 +255,13 @@ def test_hbm_read_argument_checks(lib):
     assert lib.w4_hbm_read(FAKE, 64, ctypes.c_void_p(0x1002), None) == 3
 
 
+def test_wait_selftest_argument_checks(lib):
+    # checked on the host before any device work: no GPU is needed for these
+    assert lib.w4_selftest_wait_timeout(2, 1000, None) == 1         # cluster is 0 or 1
+    assert lib.w4_selftest_wait_timeout(0, 0, None) == 1            # a limit of at least 1 us
+    assert lib.w4_selftest_wait_timeout(1, 1000001, None) == 1      # and at most one second
+
+
 def test_host_quantizer_argument_checks(lib):
     assert lib.w4_quantize_rows_host(FAKE, 4, 12, FAKE, FAKE) == 2
     assert lib.w4_quantize_rows_host(FAKE, -1, 64, FAKE, FAKE) == 1

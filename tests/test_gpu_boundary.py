@@ -6,10 +6,15 @@
 - w4_hbm_read reads every byte once: its XOR checksum equals numpy's over a
   buffer with a ragged tail (a last chunk shorter than a ring slot).
 - w4_last_device_error reads the same word as w4_device_error.
+- The timeout path of the bounded waits: a kernel whose wait nothing
+  completes (the per-warp ring form and the K-split leader's cluster-scope
+  form) ends by itself, sets the wait-timeout code in the error word, and the
+  context keeps computing correct results afterwards.  No GPU fault is made.
 """
 import numpy as np
 import pytest
 
+import oracle
 from bit_quantized_decode_gb300 import workloads as wl
 from helpers import cuda_ok, dev, host
 
@@ -66,3 +71,28 @@ def test_hbm_read_checksum(lib, nbytes):
 
 def test_last_device_error_alias(lib):
     assert lib.last_device_error() == lib.device_error() == 0
+
+
+@pytest.mark.parametrize("cluster", [False, True])
+def test_wait_timeout_sets_the_error_word_and_the_context_survives(lib, cluster):
+    import time
+
+    import torch
+    lib.clear_device_error()
+    t0 = time.perf_counter()
+    lib.selftest_wait_timeout(cluster, 2000)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 5.0                     # the wait gave up by itself
+    assert lib.device_error() == lib.WAIT_TIMEOUT_CODE
+    lib.clear_device_error()
+    # the context is usable: a GEMV on codes right after gives the oracle's sums
+    g = wl.rng(4242)
+    M, N, K = 2, 64, 256
+    q = wl.int_codes(g, (N, K), -8, 7)
+    qx = wl.int_codes(g, (M, K), -127, 127)
+    w = torch.empty(lib.w4_repacked_bytes(N, K), dtype=torch.uint8, device="cuda")
+    lib.w4_repack([dev(oracle.pack_int4(q).view(np.int32))], K, w)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    lib.w4a8_gemv(w, dev(np.ones(N, np.float32)), None, dev(qx), dev(np.ones(M, np.float32)), y)
+    assert np.array_equal(host(y), oracle.gemv_w4a8_acc(oracle.pack_int4(q), qx).astype(np.float32))
+    assert lib.device_error() == 0

@@ -21,9 +21,10 @@
 // exactly; the epilogue forms sum n x = 16 S_h + S_l and removes the bias,
 // sum q x = sum n x - 8 sum x, with each token's code sum over the split.
 //   * One block of ten warps per (128-row group, K split), two blocks per
-//     SM.  K splits of a row group form one thread-block cluster and add
-//     their partial sums in the leader's shared memory (distributed shared
-//     memory), which writes y.
+//     SM.  K splits of a row group form one thread-block cluster: the other
+//     splits add their exact integer sums into the leader's shared memory
+//     (remote atomics), arrive once on its mbarrier with cluster-scope release
+//     and exit; only the leader waits, then writes y.
 //   * Packed weights stream through a ring of stages (512 K x 128 rows,
 //     32 KB: one 2 KB bulk copy per 8-row tile) issued before the dependency
 //     wait; the operand pipeline steps through the stage in two 256-K blocks.
@@ -43,13 +44,15 @@
 //     the ring has full / empty mbarriers: no block-wide barrier sits in the
 //     K loop.  Warp 8 also allocates and frees the tensor memory, so warps
 //     0-3 go from the accumulator read straight to the epilogue.
-//   * What bounds it is the latency of the dequantizing warps' per-block
-//     chain (shared-memory loads, tensor-memory stores and their wait, the
-//     named barrier to the MMA lane, the commit's mbarrier), not HBM, the
-//     weight stages or the tensor cores' arithmetic: hence K blocks of 256
-//     (half the hand-offs of 128), three operand buffers (which the 256
-//     tensor-memory columns of a block allow with two accumulators) and no
-//     division in the loop.
+//   * In the K loop the dequantizing warps' per-block chain (shared-memory
+//     loads, tensor-memory stores and their wait, the named barrier to the
+//     MMA lane, the commit's mbarrier) is the critical path, not the tensor
+//     cores' arithmetic: hence K blocks of 256 (half the hand-offs of 128),
+//     three operand buffers, two warp groups that overlap their chains, and no
+//     division in the loop.  Around the loop, what a launch costs is latency:
+//     the set-up (cluster barrier, tensor-memory allocation, row parameters)
+//     runs before the dependency wait, and the tail is one tensor-memory read,
+//     the split reduction and the epilogue.
 #include <cuda_fp16.h>
 
 #include "fusion.cuh"

@@ -177,10 +177,17 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
 
 // Blocks of a DP4A GEMV launch over T row tiles: one per SM (or the tuned
 // cap), never more than the tiles; with K splits, clusters of ks blocks each
-// take a tile range (grid = clusters * ks).
-int gemv_grid(const DeviceInfo& d, int T, int ks = 1)
+// take a tile range (grid = clusters * ks).  A GEMV of at least 64 tiles per
+// SM whose blocks fit two per SM (smem: the planned bytes) takes both slots:
+// measured alone, the lm_head 152064 x 3584 takes 42.4 us on 304 blocks
+// against 45.2 us on 152.  Shorter GEMVs leave the second slot to the next
+// linear, which fetches its weights there (the 7B step took 0.925 ms with
+// every linear on 304 blocks against 0.876 ms).
+int gemv_grid(const DeviceInfo& d, int T, int ks = 1, int smem = 0)
 {
     int grid = d.sms;
+    const int half = d.smem_per_sm / 2 - d.smem_reserved;
+    if (ks == 1 && smem > 0 && smem <= half && T >= 64 * d.sms) grid = 2 * d.sms;
     if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
     int clusters = grid / ks;
     if (clusters < 1) clusters = 1;
@@ -231,7 +238,7 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     cp.lin[0].ks = a.ks;
     if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) return W4_ERR_UNSUPPORTED_SHAPE;
     cp.stages = p.stages;
-    const int grid = gemv_grid(*dev, a.T, a.ks);
+    const int grid = gemv_grid(*dev, a.T, a.ks, p.smem);
     const int clusters = grid / a.ks;
     cp.lin[0].tq = a.T / clusters;
     cp.lin[0].tr = a.T % clusters;
@@ -581,7 +588,7 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
                     return W4_ERR_UNSUPPORTED_SHAPE;
                 p.path = q.xmode == X_FUSED ? W4_PATH_FUSED : q.xmode == X_SMEM ? W4_PATH_CODES_SMEM
                                                                                 : W4_PATH_CODES_GLOBAL;
-                p.grid = gemv_grid(d, T, ks);
+                p.grid = gemv_grid(d, T, ks, q.smem);
                 p.k_splits = ks;
                 p.threads = kThreads;
                 p.smem_bytes = q.smem;

@@ -46,6 +46,21 @@ def test_one_token_step_is_one_fused_launch_per_linear(lib):
     assert plan(lib, "w4", 1, 152064, 3584)["smem_bytes"] == HALF
 
 
+def test_long_gemvs_take_both_block_slots(lib):
+    # at least 64 tiles per SM and two blocks' worth of shared memory per SM:
+    # the lm_heads at one token run on 2 x 152 blocks (measured faster alone);
+    # the layer linears keep one block per SM for the next linear's prefetch
+    for fmt, N, K in (("w4", 152064, 3584), ("i8g32", 262144, 1536), ("q6g32", 262144, 1536)):
+        assert plan(lib, fmt, 1, N, K)["grid"] == 304
+        assert plan(lib, fmt, 2, N, K)["grid"] == 152          # whole-SM budget: one block per SM
+    assert plan(lib, "w4", 1, 37888, 3584)["grid"] == 152
+    lib.set_tuning("grid_blocks", 100)
+    try:
+        assert plan(lib, "w4", 1, 152064, 3584)["grid"] == 100  # the tuned cap wins
+    finally:
+        lib.set_tuning("grid_blocks", 0)
+
+
 @pytest.mark.parametrize("name,grid,splits", [("qkv", 144, 4), ("o", 112, 4), ("gate_up", 296, 1), ("down", 224, 8)])
 def test_sixteen_tokens_run_on_the_tensor_cores(lib, name, grid, splits):
     lin = {l.name: l for l in wl.qwen7b_layer()}[name]

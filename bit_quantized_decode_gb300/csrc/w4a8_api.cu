@@ -182,7 +182,9 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
 // measured alone, the lm_head 152064 x 3584 takes 42.4 us on 304 blocks
 // against 45.2 us on 152.  Shorter GEMVs leave the second slot to the next
 // linear, which fetches its weights there (the 7B step took 0.925 ms with
-// every linear on 304 blocks against 0.876 ms).
+// every linear on 304 blocks against 0.876 ms, and 0.899 against 0.870 ms
+// with the gate/up projection alone on 304: alone it gains 1 us, the down
+// projection after it loses its prefetch).
 int gemv_grid(const DeviceInfo& d, int T, int ks = 1, int smem = 0)
 {
     int grid = d.sms;

@@ -143,13 +143,17 @@ int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget, int ks = 1
 // when a ring of at least two stages fits in half the SM, else the whole-block
 // budget.  Several tokens: the whole-block budget (a deeper ring pays more
 // than the early start of the next GEMV once the inner loop does M times the
-// DP4A work).  `fused` asks for the quantize prologue.
-bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p, int ks = 1)
+// DP4A work), except for a long GEMV of two tokens (`long_gemv`: at least 64
+// tiles per SM, see gemv_grid), whose blocks then run two per SM: measured on
+// the 152064 x 3584 lm_head, 44.3 us against 63.3 us on the whole-block ring.
+// `fused` asks for the quantize prologue.
+bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p, int ks = 1,
+               bool long_gemv = false)
 {
     const int half = d.smem_per_sm / 2 - d.smem_reserved;
     const int whole = d.smem_optin;
     int bps = g_tune[W4_TUNE_BLOCKS_PER_SM];
-    if (bps == 0 && MT > 1) bps = 1;
+    if (bps == 0 && MT > 1 && !(long_gemv && MT <= 2 && ks == 1)) bps = 1;
     int modes[2] = {fused ? X_FUSED : X_SMEM, fused ? -1 : X_GLOBAL};
     if (fmt_float_x(fmt)) {
         modes[0] = X_F32;
@@ -238,7 +242,8 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     Plan p;
     if (a.ks > 1 && !plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) a.ks = 1;   // no room to merge
     cp.lin[0].ks = a.ks;
-    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks, a.T >= 64 * dev->sms))
+        return W4_ERR_UNSUPPORTED_SHAPE;
     cp.stages = p.stages;
     const int grid = gemv_grid(*dev, a.T, a.ks, p.smem);
     const int clusters = grid / a.ks;
@@ -586,7 +591,8 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
                 const int T = static_cast<int>(tiles(Nw));
                 const int ks = choose_splits(d, fmt, MT, T, K / 32);
                 Plan q;
-                if (!plan_gemv(d, fmt, MT, linear && p.quantize_launches == 0, K, kAccWords / MT, q, ks))
+                if (!plan_gemv(d, fmt, MT, linear && p.quantize_launches == 0, K, kAccWords / MT, q, ks,
+                               T >= 64 * d.sms))
                     return W4_ERR_UNSUPPORTED_SHAPE;
                 p.path = q.xmode == X_FUSED ? W4_PATH_FUSED : q.xmode == X_SMEM ? W4_PATH_CODES_SMEM
                                                                                 : W4_PATH_CODES_GLOBAL;

@@ -4,8 +4,8 @@ The smaller parity tests cover each format's arithmetic; these run the
 launches the benchmark times, at sizes whose blocks take the branches small
 shapes never reach:
   - per-row INT4 lm_head 152064 x 3584 ("Jetson Orin AGX INT4 推理优化实践",
-    §模型尺寸, VOCAB 152064): two accumulation rounds per block at one token;
-    also five tokens (the tensor-core path over 1188 row groups);
+    §模型尺寸, VOCAB 152064) on two blocks per SM at one and two tokens; also
+    five tokens (the tensor-core path over 1188 row groups);
   - per-row INT4 fused gate/up 37888 x 3584 at one token;
   - the int8 group lm_head 262144 x 1536 ("在香橙派上跑 Gemma4", §3.2) in its
     int8 (I8G32) and 6-bit (Q6G32) layouts: four rounds per block and 1725
@@ -69,7 +69,7 @@ def _w4_case(lib, seed, N, K):
     return g, packed, sw, b, w
 
 
-@pytest.mark.parametrize("name,N,K,Ms", [("lm_head", 152064, 3584, (1, 5)), ("gate_up", 37888, 3584, (1,))])
+@pytest.mark.parametrize("name,N,K,Ms", [("lm_head", 152064, 3584, (1, 2, 5)), ("gate_up", 37888, 3584, (1,))])
 def test_w4_full_shape(lib, name, N, K, Ms):
     g, packed, sw, b, w = _w4_case(lib, 4100 + N, N, K)
     swd, bd = dev(sw), dev(b)

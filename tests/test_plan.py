@@ -48,11 +48,16 @@ def test_one_token_step_is_one_fused_launch_per_linear(lib):
 
 def test_long_gemvs_take_both_block_slots(lib):
     # at least 64 tiles per SM and two blocks' worth of shared memory per SM:
-    # the lm_heads at one token run on 2 x 152 blocks (measured faster alone);
-    # the layer linears keep one block per SM for the next linear's prefetch
+    # the lm_heads at one and two tokens run on 2 x 152 blocks (measured faster
+    # alone; two tokens then take the two-per-SM budget instead of the whole
+    # SM); the layer linears keep one block per SM for the next linear's
+    # prefetch, and three or more tokens keep the whole-SM ring
     for fmt, N, K in (("w4", 152064, 3584), ("i8g32", 262144, 1536), ("q6g32", 262144, 1536)):
-        assert plan(lib, fmt, 1, N, K)["grid"] == 304
-        assert plan(lib, fmt, 2, N, K)["grid"] == 152          # whole-SM budget: one block per SM
+        for M in (1, 2):
+            p = plan(lib, fmt, M, N, K)
+            assert p["grid"] == 304 and p["smem_bytes"] <= HALF
+    for fmt in ("i8g32", "q6g32"):
+        assert plan(lib, fmt, 3, 262144, 1536)["grid"] == 152
     assert plan(lib, "w4", 1, 37888, 3584)["grid"] == 152
     lib.set_tuning("grid_blocks", 100)
     try:

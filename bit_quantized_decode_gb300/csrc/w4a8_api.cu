@@ -139,21 +139,37 @@ int stages_for(int fmt, int MT, int xmode, int K, int RT, int budget, int ks = 1
     return s >= 2 ? s : 0;
 }
 
-// One token: two blocks per SM (this GEMV beside the next one in the stream)
-// when a ring of at least two stages fits in half the SM, else the whole-block
-// budget.  Several tokens: the whole-block budget (a deeper ring pays more
-// than the early start of the next GEMV once the inner loop does M times the
-// DP4A work), except for a long GEMV of two tokens (`long_gemv`: at least 64
-// tiles per SM, see gemv_grid), whose blocks then run two per SM: measured on
-// the 152064 x 3584 lm_head, 44.3 us against 63.3 us on the whole-block ring.
-// `fused` asks for the quantize prologue.
+// Whether a DP4A GEMV of MT tokens over T row tiles runs two of its own
+// blocks per SM.  Two tokens: always (see plan_gemv).  One token: for a GEMV
+// of at least 64 tiles per SM: measured alone, the lm_head 152064 x 3584 takes
+// 42.4 us on 304 blocks against 45.2 us on 152; shorter ones leave the second
+// slot to the next linear, which fetches its weights there (the 7B step took
+// 0.925 ms with every linear on 304 blocks against 0.876 ms, and 0.899
+// against 0.870 ms with the gate/up projection alone on 304: alone it gains
+// 1 us, the down projection after it loses its prefetch).
+bool two_blocks_per_sm(const DeviceInfo& d, int MT, int T, int ks)
+{
+    return ks == 1 && (MT == 2 || (MT == 1 && T >= 64 * d.sms));
+}
+
+// Shared-memory budget of a DP4A GEMV block.  One token: half an SM when a
+// ring of at least two stages fits there (two blocks per SM: this GEMV beside
+// the next one in the stream, or, for a long GEMV, two of its own; see
+// gemv_grid), else the whole-block budget.  Two tokens (`two_per_sm`): half
+// an SM too where the ring fits, the two blocks of the SM this GEMV's own,
+// else the whole block (the 7B step: 1.250 ms so, with the K = 18944 down
+// projection's fused prologue on the whole block; 1.370 ms with every linear
+// on the whole block, 1.653 with half an SM and the second slot left to the
+// next linear; the 152064 x 3584 lm_head alone 44.3 against 63.3 us).  More tokens: the whole-block budget (a deeper ring pays
+// once the inner loop does M times the DP4A work per weight byte).  `fused`
+// asks for the quantize prologue.
 bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, Plan& p, int ks = 1,
-               bool long_gemv = false)
+               bool two_per_sm = false)
 {
     const int half = d.smem_per_sm / 2 - d.smem_reserved;
     const int whole = d.smem_optin;
     int bps = g_tune[W4_TUNE_BLOCKS_PER_SM];
-    if (bps == 0 && MT > 1 && !(long_gemv && MT <= 2 && ks == 1)) bps = 1;
+    if (bps == 0 && MT > 1 && !(two_per_sm && MT <= 2 && ks == 1)) bps = 1;
     int modes[2] = {fused ? X_FUSED : X_SMEM, fused ? -1 : X_GLOBAL};
     if (fmt_float_x(fmt)) {
         modes[0] = X_F32;
@@ -181,19 +197,14 @@ bool plan_gemv(const DeviceInfo& d, int fmt, int MT, bool fused, int K, int RT, 
 
 // Blocks of a DP4A GEMV launch over T row tiles: one per SM (or the tuned
 // cap), never more than the tiles; with K splits, clusters of ks blocks each
-// take a tile range (grid = clusters * ks).  A GEMV of at least 64 tiles per
-// SM whose blocks fit two per SM (smem: the planned bytes) takes both slots:
-// measured alone, the lm_head 152064 x 3584 takes 42.4 us on 304 blocks
-// against 45.2 us on 152.  Shorter GEMVs leave the second slot to the next
-// linear, which fetches its weights there (the 7B step took 0.925 ms with
-// every linear on 304 blocks against 0.876 ms, and 0.899 against 0.870 ms
-// with the gate/up projection alone on 304: alone it gains 1 us, the down
-// projection after it loses its prefetch).
-int gemv_grid(const DeviceInfo& d, int T, int ks = 1, int smem = 0)
+// take a tile range (grid = clusters * ks).  With `two_per_sm` (see
+// two_blocks_per_sm) and blocks that fit two per SM (smem: the planned
+// bytes), two per SM.
+int gemv_grid(const DeviceInfo& d, int T, int ks = 1, int smem = 0, bool two_per_sm = false)
 {
     int grid = d.sms;
     const int half = d.smem_per_sm / 2 - d.smem_reserved;
-    if (ks == 1 && smem > 0 && smem <= half && T >= 64 * d.sms) grid = 2 * d.sms;
+    if (ks == 1 && two_per_sm && smem > 0 && smem <= half) grid = 2 * d.sms;
     if (g_tune[W4_TUNE_GRID_BLOCKS] > 0) grid = g_tune[W4_TUNE_GRID_BLOCKS];
     int clusters = grid / ks;
     if (clusters < 1) clusters = 1;
@@ -242,10 +253,10 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
     Plan p;
     if (a.ks > 1 && !plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) a.ks = 1;   // no room to merge
     cp.lin[0].ks = a.ks;
-    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks, a.T >= 64 * dev->sms))
-        return W4_ERR_UNSUPPORTED_SHAPE;
+    const bool two = two_blocks_per_sm(*dev, MT, a.T, a.ks);
+    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks, two)) return W4_ERR_UNSUPPORTED_SHAPE;
     cp.stages = p.stages;
-    const int grid = gemv_grid(*dev, a.T, a.ks, p.smem);
+    const int grid = gemv_grid(*dev, a.T, a.ks, p.smem, two);
     const int clusters = grid / a.ks;
     cp.lin[0].tq = a.T / clusters;
     cp.lin[0].tr = a.T % clusters;
@@ -591,12 +602,12 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
                 const int T = static_cast<int>(tiles(Nw));
                 const int ks = choose_splits(d, fmt, MT, T, K / 32);
                 Plan q;
-                if (!plan_gemv(d, fmt, MT, linear && p.quantize_launches == 0, K, kAccWords / MT, q, ks,
-                               T >= 64 * d.sms))
+                const bool two = two_blocks_per_sm(d, MT, T, ks);
+                if (!plan_gemv(d, fmt, MT, linear && p.quantize_launches == 0, K, kAccWords / MT, q, ks, two))
                     return W4_ERR_UNSUPPORTED_SHAPE;
                 p.path = q.xmode == X_FUSED ? W4_PATH_FUSED : q.xmode == X_SMEM ? W4_PATH_CODES_SMEM
                                                                                 : W4_PATH_CODES_GLOBAL;
-                p.grid = gemv_grid(d, T, ks, q.smem);
+                p.grid = gemv_grid(d, T, ks, q.smem, two);
                 p.k_splits = ks;
                 p.threads = kThreads;
                 p.smem_bytes = q.smem;

@@ -58,6 +58,17 @@ def test_long_gemvs_take_both_block_slots(lib):
             assert p["grid"] == 304 and p["smem_bytes"] <= HALF
     for fmt in ("i8g32", "q6g32"):
         assert plan(lib, fmt, 3, 262144, 1536)["grid"] == 152
+    # two tokens: two blocks per SM wherever the fused prologue fits half an
+    # SM; the K = 18944 down projection keeps the fused prologue on the whole
+    # SM (measured: the 7B step 1.25 ms so, 1.35 ms with down on the separate
+    # quantizer and two blocks per SM, 1.37 ms with every linear on the whole SM)
+    for lin in wl.qwen7b_layer():
+        p = plan(lib, "w4", 2, lin.N, lin.K)
+        assert p["path"] == "fused"
+        if lin.K == 18944:
+            assert p["grid"] == 152 and p["smem_bytes"] > HALF
+        else:
+            assert p["grid"] == 304 and p["smem_bytes"] <= HALF
     assert plan(lib, "w4", 1, 37888, 3584)["grid"] == 152
     lib.set_tuning("grid_blocks", 100)
     try:
@@ -161,7 +172,11 @@ def test_invariants_over_a_shape_sweep(lib):
                     assert p["path"] in ("fused", "codes_smem", "codes_global")
                     ks = p["k_splits"]                                # DP4A: clusters of ks blocks
                     assert ks in (1, 2, 4) and (ks == 1 or (M <= 2 and K // 32 // ks >= 16))
-                    assert p["grid"] == min(152 // ks, math.ceil(N / 8)) * ks
+                    T = math.ceil(N / 8)
+                    # two of the GEMV's own blocks per SM: two tokens, or one token and
+                    # at least 64 tiles per SM, when two blocks fit an SM
+                    two = ks == 1 and (M == 2 or (M == 1 and T >= 64 * 152)) and p["smem_bytes"] <= HALF
+                    assert p["grid"] == min((304 if two else 152) // ks, T) * ks
                     assert 2 <= p["stages"] and p["smem_bytes"] <= GB300["smem_optin"]
 
 

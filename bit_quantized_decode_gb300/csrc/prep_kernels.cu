@@ -154,15 +154,20 @@ __global__ void __launch_bounds__(kQuantThreads) a8_quantize_kernel(const float*
     if (tid == 0) sx[m] = ks.s;
 }
 
-// Long tokens (8192 <= K <= 32768): kQuantCluster blocks per token, in one
-// thread-block cluster.  Block r reads quarter r of the token's float4 words
+// Long tokens (8192 <= K <= 32768) and five or more of them: kQuantCluster
+// blocks per token, in one thread-block cluster.  Block r reads quarter r of the token's float4 words
 // into registers and takes its absmax; the blocks read one another's maxima
 // through distributed shared memory, so each holds the token's absmax, and
 // each quantizes its own quarter with a8_scale of that absmax: the codes and
 // the scale are the single-block kernel's, bit for bit (a maximum does not
 // depend on its order).  A block leaves only after every block has read its
-// maximum (the second half of the last cluster barrier).
+// maximum (the second half of the last cluster barrier).  Measured on the 7B
+// step (K = 18944 quantizer ahead of the down projection), against one block
+// per token: 0.003 / 0.020 / 0.008 ms faster at 5 / 8 / 16 tokens, 0.018 ms
+// slower at 3 (the cluster launch and its barriers outweigh the shorter read
+// when there are few tokens).
 constexpr int kQuantCluster = 4;
+constexpr int kQuantClusterMinTokens = 5;
 
 template <int NIT>
 __global__ void __launch_bounds__(kQuantThreads) a8_quantize_cluster_kernel(const float* __restrict__ x, int K,
@@ -256,7 +261,7 @@ cudaError_t launch_quant(const float* x, const float* gamma, float eps, int M, i
 cudaError_t launch_a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, bool pdl, cudaStream_t s)
 {
     const int per_block = (K / 4 + kQuantCluster - 1) / kQuantCluster;     // float4 words of a quarter
-    if (M > 0 && K >= 8192 && per_block <= 4 * kQuantThreads) {
+    if (M >= kQuantClusterMinTokens && K >= 8192 && per_block <= 4 * kQuantThreads) {
         cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = token_launch(M, pdl, s, attr);
         cfg.gridDim = dim3(static_cast<unsigned>(M * kQuantCluster));

@@ -35,10 +35,12 @@ def _torch():
 
 # ------------------------------------------------------ activation quant
 @pytest.mark.parametrize("M,K,outliers", [(1, 3584, True), (3, 1536, False), (16, 18944, False), (2, 32, False),
-                                           (1, 8192, True), (5, 32768, False), (4, 32800, True), (2, 40960, False)])
+                                           (1, 8192, True), (8, 8192, True), (5, 32768, False), (4, 32800, True),
+                                           (6, 32800, False), (2, 40960, False)])
 def test_a8_quantize_bit_exact(lib, M, K, outliers):
-    """Codes and scales bit-exact; 8192 <= K <= 32768 takes the kernel with four
-    blocks per token (a cluster sharing the token's absmax), the rest one block."""
+    """Codes and scales bit-exact; five or more tokens with 8192 <= K <= 32768
+    take the kernel with four blocks per token (a cluster sharing the token's
+    absmax), the rest one block per token."""
     torch = _torch()
     g = wl.rng(100 + M + K)
     x = wl.activations(g, M, K, outliers)

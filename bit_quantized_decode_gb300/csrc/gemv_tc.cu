@@ -201,6 +201,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         tmem_alloc(smem_u32(tmem_slot), kTcCols);
         tmem_relinquish();
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    auto fail = [&]() {
+        *dead_s = 1u;
+        if (A.err != nullptr) atomicExch(A.err, kErrWaitTimeout);
+    };
     // this row's output parameters do not depend on the previous kernel
     const bool row_thread = tid < kTcRows;
     const int row = g * kTcRows + tid;
@@ -211,6 +219,63 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         bv_r = A.bias != nullptr ? A.bias[prow] : 0.0f;
     }
 
+    // Warps 0-7, two groups of four on alternate K blocks (see below): A of a
+    // K block, this thread's row (tensor-memory lane t % 128, which warp t / 32
+    // reaches as warp (t / 32) % 4 does) over the block's 256 K as e4m3 (the
+    // buffer's 64 columns) in two halves of four chunks, sixteen columns per
+    // store; the group arrives on the stage's empty barrier once it is read.
+    const bool dequant = warp < kTcDqWarps;
+    const int row_a = tid & (kTcRows - 1);
+    const int grp = warp >> 2;
+    const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint8_t* my_units =
+        ring + (row_a >> 3) * (kTcStageChunks * kRows * 16) + (grp * kTcChunks) * kRows * 16 + (row_a & 7) * 16;
+    auto convert_a = [&](int slot, int j, int nch) {
+        const uint8_t* units = my_units + static_cast<size_t>(slot) * kTcStageBytes;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            constexpr int kQ = kTcChunks / 2;
+            uint4 u[kQ];
+#pragma unroll
+            for (int e = 0; e < kQ; ++e)
+                if (kQ * hf + e < nch) u[e] = *reinterpret_cast<const uint4*>(units + (kQ * hf + e) * kRows * 16);
+            if (hf == 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // this group's block of the stage is read
+            }
+#pragma unroll
+            for (int r = 0; r < kQ / 2; ++r) {
+                uint32_t h[16];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    if (kQ * hf + 2 * r + e < nch) {
+                        tc_unit_e4m3(u[2 * r + e], &h[e * 8]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) h[e * 8 + k] = 0u;
+                    }
+                }
+                tmem_st16(tbase + tlane + kTcColA + j * kTcAStride + 32 * hf + 16 * r, h);
+            }
+        }
+    };
+    // The weights do not depend on the previous kernel: each group converts its
+    // first K block (stage 0, operand buffer grp) before the dependency wait.
+    // Its loop then skips that block's stage wait and A: once both groups have
+    // read stage 0 the copy warp may refill the slot, whose barrier would then
+    // be a phase further on.
+    bool first_a_done = false;
+    if (dequant && grp < nb) {
+        bool ok = mbar_wait_bounded(full_b, 0u, kTcWaitNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0 && !*dead_s) fail();
+        } else {
+            tc_fence_after();
+            convert_a(0, grp, min(kTcChunks, ce - (cb + grp * kTcChunks)));
+            first_a_done = true;
+        }
+    }
+
     // ---- inputs produced by earlier kernels (codes, scales) from here on
     pdl_wait();
     // token scales for the epilogue, fetched while the K loop runs (the MMA
@@ -219,14 +284,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         if (lane < kTcTok) cp_async4(sx_s + lane, lane < A.M ? A.sx + lane : A.sx, lane < A.M ? 4u : 0u);
         cp_async_commit();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *tmem_slot;
-    auto fail = [&]() {
-        *dead_s = 1u;
-        if (A.err != nullptr) atomicExch(A.err, kErrWaitTimeout);
-    };
 
     int committed = 0;   // K blocks whose MMAs were committed (MMA warp)
     if (mma_warp) {
@@ -311,13 +368,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
         // group's per-block chain (waits, stores, fences, the hand-off) thus has
         // two block periods to run while the other group fills the next buffer.
         static_assert(kSubs == 2 && kTcDqWarps == 8, "two groups of four warps, one K block of a stage each");
-        const int row = tid & (kTcRows - 1);
-        const int grp = warp >> 2;
-        const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint8_t* my_units =
-            ring + (row >> 3) * (kTcStageChunks * kRows * 16) + (grp * kTcChunks) * kRows * 16 + (row & 7) * 16;
-        const int cn = row & (kTcTok - 1);
-        const int kg = row >> 4;
+        const int cn = row_a & (kTcTok - 1);
+        const int kg = row_a >> 4;
         static_assert(kTcThreadCodes == 32 && kTcRows * kTcThreadCodes == kTcTok * kTcKb,
                       "each dequantizing thread copies two 16-K groups of one token per block");
         int xsum = 0;       // this thread's code sum (token cn, its K groups) over the split's K range
@@ -352,8 +404,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
             fetch_codes(b + 2 * (kTcCodeRing - 1), cs_next);
             // buffer j is free once the commit of block b - kTcBufs arrived (the MMA
             // lane commits every block, failed or not, so this wait keeps its order)
+            const bool a_done = first_a_done && b == grp;
             bool ok = b < kTcBufs || mbar_wait_bounded(free_b + 8 * j, static_cast<uint32_t>(q - 1) & 1u, kTcWaitNs);
-            if (ok && !*dead_s) ok = mbar_wait_bounded(full_b + 8 * slot, sph, kTcWaitNs);
+            if (ok && !*dead_s && !a_done) ok = mbar_wait_bounded(full_b + 8 * slot, sph, kTcWaitNs);
             if (!__all_sync(0xffffffffu, ok) && lane == 0 && !*dead_s) fail();
             if (*dead_s) {
                 // stop working but keep the per-block handshake
@@ -362,35 +415,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_linear_kernel(const __grid_c
                 continue;
             }
             tc_fence_after();
-            // the block's 256 K of this row as e4m3 (the buffer's 64 columns) in two
-            // halves of four chunks, sixteen columns per store
-            const uint8_t* units = my_units + static_cast<size_t>(slot) * kTcStageBytes;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                constexpr int kQ = kTcChunks / 2;
-                uint4 u[kQ];
-#pragma unroll
-                for (int e = 0; e < kQ; ++e)
-                    if (kQ * hf + e < nch) u[e] = *reinterpret_cast<const uint4*>(units + (kQ * hf + e) * kRows * 16);
-                if (hf == 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty_b + 8 * slot);   // this group's block of the stage is read
-                }
-#pragma unroll
-                for (int r = 0; r < kQ / 2; ++r) {
-                    uint32_t h[16];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        if (kQ * hf + 2 * r + e < nch) {
-                            tc_unit_e4m3(u[2 * r + e], &h[e * 8]);
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) h[e * 8 + k] = 0u;
-                        }
-                    }
-                    tmem_st16(tbase + tlane + kTcColA + j * kTcAStride + 32 * hf + 16 * r, h);
-                }
-            }
+            if (!a_done) convert_a(slot, j, nch);
             // B: token cn, K groups kg and kg + 8 of the block: the high halves in
             // column cn, the low halves in column 16 + cn
             cp_async_wait_group<kTcCodeRing - 1>();

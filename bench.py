@@ -68,6 +68,9 @@ def parse_args(argv=None):
     p.add_argument("--suite-gemvs", default="",
                    help="suite: only these single GEMVs, comma-separated, each a workload (gemma_q4_0) or "
                         "workload:linear (lm_head:lm_head_q6g32); default all")
+    p.add_argument("--suite-gemv-ms", default="1",
+                   help="token counts of the suite's single-GEMV lines (the multi-token verify case: M tokens "
+                        "sharing one pass over the weights)")
     p.add_argument("--suite-ablation-ms", default="1",
                    help="token counts of the suite's weight-only ablation lines (INT4 DP4A, INT4 float unpack, "
                         "INT8 weight-only; at most 2 tokens: the float activations of the K = 18944 linear "
@@ -901,15 +904,17 @@ def run_suite(args, local_rank):
     def baseline(lin, M):
         return None if args.no_cpu_baseline else oracle_gemv_baseline(lin, M)
 
-    for wname in (() if args.suite_only_steps else ("w4a8_single", "qwen7b_layer", "gemma_q4_0", "lm_head")):
-        lins = list(wl.workload(wname).linears)
-        if wname == "lm_head":
-            lins.append(wl.gemma_lm_head_q6g32())   # the same values packed in 6 bits
-        for lin in lins:
-            if suite_selected(args.suite_gemvs, wname, lin.name):
-                line = suite_gemv(wname, lin, 1, dev, stream, args.steps, args.warmup, peak, peak_rd)
-                line["cpu_baseline"] = baseline(lin, 1)
-                print(json.dumps(line), flush=True)
+    gemv_ms = [int(m) for m in args.suite_gemv_ms.split(",") if m]
+    for M in (() if args.suite_only_steps else gemv_ms):
+        for wname in ("w4a8_single", "qwen7b_layer", "gemma_q4_0", "lm_head"):
+            lins = list(wl.workload(wname).linears)
+            if wname == "lm_head":
+                lins.append(wl.gemma_lm_head_q6g32())   # the same values packed in 6 bits
+            for lin in lins:
+                if suite_selected(args.suite_gemvs, wname, lin.name):
+                    line = suite_gemv(wname, lin, M, dev, stream, args.steps, args.warmup, peak, peak_rd)
+                    line["cpu_baseline"] = baseline(lin, M)
+                    print(json.dumps(line), flush=True)
     step_ms = [int(m) for m in args.suite_ms.split(",") if m]
     weights = build_weights(args, dev) if step_ms else None
     for M in step_ms:

@@ -27,7 +27,8 @@ STATUS = {
     5: "W4_ERR_DEVICE_TIMEOUT",
 }
 W4_FLAG_PDL = 1
-TUNE_KEYS = {"blocks_per_sm": 0, "max_stages": 1, "grid_blocks": 2, "tc_min_m": 3, "chain_prefetch_kb": 4, "k_splits": 5}
+TUNE_KEYS = {"blocks_per_sm": 0, "max_stages": 1, "grid_blocks": 2, "tc_min_m": 3, "chain_prefetch_kb": 4, "k_splits": 5,
+             "group_launch_tokens": 6}
 W4_MAX_M = 16
 W4_MAX_K = 131072
 W4_MAX_SHARDS = 8
@@ -116,7 +117,7 @@ class DeviceDesc(ctypes.Structure):
 class LaunchPlan(ctypes.Structure):
     """w4_launch_plan of include/w4a8.h."""
     _fields_ = [("path", _I), ("quantize_launches", _I), ("grid", _I), ("threads", _I), ("smem_bytes", _I),
-                ("stages", _I), ("k_splits", _I)]
+                ("stages", _I), ("k_splits", _I), ("gemv_launches", _I)]
 
 
 FORMATS = {"w4": 0, "q4_0": 1, "i8g32": 2, "q6g32": 3}

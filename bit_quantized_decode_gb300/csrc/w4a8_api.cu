@@ -33,7 +33,7 @@ std::mutex g_setup_mutex;
 std::atomic<bool> g_dev_ready[kMaxDevices];
 
 // Launch tuning set by w4_set_tuning (0 = automatic).
-int g_tune[6] = {0, 0, 0, 0, 0, 0};
+int g_tune[7] = {0, 0, 0, 0, 0, 0, 0};
 // Weight bytes a chain block prefetches into L2 ahead of its ring copies (KB):
 // none by default (measured slower: the prefetches slowed the stream they lead).
 constexpr int kChainPrefetchKB = 0;
@@ -92,6 +92,38 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 inline w4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4_OK : W4_ERR_CUDA; }
 
 inline int round_pow2_tokens(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+
+// A DP4A GEMV of a group format (Q4_0, I8G32, Q6G32) with more than eight
+// tokens runs as two launches over the same weights, tokens 0-7 and the rest,
+// when it streams at least kGroupSplitTiles 8-row tiles per SM or has more
+// than kGroupSplitAbove tokens; otherwise as one launch.  Every step of the
+// GEMV is per token (the quantize prologue, the epilogue, the residual), so
+// the split changes no result.  The sixteen-token inner loop holds twice the
+// accumulators and spills.  Measured on GB300 (single GEMVs, weights rotated
+// past L2, us, two launches / one launch):
+//   I8G32 lm_head 262144x1536   M = 9: 234 / 380    12: 272 / 417   16: 324 / 467
+//   Q6G32 lm_head 262144x1536   M = 9: 304 / 557    12: 403 / 666   16: 495 / 847
+//   Q4_0 gate/up 12288x1536     M = 9: 20.4 / 23.4  12: 24.5 / 26.2  16: 24.8 / 30.3
+//   Q4_0 QKV 2560x1536          M = 9: 13.0 / 13.0  12: 16.6 / 14.2  14: 12.8 / 14.9  16: 13.6 / 15.5
+//   Q4_0 down 1536x6144         M = 9: 21.5 / 22.4  12: 29.0 / 24.7  14: 26.8 / 26.6  16: 28.4 / 28.3
+// The short GEMVs lose at 10-12 tokens: their second launch (two or four
+// tokens, another shared-memory configuration) cannot start until the first
+// has left the SM, and their weights take only a few microseconds to stream.
+constexpr int kGroupLaunchTokens = 8;
+constexpr int kGroupSplitAbove = 12;
+constexpr int kGroupSplitTiles = 8;
+
+// Tokens in the first (and every full) launch of an M-token call over T row
+// tiles; M for one launch.  W4_TUNE_GROUP_LAUNCH_TOKENS = t > 0 replaces the
+// rule for the group formats by launches of at most t tokens.
+inline int launch_tokens(const DeviceInfo& d, int fmt, int M, int T)
+{
+    if (fmt == FMT_W4 || fmt_float_x(fmt)) return M;
+    const int t = g_tune[W4_TUNE_GROUP_LAUNCH_TOKENS];
+    if (t > 0) return M > t ? t : M;
+    const bool split = M > kGroupSplitAbove || (M > kGroupLaunchTokens && T >= kGroupSplitTiles * d.sms);
+    return split ? kGroupLaunchTokens : M;
+}
 
 w4_status check_mk(int M, int K)
 {
@@ -233,41 +265,81 @@ int choose_splits(const DeviceInfo& d, int fmt, int MT, int T, int C)
     return 1;
 }
 
-// Launch one GEMV.
+// One planned DP4A GEMV launch.
+struct GemvLaunch {
+    ChainParams<1> cp;
+    int MT, xmode, grid, smem;
+};
+
+// Plan one launch of a.M tokens (at most 16).
+w4_status plan_launch(const DeviceInfo& dev, int fmt, GemvArgs a, bool fused, GemvLaunch& L)
+{
+    const int MT = round_pow2_tokens(a.M);
+    a.C = a.K / 32;
+    a.T = static_cast<int>(tiles(a.N));
+    a.ks = choose_splits(dev, fmt, MT, a.T, a.C);
+    ChainParams<1>& cp = L.cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.n = 1;
+    cp.kmax = a.K;
+    cp.round_tiles = kAccWords / MT;
+    cp.err = dev.err;
+    Plan p;
+    if (a.ks > 1 && !plan_gemv(dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) a.ks = 1;   // no room to merge
+    const bool two = two_blocks_per_sm(dev, MT, a.T, a.ks);
+    if (!plan_gemv(dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks, two)) return W4_ERR_UNSUPPORTED_SHAPE;
+    cp.stages = p.stages;
+    const int grid = gemv_grid(dev, a.T, a.ks, p.smem, two);
+    const int clusters = grid / a.ks;
+    a.tq = a.T / clusters;
+    a.tr = a.T % clusters;
+    cp.lin[0] = a;
+    L.MT = MT;
+    L.xmode = p.xmode;
+    L.grid = grid;
+    L.smem = p.smem;
+    return W4_OK;
+}
+
+// Launch one GEMV: one kernel, or for a group format with more than
+// kGroupLaunchTokens tokens one kernel per group of tokens, each a
+// programmatic dependent of the one before.  Every launch is planned before
+// the first is issued, so a failed check launches nothing.
 w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t s)
 {
     DeviceInfo* dev = nullptr;
     w4_status st = device_info(&dev);
     if (st != W4_OK) return st;
-    const int MT = round_pow2_tokens(a.M);
-    a.C = a.K / 32;
-    a.T = static_cast<int>(tiles(a.N));
-    a.ks = choose_splits(*dev, fmt, MT, a.T, a.C);
-    ChainParams<1> cp;
-    std::memset(&cp, 0, sizeof(cp));
-    cp.lin[0] = a;
-    cp.n = 1;
-    cp.kmax = a.K;
-    cp.round_tiles = kAccWords / MT;
-    cp.err = dev->err;
-    Plan p;
-    if (a.ks > 1 && !plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks)) a.ks = 1;   // no room to merge
-    cp.lin[0].ks = a.ks;
-    const bool two = two_blocks_per_sm(*dev, MT, a.T, a.ks);
-    if (!plan_gemv(*dev, fmt, MT, fused, a.K, cp.round_tiles, p, a.ks, two)) return W4_ERR_UNSUPPORTED_SHAPE;
-    cp.stages = p.stages;
-    const int grid = gemv_grid(*dev, a.T, a.ks, p.smem, two);
-    const int clusters = grid / a.ks;
-    cp.lin[0].tq = a.T / clusters;
-    cp.lin[0].tr = a.T % clusters;
-    const bool pdl = (flags & W4_FLAG_PDL) != 0;
-    cudaError_t e;
-    if (fmt_float_x(fmt)) e = launch_gemv_a32(fmt, cp, MT, grid, p.smem, pdl, s);
-    else if (fmt == FMT_W4) e = launch_gemv_w4(cp, MT, p.xmode, grid, p.smem, pdl, s);
-    else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(cp, MT, p.xmode, grid, p.smem, pdl, s);
-    else if (fmt == FMT_I8G32) e = launch_gemv_i8g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
-    else e = launch_gemv_q6g32(cp, MT, p.xmode, grid, p.smem, pdl, s);
-    return cuda_status(e);
+    const int mc = launch_tokens(*dev, fmt, a.M, static_cast<int>(tiles(a.N)));
+    const int nl = (a.M + mc - 1) / mc;
+    GemvLaunch L[W4_MAX_M];
+    for (int c = 0; c < nl; ++c) {
+        const size_t m0 = static_cast<size_t>(c) * mc;
+        GemvArgs t = a;
+        t.M = a.M - static_cast<int>(m0) < mc ? a.M - static_cast<int>(m0) : mc;
+        const size_t xo = m0 * static_cast<size_t>(a.K), yo = m0 * static_cast<size_t>(a.n_out);
+        if (t.x) t.x += xo;
+        if (t.qx_in) t.qx_in += xo;
+        if (t.sx_in) t.sx_in += m0;
+        if (t.qx_out) t.qx_out += xo;
+        if (t.sx_out) t.sx_out += m0;
+        t.y += yo;
+        if (t.residual) t.residual += yo;
+        st = plan_launch(*dev, fmt, t, fused, L[c]);
+        if (st != W4_OK) return st;
+    }
+    for (int c = 0; c < nl; ++c) {
+        const GemvLaunch& l = L[c];
+        const bool pdl = c > 0 || (flags & W4_FLAG_PDL) != 0;
+        cudaError_t e;
+        if (fmt_float_x(fmt)) e = launch_gemv_a32(fmt, l.cp, l.MT, l.grid, l.smem, pdl, s);
+        else if (fmt == FMT_W4) e = launch_gemv_w4(l.cp, l.MT, l.xmode, l.grid, l.smem, pdl, s);
+        else if (fmt == FMT_Q4_0) e = launch_gemv_q4_0(l.cp, l.MT, l.xmode, l.grid, l.smem, pdl, s);
+        else if (fmt == FMT_I8G32) e = launch_gemv_i8g32(l.cp, l.MT, l.xmode, l.grid, l.smem, pdl, s);
+        else e = launch_gemv_q6g32(l.cp, l.MT, l.xmode, l.grid, l.smem, pdl, s);
+        if (e != cudaSuccess) return W4_ERR_CUDA;
+    }
+    return W4_OK;
 }
 
 // Chain of per-row INT4 linears in one cooperative launch.
@@ -331,19 +403,19 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
 }
 
 // Would the fused kernel (x quantized into shared memory) fit on device d?
-bool fused_fits_on(const DeviceInfo& d, int fmt, int M, int K, bool norm)
+bool fused_fits_on(const DeviceInfo& d, int fmt, int M, int K, int T, bool norm)
 {
-    const int MT = round_pow2_tokens(M);
+    const int MT = round_pow2_tokens(launch_tokens(d, fmt, M, T));
     if (norm && (MT > 4 || (K / 4 + kThreads - 1) / kThreads > norm_max_nit(MT))) return false;
     Plan p;
     return plan_gemv(d, fmt, MT, true, K, kAccWords / MT, p);
 }
 
-bool fused_fits(int fmt, int M, int K, bool norm = false)
+bool fused_fits(int fmt, int M, int K, int T, bool norm)
 {
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != W4_OK) return false;
-    return fused_fits_on(*dev, fmt, M, K, norm);
+    return fused_fits_on(*dev, fmt, M, K, T, norm);
 }
 
 // Operators fused around one linear (w4_fusion, checked).
@@ -503,7 +575,7 @@ w4_status linear_common(int fmt, const void* w, const float* s_w, const float* b
     if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
     const bool norm = fz.gamma != nullptr;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
-    if (N == 0 || use_tc(fmt, M, K) || !fused_fits(fmt, M, K, norm)) {
+    if (N == 0 || use_tc(fmt, M, K) || !fused_fits(fmt, M, K, static_cast<int>(tiles(weight_rows(N, fz.glu))), norm)) {
         // quantize (normalize first if asked) into the caller's qx/sx once, then
         // the GEMV on int8 codes (tensor cores for many tokens), chained by
         // programmatic dependent launch
@@ -582,11 +654,12 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
     w4_launch_plan p = {};
     p.k_splits = 1;
     if (M > 0) {
+        if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
+        const int Nw = weight_rows(N, glu ? GLU_SILU : GLU_NONE);
+        const int T = static_cast<int>(tiles(Nw));
         const bool tc = use_tc(fmt, M, K);
-        if (linear && (N == 0 || tc || !fused_fits_on(d, fmt, M, K, norm))) p.quantize_launches = 1;
+        if (linear && (N == 0 || tc || !fused_fits_on(d, fmt, M, K, T, norm))) p.quantize_launches = 1;
         if (N > 0) {
-            if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
-            const int Nw = weight_rows(N, glu ? GLU_SILU : GLU_NONE);
             if (tc) {
                 int ks = 0, S = 0;
                 st = tc_plan(d, Nw, K, ks, S);
@@ -597,9 +670,10 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
                 p.smem_bytes = tc_smem(S, ks).total;
                 p.stages = S;
                 p.k_splits = ks;
+                p.gemv_launches = 1;
             } else {
-                const int MT = round_pow2_tokens(M);
-                const int T = static_cast<int>(tiles(Nw));
+                const int mc = launch_tokens(d, fmt, M, T);
+                const int MT = round_pow2_tokens(mc);
                 const int ks = choose_splits(d, fmt, MT, T, K / 32);
                 Plan q;
                 const bool two = two_blocks_per_sm(d, MT, T, ks);
@@ -612,6 +686,7 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
                 p.threads = kThreads;
                 p.smem_bytes = q.smem;
                 p.stages = q.stages;
+                p.gemv_launches = (M + mc - 1) / mc;
             }
         }
     }
@@ -634,7 +709,8 @@ w4_status w4_describe_device(w4_device_desc* out)
 
 w4_status w4_set_tuning(int key, int value)
 {
-    if (key < 0 || key > W4_TUNE_K_SPLITS || value < 0) return W4_ERR_INVALID_ARG;
+    if (key < 0 || key > W4_TUNE_GROUP_LAUNCH_TOKENS || value < 0) return W4_ERR_INVALID_ARG;
+    if (key == W4_TUNE_GROUP_LAUNCH_TOKENS && value > W4_MAX_M) return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_K_SPLITS && value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
         return W4_ERR_INVALID_ARG;
     if (key == W4_TUNE_CHAIN_PREFETCH_KB && value > 4096) return W4_ERR_INVALID_ARG;
@@ -647,7 +723,7 @@ w4_status w4_set_tuning(int key, int value)
 
 int w4_get_tuning(int key)
 {
-    if (key < 0 || key > W4_TUNE_K_SPLITS) return -1;
+    if (key < 0 || key > W4_TUNE_GROUP_LAUNCH_TOKENS) return -1;
     return g_tune[key];
 }
 

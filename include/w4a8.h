@@ -108,7 +108,11 @@ int w4_version(void);
  *                          cluster of 2, 4 or 8 blocks sharing a tile range
  *                          (where each split keeps at least 16 chunks of 32 K);
  *                          0 or 1: no split, the default (a split measured
- *                          slower on every shape tried, see DESIGN notes).
+ *                          slower on every shape tried).
+ *   W4_TUNE_GROUP_LAUNCH_TOKENS  Q4_0 / I8G32 / Q6G32 calls with more tokens
+ *                          than this run as launches of at most this many
+ *                          tokens (1..16; default 0: the rule given under
+ *                          gemv_launches in w4_plan).
  *   W4_TUNE_CHAIN_PREFETCH_KB  w4a8_linear_chain: weight bytes (KB, at most
  *                          4096) each block prefetches into L2 ahead of the
  *                          weights it copies into shared memory (default
@@ -122,6 +126,7 @@ int w4_version(void);
 #define W4_TUNE_TC_MIN_M 3
 #define W4_TUNE_CHAIN_PREFETCH_KB 4
 #define W4_TUNE_K_SPLITS 5
+#define W4_TUNE_GROUP_LAUNCH_TOKENS 6
 w4_status w4_set_tuning(int key, int value);
 int w4_get_tuning(int key); /* current value, -1 for an unknown key */
 
@@ -144,7 +149,12 @@ int w4_get_tuning(int key); /* current value, -1 for an unknown key */
  *         launch: grid, threads, smem_bytes (dynamic, per block), stages
  *         (weight-ring depth), k_splits (K splits per tile range, which form
  *         one thread-block cluster: per 128-row group on the tensor cores, per
- *         range of 8-row tiles on DP4A; 1 without a split).
+ *         range of 8-row tiles on DP4A; 1 without a split), gemv_launches
+ *         (GEMV kernels per call: 0 without a GEMV; 2 for a Q4_0 / I8G32 /
+ *         Q6G32 call of more than 8 tokens over at least 8 row tiles of 8
+ *         per SM, or of more than 12 tokens, which runs tokens 0-7 and the
+ *         rest as two launches over the same weights, the fields above
+ *         describing the first; otherwise 1).
  * Paths:
  *   W4_PATH_NONE          nothing (M = 0, or N = 0 where only the quantizer
  *                         of a *_linear call runs);
@@ -183,6 +193,7 @@ typedef struct {
     int smem_bytes;
     int stages;
     int k_splits;
+    int gemv_launches;
 } w4_launch_plan;
 w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_desc* dev, w4_launch_plan* out);
 /* The current device's description (W4_ERR_CUDA without a usable device). */
@@ -288,6 +299,10 @@ w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_st
  * q4_0_gemv / i8g32_gemv / q6g32_gemv, [310B-Gemma4] §3.1 / §3.2:
  *   acc_g = exact int32 sum over 32-block g,
  *   y[m][j] = fmaf(sx[m], sum_g d_g * acc_g, b[j])  (fp32; group order unspecified).
+ *   With more than 8 tokens these (and the *_linear calls of these formats)
+ *   may run as two launches, tokens 0-7 and the rest (w4_plan's
+ *   gemv_launches), each reading the weights once; every step is per token,
+ *   so each token's result is that of a call of its launch's tokens.
  * w: repacked weights; s_w: float [N]; bias: float [N] or NULL; qx: int8 [M][K];
  * sx: float [M]; y: float [M][N] (row m at y + m*N).
  * ------------------------------------------------------------------------ */
@@ -434,7 +449,7 @@ w4_status w8a32_gemv(const void* w, const float* s_w, const float* bias, const f
  * three or more tokens are faster through the per-linear entry points
  * (w4a8_linear with W4_FLAG_PDL, on the tensor cores), which need the qx / sx
  * buffers the chain may leave out.  On the 7B step the per-linear launches
- * chained with W4_FLAG_PDL are also faster at one token (0.874 against
+ * chained with W4_FLAG_PDL are also faster at one token (0.872 against
  * 1.03-1.07 ms); the chain is the single-launch alternative. 
  * ------------------------------------------------------------------------ */
 #define W4_MAX_CHAIN 128

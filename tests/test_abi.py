@@ -61,6 +61,10 @@ def test_tuning_roundtrip_and_checks(lib):
     assert lib.w4_set_tuning(1, 1) == 1          # a ring needs two stages
     assert lib.w4_set_tuning(7, 0) == 1          # unknown key
     assert lib.w4_get_tuning(7) == -1
+    assert lib.w4_set_tuning(6, 17) == 1         # tokens per group-format launch: at most 16
+    _lib.set_tuning("group_launch_tokens", 16)
+    assert _lib.get_tuning("group_launch_tokens") == 16
+    _lib.set_tuning("group_launch_tokens", 0)
     assert lib.w4_set_tuning(4, 5000) == 1       # chain L2 lookahead: at most 4096 KB
     _lib.set_tuning("chain_prefetch_kb", 32)
     assert _lib.get_tuning("chain_prefetch_kb") == 32

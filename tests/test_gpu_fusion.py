@@ -279,7 +279,8 @@ class GatedLayer:
 
 
 @pytest.mark.parametrize("fmt,kind", [("w4", 1), ("w4", 2), ("q4_0", 1), ("q4_0", 2)])
-@pytest.mark.parametrize("M,I,K", [(1, 2368, 3584), (3, 101, 1536), (4, 3, 256), (16, 1000, 3584), (8, 516, 96)])
+@pytest.mark.parametrize("M,I,K", [(1, 2368, 3584), (3, 101, 1536), (4, 3, 256), (16, 1000, 3584), (8, 516, 96),
+                                   (12, 260, 1536)])
 def test_glu_linear(lib, fmt, kind, M, I, K):
     """Gate/up paired per tile, the activation in the epilogue: within the
     propagated bound of the oracle, and equal to the plain linear on the
@@ -328,7 +329,9 @@ def test_glu_linear_tensor_cores_and_uncached_rows(lib):
 @pytest.mark.parametrize("fmt,M,N,K,tc", [("w4", 1, 3584, 3584, False), ("w4", 2, 3584, 18944, False),
                                           ("q4_0", 3, 1536, 6144, False), ("w4", 16, 3584, 3584, True),
                                           ("i8g32", 1, 200, 1536, False), ("w4", 7, 1000, 3584, True),
-                                          ("w4", 4, 264, 3584, False), ("w4", 3, 520, 6144, False)])
+                                          ("w4", 4, 264, 3584, False), ("w4", 3, 520, 6144, False),
+                                          ("q4_0", 12, 1536, 6144, False), ("q6g32", 16, 300, 1536, False),
+                                          ("i8g32", 9, 1000, 1536, False)])
 def test_residual_linear_in_place(lib, fmt, M, N, K, tc):
     """y = residual + linear(x), with the residual buffer as the output (the
     decoder's in-place update): within the linear's tolerance plus the final

@@ -354,6 +354,79 @@ def test_i8g32_linear(lib, M, N, K):
                 "i8g32_linear")
 
 
+# ------------------------------------------ group formats past eight tokens
+def _group_weights(lib, fmt, W, K):
+    """fmt weights from the oracle's quantizer, repacked on the device, with the
+    oracle GEMV on them and their group scales."""
+    torch = _torch()
+    N = W.shape[0]
+    if fmt == "q4_0":
+        blocks = oracle.quantize_q4_0(W)
+        return (_prep_q4_0(lib, [blocks], K),
+                lambda qx, sx, b: oracle.gemv_q4_0(blocks, qx, sx, b, want_acc=True), q4_0_scales(blocks))
+    q, d = oracle.quantize_i8g32(W)
+    size, repack = ((lib.q6g32_repacked_bytes, lib.q6g32_repack) if fmt == "q6g32"
+                    else (lib.i8g32_repacked_bytes, lib.i8g32_repack))
+    w = torch.empty(size(N, K), dtype=torch.uint8, device="cuda")
+    repack([dev(q)], [dev(d.view(np.int16))], K, w)
+    return (w, lambda qx, sx, b: oracle.gemv_i8g32(q, d, qx, sx, b, want_acc=True),
+            d.view(np.float16).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "i8g32", "q6g32"])
+@pytest.mark.parametrize("M,N,K,t", [(16, 1000, 1536, 0), (13, 77, 6144, 0), (10, 9728, 1536, 0), (12, 300, 1536, 0),
+                                     (9, 300, 1536, 8), (16, 5, 64, 4)])
+def test_group_formats_past_eight_tokens(lib, fmt, M, N, K, t):
+    """More than eight tokens run as two launches over the same weights
+    (tokens 0-7, then the rest) where the planner says so, and as launches of
+    at most t tokens under W4_TUNE_GROUP_LAUNCH_TOKENS = t: every token's
+    codes and scale bit-exact, y within the group tolerance through both entry
+    points, and each token's y bit-identical to the same token in a call of
+    one launch on the same path."""
+    torch = _torch()
+    g = wl.rng(41 * M + N + K + t)
+    W = wl.weights(g, N, K, 0.03)
+    x = wl.activations(g, M, K, outliers=True)
+    b = wl.bias(g, N)
+    w, ref, scales = _group_weights(lib, fmt, W, K)
+    qx_ref, sx_ref = oracle.quantize_act_int8(x)
+    y_ref, acc = ref(qx_ref, sx_ref, b)
+    tol = group_scale(acc, scales, sx_ref, b)
+    linear, gemv = getattr(lib, f"{fmt}_linear"), getattr(lib, f"{fmt}_gemv")
+    device = lib.w4_describe_device()
+
+    def bufs(m):
+        return (torch.empty((m, N), dtype=torch.float32, device="cuda"),
+                torch.empty((m, K), dtype=torch.int8, device="cuda"),
+                torch.empty(m, dtype=torch.float32, device="cuda"))
+
+    lib.set_tuning("group_launch_tokens", t)
+    try:
+        p = lib.w4_plan(fmt, M, N, K, device)
+        c = t if t else (8 if M > 12 or (N + 7) // 8 >= 8 * device["sms"] else M)
+        assert p["gemv_launches"] == (M + c - 1) // c
+        y, qx, sx = bufs(M)
+        linear(w, dev(b), dev(x), y, qx, sx)
+        assert np.array_equal(host(qx), qx_ref) and np.array_equal(host(sx), sx_ref)
+        check_close(host(y), y_ref, tol, RTOL_GROUP, f"{fmt}_linear M={M}")
+        yg = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        gemv(w, dev(b), qx, sx, yg)
+        check_close(host(yg), y_ref, tol, RTOL_GROUP, f"{fmt}_gemv M={M}")
+        for lo in range(0, M, c):
+            hi = min(M, lo + c)
+            assert lib.w4_plan(fmt, hi - lo, N, K, device)["gemv_launches"] == 1
+            ys, qxs, sxs = bufs(hi - lo)
+            linear(w, dev(b), dev(x[lo:hi]), ys, qxs, sxs)
+            assert np.array_equal(host(qxs), qx_ref[lo:hi])
+            if lib.w4_plan(fmt, hi - lo, N, K, device)["path"] == p["path"]:
+                assert np.array_equal(host(ys).view(np.uint32), host(y)[lo:hi].view(np.uint32)), (lo, hi)
+            yc = torch.empty((hi - lo, N), dtype=torch.float32, device="cuda")
+            gemv(w, dev(b), qx[lo:hi], sx[lo:hi], yc)
+            assert np.array_equal(host(yc).view(np.uint32), host(yg)[lo:hi].view(np.uint32)), (lo, hi)
+    finally:
+        lib.set_tuning("group_launch_tokens", 0)
+
+
 def test_i8g32_accumulators_bit_exact(lib):
     torch = _torch()
     M, N, K = 2, 50, 1536

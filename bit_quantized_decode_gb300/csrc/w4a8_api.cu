@@ -301,9 +301,8 @@ w4_status plan_launch(const DeviceInfo& dev, int fmt, GemvArgs a, bool fused, Ge
     return W4_OK;
 }
 
-// Launch one GEMV: one kernel, or for a group format with more than
-// kGroupLaunchTokens tokens one kernel per group of tokens, each a
-// programmatic dependent of the one before.  Every launch is planned before
+// Launch one GEMV: one kernel, or, where launch_tokens splits the tokens, one
+// kernel per group of them, each a programmatic dependent of the one before.  Every launch is planned before
 // the first is issued, so a failed check launches nothing.
 w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t s)
 {

@@ -94,3 +94,9 @@ def test_suite_gemv_selection():
     assert not bench.suite_selected("gemma_q4_0", "lm_head", "lm_head")
     assert bench.suite_selected("gemma_q4_0:down, lm_head:lm_head_q6g32", "lm_head", "lm_head_q6g32")
     assert not bench.suite_selected("lm_head:lm_head_q6g32", "lm_head", "lm_head_i8g32")
+
+
+def test_suite_token_count_options():
+    args = bench.parse_args(["--suite", "--suite-gemv-ms", "1,9,16", "--suite-ms", ""])
+    assert args.suite and args.suite_gemv_ms == "1,9,16" and args.suite_ms == ""
+    assert bench.parse_args([]).suite_gemv_ms == "1"      # single GEMVs at one token by default

@@ -94,35 +94,31 @@ inline w4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4_OK : 
 inline int round_pow2_tokens(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 
 // A DP4A GEMV of a group format (Q4_0, I8G32, Q6G32) with more than eight
-// tokens runs as two launches over the same weights, tokens 0-7 and the rest,
-// when it streams at least kGroupSplitTiles 8-row tiles per SM or has more
-// than kGroupSplitAbove tokens; otherwise as one launch.  Every step of the
-// GEMV is per token (the quantize prologue, the epilogue, the residual), so
-// the split changes no result.  The sixteen-token inner loop holds twice the
-// accumulators and spills.  Measured on GB300 (single GEMVs, weights rotated
-// past L2, us, two launches / one launch):
-//   I8G32 lm_head 262144x1536   M = 9: 234 / 380    12: 272 / 417   16: 324 / 467
-//   Q6G32 lm_head 262144x1536   M = 9: 304 / 557    12: 403 / 666   16: 495 / 847
-//   Q4_0 gate/up 12288x1536     M = 9: 20.4 / 23.4  12: 24.5 / 26.2  16: 24.8 / 30.3
-//   Q4_0 QKV 2560x1536          M = 9: 13.0 / 13.0  12: 16.6 / 14.2  14: 12.8 / 14.9  16: 13.6 / 15.5
-//   Q4_0 down 1536x6144         M = 9: 21.5 / 22.4  12: 29.0 / 24.7  14: 26.8 / 26.6  16: 28.4 / 28.3
-// The short GEMVs lose at 10-12 tokens: their second launch (two or four
-// tokens, another shared-memory configuration) cannot start until the first
-// has left the SM, and their weights take only a few microseconds to stream.
+// tokens runs as two launches of the eight-token kernel over the same
+// weights, tokens 0-7 and the rest.  Every step of the GEMV is per token (the
+// quantize prologue, the epilogue, the residual), so the split changes no
+// token's codes or integer group sums.  The sixteen-token inner loop holds
+// twice the accumulators and spills.  Measured on GB300 (single GEMVs, weights
+// rotated past L2, us, two launches / one launch):
+//   I8G32 lm_head 262144x1536   M = 9: 234 / 380    12: 288 / 417    16: 324 / 467
+//   Q6G32 lm_head 262144x1536   M = 9: 304 / 557    12: 403 / 666    16: 495 / 847
+//   Q4_0 gate/up 12288x1536     M = 9: 19.1 / 23.4  12: 21.4 / 26.2  16: 24.8 / 30.3
+//   Q4_0 QKV 2560x1536          M = 9: 10.7 / 13.0  12: 12.0 / 14.2  16: 13.6 / 15.5
+//   Q4_0 down 1536x6144         M = 9: 22.4 / 22.3  12: 25.0 / 24.7  16: 28.4 / 28.3
+// (the M = 9 lm_head rows and the Q6G32 M = 12 row ran the second launch on its
+// own token count's kernel; the second launch now takes the first's kernel
+// and shared-memory plan, which took the short GEMVs' split from 13.0 to
+// 10.7 us (QKV, 9 tokens) and from 16.6 to 12.0 us (12 tokens): launches of
+// one configuration follow each other on an SM without draining it.)
 constexpr int kGroupLaunchTokens = 8;
-constexpr int kGroupSplitAbove = 12;
-constexpr int kGroupSplitTiles = 8;
 
-// Tokens in the first (and every full) launch of an M-token call over T row
-// tiles; M for one launch.  W4_TUNE_GROUP_LAUNCH_TOKENS = t > 0 replaces the
-// rule for the group formats by launches of at most t tokens.
-inline int launch_tokens(const DeviceInfo& d, int fmt, int M, int T)
+// Tokens in the first (and every full) launch of an M-token call; M for one
+// launch.  W4_TUNE_GROUP_LAUNCH_TOKENS = t > 0 sets the limit to t tokens.
+inline int launch_tokens(int fmt, int M)
 {
     if (fmt == FMT_W4 || fmt_float_x(fmt)) return M;
-    const int t = g_tune[W4_TUNE_GROUP_LAUNCH_TOKENS];
-    if (t > 0) return M > t ? t : M;
-    const bool split = M > kGroupSplitAbove || (M > kGroupLaunchTokens && T >= kGroupSplitTiles * d.sms);
-    return split ? kGroupLaunchTokens : M;
+    const int t = g_tune[W4_TUNE_GROUP_LAUNCH_TOKENS] > 0 ? g_tune[W4_TUNE_GROUP_LAUNCH_TOKENS] : kGroupLaunchTokens;
+    return M > t ? t : M;
 }
 
 w4_status check_mk(int M, int K)
@@ -271,10 +267,10 @@ struct GemvLaunch {
     int MT, xmode, grid, smem;
 };
 
-// Plan one launch of a.M tokens (at most 16).
-w4_status plan_launch(const DeviceInfo& dev, int fmt, GemvArgs a, bool fused, GemvLaunch& L)
+// Plan one launch of a.M tokens on the kernel for MT tokens (a.M <= MT; the
+// kernel skips the tokens past a.M at run time).
+w4_status plan_launch(const DeviceInfo& dev, int fmt, GemvArgs a, bool fused, int MT, GemvLaunch& L)
 {
-    const int MT = round_pow2_tokens(a.M);
     a.C = a.K / 32;
     a.T = static_cast<int>(tiles(a.N));
     a.ks = choose_splits(dev, fmt, MT, a.T, a.C);
@@ -302,15 +298,19 @@ w4_status plan_launch(const DeviceInfo& dev, int fmt, GemvArgs a, bool fused, Ge
 }
 
 // Launch one GEMV: one kernel, or, where launch_tokens splits the tokens, one
-// kernel per group of them, each a programmatic dependent of the one before.  Every launch is planned before
+// kernel per group of them, each a programmatic dependent of the one before.
+// Every launch of a call runs the first launch's kernel and shared-memory
+// plan, so the next launch's blocks can take an SM as soon as this one's
+// leave it.  Every launch is planned before
 // the first is issued, so a failed check launches nothing.
 w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t s)
 {
     DeviceInfo* dev = nullptr;
     w4_status st = device_info(&dev);
     if (st != W4_OK) return st;
-    const int mc = launch_tokens(*dev, fmt, a.M, static_cast<int>(tiles(a.N)));
+    const int mc = launch_tokens(fmt, a.M);
     const int nl = (a.M + mc - 1) / mc;
+    const int MT = round_pow2_tokens(mc);
     GemvLaunch L[W4_MAX_M];
     for (int c = 0; c < nl; ++c) {
         const size_t m0 = static_cast<size_t>(c) * mc;
@@ -324,7 +324,7 @@ w4_status run_gemv(int fmt, GemvArgs a, bool fused, unsigned flags, cudaStream_t
         if (t.sx_out) t.sx_out += m0;
         t.y += yo;
         if (t.residual) t.residual += yo;
-        st = plan_launch(*dev, fmt, t, fused, L[c]);
+        st = plan_launch(*dev, fmt, t, fused, MT, L[c]);
         if (st != W4_OK) return st;
     }
     for (int c = 0; c < nl; ++c) {
@@ -402,19 +402,19 @@ w4_status run_chain(const w4_linear_desc* d, int n, int M, unsigned* barrier, cu
 }
 
 // Would the fused kernel (x quantized into shared memory) fit on device d?
-bool fused_fits_on(const DeviceInfo& d, int fmt, int M, int K, int T, bool norm)
+bool fused_fits_on(const DeviceInfo& d, int fmt, int M, int K, bool norm)
 {
-    const int MT = round_pow2_tokens(launch_tokens(d, fmt, M, T));
+    const int MT = round_pow2_tokens(launch_tokens(fmt, M));
     if (norm && (MT > 4 || (K / 4 + kThreads - 1) / kThreads > norm_max_nit(MT))) return false;
     Plan p;
     return plan_gemv(d, fmt, MT, true, K, kAccWords / MT, p);
 }
 
-bool fused_fits(int fmt, int M, int K, int T, bool norm)
+bool fused_fits(int fmt, int M, int K, bool norm)
 {
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != W4_OK) return false;
-    return fused_fits_on(*dev, fmt, M, K, T, norm);
+    return fused_fits_on(*dev, fmt, M, K, norm);
 }
 
 // Operators fused around one linear (w4_fusion, checked).
@@ -574,7 +574,7 @@ w4_status linear_common(int fmt, const void* w, const float* s_w, const float* b
     if (N > (1 << 30) - 8) return W4_ERR_UNSUPPORTED_SHAPE;
     const bool norm = fz.gamma != nullptr;
     const bool pdl = (flags & W4_FLAG_PDL) != 0;
-    if (N == 0 || use_tc(fmt, M, K) || !fused_fits(fmt, M, K, static_cast<int>(tiles(weight_rows(N, fz.glu))), norm)) {
+    if (N == 0 || use_tc(fmt, M, K) || !fused_fits(fmt, M, K, norm)) {
         // quantize (normalize first if asked) into the caller's qx/sx once, then
         // the GEMV on int8 codes (tensor cores for many tokens), chained by
         // programmatic dependent launch
@@ -657,7 +657,7 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
         const int Nw = weight_rows(N, glu ? GLU_SILU : GLU_NONE);
         const int T = static_cast<int>(tiles(Nw));
         const bool tc = use_tc(fmt, M, K);
-        if (linear && (N == 0 || tc || !fused_fits_on(d, fmt, M, K, T, norm))) p.quantize_launches = 1;
+        if (linear && (N == 0 || tc || !fused_fits_on(d, fmt, M, K, norm))) p.quantize_launches = 1;
         if (N > 0) {
             if (tc) {
                 int ks = 0, S = 0;
@@ -671,7 +671,7 @@ w4_status w4_plan(int fmt, int M, int N, int K, unsigned what, const w4_device_d
                 p.k_splits = ks;
                 p.gemv_launches = 1;
             } else {
-                const int mc = launch_tokens(d, fmt, M, T);
+                const int mc = launch_tokens(fmt, M);
                 const int MT = round_pow2_tokens(mc);
                 const int ks = choose_splits(d, fmt, MT, T, K / 32);
                 Plan q;

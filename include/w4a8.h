@@ -111,8 +111,7 @@ int w4_version(void);
  *                          slower on every shape tried).
  *   W4_TUNE_GROUP_LAUNCH_TOKENS  Q4_0 / I8G32 / Q6G32 calls with more tokens
  *                          than this run as launches of at most this many
- *                          tokens (1..16; default 0: the rule given under
- *                          gemv_launches in w4_plan).
+ *                          tokens (1..16; default 0: 8).
  *   W4_TUNE_CHAIN_PREFETCH_KB  w4a8_linear_chain: weight bytes (KB, at most
  *                          4096) each block prefetches into L2 ahead of the
  *                          weights it copies into shared memory (default
@@ -151,10 +150,9 @@ int w4_get_tuning(int key); /* current value, -1 for an unknown key */
  *         one thread-block cluster: per 128-row group on the tensor cores, per
  *         range of 8-row tiles on DP4A; 1 without a split), gemv_launches
  *         (GEMV kernels per call: 0 without a GEMV; 2 for a Q4_0 / I8G32 /
- *         Q6G32 call of more than 8 tokens over at least 8 row tiles of 8
- *         per SM, or of more than 12 tokens, which runs tokens 0-7 and the
- *         rest as two launches over the same weights, the fields above
- *         describing the first; otherwise 1).
+ *         Q6G32 call of more than 8 tokens, which runs tokens 0-7 and the
+ *         rest as two launches of one kernel over the same weights, both
+ *         as the fields above describe; otherwise 1).
  * Paths:
  *   W4_PATH_NONE          nothing (M = 0, or N = 0 where only the quantizer
  *                         of a *_linear call runs);
@@ -300,9 +298,10 @@ w4_status a8_quantize(const float* x, int M, int K, int8_t* qx, float* sx, w4_st
  *   acc_g = exact int32 sum over 32-block g,
  *   y[m][j] = fmaf(sx[m], sum_g d_g * acc_g, b[j])  (fp32; group order unspecified).
  *   With more than 8 tokens these (and the *_linear calls of these formats)
- *   may run as two launches, tokens 0-7 and the rest (w4_plan's
- *   gemv_launches), each reading the weights once; every step is per token,
- *   so each token's result is that of a call of its launch's tokens.
+ *   run as two launches of the eight-token kernel, tokens 0-7 and the rest,
+ *   each reading the weights once.  Every step is per token: codes, scales
+ *   and integer group sums are those of one launch; y may differ from a call
+ *   of other token counts only in the fp32 group-sum order.
  * w: repacked weights; s_w: float [N]; bias: float [N] or NULL; qx: int8 [M][K];
  * sx: float [M]; y: float [M][N] (row m at y + m*N).
  * ------------------------------------------------------------------------ */

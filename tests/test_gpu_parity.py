@@ -377,12 +377,13 @@ def _group_weights(lib, fmt, W, K):
 @pytest.mark.parametrize("M,N,K,t", [(16, 1000, 1536, 0), (13, 77, 6144, 0), (10, 9728, 1536, 0), (12, 300, 1536, 0),
                                      (9, 300, 1536, 8), (16, 5, 64, 4)])
 def test_group_formats_past_eight_tokens(lib, fmt, M, N, K, t):
-    """More than eight tokens run as two launches over the same weights
-    (tokens 0-7, then the rest) where the planner says so, and as launches of
-    at most t tokens under W4_TUNE_GROUP_LAUNCH_TOKENS = t: every token's
+    """More than eight tokens run as two launches of the eight-token kernel
+    over the same weights (tokens 0-7, then the rest), and as launches of at
+    most t tokens under W4_TUNE_GROUP_LAUNCH_TOKENS = t: every token's
     codes and scale bit-exact, y within the group tolerance through both entry
     points, and each token's y bit-identical to the same token in a call of
-    one launch on the same path."""
+    one launch of the same kernel on the same path (every launch of a call runs
+    the first launch's kernel; the group sums' fp32 order depends on it)."""
     torch = _torch()
     g = wl.rng(41 * M + N + K + t)
     W = wl.weights(g, N, K, 0.03)
@@ -403,7 +404,7 @@ def test_group_formats_past_eight_tokens(lib, fmt, M, N, K, t):
     lib.set_tuning("group_launch_tokens", t)
     try:
         p = lib.w4_plan(fmt, M, N, K, device)
-        c = t if t else (8 if M > 12 or (N + 7) // 8 >= 8 * device["sms"] else M)
+        c = t if t else 8
         assert p["gemv_launches"] == (M + c - 1) // c
         y, qx, sx = bufs(M)
         linear(w, dev(b), dev(x), y, qx, sx)
@@ -412,17 +413,23 @@ def test_group_formats_past_eight_tokens(lib, fmt, M, N, K, t):
         yg = torch.empty((M, N), dtype=torch.float32, device="cuda")
         gemv(w, dev(b), qx, sx, yg)
         check_close(host(yg), y_ref, tol, RTOL_GROUP, f"{fmt}_gemv M={M}")
+        def bucket(m):
+            return 1 if m <= 1 else 2 if m <= 2 else 4 if m <= 4 else 8 if m <= 8 else 16
+
         for lo in range(0, M, c):
             hi = min(M, lo + c)
-            assert lib.w4_plan(fmt, hi - lo, N, K, device)["gemv_launches"] == 1
+            q = lib.w4_plan(fmt, hi - lo, N, K, device)
+            assert q["gemv_launches"] == 1
             ys, qxs, sxs = bufs(hi - lo)
             linear(w, dev(b), dev(x[lo:hi]), ys, qxs, sxs)
             assert np.array_equal(host(qxs), qx_ref[lo:hi])
-            if lib.w4_plan(fmt, hi - lo, N, K, device)["path"] == p["path"]:
+            same_kernel = bucket(hi - lo) == bucket(c)
+            if same_kernel and q["path"] == p["path"]:
                 assert np.array_equal(host(ys).view(np.uint32), host(y)[lo:hi].view(np.uint32)), (lo, hi)
             yc = torch.empty((hi - lo, N), dtype=torch.float32, device="cuda")
             gemv(w, dev(b), qx[lo:hi], sx[lo:hi], yc)
-            assert np.array_equal(host(yc).view(np.uint32), host(yg)[lo:hi].view(np.uint32)), (lo, hi)
+            if same_kernel:
+                assert np.array_equal(host(yc).view(np.uint32), host(yg)[lo:hi].view(np.uint32)), (lo, hi)
     finally:
         lib.set_tuning("group_launch_tokens", 0)
 

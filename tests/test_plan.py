@@ -127,30 +127,22 @@ def test_norm_limits_the_fused_prologue(lib):
 
 def test_group_formats_past_eight_tokens(lib):
     """Q4_0 / I8G32 / Q6G32 with more than eight tokens run as two GEMV
-    launches (tokens 0-7, then the rest), each planned as the eight-token call,
-    when the GEMV streams at least 8 row tiles per SM or has more than 12
-    tokens; otherwise one launch.  W4_TUNE_GROUP_LAUNCH_TOKENS = t makes
+    launches of the eight-token kernel (tokens 0-7, then the rest), each
+    planned as the eight-token call.  W4_TUNE_GROUP_LAUNCH_TOKENS = t makes
     launches of at most t tokens.  Per-row INT4 stays one launch (the tensor
     cores take any M)."""
     keys = ("path", "quantize_launches", "grid", "threads", "smem_bytes", "stages", "k_splits")
-    long_rows = 8 * 8 * GB300["sms"]                  # 8 tiles of 8 rows per SM
     for fmt, N, K in (("q4_0", 12288, 1536), ("q4_0", 1536, 6144), ("i8g32", 262144, 1536),
-                      ("q6g32", 262144, 1536), ("q4_0", 77, 96), ("q4_0", long_rows, 1536),
-                      ("q4_0", long_rows - 8, 1536), ("i8g32", 2560, 1536)):
+                      ("q6g32", 262144, 1536), ("q4_0", 77, 96), ("i8g32", 2560, 1536)):
         for linear in (True, False):
             p8 = plan(lib, fmt, 8, N, K, linear=linear)
             assert p8["gemv_launches"] == 1
             for M in (9, 10, 12, 13, 16):
                 p = plan(lib, fmt, M, N, K, linear=linear)
-                split = M > 12 or N >= long_rows
-                assert p["gemv_launches"] == (2 if split else 1), (fmt, M, N, K, linear)
-                if split:
-                    assert {k: p[k] for k in keys} == {k: p8[k] for k in keys}, (fmt, M, N, K, linear)
-    assert plan(lib, "q4_0", 16, 2560, 1536, norm=True)["gemv_launches"] == 2
-    assert plan(lib, "q4_0", 12, 2560, 1536, norm=True)["gemv_launches"] == 1
-    assert plan(lib, "q4_0", 10, 6144, 1536, glu=True)["gemv_launches"] == 2      # 12288 weight rows
-    assert plan(lib, "q4_0", 10, 4864, 1536, glu=True)["gemv_launches"] == 2      # 9728: 8 tiles per SM
-    assert plan(lib, "q4_0", 10, 4860, 1536, glu=True)["gemv_launches"] == 1      # 9720: one tile short
+                assert p["gemv_launches"] == 2, (fmt, M, N, K, linear)
+                assert {k: p[k] for k in keys} == {k: p8[k] for k in keys}, (fmt, M, N, K, linear)
+    assert plan(lib, "q4_0", 12, 2560, 1536, norm=True)["gemv_launches"] == 2
+    assert plan(lib, "q4_0", 10, 2000, 1536, glu=True)["gemv_launches"] == 2
     for M in (1, 2, 4, 8):
         assert plan(lib, "i8g32", M, 262144, 1536)["gemv_launches"] == 1
     for M in (1, 9, 16):
